@@ -1,0 +1,361 @@
+/*
+ * qlora_oracle.c -- plain, slow, obviously-correct CPU oracle for the QLoRA
+ * NF4 linear-layer hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may call, link or
+ * load this file; only the tests, the smoke check and the CPU-baseline leg of
+ * the benchmark use it.  It shares no code, header, table generator or helper
+ * with the CUDA library: every step below is written out from the method's
+ * definition on the source pages, cited per function as
+ *   <page title> -- <section>.
+ * Page titles used below:
+ *   [QLoRA-26]  "QLoRA and 4bit Quantization | QLoRA 与 4-bit 量化" (datawhale, ch. 26)
+ *   [QLoRA-22]  "QLoRA and 4bit Quantization | QLoRA 与 4-bit NormalFloat 量化核心机制" (datawhale, ch. 22)
+ *   [Gemma-9]   "第 09 期 | QLoRA 4-bit 量化微调：消费级显卡也能训" (agentupdate gemma lesson 9)
+ *   [Finetune-4] "QLoRA 的三个核心技术" (gufacode finetune chapter 4)
+ *
+ * Precision rules (what the pages fix, and the readings taken where they do
+ * not):
+ *   - quantisation decisions are taken in IEEE binary32 (round to nearest
+ *     even, no fused multiply-add, no fast math; build with -ffp-contract=off);
+ *   - dequantised weights are bf16 values (compute dtype bf16, [Gemma-9]
+ *     section 9.3) obtained by ONE round-to-nearest-even of a binary32
+ *     product;
+ *   - forward and backward contractions run in binary64 over inputs that are
+ *     exactly representable (bf16 values widened to float).
+ *
+ * Parity pins: every function here is pinned by the not-gpu tests in
+ * tests/test_oracle_*.py against values printed on the pages, closed forms,
+ * invariants, brute force on tiny inputs and fp64 torch autograd.  The
+ * conventions the pages leave open (double-quantisation group layout and
+ * rounding, nibble order, tie-break) are pinned only by the conventions
+ * stated here: "parity unpinned" by the pages for those three choices.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* Codebook.  [QLoRA-26] Step 4 (create_nf4_lookup_table) and [QLoRA-22]
+ * Step 4 print the same 16 decimal values; each entry is the binary32 value
+ * nearest to the printed decimal (the C compiler converts literals with
+ * correct rounding).  Index 7 is the exact zero. */
+static const float ORACLE_NF4[16] = {
+    -1.0f,  -0.696f, -0.525f, -0.395f, -0.284f, -0.185f, -0.091f, 0.0f,
+    0.080f, 0.161f,  0.246f,  0.338f,  0.441f,  0.563f,  0.723f,  1.0f};
+
+#define ORACLE_ZERO_INDEX 7
+
+void oracle_nf4_codebook(float out[16]) {
+  for (int k = 0; k < 16; ++k) out[k] = ORACLE_NF4[k];
+}
+
+/* Nearest codepoint.  [QLoRA-26] Step 2: a normalised weight is mapped to
+ * the closest entry of the table (0.20 -> 0.161).  Distances are binary32
+ * |xn - c_k|; on an exact tie of the binary32 distances the lower index wins
+ * (the pages are silent on ties). */
+int oracle_nearest_code(float xn) {
+  int best = 0;
+  float bestd = fabsf(xn - ORACLE_NF4[0]);
+  for (int k = 1; k < 16; ++k) {
+    float d = fabsf(xn - ORACLE_NF4[k]);
+    if (d < bestd) {
+      bestd = d;
+      best = k;
+    }
+  }
+  return best;
+}
+
+/* Indices for `count` consecutive binary32 bit patterns starting at
+ * `start_bits` (used to compare against an exhaustive device sweep). */
+void oracle_nearest_codes_bits(uint32_t start_bits, int64_t count, uint8_t *out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < count; ++i) {
+    uint32_t b = start_bits + (uint32_t)i;
+    float f;
+    memcpy(&f, &b, 4);
+    out[i] = (uint8_t)oracle_nearest_code(f);
+  }
+}
+
+/* binary32 -> bf16 bits, round to nearest, ties to even, on the bit
+ * pattern.  NaN stays NaN (quiet bit set). */
+uint16_t oracle_bf16_rne(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x0040u);
+  uint32_t lsb = (u >> 16) & 1u;
+  u += 0x7fffu + lsb;
+  return (uint16_t)(u >> 16);
+}
+
+void oracle_bf16_rne_array(const float *in, int64_t n, uint16_t *out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_rne(in[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Status codes (oracle-local). */
+#define ORACLE_OK 0
+#define ORACLE_EINVAL 1
+
+/* Blockwise NF4 quantisation with optional double quantisation.
+ *
+ *  [Gemma-9] 9.2.1: weights are split into blocks, each block is normalised
+ *  to [-1, 1] by its absolute maximum, and each normalised value is stored as
+ *  the 4-bit index of its nearest NF4 codepoint ([QLoRA-26] Step 2).
+ *  [QLoRA-22] "engineering notes": 64 or 128 weights share one scale; blocks
+ *  here are `block` consecutive weights of the row-major flattened matrix
+ *  (cols % block == 0 keeps blocks inside one row).
+ *  [QLoRA-22] Step 3/4 docstring: real QLoRA stores two 4-bit indices per
+ *  uint8.  Reading (pages silent on order): element 2j in the HIGH nibble,
+ *  element 2j+1 in the LOW nibble.
+ *  [Gemma-9] 9.2.2 and [Finetune-4]: the per-block constants are themselves
+ *  quantised to 8 bits (double quantisation).  Reading: `group` consecutive
+ *  block constants share one binary32 scale s2 = max/127; each constant is
+ *  stored as clamp(rint_even(a / s2), -127, 127) in int8.  group == 0 keeps
+ *  the constants in binary32 (absmax_f32).
+ *
+ *  Steps per block b with weights w_i:
+ *    a_b = max_i |w_i|                       (exact)
+ *    xn_i = w_i / a_b                        (binary32 IEEE division)
+ *    idx_i = nearest codepoint of xn_i       (oracle_nearest_code)
+ *    a_b == 0  ->  idx_i = 7 (the zero codepoint), no division.
+ *  Steps per group g (group > 0):
+ *    gmax = max_b a_b; s2 = gmax / 127 (binary32); code_b = clamp(rint(a_b/s2))
+ *    gmax == 0 -> s2 = 0 and every code 0.
+ *
+ *  Returns the number of non-finite input weights (those blocks produce
+ *  unspecified indices), or -1 on invalid arguments.
+ */
+int64_t oracle_quantize_nf4(const float *w, int64_t rows, int64_t cols, int32_t block,
+                            int32_t group, uint8_t *packed, int8_t *absmax_code,
+                            float *absmax_f32, float *scale2, uint8_t *idx_out) {
+  if (rows < 0 || cols < 0 || block <= 0 || (block & 1) || group < 0) return -1;
+  if (cols % block) return -1;
+  const int64_t n = rows * cols;
+  const int64_t nblocks = n / block;
+  float *a = (float *)malloc((size_t)(nblocks > 0 ? nblocks : 1) * sizeof(float));
+  if (!a) return -1;
+  int64_t nonfinite = 0;
+
+#pragma omp parallel for schedule(static) reduction(+ : nonfinite)
+  for (int64_t b = 0; b < nblocks; ++b) {
+    const float *wb = w + b * block;
+    float amax = 0.0f;
+    for (int32_t i = 0; i < block; ++i) {
+      float v = wb[i];
+      if (!isfinite(v)) {
+        nonfinite++;
+        continue;
+      }
+      float m = fabsf(v);
+      if (m > amax) amax = m;
+    }
+    a[b] = amax;
+    for (int32_t i = 0; i < block; i += 2) {
+      int q0, q1;
+      if (amax == 0.0f) {
+        q0 = q1 = ORACLE_ZERO_INDEX;
+      } else {
+        float xn0 = wb[i] / amax;
+        float xn1 = wb[i + 1] / amax;
+        q0 = oracle_nearest_code(xn0);
+        q1 = oracle_nearest_code(xn1);
+      }
+      int64_t e = b * block + i;
+      if (idx_out) {
+        idx_out[e] = (uint8_t)q0;
+        idx_out[e + 1] = (uint8_t)q1;
+      }
+      packed[e / 2] = (uint8_t)((q0 << 4) | q1);
+    }
+  }
+
+  if (group == 0) {
+    if (absmax_f32)
+      for (int64_t b = 0; b < nblocks; ++b) absmax_f32[b] = a[b];
+  } else {
+    const int64_t ngroups = (nblocks + group - 1) / group;
+    for (int64_t g = 0; g < ngroups; ++g) {
+      int64_t b0 = g * group, b1 = b0 + group;
+      if (b1 > nblocks) b1 = nblocks;
+      float gmax = 0.0f;
+      for (int64_t b = b0; b < b1; ++b)
+        if (a[b] > gmax) gmax = a[b];
+      float s2 = gmax / 127.0f;
+      scale2[g] = s2;
+      for (int64_t b = b0; b < b1; ++b) {
+        float c = 0.0f;
+        if (s2 != 0.0f) c = rintf(a[b] / s2);
+        if (c > 127.0f) c = 127.0f;
+        if (c < -127.0f) c = -127.0f;
+        absmax_code[b] = (int8_t)c;
+      }
+    }
+  }
+  free(a);
+  return nonfinite;
+}
+
+/* Dequantisation to bf16.  [QLoRA-26] Step 3 / Step 4 (TODO 1): the
+ * approximate weight is the codepoint selected by the stored index times the
+ * block's scale factor; [Gemma-9] 9.2.2 (mermaid): the 8-bit constants are
+ * dequantised first, then used on the 4-bit weights; [Gemma-9] 9.3: compute
+ * dtype bf16.
+ *    a_hat = (float)code_b * s2_g            (binary32 product; DQ)
+ *    a_hat = absmax_f32[b]                   (no DQ)
+ *    w_hat = bf16_rne((float)c_idx * a_hat)  (binary32 product, one rounding)
+ */
+int oracle_dequant_bf16(const uint8_t *packed, const int8_t *absmax_code,
+                        const float *absmax_f32, const float *scale2, int64_t rows,
+                        int64_t cols, int32_t block, int32_t group, uint16_t *w_out) {
+  if (rows < 0 || cols < 0 || block <= 0 || (block & 1) || group < 0) return ORACLE_EINVAL;
+  if (cols % block) return ORACLE_EINVAL;
+  const int64_t n = rows * cols;
+  const int64_t nblocks = n / block;
+#pragma omp parallel for schedule(static)
+  for (int64_t b = 0; b < nblocks; ++b) {
+    float ahat;
+    if (group > 0)
+      ahat = (float)absmax_code[b] * scale2[b / group];
+    else
+      ahat = absmax_f32[b];
+    for (int32_t i = 0; i < block; ++i) {
+      int64_t e = b * block + i;
+      uint8_t byte = packed[e / 2];
+      int q = (e & 1) ? (byte & 0x0f) : (byte >> 4);
+      float prod = ORACLE_NF4[q] * ahat;
+      w_out[e] = oracle_bf16_rne(prod);
+    }
+  }
+  return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Forward.  [QLoRA-26] Step 3 (garbled formula, read as
+ *   y = x W_hat^T + (x A^T) B^T * alpha / r )
+ * and Step 4 (TODO 2: base output through F.linear with the dequantised
+ * weight, LoRA increment through lora_A then lora_B then the scaling).  No
+ * bias, no dropout.
+ *   x: [M, K]   W_hat: [N, K]   A: [r, K]   B: [N, r]
+ * All inputs are binary32 arrays holding bf16-exact values; every dot product
+ * is accumulated in binary64 in ascending index order.
+ * Only the rows listed in `rows` (nrows of them) are evaluated; outputs are
+ * packed in that order: y is [nrows, N], t is [nrows, r] (t = x A^T). */
+void oracle_linear_fwd(const float *x, int64_t M, int64_t K, const float *w, int64_t N,
+                       const float *A, const float *B, int32_t r, double alpha,
+                       const int64_t *rows, int64_t nrows, double *y, double *t) {
+  (void)M;
+  const double s = alpha / (double)r;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t ri = 0; ri < nrows; ++ri) {
+    const float *xm = x + rows[ri] * K;
+    double *tm = t + ri * r;
+    for (int32_t j = 0; j < r; ++j) {
+      double acc = 0.0;
+      for (int64_t k = 0; k < K; ++k) acc += (double)xm[k] * (double)A[j * K + k];
+      tm[j] = acc;
+    }
+    for (int64_t n = 0; n < N; ++n) {
+      const float *wn = w + n * K;
+      double base = 0.0;
+      for (int64_t k = 0; k < K; ++k) base += (double)xm[k] * (double)wn[k];
+      double lora = 0.0;
+      for (int32_t j = 0; j < r; ++j) lora += tm[j] * (double)B[n * r + j];
+      y[ri * N + n] = base + s * lora;
+    }
+  }
+}
+
+/* Backward.  [QLoRA-26] Step 3 (gradients reach x, A and B; the NF4 state is
+ * frozen) and Step 4 test "frozen base gradient contract"; [QLoRA-22] Step 1
+ * item 4: the gradient also flows through the base weight (to x) but never
+ * updates it.  With s = alpha / r and t = x A^T:
+ *   u  = dY B                       [M, r]
+ *   dX = dY W_hat + s * u A         [M, K]   (rows listed in `rows` only)
+ *   dA = s * u^T x                  [r, K]
+ *   dB = s * dY^T t                 [N, r]
+ * Binary64 accumulation in ascending index order.  t_out and u_out are
+ * [M, r] (all rows); dX is [nrows, K]. */
+void oracle_linear_bwd(const float *x, const float *dY, int64_t M, int64_t K, int64_t N,
+                       const float *w, const float *A, const float *B, int32_t r,
+                       double alpha, const int64_t *rows, int64_t nrows, double *dX,
+                       double *dA, double *dB, double *t_out, double *u_out) {
+  const double s = alpha / (double)r;
+#pragma omp parallel for schedule(static)
+  for (int64_t m = 0; m < M; ++m) {
+    const float *xm = x + m * K;
+    const float *gm = dY + m * N;
+    for (int32_t j = 0; j < r; ++j) {
+      double acc = 0.0;
+      for (int64_t k = 0; k < K; ++k) acc += (double)xm[k] * (double)A[j * K + k];
+      t_out[m * r + j] = acc;
+      double acc2 = 0.0;
+      for (int64_t n = 0; n < N; ++n) acc2 += (double)gm[n] * (double)B[n * r + j];
+      u_out[m * r + j] = acc2;
+    }
+  }
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t ri = 0; ri < nrows; ++ri) {
+    const int64_t m = rows[ri];
+    const float *gm = dY + m * N;
+    const double *um = u_out + m * r;
+    for (int64_t k = 0; k < K; ++k) {
+      double base = 0.0;
+      for (int64_t n = 0; n < N; ++n) base += (double)gm[n] * (double)w[n * K + k];
+      double lora = 0.0;
+      for (int32_t j = 0; j < r; ++j) lora += um[j] * (double)A[j * K + k];
+      dX[ri * K + k] = base + s * lora;
+    }
+  }
+#pragma omp parallel for schedule(static)
+  for (int64_t k = 0; k < K; ++k) {
+    for (int32_t j = 0; j < r; ++j) {
+      double acc = 0.0;
+      for (int64_t m = 0; m < M; ++m) acc += u_out[m * r + j] * (double)x[m * K + k];
+      dA[j * K + k] = s * acc;
+    }
+  }
+#pragma omp parallel for schedule(static)
+  for (int64_t n = 0; n < N; ++n) {
+    for (int32_t j = 0; j < r; ++j) {
+      double acc = 0.0;
+      for (int64_t m = 0; m < M; ++m) acc += (double)dY[m * N + n] * t_out[m * r + j];
+      dB[n * r + j] = s * acc;
+    }
+  }
+}
+
+/* Storage accounting.  [QLoRA-26] Step 4 (qlora_trainable_state_ledger:
+ * packed size (numel + 1) // 2 bytes) and [Finetune-4] (4.5 -> ~4.127 bits
+ * per parameter): bytes of packed indices, block constants and second-level
+ * scales for one matrix. */
+int oracle_nf4_storage_bytes(int64_t rows, int64_t cols, int32_t block, int32_t group,
+                             int64_t *packed_b, int64_t *const_b, int64_t *scale_b) {
+  if (rows < 0 || cols < 0 || block <= 0 || group < 0) return ORACLE_EINVAL;
+  const int64_t n = rows * cols;
+  const int64_t nblocks = (n + block - 1) / block;
+  *packed_b = (n + 1) / 2;
+  if (group == 0) {
+    *const_b = nblocks * 4; /* binary32 absmax per block */
+    *scale_b = 0;
+  } else {
+    *const_b = nblocks * 1; /* int8 code per block */
+    *scale_b = ((nblocks + group - 1) / group) * 4;
+  }
+  return ORACLE_OK;
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
