@@ -1,0 +1,405 @@
+// capi.cu -- the extern "C" boundary of the QLoRA NF4 library: argument
+// validation, workspace layout, TMA descriptor encoding and kernel
+// selection.  Every compute step runs in the CUDA kernels of this library.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+
+using namespace qlora;
+
+namespace {
+
+// ---------------------------------------------------------------- helpers
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int round_up(int v, int m) { return (v + m - 1) / m * m; }
+inline size_t round_up_sz(size_t v, size_t m) { return (v + m - 1) / m * m; }
+
+int num_sms_current() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
+}
+
+// Decision thresholds of the nearest-codepoint rule.  For each pair of
+// neighbouring codepoints (c_k, c_{k+1}) the threshold is the smallest fp32 x
+// in [c_k, c_{k+1}] whose fp32 distance to c_{k+1} is strictly smaller than
+// its fp32 distance to c_k (an exact tie keeps the lower index).  Both
+// distances are monotone in x, so a bisection over the ordered fp32 values
+// finds it.
+uint32_t fkey(float f) {
+  uint32_t b;
+  std::memcpy(&b, &f, 4);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+float funkey(uint32_t k) {
+  const uint32_t b = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+  float f;
+  std::memcpy(&f, &b, 4);
+  return f;
+}
+float g_th[15];
+std::once_flag g_th_once;
+void compute_thresholds() {
+  static const float c[16] = {QLORA_NF4_VALUES};
+  for (int k = 0; k < 15; ++k) {
+    const float lo = c[k], hi = c[k + 1];
+    auto closer_to_hi = [&](float x) {
+      volatile float dh = std::fabs(x - hi);
+      volatile float dl = std::fabs(x - lo);
+      return dh < dl;
+    };
+    uint32_t a = fkey(lo), b = fkey(hi);  // closer_to_hi(lo) false, (hi) true
+    while (b - a > 1) {
+      const uint32_t mid = a + (b - a) / 2;
+      if (closer_to_hi(funkey(mid)))
+        b = mid;
+      else
+        a = mid;
+    }
+    g_th[k] = funkey(b);
+  }
+}
+const float *thresholds() {
+  std::call_once(g_th_once, compute_thresholds);
+  return g_th;
+}
+
+qlora_status check_weight(const qlora_nf4_weight *w, bool need_buffers) {
+  if (!w) return QLORA_ERR_INVALID_ARG;
+  if (w->rows < 0 || w->cols < 0) return QLORA_ERR_SHAPE;
+  if (w->block != kBlock) return QLORA_ERR_SHAPE;
+  if (!(w->group == 0 || w->group == 32 || w->group == 64 || w->group == 128 ||
+        w->group == 256))
+    return QLORA_ERR_SHAPE;
+  if (w->cols % kBlock) return QLORA_ERR_SHAPE;
+  if (!need_buffers) return QLORA_OK;
+  if (!w->packed) return QLORA_ERR_INVALID_ARG;
+  if (w->group > 0 && (!w->absmax_code || !w->scale2)) return QLORA_ERR_INVALID_ARG;
+  if (w->group == 0 && !w->absmax_f32) return QLORA_ERR_INVALID_ARG;
+  if (!aligned16(w->packed)) return QLORA_ERR_ALIGN;
+  if (w->absmax_f32 && (reinterpret_cast<uintptr_t>(w->absmax_f32) & 3u)) return QLORA_ERR_ALIGN;
+  if (w->scale2 && (reinterpret_cast<uintptr_t>(w->scale2) & 3u)) return QLORA_ERR_ALIGN;
+  return QLORA_OK;
+}
+
+// Workspace layout for (M, N, K, r).
+struct WsLayout {
+  size_t status, t, u, bt, at, part, total;
+};
+WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int r) {
+  const int RP = round_up(r, 16);
+  WsLayout L;
+  size_t off = 0;
+  L.status = off;
+  off += 256;
+  L.t = off;
+  off += round_up_sz((size_t)M * RP * 4, 256);
+  L.u = off;
+  off += round_up_sz((size_t)M * RP * 4, 256);
+  L.bt = off;
+  off += round_up_sz((size_t)RP * N * 2, 256);
+  L.at = off;
+  off += round_up_sz((size_t)K * RP * 2, 256);
+  L.part = off;
+  const size_t pn = (size_t)skinny_splits(M, (int)N) * N, pk = (size_t)skinny_splits(M, (int)K) * K;
+  off += round_up_sz((pn > pk ? pn : pk) * RP * 4, 256);
+  L.total = off;
+  return L;
+}
+
+// 2-D bf16 tensor map: dims {inner, outer}, row pitch in bytes.
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool make_tmap(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
+               uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swz) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+qlora_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA; }
+
+qlora_status check_linear_common(const qlora_nf4_weight *w, const uint16_t *x, int64_t M,
+                                 const uint16_t *A, const uint16_t *B, int32_t r, void *ws,
+                                 size_t ws_bytes) {
+  qlora_status st = check_weight(w, true);
+  if (st != QLORA_OK) return st;
+  if (!x || !A || !B) return QLORA_ERR_INVALID_ARG;
+  if (M < 1 || M > (int64_t)INT32_MAX) return QLORA_ERR_SHAPE;
+  if (w->rows < 1 || w->cols < kBlock) return QLORA_ERR_SHAPE;
+  if (w->rows % 8 || w->rows > (int64_t)INT32_MAX || w->cols > (int64_t)INT32_MAX)
+    return QLORA_ERR_SHAPE;
+  if (r < 8 || r > 64 || r % 8) return QLORA_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(A) || !aligned16(B)) return QLORA_ERR_ALIGN;
+  if (!ws) return QLORA_ERR_WORKSPACE;
+  if (!aligned16(ws)) return QLORA_ERR_ALIGN;
+  if (ws_bytes < ws_layout(M, w->rows, w->cols, r).total) return QLORA_ERR_WORKSPACE;
+  return QLORA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *qlora_status_string(qlora_status s) {
+  switch (s) {
+    case QLORA_OK: return "ok";
+    case QLORA_ERR_INVALID_ARG: return "invalid argument";
+    case QLORA_ERR_SHAPE: return "unsupported shape";
+    case QLORA_ERR_ALIGN: return "pointer or stride not 16-byte aligned";
+    case QLORA_ERR_DTYPE: return "unsupported dtype";
+    case QLORA_ERR_NONFINITE: return "non-finite input";
+    case QLORA_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case QLORA_ERR_CUDA: return "CUDA error";
+    case QLORA_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+qlora_status qlora_nf4_codebook(float out[16]) {
+  if (!out) return QLORA_ERR_INVALID_ARG;
+  static const float c[16] = {QLORA_NF4_VALUES};
+  for (int i = 0; i < 16; ++i) out[i] = c[i];
+  return QLORA_OK;
+}
+
+qlora_status qlora_nf4_thresholds(float out[15]) {
+  if (!out) return QLORA_ERR_INVALID_ARG;
+  const float *t = thresholds();
+  for (int i = 0; i < 15; ++i) out[i] = t[i];
+  return QLORA_OK;
+}
+
+qlora_status qlora_nf4_sizes(int64_t rows, int64_t cols, int32_t block, int32_t group,
+                             size_t *packed_bytes, size_t *code_bytes, size_t *scale_bytes) {
+  if (rows < 0 || cols < 0 || block <= 0 || (block & 1) || group < 0) return QLORA_ERR_SHAPE;
+  if (cols % block) return QLORA_ERR_SHAPE;
+  const int64_t n = rows * cols, nb = n / block;
+  if (packed_bytes) *packed_bytes = (size_t)(n / 2);
+  if (code_bytes) *code_bytes = (size_t)(group > 0 ? nb : nb * 4);
+  if (scale_bytes) *scale_bytes = (size_t)(group > 0 ? ((nb + group - 1) / group) * 4 : 0);
+  return QLORA_OK;
+}
+
+qlora_status qlora_quantize_nf4(const void *W, qlora_dtype w_dtype, const qlora_nf4_weight *out,
+                                int32_t *nonfinite_flag, void *stream) {
+  qlora_status st = check_weight(out, true);
+  if (st != QLORA_OK) return st;
+  if (!W) return QLORA_ERR_INVALID_ARG;
+  if (w_dtype != QLORA_F32 && w_dtype != QLORA_BF16) return QLORA_ERR_DTYPE;
+  if (!aligned16(W)) return QLORA_ERR_ALIGN;
+  const int64_t nblocks = out->rows * out->cols / kBlock;
+  return cuda_status(launch_quantize(W, w_dtype == QLORA_BF16, nblocks, out->group, out->packed,
+                                     out->absmax_code, out->absmax_f32, out->scale2,
+                                     nonfinite_flag, thresholds(),
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+qlora_status qlora_dequant(const qlora_nf4_weight *w, uint16_t *W_out, void *stream) {
+  qlora_status st = check_weight(w, true);
+  if (st != QLORA_OK) return st;
+  if (!W_out) return QLORA_ERR_INVALID_ARG;
+  if (!aligned16(W_out)) return QLORA_ERR_ALIGN;
+  const int64_t nblocks = w->rows * w->cols / kBlock;
+  return cuda_status(launch_dequant(w->packed, w->absmax_code, w->absmax_f32, w->scale2, w->group,
+                                    nblocks, W_out, num_sms_current(),
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+qlora_status qlora_workspace_size(int64_t M, int64_t N, int64_t K, int32_t r, size_t *bytes) {
+  if (!bytes) return QLORA_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || r < 1 || r > 64) return QLORA_ERR_SHAPE;
+  *bytes = ws_layout(M, N, K, r).total;
+  return QLORA_OK;
+}
+
+qlora_status qlora_workspace_init(void *ws, size_t ws_bytes, void *stream) {
+  if (!ws) return QLORA_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream)));
+}
+
+qlora_status qlora_device_status(void *ws, int32_t *status, void *stream) {
+  if (!ws || !status) return QLORA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && v != 0) e = cudaMemsetAsync(ws, 0, sizeof(int32_t), s);
+  if (e != cudaSuccess) return QLORA_ERR_CUDA;
+  *status = v;
+  return QLORA_OK;
+}
+
+qlora_status qlora_linear_fwd(const qlora_nf4_weight *w, const uint16_t *x, int64_t M,
+                              const uint16_t *A, const uint16_t *B, int32_t r, float alpha,
+                              void *y, qlora_dtype y_dtype, float *t_save, void *ws,
+                              size_t ws_bytes, uint32_t flags, void *stream) {
+  qlora_status st = check_linear_common(w, x, M, A, B, r, ws, ws_bytes);
+  if (st != QLORA_OK) return st;
+  if (!y) return QLORA_ERR_INVALID_ARG;
+  if (y_dtype != QLORA_F32 && y_dtype != QLORA_BF16) return QLORA_ERR_DTYPE;
+  if (!aligned16(y) || (t_save && !aligned16(t_save))) return QLORA_ERR_ALIGN;
+  if ((flags & QLORA_FLAG_FORCE_GEMV) && (flags & QLORA_FLAG_FORCE_GEMM))
+    return QLORA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int N = (int)w->rows, K = (int)w->cols;
+  const float sc = alpha / (float)r;
+  const WsLayout L = ws_layout(M, N, K, r);
+  uint8_t *wsb = static_cast<uint8_t *>(ws);
+  int gw, gS;
+  const bool gemv_ok = M <= 16 && gemv_plan(K, &gw, &gS) == 0;
+  const bool use_gemv =
+      (flags & QLORA_FLAG_FORCE_GEMV) || (M <= 16 && gemv_ok && !(flags & QLORA_FLAG_FORCE_GEMM));
+  if (use_gemv) {
+    if (!gemv_ok) return QLORA_ERR_SHAPE;
+    float *t = t_save ? t_save : reinterpret_cast<float *>(wsb + L.t);
+    cudaError_t e = launch_lora_down(x, A, M, K, r, t, s);
+    if (e != cudaSuccess) return QLORA_ERR_CUDA;
+    GemvArgs a{};
+    a.packed = w->packed;
+    a.codes = w->absmax_code;
+    a.absf = w->absmax_f32;
+    a.scale2 = w->scale2;
+    a.group = w->group;
+    a.N = N;
+    a.K = K;
+    a.x = x;
+    a.M = (int)M;
+    a.t = t;
+    a.B = B;
+    a.r = r;
+    a.s = sc;
+    a.y = y;
+    a.y_bf16 = y_dtype == QLORA_BF16;
+    return cuda_status(launch_gemv(a, num_sms_current(), s));
+  }
+  const int RP = round_up(r, 16);
+  CUtensorMap tmA, tmL1, tmL2;
+  if (!make_tmap(&tmA, x, K, M, (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap(&tmL1, A, K, r, (uint64_t)K * 2, 64, RP, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap(&tmL2, B, r, N, (uint64_t)r * 2, 16, 256, CU_TENSOR_MAP_SWIZZLE_32B))
+    return QLORA_ERR_CUDA;
+  GemmArgs g{};
+  g.packed = w->packed;
+  g.codes = w->absmax_code;
+  g.absf = w->absmax_f32;
+  g.scale2 = w->scale2;
+  g.group = w->group;
+  g.wrows = N;
+  g.wcols = K;
+  g.M = (int)M;
+  g.out_cols = N;
+  g.kdim = K;
+  g.r = r;
+  g.r_pad = RP;
+  g.s = sc;
+  g.out = y;
+  g.out_bf16 = y_dtype == QLORA_BF16;
+  g.aux_out = t_save;
+  g.stages = gemm_pick_stages(RP);
+  g.status = reinterpret_cast<int *>(wsb + L.status);
+  return cuda_status(launch_gemm(false, tmA, tmL1, tmL2, g, s));
+}
+
+qlora_status qlora_linear_bwd(const qlora_nf4_weight *w, const uint16_t *x, const uint16_t *dY,
+                              int64_t M, const uint16_t *A, const uint16_t *B, int32_t r,
+                              float alpha, const float *t_saved, void *dX, qlora_dtype dx_dtype,
+                              float *dA, float *dB, void *ws, size_t ws_bytes, uint32_t flags,
+                              void *stream) {
+  (void)flags;
+  qlora_status st = check_linear_common(w, x, M, A, B, r, ws, ws_bytes);
+  if (st != QLORA_OK) return st;
+  if (!dY || !dX || !dA || !dB) return QLORA_ERR_INVALID_ARG;
+  if (dx_dtype != QLORA_F32 && dx_dtype != QLORA_BF16) return QLORA_ERR_DTYPE;
+  if (!aligned16(dY) || !aligned16(dX) || !aligned16(dA) || !aligned16(dB) ||
+      (t_saved && !aligned16(t_saved)))
+    return QLORA_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int N = (int)w->rows, K = (int)w->cols;
+  const int RP = round_up(r, 16);
+  const float sc = alpha / (float)r;
+  const int nsm = num_sms_current();
+  const WsLayout L = ws_layout(M, N, K, r);
+  uint8_t *wsb = static_cast<uint8_t *>(ws);
+  float *u = reinterpret_cast<float *>(wsb + L.u);
+  uint16_t *Bt = reinterpret_cast<uint16_t *>(wsb + L.bt);
+  uint16_t *At = reinterpret_cast<uint16_t *>(wsb + L.at);
+  float *part = reinterpret_cast<float *>(wsb + L.part);
+  const float *t = t_saved;
+  cudaError_t e;
+  if (!t) {
+    float *tw = reinterpret_cast<float *>(wsb + L.t);
+    e = launch_lora_down(x, A, M, K, r, tw, s);
+    if (e != cudaSuccess) return QLORA_ERR_CUDA;
+    t = tw;
+  }
+  e = launch_transposes(A, B, N, K, r, RP, At, Bt, nsm, s);
+  if (e != cudaSuccess) return QLORA_ERR_CUDA;
+  CUtensorMap tmA, tmL1, tmL2;
+  if (!make_tmap(&tmA, dY, N, M, (uint64_t)N * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap(&tmL1, Bt, N, RP, (uint64_t)N * 2, 64, RP, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap(&tmL2, At, RP, K, (uint64_t)RP * 2, 16, 256, CU_TENSOR_MAP_SWIZZLE_32B))
+    return QLORA_ERR_CUDA;
+  GemmArgs g{};
+  g.packed = w->packed;
+  g.codes = w->absmax_code;
+  g.absf = w->absmax_f32;
+  g.scale2 = w->scale2;
+  g.group = w->group;
+  g.wrows = N;
+  g.wcols = K;
+  g.M = (int)M;
+  g.out_cols = K;
+  g.kdim = N;
+  g.r = r;
+  g.r_pad = RP;
+  g.s = sc;
+  g.out = dX;
+  g.out_bf16 = dx_dtype == QLORA_BF16;
+  g.aux_out = u;
+  g.stages = gemm_pick_stages(RP);
+  g.status = reinterpret_cast<int *>(wsb + L.status);
+  e = launch_gemm(true, tmA, tmL1, tmL2, g, s);
+  if (e != cudaSuccess) return QLORA_ERR_CUDA;
+  // dB = s . dY^T . t
+  const int spN = skinny_splits(M, N);
+  e = launch_skinny(dY, M, N, t, r, RP, part, spN, s);
+  if (e == cudaSuccess) e = launch_reduce_parts(part, spN, N, RP, r, sc, false, dB, nsm, s);
+  if (e != cudaSuccess) return QLORA_ERR_CUDA;
+  // dA = s . u^T . x
+  const int spK = skinny_splits(M, K);
+  e = launch_skinny(x, M, K, u, r, RP, part, spK, s);
+  if (e == cudaSuccess) e = launch_reduce_parts(part, spK, K, RP, r, sc, true, dA, nsm, s);
+  return cuda_status(e);
+}
+
+}  // extern "C"

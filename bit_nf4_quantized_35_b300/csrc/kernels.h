@@ -1,0 +1,77 @@
+// kernels.h -- internal declarations shared by the kernel files and the C ABI
+// implementation (argument structs and host-side launchers).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qlora {
+
+// Fused dequantise + tcgen05 GEMM (gemm_tc.cu).
+struct GemmArgs {
+  const uint8_t *packed;
+  const int8_t *codes;
+  const float *absf;
+  const float *scale2;
+  int group;
+  int64_t wrows;  // N
+  int64_t wcols;  // K
+  int M;
+  int out_cols;   // N (forward) or K (dX)
+  int kdim;       // contraction length: K (forward) or N (dX)
+  int r;
+  int r_pad;
+  float s;
+  void *out;
+  int out_bf16;
+  float *aux_out;  // t or u, fp32 [M, r]; written by the CTAs of output column tile 0
+  int stages;
+  int *status;
+};
+cudaError_t launch_gemm(bool dx, const CUtensorMap &tmA, const CUtensorMap &tmL1,
+                        const CUtensorMap &tmL2, const GemmArgs &args, cudaStream_t s);
+int gemm_pick_stages(int r_pad);
+
+// Split-K decode GEMV (gemv.cu).
+struct GemvArgs {
+  const uint8_t *packed;
+  const int8_t *codes;
+  const float *absf;
+  const float *scale2;
+  int group;
+  int N, K;
+  const uint16_t *x;
+  int M;
+  const float *t;     // [M, r] fp32
+  const uint16_t *B;  // [N, r] bf16
+  int r;
+  float s;
+  void *y;
+  int y_bf16;
+  int row_tiles;  // ceil(N / 16), set by the launcher
+  int clusters;   // gridDim.x, set by the launcher
+};
+int gemv_plan(int K, int *warps, int *S);
+cudaError_t launch_gemv(GemvArgs a, int num_sms, cudaStream_t s);
+cudaError_t launch_lora_down(const uint16_t *x, const uint16_t *A, int64_t M, int K, int r,
+                             float *t, cudaStream_t s);
+
+// Quantise / dequantise (quantize.cu).
+cudaError_t launch_quantize(const void *W, bool bf16_in, int64_t nblocks, int group,
+                            uint8_t *packed, int8_t *codes, float *absf, float *scale2,
+                            int *nonfinite_flag, const float th[15], cudaStream_t s);
+cudaError_t launch_dequant(const uint8_t *packed, const int8_t *codes, const float *absf,
+                           const float *scale2, int group, int64_t nblocks, uint16_t *out,
+                           int num_sms, cudaStream_t s);
+
+// Rank-r gradient contractions and layout helpers (lora_grad.cu).
+int skinny_splits(int64_t M, int C);
+cudaError_t launch_skinny(const uint16_t *G, int64_t M, int C, const float *V, int r, int RP,
+                          float *part, int splits, cudaStream_t s);
+cudaError_t launch_reduce_parts(const float *part, int splits, int C, int RP, int r, float sc,
+                                bool transpose, float *dst, int num_sms, cudaStream_t s);
+cudaError_t launch_transposes(const uint16_t *A, const uint16_t *B, int N, int K, int r, int RP,
+                              uint16_t *At, uint16_t *Bt, int num_sms, cudaStream_t s);
+
+}  // namespace qlora
