@@ -146,6 +146,13 @@ bool make_tmap(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
   return r == CUDA_SUCCESS;
 }
 
+void set_block_constants(GemmArgs &g, const qlora_nf4_weight *w) {
+  g.use_code = w->group > 0;
+  g.cvec = w->group > 0 ? w->scale2 : w->absmax_f32;
+  g.cdiv = w->group > 0 ? w->group : 1;
+  if (!g.use_code) g.codes = reinterpret_cast<const int8_t *>(w->packed);
+}
+
 qlora_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA; }
 
 qlora_status check_linear_common(const qlora_nf4_weight *w, const uint16_t *x, int64_t M,
@@ -276,14 +283,11 @@ qlora_status qlora_linear_fwd(const qlora_nf4_weight *w, const uint16_t *x, int6
   const WsLayout L = ws_layout(M, N, K, r);
   uint8_t *wsb = static_cast<uint8_t *>(ws);
   int gw, gS;
-  const bool gemv_ok = M <= 16 && gemv_plan(K, &gw, &gS) == 0;
+  const bool gemv_ok = M <= 16 && gemv_plan(K, (int)M, &gw, &gS) == 0;
   const bool use_gemv =
       (flags & QLORA_FLAG_FORCE_GEMV) || (M <= 16 && gemv_ok && !(flags & QLORA_FLAG_FORCE_GEMM));
   if (use_gemv) {
     if (!gemv_ok) return QLORA_ERR_SHAPE;
-    float *t = t_save ? t_save : reinterpret_cast<float *>(wsb + L.t);
-    cudaError_t e = launch_lora_down(x, A, M, K, r, t, s);
-    if (e != cudaSuccess) return QLORA_ERR_CUDA;
     GemvArgs a{};
     a.packed = w->packed;
     a.codes = w->absmax_code;
@@ -294,8 +298,13 @@ qlora_status qlora_linear_fwd(const qlora_nf4_weight *w, const uint16_t *x, int6
     a.K = K;
     a.x = x;
     a.M = (int)M;
-    a.t = t;
+    a.A = A;
     a.B = B;
+    a.t_save = t_save;
+    a.use_code = w->group > 0;
+    a.cvec = w->group > 0 ? w->scale2 : w->absmax_f32;
+    a.cdiv = w->group > 0 ? w->group : 1;
+    if (!a.use_code) a.codes = reinterpret_cast<const int8_t *>(w->packed);
     a.r = r;
     a.s = sc;
     a.y = y;
@@ -305,8 +314,8 @@ qlora_status qlora_linear_fwd(const qlora_nf4_weight *w, const uint16_t *x, int6
   const int RP = round_up(r, 16);
   CUtensorMap tmA, tmL1, tmL2;
   if (!make_tmap(&tmA, x, K, M, (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap(&tmL1, A, K, r, (uint64_t)K * 2, 64, RP, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap(&tmL2, B, r, N, (uint64_t)r * 2, 16, 256, CU_TENSOR_MAP_SWIZZLE_32B))
+      !make_tmap(&tmL1, A, K, r, (uint64_t)K * 2, 64, RP / 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap(&tmL2, B, r, N, (uint64_t)r * 2, 16, 128, CU_TENSOR_MAP_SWIZZLE_32B))
     return QLORA_ERR_CUDA;
   GemmArgs g{};
   g.packed = w->packed;
@@ -327,6 +336,7 @@ qlora_status qlora_linear_fwd(const qlora_nf4_weight *w, const uint16_t *x, int6
   g.aux_out = t_save;
   g.stages = gemm_pick_stages(RP);
   g.status = reinterpret_cast<int *>(wsb + L.status);
+  set_block_constants(g, w);
   return cuda_status(launch_gemm(false, tmA, tmL1, tmL2, g, s));
 }
 
@@ -366,8 +376,8 @@ qlora_status qlora_linear_bwd(const qlora_nf4_weight *w, const uint16_t *x, cons
   if (e != cudaSuccess) return QLORA_ERR_CUDA;
   CUtensorMap tmA, tmL1, tmL2;
   if (!make_tmap(&tmA, dY, N, M, (uint64_t)N * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap(&tmL1, Bt, N, RP, (uint64_t)N * 2, 64, RP, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap(&tmL2, At, RP, K, (uint64_t)RP * 2, 16, 256, CU_TENSOR_MAP_SWIZZLE_32B))
+      !make_tmap(&tmL1, Bt, N, RP, (uint64_t)N * 2, 64, RP / 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap(&tmL2, At, RP, K, (uint64_t)RP * 2, 16, 128, CU_TENSOR_MAP_SWIZZLE_32B))
     return QLORA_ERR_CUDA;
   GemmArgs g{};
   g.packed = w->packed;
@@ -388,6 +398,7 @@ qlora_status qlora_linear_bwd(const qlora_nf4_weight *w, const uint16_t *x, cons
   g.aux_out = u;
   g.stages = gemm_pick_stages(RP);
   g.status = reinterpret_cast<int *>(wsb + L.status);
+  set_block_constants(g, w);
   e = launch_gemm(true, tmA, tmL1, tmL2, g, s);
   if (e != cudaSuccess) return QLORA_ERR_CUDA;
   // dB = s . dY^T . t

@@ -10,97 +10,100 @@
 //                           aux[M, r] = dY . B                  (u, saved)
 //                           out     += (s . aux) . A
 //
-// Tile 128 (M) x 256 (output columns), contraction step 64, one CTA per SM.
-// Warp roles (320 threads):
-//   warps 0-7  dequantising producers: every thread turns the 32 packed
-//              bytes of one (row, 64-block) into 64 bf16 values through the
-//              per-block table T[i] = bf16(c_i * a_hat) (byte permutes, no
-//              smem lookups) and stores them straight into the B operand
-//              tile in the 128-byte-swizzled layout the tensor core reads
-//              (K-major for the forward, MN-major for dX).  After the main
-//              loop the same warps run the epilogue.
-//   warp 8     TMA producer: activation tile (x or dY) and the rank-r
-//              down-projection tile per stage; the up-projection tile once.
-//   warp 9     TMEM owner and single-thread tcgen05.mma issuer.
-// Per stage the MMA thread issues 4 x (128x256x16) for the base product and
-// 4 x (128 x r_pad x 16) for the LoRA down-projection, both reading the same
-// activation tile, accumulating in TMEM columns [0,256) and [256,256+r_pad).
-// After the contraction the epilogue warps read the down-projection, scale
-// it by s, round it to bf16 into shared memory, and the MMA thread adds the
-// rank-r up-projection into the base accumulator with r_pad/16 more MMAs
-// before the final TMEM -> register -> global store.
+// CTA pairs (a cluster of 2) share one 256 x 256 output tile through
+// tcgen05 cta_group::2: CTA r owns rows [128r, 128r+128) of the tile and
+// half of the B operand (output columns [128r, 128r+128)); one thread of the
+// leader CTA issues every MMA for both.  Contraction step 64.
+// Per CTA, 320 threads:
+//   warps 0-7  dequantising producers: two threads per B row, 32 packed
+//              nibbles each, through the per-block table
+//              T[i] = bf16(c_i * a_hat) indexed with byte permutes; the bf16
+//              values go straight into the 128-byte-swizzled operand layout
+//              the tensor core reads (K-major forward, MN-major dX).  After
+//              the main loop the same warps run the epilogue.
+//   warp 8     TMA: activation rows of this CTA and its half of the LoRA
+//              down-projection operand per stage; its half of the
+//              up-projection operand once.
+//   warp 9     TMEM allocation (both CTAs); in the leader the single MMA
+//              issuer, in the peer a relay that forwards "stage ready" to the
+//              leader's barrier.
+// Per stage the leader issues 4 x (256x256x16) for the base product and
+// 4 x (256 x r_pad x 16) for the LoRA down-projection, both reading the same
+// activation tiles; accumulators live in TMEM columns [0,256) and
+// [256, 256 + r_pad) of both CTAs.  After the contraction each CTA's
+// epilogue scales its down-projection rows by s, rounds them to bf16 into
+// shared memory, and the leader adds the rank-r up-projection with r_pad/16
+// more MMAs before the TMEM -> register -> global store.
+//
+// Each SM dequantises 128 x 64 weights per stage for 2 x 128 x 256 x 64
+// MMA work, half of what a single-CTA 128 x 256 tile needs; the integer
+// pipe that runs the byte permutes is the resource this saves.
 //
 // Every mbarrier wait is bounded (common.cuh): a wait that runs out writes
 // QLORA_ERR_TIMEOUT to the device status word and every role runs to the
-// end of the kernel without blocking, so the context stays usable.
+// end of the kernel without blocking.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace qlora {
 
-constexpr int GBM = 128, GBN = 256, GBK = 64;
+constexpr int GBM = 128;  // rows per CTA (the pair covers 256)
+constexpr int GBN = 256;  // output columns per pair tile
+constexpr int GBK = 64;
+constexpr int kHalfN = GBN / 2;
 constexpr int kGemmThreads = 320;
-constexpr int kABytes = GBM * GBK * 2;  // 16 KB
-constexpr int kBBytes = GBN * GBK * 2;  // 32 KB
+constexpr int kABytes = GBM * GBK * 2;     // 16 KB
+constexpr int kBBytes = kHalfN * GBK * 2;  // 16 KB (this CTA's half of B)
 
-__host__ __device__ inline int gemm_stage_bytes(int r_pad) { return kABytes + kBBytes + r_pad * 128; }
+__host__ __device__ inline int gemm_stage_bytes(int r_pad) {
+  return kABytes + kBBytes + (r_pad / 2) * 128;
+}
 __host__ __device__ inline int gemm_upa_bytes(int r_pad) { return (r_pad / 16) * GBM * 32; }
-__host__ __device__ inline int gemm_upb_bytes(int r_pad) { return (r_pad / 16) * GBN * 32; }
+__host__ __device__ inline int gemm_upb_bytes(int r_pad) { return (r_pad / 16) * kHalfN * 32; }
 __host__ inline int gemm_smem_bytes(int stages, int r_pad) {
   return 1024 + stages * gemm_stage_bytes(r_pad) + gemm_upa_bytes(r_pad) + gemm_upb_bytes(r_pad) +
          256;
 }
 
-
-// Raw packed bytes + block constant of one (row, 64-block) for one stage.
+// Raw packed bytes + block constant of one half (32 weights) of a 64-block.
+// Loaded values stay raw until use: converting a value right after its load
+// would stall the thread for the whole load latency at prefetch time.
 struct Fetch {
-  uint4 lo, hi;
-  float c;   // code (DQ) or fp32 absmax
-  float s2;  // second-level scale (DQ) or 1
+  uint4 q;   // 16 packed bytes
+  int code;  // int8 block constant (DQ)
+  float c;   // second-level scale s2 (DQ) or fp32 absmax (no DQ)
   bool valid;
 };
 
-__device__ __forceinline__ Fetch fetch_block(const GemmArgs &p, int64_t n, int64_t kcol,
-                                             bool valid) {
+// Loads are unconditional (the caller clamps the address into range).
+__device__ __forceinline__ Fetch fetch_half(const GemmArgs &p, int64_t n, int64_t kcol, int half,
+                                            bool valid) {
   Fetch f;
   f.valid = valid;
-  f.lo = make_uint4(0, 0, 0, 0);
-  f.hi = f.lo;
-  f.c = 0.0f;
-  f.s2 = 1.0f;
-  if (valid) {
-    const uint8_t *src = p.packed + n * (p.wcols >> 1) + (kcol >> 1);
-    f.lo = ldg_nc_v4(src);
-    f.hi = ldg_nc_v4(src + 16);
-    const int64_t blk = n * (p.wcols >> 6) + (kcol >> 6);
-    if (p.group > 0) {
-      f.c = (float)__ldg(p.codes + blk);
-      f.s2 = __ldg(p.scale2 + blk / p.group);
-    } else {
-      f.c = __ldg(p.absf + blk);
-    }
-  }
+  f.q = ldg_nc_v4(p.packed + n * (p.wcols >> 1) + (kcol >> 1) + 16 * half);
+  const int64_t blk = n * (p.wcols >> 6) + (kcol >> 6);
+  f.code = __ldg(p.codes + (p.use_code ? blk : 0));
+  f.c = __ldg(p.cvec + blk / p.cdiv);
   return f;
 }
 
-// Dequantise one fetched block into 64 bf16 values and store them as the
-// 8 16-byte chunks of one 128-byte swizzled row at `row_addr` (chunk c goes
-// to position c ^ swz).
-__device__ __forceinline__ void dequant_store_row(const GemmArgs &p, const Fetch &f,
-                                                  uint32_t row_addr, uint32_t swz) {
+// Dequantise 32 weights into the 4 16-byte chunks [4*half, 4*half+4) of one
+// 128-byte swizzled row at `row_addr` (chunk c goes to position c ^ swz).
+__device__ __forceinline__ void dequant_store_half(const GemmArgs &p, const Fetch &f,
+                                                   uint32_t row_addr, uint32_t swz, int half) {
   if (!f.valid) {
 #pragma unroll
-    for (int c = 0; c < 8; ++c) sts_v4(row_addr + ((c ^ swz) << 4), 0, 0, 0, 0);
+    for (int c = 0; c < 4; ++c) sts_v4(row_addr + (((4 * half + c) ^ swz) << 4), 0, 0, 0, 0);
     return;
   }
-  const float ahat = (p.group > 0) ? __fmul_rn(f.c, f.s2) : f.c;
+  const float ahat = p.use_code ? __fmul_rn((float)f.code, f.c) : f.c;
   const Nf4Table t = make_table(ahat);
-  const uint32_t w[8] = {f.lo.x, f.lo.y, f.lo.z, f.lo.w, f.hi.x, f.hi.y, f.hi.z, f.hi.w};
+  const uint32_t w[4] = {f.q.x, f.q.y, f.q.z, f.q.w};
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
+  for (int c = 0; c < 4; ++c) {
     uint32_t o[4];
     lookup8(t, w[c], o);
-    sts_v4(row_addr + ((c ^ swz) << 4), o[0], o[1], o[2], o[3]);
+    sts_v4(row_addr + (((4 * half + c) ^ swz) << 4), o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -121,32 +124,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const int S = p.stages, RP = p.r_pad;
+  const int S = p.stages, RP = p.r_pad, RH = p.r_pad / 2;
   const int SB = gemm_stage_bytes(RP);
   uint8_t *upa = smem + S * SB;
   uint8_t *upb = upa + gemm_upa_bytes(RP);
   uint64_t *bars = reinterpret_cast<uint64_t *>(upb + gemm_upb_bytes(RP));
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 4);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 3);
   volatile int *cta_err = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const uint32_t smem0 = smem_u32(smem);
   const uint32_t upa_u = smem_u32(upa), upb_u = smem_u32(upb);
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
   auto empty_bar = [&](int s) { return smem_u32(bars + S + s); };
-  const uint32_t upa_bar = smem_u32(bars + 2 * S), upb_bar = smem_u32(bars + 2 * S + 1);
-  const uint32_t acc_bar = smem_u32(bars + 2 * S + 2), acc2_bar = smem_u32(bars + 2 * S + 3);
+  const uint32_t up_bar = smem_u32(bars + 2 * S);
+  const uint32_t acc_bar = smem_u32(bars + 2 * S + 1), acc2_bar = smem_u32(bars + 2 * S + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.y * GBM, c0 = blockIdx.x * GBN;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int m0 = (blockIdx.x >> 1) * (2 * GBM) + (int)rank * GBM;  // this CTA's rows
+  const int c0 = blockIdx.y * GBN;                                 // pair's output columns
+  const int cb0 = c0 + (int)rank * kHalfN;                         // this CTA's B half
   const int num_k = (p.kdim + GBK - 1) / GBK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full_bar(s), 1 + 8);  // TMA expect_tx arrive + 8 producer warps
-      mbar_init(empty_bar(s), 1);     // tcgen05.commit
+      // TMA arrive + 8 producer warps (+ the peer's relay in the leader)
+      mbar_init(full_bar(s), 1 + 8 + (leader ? 1 : 0));
+      mbar_init(empty_bar(s), 1);  // multicast tcgen05.commit
     }
-    mbar_init(upa_bar, 4);
-    mbar_init(upb_bar, 1);
+    mbar_init(up_bar, 4 + 1 + (leader ? 1 : 0));
     mbar_init(acc_bar, 1);
     mbar_init(acc2_bar, 1);
     *cta_err = 0;
@@ -157,9 +164,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tmL1);
     tma_prefetch_desc(&tmL2);
   }
-  if (warp == 9) tmem_alloc(smem_u32(tmem_slot), 512);
+  if (warp == 9) tmem_alloc2(smem_u32(tmem_slot), 512);
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // both CTAs' barriers initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tmem_aux = tmem + 256;
@@ -167,45 +175,62 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp < 8) {
     // ------------------------------------------------ dequantising producers
     const int pid = threadIdx.x;  // 0..255
+    const int half = pid & 1;     // which 32 weights of the 64-block
+    const int rowi = pid >> 1;    // 0..127: row of this CTA's B half
     int64_t n_fixed = 0, kcol_fixed = 0;
     uint32_t row_off, swz;
     int nl = 0;
     if (!kDx) {
-      n_fixed = (int64_t)c0 + pid;  // weight row = output column
-      row_off = (pid >> 3) * 1024 + (pid & 7) * 128;
-      swz = pid & 7;
+      n_fixed = (int64_t)cb0 + rowi;  // weight row = output column
+      row_off = (rowi >> 3) * 1024 + (rowi & 7) * 128;
+      swz = rowi & 7;
     } else {
-      const int bsub = pid >> 6;  // which 64-column atom of the 256 outputs
-      nl = pid & 63;              // contraction row inside the stage
-      kcol_fixed = (int64_t)c0 + 64 * bsub;
+      const int bsub = rowi >> 6;  // which 64-column atom of this CTA's 128 outputs
+      nl = rowi & 63;              // contraction row inside the stage
+      kcol_fixed = (int64_t)cb0 + 64 * bsub;
       row_off = bsub * 8192 + (nl >> 3) * 1024 + (nl & 7) * 128;
       swz = nl & 7;
     }
     auto fetch_k = [&](int kb) -> Fetch {
-      if (kb >= num_k) return fetch_block(p, 0, 0, false);
+      const bool in_k = kb < num_k;
+      const int kbc = in_k ? kb : num_k - 1;
+      int64_t n, kcol;
+      bool valid;
       if (!kDx) {
-        const int64_t kcol = (int64_t)kb * GBK;
-        return fetch_block(p, n_fixed, kcol, n_fixed < p.wrows);
+        n = n_fixed;
+        kcol = (int64_t)kbc * GBK;
+        valid = in_k && n < p.wrows;
       } else {
-        const int64_t n = (int64_t)kb * GBK + nl;
-        return fetch_block(p, n, kcol_fixed, n < p.wrows && kcol_fixed < p.wcols);
+        n = (int64_t)kbc * GBK + nl;
+        kcol = kcol_fixed;
+        valid = in_k && n < p.wrows && kcol < p.wcols;
       }
+      return fetch_half(p, valid ? n : 0, valid ? kcol : 0, half, valid);
     };
-    Fetch f0 = fetch_k(0), f1 = fetch_k(1);
+    // Three-slot ring of prefetched blocks, indexed by compile-time
+    // constants only: iteration kb consumes slot kb % 3 and refills slot
+    // (kb + 2) % 3, so no register ever copies a load still in flight.
+    Fetch f[3];
+    f[0] = fetch_k(0);
+    f[1] = fetch_k(1);
     int stage = 0;
     uint32_t ph = 0;
-    for (int kb = 0; kb < num_k; ++kb) {
-      const Fetch f2 = fetch_k(kb + 2);
-      const bool ok = mbar_wait_bounded(empty_bar(stage), ph ^ 1, cta_err, p.status);
-      if (ok) dequant_store_row(p, f0, smem0 + stage * SB + kABytes + row_off, swz);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(full_bar(stage));
-      f0 = f1;
-      f1 = f2;
-      if (++stage == S) {
-        stage = 0;
-        ph ^= 1;
+    for (int kb0 = 0; kb0 < num_k; kb0 += 3) {
+#pragma unroll
+      for (int u = 0; u < 3; ++u) {
+        const int kb = kb0 + u;
+        if (kb < num_k) {
+          f[(u + 2) % 3] = fetch_k(kb + 2);
+          const bool ok = mbar_wait_bounded(empty_bar(stage), ph ^ 1, cta_err, p.status);
+          if (ok) dequant_store_half(p, f[u], smem0 + stage * SB + kABytes + row_off, swz, half);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full_bar(stage));
+          if (++stage == S) {
+            stage = 0;
+            ph ^= 1;
+          }
+        }
       }
     }
 
@@ -213,10 +238,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     mbar_wait_bounded(acc_bar, 0, cta_err, p.status);
     tc_fence_after();
     if (warp < 4) {
-      // LoRA down-projection (t or u): save fp32, stage s * aux as bf16.
+      // LoRA down-projection (t or u) of this CTA's 128 rows: save fp32,
+      // stage s * aux as bf16 for the up-projection.
       const int rl = warp * 32 + lane;
       const int row = m0 + rl;
-      const bool save = p.aux_out != nullptr && blockIdx.x == 0 && row < p.M;
+      const bool save = p.aux_out != nullptr && blockIdx.y == 0 && row < p.M;
       for (int cb = 0; cb < RP / 16; ++cb) {
         uint32_t v[16];
         tmem_ld16(tmem_aux + ((uint32_t)(warp * 32) << 16) + cb * 16, v);
@@ -238,14 +264,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(upa_bar);
+      if (lane == 0) mbar_arrive(up_bar);
     }
     mbar_wait_bounded(acc2_bar, 0, cta_err, p.status);
     tc_fence_after();
-    const int quarter = warp & 3, half = warp >> 2;
+    const int quarter = warp & 3, hcol = warp >> 2;
     const int row = m0 + quarter * 32 + lane;
     for (int ch = 0; ch < 4; ++ch) {
-      const int col = half * 128 + ch * 32;
+      const int col = hcol * 128 + ch * 32;
       uint32_t v[32];
       tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + col, v);
       tmem_ld_wait();
@@ -280,18 +306,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // --------------------------------------------------------- TMA producer
     if (lane == 0) {
       const int ncb = RP / 16;
-      mbar_arrive_expect_tx(upb_bar, ncb * GBN * 32);
+      mbar_arrive_expect_tx(up_bar, ncb * kHalfN * 32);
       for (int cb = 0; cb < ncb; ++cb)
-        tma_load_2d(upb_u + cb * (GBN * 32), &tmL2, upb_bar, cb * 16, c0);
+        tma_load_2d(upb_u + cb * (kHalfN * 32), &tmL2, up_bar, cb * 16, cb0);
       int stage = 0;
       uint32_t ph = 0;
       int issued = 0;
       for (int kb = 0; kb < num_k; ++kb) {
         if (!mbar_wait_bounded(empty_bar(stage), ph ^ 1, cta_err, p.status)) break;
         const uint32_t a_dst = smem0 + stage * SB;
-        mbar_arrive_expect_tx(full_bar(stage), kABytes + RP * 128);
+        mbar_arrive_expect_tx(full_bar(stage), kABytes + RH * 128);
         tma_load_2d(a_dst, &tmA, full_bar(stage), kb * GBK, m0);
-        tma_load_2d(a_dst + kABytes + kBBytes, &tmL1, full_bar(stage), kb * GBK, 0);
+        tma_load_2d(a_dst + kABytes + kBBytes, &tmL1, full_bar(stage), kb * GBK, (int)rank * RH);
         ++issued;
         if (++stage == S) {
           stage = 0;
@@ -300,23 +326,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       if (*cta_err) {
         // Error path: let every issued copy land before the CTA exits.
-        mbar_drain(upb_bar, 0);
+        mbar_drain(up_bar, 0);
         const int first = issued > S ? issued - S : 0;
         for (int i = first; i < issued; ++i) mbar_drain(full_bar(i % S), (i / S) & 1);
       }
     }
     __syncwarp();
-  } else {
-    // ----------------------------------------------------------- MMA issuer
+  } else if (leader) {
+    // ------------------------------------------------- MMA issuer (leader)
     if (lane == 0) {
-      constexpr uint32_t idesc_main = make_idesc_bf16(GBM, GBN, kDx);
-      const uint32_t idesc_aux = make_idesc_bf16(GBM, RP, false);
-      constexpr uint32_t idesc_up = make_idesc_bf16(GBM, GBN, false);
+      constexpr uint32_t idesc_main = make_idesc_bf16(2 * GBM, GBN, kDx);
+      const uint32_t idesc_aux = make_idesc_bf16(2 * GBM, RP, false);
+      constexpr uint32_t idesc_up = make_idesc_bf16(2 * GBM, GBN, false);
       int stage = 0;
       uint32_t ph = 0;
       bool ok = true;
       for (int kb = 0; kb < num_k && ok; ++kb) {
-        ok = mbar_wait_bounded(full_bar(stage), ph, cta_err, p.status);
+        ok = mbar_wait_bounded_cluster(full_bar(stage), ph, cta_err, p.status);
         if (!ok) break;
         tc_fence_after();
         const uint32_t a_base = smem0 + stage * SB;
@@ -329,36 +355,55 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                   : make_sdesc(b_base + kk * 32, 16, 1024, kSwz128);
           const uint64_t ld = make_sdesc(l_base + kk * 32, 16, 1024, kSwz128);
           const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
-          tc_mma(tmem, ad, bd, idesc_main, accum);
-          tc_mma(tmem_aux, ad, ld, idesc_aux, accum);
+          tc_mma2(tmem, ad, bd, idesc_main, accum);
+          tc_mma2(tmem_aux, ad, ld, idesc_aux, accum);
         }
-        tc_commit(empty_bar(stage));
+        tc_commit2_mc(empty_bar(stage), 0x3);
         if (++stage == S) {
           stage = 0;
           ph ^= 1;
         }
       }
-      tc_commit(acc_bar);
-      if (ok && mbar_wait_bounded(upa_bar, 0, cta_err, p.status) &&
-          mbar_wait_bounded(upb_bar, 0, cta_err, p.status)) {
+      tc_commit2_mc(acc_bar, 0x3);
+      if (ok && mbar_wait_bounded_cluster(up_bar, 0, cta_err, p.status)) {
         tc_fence_after();
         for (int cb = 0; cb < RP / 16; ++cb) {
           const uint64_t ad = make_sdesc(upa_u + cb * (GBM * 32), 16, 256, kSwz32);
-          const uint64_t bd = make_sdesc(upb_u + cb * (GBN * 32), 16, 256, kSwz32);
-          tc_mma(tmem, ad, bd, idesc_up, 1u);
+          const uint64_t bd = make_sdesc(upb_u + cb * (kHalfN * 32), 16, 256, kSwz32);
+          tc_mma2(tmem, ad, bd, idesc_up, 1u);
         }
       }
-      tc_commit(acc2_bar);
+      tc_commit2_mc(acc2_bar, 0x3);
       if (*cta_err) mbar_drain(acc2_bar, 0);  // all issued MMAs retired
+    }
+    __syncwarp();
+  } else {
+    // ----------------------------------------------- relay (peer CTA)
+    // Forwards "this CTA's half of stage s is ready" (its TMA bytes landed
+    // and its 8 producer warps arrived) to the leader's full barrier.
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t ph = 0;
+      for (int kb = 0; kb < num_k; ++kb) {
+        if (!mbar_wait_bounded(full_bar(stage), ph, cta_err, p.status)) break;
+        mbar_arrive_remote(mapa_shared(full_bar(stage), 0));
+        if (++stage == S) {
+          stage = 0;
+          ph ^= 1;
+        }
+      }
+      if (mbar_wait_bounded(up_bar, 0, cta_err, p.status))
+        mbar_arrive_remote(mapa_shared(up_bar, 0));
     }
     __syncwarp();
   }
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // the pair is done with TMEM and with each other's smem
   if (warp == 9) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc2(tmem, 512);
   }
 }
 
@@ -378,16 +423,28 @@ cudaError_t launch_gemm(bool dx, const CUtensorMap &tmA, const CUtensorMap &tmL1
     if (e != cudaSuccess) return e;
     attr_set[dx] = true;
   }
-  dim3 grid((args.out_cols + GBN - 1) / GBN, (args.M + GBM - 1) / GBM);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * ((args.M + 2 * GBM - 1) / (2 * GBM)), (args.out_cols + GBN - 1) / GBN, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = 2;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
   if (dx)
-    qlora_gemm_kernel<true><<<grid, kGemmThreads, smem, s>>>(tmA, tmL1, tmL2, args);
+    e = cudaLaunchKernelEx(&cfg, qlora_gemm_kernel<true>, tmA, tmL1, tmL2, args);
   else
-    qlora_gemm_kernel<false><<<grid, kGemmThreads, smem, s>>>(tmA, tmL1, tmL2, args);
+    e = cudaLaunchKernelEx(&cfg, qlora_gemm_kernel<false>, tmA, tmL1, tmL2, args);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 int gemm_pick_stages(int r_pad) {
-  for (int st = 4; st >= 2; --st)
+  for (int st = 6; st >= 2; --st)
     if (gemm_smem_bytes(st, r_pad) <= 232448) return st;
   return 0;
 }

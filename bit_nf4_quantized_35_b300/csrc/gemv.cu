@@ -28,7 +28,15 @@
 
 namespace qlora {
 
-constexpr int kGemvMaxWarps = 16;
+__constant__ float kNf4Const[16] = {QLORA_NF4_VALUES};
+
+// Warps per CTA: 16 for up to 8 tokens; 12 for 9..16 tokens, whose larger
+// register footprint needs the 168 registers a thread gets with 3 warps per
+// SM sub-partition.
+template <int NT>
+struct GemvWarps {
+  static constexpr int value = NT == 1 ? 16 : 12;
+};
 
 
 __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -69,43 +77,76 @@ __device__ __forceinline__ uint32_t lut(const uint8_t *tab, uint32_t w, uint32_t
   return *reinterpret_cast<const uint32_t *>(tab + off);
 }
 
+// bf16 pair -> f16 pair (both halves), round to nearest.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, float sc = 1.0f) {
+  return pack_f16x2(bf16_lo(w) * sc, bf16_hi(w) * sc);
+}
+
+// Shared-memory layout of the GEMV kernel (bytes).
+struct GemvSmem {
+  int tab, red, tpart, tfull, part, bsm, total;
+};
+__host__ __device__ inline GemvSmem gemv_smem_layout(int warps, int rows_max) {
+  GemvSmem L;
+  L.tab = 0;                                    // 256 x 32 lanes x u32
+  L.red = 32768;                                // 2 x W x 32 rows x 16 tok f32 (also t staging)
+  L.tpart = L.red + 2 * warps * 32 * 16 * 4;    // 64 j x 16 tok f32: this CTA's partial t
+  L.tfull = L.tpart + 64 * 16 * 4;              // 16 tok x 64 j f32: full t (cluster rank 0)
+  L.part = L.tfull + 16 * 64 * 4;               // rows_max x 16 tok f32: this CTA's partial y
+  L.bsm = L.part + rows_max * 16 * 4;           // rows_max x 64 bf16: LoRA B rows (rank 0)
+  L.total = L.bsm + rows_max * 64 * 2;
+  return L;
+}
+
 template <int NT>
-__global__ void __launch_bounds__(kGemvMaxWarps * 32, 1) qlora_gemv_kernel(const GemvArgs p) {
+__global__ void __launch_bounds__(GemvWarps<NT>::value * 32, 1) qlora_gemv_kernel(const GemvArgs p) {
   extern __shared__ __align__(16) uint8_t smem[];
-  uint8_t *tab = smem;                                                   // 32 KB
-  float *red = reinterpret_cast<float *>(smem + 32768);                 // [W][64][16]
   const int W = blockDim.x >> 5;
-  float *part = red + W * 64 * 16;                                       // [64][16]
-  float *t_s = part + 64 * 16;                                           // [16][r]
+  const GemvSmem SL = gemv_smem_layout(W, p.rows_max);
+  const uint8_t *tab = smem + SL.tab;
+  float *red = reinterpret_cast<float *>(smem + SL.red);
+  float *tpart = reinterpret_cast<float *>(smem + SL.tpart);
+  float *tfull = reinterpret_cast<float *>(smem + SL.tfull);
+  float *part = reinterpret_cast<float *>(smem + SL.part);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tq = lane & 3;
   const uint32_t rank = cluster_ctarank();
   const int S = gridDim.y;
+  const int MT = NT * 8;
+  const int RP = (p.r + 15) & ~15;
 
   // Codepoint-pair table: entry b holds f16(c[b >> 4]) (low half, element
   // 2j) and f16(c[b & 15]) (high half, element 2j+1), 32 copies.
   {
-    constexpr float c[16] = {QLORA_NF4_VALUES};
+    uint32_t *t32 = reinterpret_cast<uint32_t *>(smem + SL.tab);
     for (int i = threadIdx.x; i < 256 * 32; i += blockDim.x) {
       const int b = i >> 5;
-      float lo = 0.f, hi = 0.f;
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        if ((b >> 4) == q) lo = c[q];
-        if ((b & 15) == q) hi = c[q];
-      }
-      reinterpret_cast<uint32_t *>(tab)[i] = pack_f16x2(lo, hi);
+      t32[i] = pack_f16x2(kNf4Const[b >> 4], kNf4Const[b & 15]);
     }
-    for (int i = threadIdx.x; i < p.M * p.r; i += blockDim.x) t_s[i] = p.t[i];
   }
 
-  // This warp's 128-wide slice of K and its x fragments (f16, scaled).
+  const int rt_begin = (int)((int64_t)p.row_tiles * blockIdx.x / p.clusters);
+  const int rt_end = (int)((int64_t)p.row_tiles * (blockIdx.x + 1) / p.clusters);
+  const int row_lo = rt_begin * 16;
+  const int row_hi = min(rt_end * 16, p.N);
+  uint16_t *bsm = reinterpret_cast<uint16_t *>(smem + SL.bsm);
+  if (rank == 0) {
+    // LoRA B rows of this cluster's range, [row][j] with row stride 64
+    const int nb = (row_hi - row_lo) * p.r;
+    for (int i = threadIdx.x; i < nb; i += blockDim.x) {
+      const int row = i / p.r, j = i % p.r;
+      bsm[row * 64 + j] = p.B[(int64_t)(row_lo + row) * p.r + j];
+    }
+  }
+
+  // This warp's 128-wide slice of K and its x fragments (f16, scaled by a
+  // per-token power of two so any bf16 magnitude fits f16).
   const int chunk = (int)rank * W + warp;
   const int kc0 = chunk * 128;
   const bool kvalid = kc0 < p.K;
   uint32_t xf[2][4][NT][2];
-  int xe[NT];  // per-token exponent shift of this lane's token (nt*8 + g)
+  int xe[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int tok = nt * 8 + g;
@@ -141,7 +182,7 @@ __global__ void __launch_bounds__(kGemvMaxWarps * 32, 1) qlora_gemv_kernel(const
         xf[blk][j][nt][1] = pack_f16x2(v[blk][4 * j + 2] * sc, v[blk][4 * j + 3] * sc);
       }
   }
-  // Scale factors 2^e of the two tokens (nt*8 + 2tq, +1) whose C columns this lane holds.
+  // 2^e of the two tokens (nt*8 + 2tq, +1) whose accumulator columns this lane holds.
   float csc[NT][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
@@ -150,62 +191,135 @@ __global__ void __launch_bounds__(kGemvMaxWarps * 32, 1) qlora_gemv_kernel(const
     csc[nt][0] = __uint_as_float((uint32_t)(127 + e0) << 23);
     csc[nt][1] = __uint_as_float((uint32_t)(127 + e1) << 23);
   }
-  __syncthreads();
 
-  const uint32_t lane4 = lane * 4;
-  const int64_t kblocks_row = p.K >> 6;
-  const int MT = NT * 8;
-  // Contiguous share of row tiles for this cluster.
-  const int rt_begin = (int)((int64_t)p.row_tiles * blockIdx.x / p.clusters);
-  const int rt_end = (int)((int64_t)p.row_tiles * (blockIdx.x + 1) / p.clusters);
-
-  for (int rt0 = rt_begin; rt0 < rt_end; rt0 += 4) {
-    // ---- loads: 4 row tiles x rows (g, g+8) x 2 blocks, 8 bytes each
-    uint2 pk[4][2][2];
-    float ah[4][2][2];
+  // ---- LoRA down-projection t = x A^T on the tensor cores: rows j of A
+  // play the weight rows, the same x fragments the tokens.
+  for (int jt = 0; jt < RP / 16; ++jt) {
+    float d[NT][4];
 #pragma unroll
-    for (int rt = 0; rt < 4; ++rt)
+    for (int nt = 0; nt < NT; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+      uint32_t a0w[8], a8w[8];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int row = (rt0 + rt) * 16 + g + 8 * h;
-        const bool ok = kvalid && (rt0 + rt) < rt_end && row < p.N;
+        const int j = jt * 16 + g + 8 * h;
+        uint4 u0 = make_uint4(0, 0, 0, 0), u1 = u0;
+        if (j < p.r && kc0 + blk * 64 < p.K) {
+          const uint16_t *src = p.A + (int64_t)j * p.K + kc0 + blk * 64 + tq * 16;
+          u0 = ldg_nc_v4(src);
+          u1 = ldg_nc_v4(src + 8);
+        }
+        uint32_t *dst = h ? a8w : a0w;
+        dst[0] = u0.x, dst[1] = u0.y, dst[2] = u0.z, dst[3] = u0.w;
+        dst[4] = u1.x, dst[5] = u1.y, dst[6] = u1.z, dst[7] = u1.w;
+      }
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        // elements 4jj..4jj+3 of the lane's 16: words 2jj (k, k+1) and 2jj+1 (k+2, k+3)
+        const uint32_t a[4] = {bf16x2_to_f16x2(a0w[2 * jj]), bf16x2_to_f16x2(a8w[2 * jj]),
+                               bf16x2_to_f16x2(a0w[2 * jj + 1]), bf16x2_to_f16x2(a8w[2 * jj + 1])};
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_f16_16816(d[nt], a, xf[blk][jj][nt][0], xf[blk][jj][nt][1]);
+      }
+    }
+    // stage this warp's partial t in `red` as [warp][j][tok]
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int tok = nt * 8 + 2 * tq;
+      float *r0 = red + ((warp * 64) + jt * 16 + g) * 16 + tok;
+      float *r8 = r0 + 8 * 16;
+      r0[0] = d[nt][0] * csc[nt][0];
+      r0[1] = d[nt][1] * csc[nt][1];
+      r8[0] = d[nt][2] * csc[nt][0];
+      r8[1] = d[nt][3] * csc[nt][1];
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < RP * 16; i += blockDim.x) {
+    const int j = i >> 4, tok = i & 15;
+    float v = 0.f;
+    for (int w = 0; w < W; ++w) v += red[(w * 64 + j) * 16 + tok];
+    tpart[i] = v;
+  }
+  cluster_sync_all();
+  // Rank 0 of every cluster assembles the full t (fixed rank order); the
+  // first cluster also saves it for the backward pass.
+  if (rank == 0) {
+    for (int i = threadIdx.x; i < 16 * RP; i += blockDim.x) {
+      const int tok = i / RP, j = i % RP;
+      float v = 0.f;
+      for (int q = 0; q < S; ++q) v += ld_dsmem_f32(tpart + j * 16 + tok, (uint32_t)q);
+      tfull[tok * 64 + j] = v;
+      if (p.t_save && blockIdx.x == 0 && tok < p.M && j < p.r) p.t_save[tok * p.r + j] = v;
+    }
+  }
+  __syncthreads();
+  // Rank 0 seeds its partial y with the LoRA term s . t . B^T (fp32).
+  if (rank == 0) {
+    const int nrows = row_hi - row_lo;
+    for (int i = threadIdx.x; i < nrows * MT; i += blockDim.x) {
+      const int row = i / MT, tok = i % MT;
+      float l = 0.f;
+      for (int j = 0; j < p.r; ++j)
+        l = fmaf(tfull[tok * 64 + j], __uint_as_float((uint32_t)bsm[row * 64 + j] << 16), l);
+      part[row * 16 + tok] = p.s * l;
+    }
+  }
+
+  // ---- main loop over pairs of 16-row tiles of this cluster's row range
+  const uint32_t lane4 = lane * 4;
+  const int64_t kblocks_row = p.K >> 6;
+  const int n_it = (rt_end - rt_begin + 1) / 2;
+
+  struct Piece {
+    uint2 pk[2][2][2];  // [rt][row g / g+8][blk]
+    int code[2][2][2];  // raw until use (see the GEMM producer)
+    float cv[2][2][2];  // s2 (DQ) or fp32 absmax
+    uint32_t valid;     // bit (rt*4 + h*2 + blk): block holds real weights
+  };
+  auto load_piece = [&](int it, Piece &P) {
+    P.valid = 0;
+#pragma unroll
+    for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int rtile = rt_begin + 2 * it + rt;
+        const int row = rtile * 16 + g + 8 * h;
+        const bool ok = it < n_it && rtile < rt_end && row < p.N && kvalid;
+        // unconditional loads from a clamped address; validity applied at use
+        const int rowc = ok ? row : 0;
 #pragma unroll
         for (int blk = 0; blk < 2; ++blk) {
-          pk[rt][h][blk] = make_uint2(0, 0);
-          ah[rt][h][blk] = 0.f;
-          if (ok && kc0 + blk * 64 < p.K) {
-            const int64_t kb = (kc0 >> 6) + blk;
-            pk[rt][h][blk] =
-                ldg_nc_v2(p.packed + (int64_t)row * (p.K >> 1) + (kb << 5) + tq * 8);
-            const int64_t b = (int64_t)row * kblocks_row + kb;
-            ah[rt][h][blk] = p.group > 0 ? __fmul_rn((float)__ldg(p.codes + b),
-                                                     __ldg(p.scale2 + b / p.group))
-                                         : __ldg(p.absf + b);
-          }
+          const bool okb = ok && kc0 + blk * 64 < p.K;
+          const int64_t kb = okb ? (kc0 >> 6) + blk : 0;
+          P.pk[rt][h][blk] = ldg_nc_v2(p.packed + (int64_t)rowc * (p.K >> 1) + (kb << 5) + tq * 8);
+          const int64_t b = (int64_t)rowc * kblocks_row + kb;
+          P.code[rt][h][blk] = __ldg(p.codes + (p.use_code ? b : 0));
+          P.valid |= okb ? (1u << (rt * 4 + h * 2 + blk)) : 0u;
+          P.cv[rt][h][blk] = __ldg(p.cvec + b / p.cdiv);
         }
       }
-    // ---- tensor-core partial sums
-    float acc[4][NT][4];
+  };
+  auto compute_piece = [&](int it, const Piece &P) {
+    float acc[2][NT][4];
 #pragma unroll
-    for (int rt = 0; rt < 4; ++rt)
+    for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[rt][nt][i] = 0.f;
 #pragma unroll
-    for (int rt = 0; rt < 4; ++rt)
+    for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
       for (int blk = 0; blk < 2; ++blk) {
         float tmp[NT][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) tmp[nt][i] = 0.f;
-        const uint32_t w0[2] = {pk[rt][0][blk].x, pk[rt][0][blk].y};
-        const uint32_t w8[2] = {pk[rt][1][blk].x, pk[rt][1][blk].y};
+        for (int nt = 0; nt < NT; ++nt) tmp[nt][0] = tmp[nt][1] = tmp[nt][2] = tmp[nt][3] = 0.f;
+        const uint32_t w0[2] = {P.pk[rt][0][blk].x, P.pk[rt][0][blk].y};
+        const uint32_t w8[2] = {P.pk[rt][1][blk].x, P.pk[rt][1][blk].y};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          // bytes 2j and 2j+1 of the lane's 8-byte piece
           const int wi = j >> 1;
           uint32_t a[4];
           if ((j & 1) == 0) {
@@ -222,21 +336,27 @@ __global__ void __launch_bounds__(kGemvMaxWarps * 32, 1) qlora_gemv_kernel(const
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma_f16_16816(tmp[nt], a, xf[blk][j][nt][0], xf[blk][j][nt][1]);
         }
+        const float ah0 = ((P.valid >> (rt * 4 + blk)) & 1u ? 1.0f : 0.0f) * (p.use_code ? __fmul_rn((float)P.code[rt][0][blk],
+                                                                      P.cv[rt][0][blk])
+                                                            : P.cv[rt][0][blk]);
+        const float ah8 = ((P.valid >> (rt * 4 + 2 + blk)) & 1u ? 1.0f : 0.0f) * (p.use_code ? __fmul_rn((float)P.code[rt][1][blk],
+                                                                      P.cv[rt][1][blk])
+                                                            : P.cv[rt][1][blk]);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          acc[rt][nt][0] = fmaf(ah[rt][0][blk], tmp[nt][0], acc[rt][nt][0]);
-          acc[rt][nt][1] = fmaf(ah[rt][0][blk], tmp[nt][1], acc[rt][nt][1]);
-          acc[rt][nt][2] = fmaf(ah[rt][1][blk], tmp[nt][2], acc[rt][nt][2]);
-          acc[rt][nt][3] = fmaf(ah[rt][1][blk], tmp[nt][3], acc[rt][nt][3]);
+          acc[rt][nt][0] = fmaf(ah0, tmp[nt][0], acc[rt][nt][0]);
+          acc[rt][nt][1] = fmaf(ah0, tmp[nt][1], acc[rt][nt][1]);
+          acc[rt][nt][2] = fmaf(ah8, tmp[nt][2], acc[rt][nt][2]);
+          acc[rt][nt][3] = fmaf(ah8, tmp[nt][3], acc[rt][nt][3]);
         }
       }
-    // ---- warp partials -> shared memory
+    float *rb = red + (it & 1) * (W * 32 * 16);
 #pragma unroll
-    for (int rt = 0; rt < 4; ++rt)
+    for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int tok = nt * 8 + 2 * tq;
-        float *r0 = red + ((warp * 64) + rt * 16 + g) * 16 + tok;
+        float *r0 = rb + ((warp * 32) + rt * 16 + g) * 16 + tok;
         float *r8 = r0 + 8 * 16;
         *reinterpret_cast<float2 *>(r0) =
             make_float2(acc[rt][nt][0] * csc[nt][0], acc[rt][nt][1] * csc[nt][1]);
@@ -244,36 +364,46 @@ __global__ void __launch_bounds__(kGemvMaxWarps * 32, 1) qlora_gemv_kernel(const
             make_float2(acc[rt][nt][2] * csc[nt][0], acc[rt][nt][3] * csc[nt][1]);
       }
     __syncthreads();
-    for (int i = threadIdx.x; i < 64 * MT; i += blockDim.x) {
+    // warp partials of these 32 rows -> this CTA's partial y (fixed order)
+    const int rows_here = min(32, (rt_end - rt_begin - 2 * it) * 16);
+    for (int i = threadIdx.x; i < rows_here * MT; i += blockDim.x) {
       const int row = i / MT, tok = i % MT;
       float v = 0.f;
-      for (int w = 0; w < W; ++w) v += red[(w * 64 + row) * 16 + tok];
-      part[row * 16 + tok] = v;
+      for (int w = 0; w < W; ++w) v += rb[(w * 32 + row) * 16 + tok];
+      float *dst = part + (2 * it * 16 + row) * 16 + tok;
+      *dst = (rank == 0) ? *dst + v : v;
     }
-    cluster_sync_all();
-    if (rank == 0) {
-      const int row_lo = rt0 * 16;
-      int row_hi = min(rt0 + 4, rt_end) * 16;
-      if (row_hi > p.N) row_hi = p.N;
-      const int nrows = row_hi - row_lo;
-      for (int i = threadIdx.x; i < nrows * p.M; i += blockDim.x) {
-        const int tok = i / nrows, row = i % nrows;
-        float v = 0.f;
-        for (int q = 0; q < S; ++q) v += ld_dsmem_f32(part + row * 16 + tok, (uint32_t)q);
-        const int n = row_lo + row;
-        float l = 0.f;
-        const uint16_t *Bn = p.B + (int64_t)n * p.r;
-        for (int jj = 0; jj < p.r; ++jj)
-          l = fmaf(t_s[tok * p.r + jj], __uint_as_float((uint32_t)Bn[jj] << 16), l);
-        v = v + p.s * l;
-        if (p.y_bf16)
-          reinterpret_cast<__nv_bfloat16 *>(p.y)[(int64_t)tok * p.N + n] = __float2bfloat16_rn(v);
-        else
-          reinterpret_cast<float *>(p.y)[(int64_t)tok * p.N + n] = v;
+  };
+
+  // Two-slot prefetch ring, compile-time slot indices.
+  Piece P[2];
+  load_piece(0, P[0]);
+  for (int it0 = 0; it0 < n_it; it0 += 2) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int it = it0 + u;
+      if (it < n_it) {
+        load_piece(it + 1, P[(u + 1) & 1]);
+        compute_piece(it, P[u]);
       }
     }
-    cluster_sync_all();
   }
+  __syncthreads();
+  cluster_sync_all();
+  if (rank == 0) {
+    const int nrows = row_hi - row_lo;
+    for (int i = threadIdx.x; i < nrows * p.M; i += blockDim.x) {
+      const int tok = i / nrows, row = i % nrows;
+      float v = 0.f;
+      for (int q = 0; q < S; ++q) v += ld_dsmem_f32(part + row * 16 + tok, (uint32_t)q);
+      const int n = row_lo + row;
+      if (p.y_bf16)
+        reinterpret_cast<__nv_bfloat16 *>(p.y)[(int64_t)tok * p.N + n] = __float2bfloat16_rn(v);
+      else
+        reinterpret_cast<float *>(p.y)[(int64_t)tok * p.N + n] = v;
+    }
+  }
+  cluster_sync_all();  // keep every CTA's shared memory alive until rank 0 has read it
 }
 
 // t[m, j] = sum_k x[m, k] A[j, k]  (fp32 accumulation), one warp per (m, j).
@@ -303,9 +433,10 @@ __global__ void __launch_bounds__(256) lora_down_kernel(const uint16_t *__restri
 }
 
 // ------------------------------------------------------------ launchers
-int gemv_plan(int K, int *warps, int *S) {
+int gemv_plan(int K, int M, int *warps, int *S) {
+  const int maxw = M > 8 ? GemvWarps<2>::value : GemvWarps<1>::value;
   const int chunks = (K + 127) / 128;
-  int s = (chunks + kGemvMaxWarps - 1) / kGemvMaxWarps;
+  int s = (chunks + maxw - 1) / maxw;
   if (s > 8) return -1;
   if (s < 1) s = 1;
   const int w = (chunks + s - 1) / s;
@@ -314,20 +445,18 @@ int gemv_plan(int K, int *warps, int *S) {
   return 0;
 }
 
-size_t gemv_smem_bytes(int warps, int r) {
-  return 32768 + (size_t)warps * 64 * 16 * 4 + 64 * 16 * 4 + (size_t)16 * r * 4;
-}
-
 cudaError_t launch_gemv(GemvArgs a, int num_sms, cudaStream_t s) {
   int warps, S;
-  if (gemv_plan(a.K, &warps, &S) != 0) return cudaErrorInvalidValue;
+  if (a.M < 1 || a.M > 16 || gemv_plan(a.K, a.M, &warps, &S) != 0) return cudaErrorInvalidValue;
   a.row_tiles = (a.N + 15) / 16;
   int clusters = num_sms / S;
-  const int need = (a.row_tiles + 3) / 4;
+  const int need = (a.row_tiles + 1) / 2;
   if (clusters > need) clusters = need;
   if (clusters < 1) clusters = 1;
   a.clusters = clusters;
-  const size_t smem = gemv_smem_bytes(warps, a.r);
+  a.rows_max = ((a.row_tiles + clusters - 1) / clusters + 1) * 16;
+  const size_t smem = gemv_smem_layout(warps, a.rows_max).total;
+  if (smem > 232448) return cudaErrorInvalidValue;
   static bool attr[2] = {false, false};
   const int nt = a.M > 8 ? 2 : 1;
   cudaError_t e;

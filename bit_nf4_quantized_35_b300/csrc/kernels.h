@@ -28,6 +28,11 @@ struct GemmArgs {
   float *aux_out;  // t or u, fp32 [M, r]; written by the CTAs of output column tile 0
   int stages;
   int *status;
+  // Branch-free block constant: a_hat = use_code ? code[b] * cvec[b / cdiv] : cvec[b / cdiv]
+  // (set by the launcher; `codes` points at readable memory even without DQ).
+  const float *cvec;
+  int cdiv;
+  int use_code;
 };
 cudaError_t launch_gemm(bool dx, const CUtensorMap &tmA, const CUtensorMap &tmL1,
                         const CUtensorMap &tmL2, const GemmArgs &args, cudaStream_t s);
@@ -43,16 +48,21 @@ struct GemvArgs {
   int N, K;
   const uint16_t *x;
   int M;
-  const float *t;     // [M, r] fp32
+  const uint16_t *A;  // [r, K] bf16
   const uint16_t *B;  // [N, r] bf16
+  float *t_save;      // [M, r] fp32 or null
   int r;
   float s;
   void *y;
   int y_bf16;
+  const float *cvec;  // as in GemmArgs
+  int cdiv;
+  int use_code;
   int row_tiles;  // ceil(N / 16), set by the launcher
   int clusters;   // gridDim.x, set by the launcher
+  int rows_max;   // rows of the largest per-cluster row range, set by the launcher
 };
-int gemv_plan(int K, int *warps, int *S);
+int gemv_plan(int K, int M, int *warps, int *S);
 cudaError_t launch_gemv(GemvArgs a, int num_sms, cudaStream_t s);
 cudaError_t launch_lora_down(const uint16_t *x, const uint16_t *A, int64_t M, int K, int r,
                              float *t, cudaStream_t s);
