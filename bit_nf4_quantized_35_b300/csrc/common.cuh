@@ -9,7 +9,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/qlora.h"
+#include "qlora.h"
 
 namespace qlora {
 
@@ -128,6 +128,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -135,26 +147,52 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Bounded wait: gives up after ~`limit_cycles` SM cycles, records `code` in
-// the device status word and in the CTA's shared error flag, and returns
-// false.  Once the CTA flag is set every later wait returns false at once,
-// so all roles run to the end of the kernel without blocking.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  volatile int *cta_err, int *status) {
-  if (*cta_err) return false;
+// Shared-memory error flag of a CTA, accessed with explicit shared-space
+// instructions (a generic access would queue behind in-flight global loads).
+__device__ __forceinline__ uint32_t ld_shared_volatile(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_shared_volatile(uint32_t addr, uint32_t v) {
+  asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Bounded wait: tries the barrier first (the common, fast case touches
+// nothing else); otherwise spins for at most ~2 s of SM cycles, then
+// records QLORA_ERR_TIMEOUT in the device status word and in the CTA's
+// shared error flag (at shared address `err`) and returns false.  Once the
+// flag is set every later wait that would block returns false at once, so
+// all roles run to the end of the kernel.
+template <bool kCluster>
+__device__ __forceinline__ bool mbar_wait_bounded_t(uint32_t bar, uint32_t parity, uint32_t err,
+                                                    int *status) {
+  auto try_once = [&]() {
+    return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  };
+  if (try_once()) return true;
+  if (ld_shared_volatile(err)) return false;
   const long long t0 = clock64();
   uint32_t n = 0;
-  while (!mbar_try_wait(bar, parity)) {
+  while (!try_once()) {
     if ((++n & 255u) == 0) {
-      if (*cta_err) return false;
+      if (ld_shared_volatile(err)) return false;
       if (clock64() - t0 > (1ll << 32)) {  // ~2 s at 2 GHz
-        *cta_err = 1;
+        st_shared_volatile(err, 1u);
         if (status) atomicExch(status, kStatusTimeout);
         return false;
       }
     }
   }
   return true;
+}
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t err,
+                                                  int *status) {
+  return mbar_wait_bounded_t<false>(bar, parity, err, status);
+}
+__device__ __forceinline__ bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t parity,
+                                                          uint32_t err, int *status) {
+  return mbar_wait_bounded_t<true>(bar, parity, err, status);
 }
 
 // ------------------------------------------------------------------------ TMA
@@ -256,37 +294,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t local, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// As mbar_wait_bounded, with cluster-scope acquire (the barrier also counts
-// arrivals released by the peer CTA of a pair).
-__device__ __forceinline__ bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t parity,
-                                                          volatile int *cta_err, int *status) {
-  if (*cta_err) return false;
-  const long long t0 = clock64();
-  uint32_t n = 0;
-  while (!mbar_try_wait_cluster(bar, parity)) {
-    if ((++n & 255u) == 0) {
-      if (*cta_err) return false;
-      if (clock64() - t0 > (1ll << 32)) {
-        *cta_err = 1;
-        if (status) atomicExch(status, kStatusTimeout);
-        return false;
-      }
-    }
-  }
-  return true;
 }
 
 __device__ __forceinline__ void tc_commit(uint32_t bar) {

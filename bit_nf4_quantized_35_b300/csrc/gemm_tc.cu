@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t *upb = upa + gemm_upa_bytes(RP);
   uint64_t *bars = reinterpret_cast<uint64_t *>(upb + gemm_upb_bytes(RP));
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 3);
-  volatile int *cta_err = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  const uint32_t cta_err = smem_u32(tmem_slot + 1);  // shared address of the error flag
 
   const uint32_t smem0 = smem_u32(smem);
   const uint32_t upa_u = smem_u32(upa), upb_u = smem_u32(upb);
@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     mbar_init(up_bar, 4 + 1 + (leader ? 1 : 0));
     mbar_init(acc_bar, 1);
     mbar_init(acc2_bar, 1);
-    *cta_err = 0;
+    st_shared_volatile(cta_err, 0u);
     fence_barrier_init();
   }
   if (warp == 8 && lane == 0) {
@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   cluster_sync();  // both CTAs' barriers initialised before any remote arrive
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem = ld_shared_volatile(smem_u32(tmem_slot));
   const uint32_t tmem_aux = tmem + 256;
 
   if (warp < 8) {
@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           ph ^= 1;
         }
       }
-      if (*cta_err) {
+      if (ld_shared_volatile(cta_err)) {
         // Error path: let every issued copy land before the CTA exits.
         mbar_drain(up_bar, 0);
         const int first = issued > S ? issued - S : 0;
@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
       tc_commit2_mc(acc2_bar, 0x3);
-      if (*cta_err) mbar_drain(acc2_bar, 0);  // all issued MMAs retired
+      if (ld_shared_volatile(cta_err)) mbar_drain(acc2_bar, 0);  // all issued MMAs retired
     }
     __syncwarp();
   } else {
