@@ -313,8 +313,13 @@ def run_ours(args, ws_n, rank, device):
     ms_total = max_over_ranks(ms_total, ws_n, device)
     ms_step = ms_total / args.steps
     value = sum_over_ranks(step_flops * args.steps, ws_n, device) / (ms_total * 1e-3) / 1e12
-    fwd_ms = sum(e0.elapsed_time(e1) for row in ev_pairs for e0, e1 in row) / args.steps
-    gemm_achieved = fwd_gemm_flops / (fwd_ms * 1e-3) / 1e12  # TFLOP/s, forward GEMM launches
+    # Per-layer forward GEMM launch times (each forward call is one GEMM launch).
+    layer_ms = [sum(ev_pairs[s][li][0].elapsed_time(ev_pairs[s][li][1]) for s in range(args.steps))
+                / args.steps for li in range(len(layers))]
+    fwd_ms = sum(layer_ms)
+    gi = [L["name"] for L in layers].index("gate_proj")
+    gate_flops = fwd_flops(M, layers[gi]["N"], layers[gi]["K"], RANK_R)
+    gemm_achieved = gate_flops / (layer_ms[gi] * 1e-3) / 1e12  # TFLOP/s, gate_proj forward
     clocks = sampler.summary()
 
     # --- e2e: host buffers through the C ABI, copies inside the timed region
@@ -354,7 +359,7 @@ def run_ours(args, ws_n, rank, device):
 
     peaks, peak_kind = measured_peaks()
     peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    traffic = profile_traffic("qlora_gemm_kernel<false>",
+    traffic = profile_traffic("qlora_gemm_kernel<false>:gate_proj_14336x4096_M2048",
                               os.path.join(ROOT, "bit_nf4_quantized_35_b300", "csrc",
                                             "gemm_tc.cu"))
     out = {
@@ -381,8 +386,10 @@ def run_ours(args, ws_n, rank, device):
             "wall_s_timed": round(t_wall, 3),
         },
         "roofline": {
-            "kernel": "qlora_gemm_kernel<false> (fused NF4 dequant + tcgen05 GEMM + LoRA), "
-                      "forward launches of the timed steps",
+            "kernel": "qlora_gemm_kernel<false> (fused NF4 dequant + tcgen05 GEMM + LoRA) on "
+                      "gate_proj 14336x4096 at M=2048: its forward launches in the timed steps",
+            "flops_per_launch": gate_flops,
+            "avg_launch_ms": round(layer_ms[gi], 4),
             "bound": "tensor",
             "achieved": round(gemm_achieved, 2),
             "peak": peak,
@@ -394,6 +401,10 @@ def run_ours(args, ws_n, rank, device):
         "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": KERNELS_PER_LAYER_STEP * len(layers) * args.steps,
+        "fwd_gemm_per_layer": {L["name"]: {"ms": round(ms, 4), "tflops": round(
+            fwd_flops(M, L["N"], L["K"], RANK_R) / (ms * 1e-3) / 1e12, 1)}
+            for L, ms in zip(layers, layer_ms)},
+        "fwd_gemm_all_layers_tflops": round(fwd_gemm_flops / (fwd_ms * 1e-3) / 1e12, 1),
         "clocks": clocks,
         "rows": rows,
     }
