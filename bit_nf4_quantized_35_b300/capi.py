@@ -31,6 +31,7 @@ EXPORTED = (
     "qlora_nf4_sizes", "qlora_quantize_nf4", "qlora_dequant", "qlora_workspace_size",
     "qlora_workspace_init", "qlora_device_status", "qlora_linear_fwd", "qlora_linear_bwd",
     "qlora_nf4_thresholds", "qlora_nf4_codebook", "qlora_status_string",
+    "qlora_linear_bwd_noalloc",
 )
 
 
@@ -71,6 +72,7 @@ def load(path: str = LIB_PATH):
         "qlora_device_status": [P, P, P],
         "qlora_linear_fwd": [P, P, i64, P, P, i32, f32, P, st, P, P, sz, u32, P],
         "qlora_linear_bwd": [P, P, P, i64, P, P, i32, f32, P, P, st, P, P, P, sz, u32, P],
+        "qlora_linear_bwd_noalloc": [P, P, P, i64, P, P, i32, f32, P, P, st, P, P, u32, P],
         "qlora_nf4_thresholds": [P],
         "qlora_nf4_codebook": [P],
     }
@@ -210,6 +212,30 @@ def linear_fwd(w: NF4Weight, x: torch.Tensor, A: torch.Tensor, B: torch.Tensor, 
         ctypes.byref(s), _ptr(x), M, _ptr(A), _ptr(B), r, float(alpha), _ptr(y), ydt,
         _ptr(t_save), _ptr(ws.buf), ws.nbytes, flags, _stream(stream)))
     return y
+
+
+def linear_bwd_noalloc(w: NF4Weight, x: torch.Tensor, dY: torch.Tensor, A: torch.Tensor,
+                       B: torch.Tensor, alpha: float, t_saved: torch.Tensor | None = None,
+                       dX: torch.Tensor | None = None, dx_dtype=torch.float32,
+                       dA: torch.Tensor | None = None, dB: torch.Tensor | None = None,
+                       flags: int = 0, stream=None):
+    """qlora_linear_bwd_noalloc -> (dX, dA, dB): the backward without a
+    caller workspace (the library's fixed device scratch array is used)."""
+    M = x.shape[0]
+    r = A.shape[0]
+    dev = x.device
+    if dX is None:
+        dX = torch.empty((M, w.cols), dtype=dx_dtype, device=dev)
+    if dA is None:
+        dA = torch.empty((r, w.cols), dtype=torch.float32, device=dev)
+    if dB is None:
+        dB = torch.empty((w.rows, r), dtype=torch.float32, device=dev)
+    dxt = {torch.float32: QLORA_F32, torch.bfloat16: QLORA_BF16}[dX.dtype]
+    s = w.struct()
+    _check("qlora_linear_bwd_noalloc", load().qlora_linear_bwd_noalloc(
+        ctypes.byref(s), _ptr(x), _ptr(dY), M, _ptr(A), _ptr(B), r, float(alpha),
+        _ptr(t_saved), _ptr(dX), dxt, _ptr(dA), _ptr(dB), flags, _stream(stream)))
+    return dX, dA, dB
 
 
 def linear_bwd(w: NF4Weight, x: torch.Tensor, dY: torch.Tensor, A: torch.Tensor,

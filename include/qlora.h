@@ -187,6 +187,33 @@ qlora_status qlora_linear_bwd(const qlora_nf4_weight *w, const uint16_t *x, cons
                               float *dA, float *dB, void *ws, size_t ws_bytes, uint32_t flags,
                               void *stream);
 
+/* Backward without a caller workspace, for callers that cannot allocate
+ * device memory (code that runs during CUDA graph capture, hosts whose
+ * allocator forbids allocation on a hot path, or that give the library only
+ * its inputs and outputs).  The pages have no counterpart: this is a
+ * deployment convenience of this library.
+ * Same arguments, results and errors as qlora_linear_bwd, minus ws and
+ * ws_bytes.  Its workspace is a fixed array of QLORA_NOALLOC_SCRATCH_BYTES
+ * in the library's device memory, held by every GPU that loads the library
+ * until the process exits; the call allocates and frees nothing.
+ *   - Sizes whose qlora_workspace_size exceeds QLORA_NOALLOC_SCRATCH_BYTES
+ *     return QLORA_ERR_WORKSPACE (16 MiB covers the Llama-3-8B projection
+ *     shapes at r = 16 up to 8192 tokens).
+ *   - The first call on a device looks up the array's device address (a
+ *     CUDA runtime query, no allocation) and caches it; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array and nothing in it needs to
+ *     start at zero.  Calls that overlap on the GPU (different streams, no
+ *     ordering between them) race on it and give undefined results.
+ *   - A device-side timeout is not reported by this entry point (it has no
+ *     workspace the caller could read). */
+#define QLORA_NOALLOC_SCRATCH_BYTES (16u << 20)
+qlora_status qlora_linear_bwd_noalloc(const qlora_nf4_weight *w, const uint16_t *x,
+                                      const uint16_t *dY, int64_t M, const uint16_t *A,
+                                      const uint16_t *B, int32_t r, float alpha,
+                                      const float *t_saved, void *dX, qlora_dtype dx_dtype,
+                                      float *dA, float *dB, uint32_t flags, void *stream);
+
 /* The 15 fp32 decision thresholds the quantiser uses: element index =
  * number of thresholds <= (w / absmax).  Derived on the host from the NF4
  * table and the nearest-codepoint rule above.  Host only, no GPU needed. */
