@@ -93,7 +93,7 @@ qlora_status check_weight(const qlora_nf4_weight *w, bool need_buffers) {
 
 // Workspace layout for (M, N, K, r).
 struct WsLayout {
-  size_t status, t, u, bt, at, part, total;
+  size_t status, t, u, lb, bt, at, part, total;
 };
 WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int r) {
   const int RP = round_up(r, 16);
@@ -105,6 +105,8 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int r) {
   off += round_up_sz((size_t)M * RP * 4, 256);
   L.u = off;
   off += round_up_sz((size_t)M * RP * 4, 256);
+  L.lb = off;  // bf16(s.t) or bf16(s.u), [M, RP]: operand of the GEMM's rank-r MMAs
+  off += round_up_sz((size_t)M * RP * 2, 256);
   L.bt = off;
   off += round_up_sz((size_t)RP * N * 2, 256);
   L.at = off;
@@ -150,6 +152,8 @@ void set_block_constants(GemmArgs &g, const qlora_nf4_weight *w) {
   g.use_code = w->group > 0;
   g.cvec = w->group > 0 ? w->scale2 : w->absmax_f32;
   g.cdiv = w->group > 0 ? w->group : 1;
+  g.cshift = 0;
+  while ((1 << g.cshift) < g.cdiv) ++g.cshift;
   if (!g.use_code) g.codes = reinterpret_cast<const int8_t *>(w->packed);
 }
 
@@ -304,6 +308,8 @@ qlora_status qlora_linear_fwd(const qlora_nf4_weight *w, const uint16_t *x, int6
     a.use_code = w->group > 0;
     a.cvec = w->group > 0 ? w->scale2 : w->absmax_f32;
     a.cdiv = w->group > 0 ? w->group : 1;
+    a.cshift = 0;
+    while ((1 << a.cshift) < a.cdiv) ++a.cshift;
     if (!a.use_code) a.codes = reinterpret_cast<const int8_t *>(w->packed);
     a.r = r;
     a.s = sc;
@@ -312,9 +318,12 @@ qlora_status qlora_linear_fwd(const qlora_nf4_weight *w, const uint16_t *x, int6
     return cuda_status(launch_gemv(a, num_sms_current(), s));
   }
   const int RP = round_up(r, 16);
+  uint16_t *lb = reinterpret_cast<uint16_t *>(wsb + L.lb);
+  cudaError_t e = launch_lora_down(x, M, K, A, r, sc, t_save, lb, RP, num_sms_current(), s);
+  if (e != cudaSuccess) return QLORA_ERR_CUDA;
   CUtensorMap tmA, tmL1, tmL2;
   if (!make_tmap(&tmA, x, K, M, (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap(&tmL1, A, K, r, (uint64_t)K * 2, 64, RP / 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap(&tmL1, lb, RP, M, (uint64_t)RP * 2, 16, 128, CU_TENSOR_MAP_SWIZZLE_32B) ||
       !make_tmap(&tmL2, B, r, N, (uint64_t)r * 2, 16, 128, CU_TENSOR_MAP_SWIZZLE_32B))
     return QLORA_ERR_CUDA;
   GemmArgs g{};
@@ -333,7 +342,6 @@ qlora_status qlora_linear_fwd(const qlora_nf4_weight *w, const uint16_t *x, int6
   g.s = sc;
   g.out = y;
   g.out_bf16 = y_dtype == QLORA_BF16;
-  g.aux_out = t_save;
   g.stages = gemm_pick_stages(RP);
   g.status = reinterpret_cast<int *>(wsb + L.status);
   set_block_constants(g, w);
@@ -364,19 +372,23 @@ qlora_status qlora_linear_bwd(const qlora_nf4_weight *w, const uint16_t *x, cons
   uint16_t *Bt = reinterpret_cast<uint16_t *>(wsb + L.bt);
   uint16_t *At = reinterpret_cast<uint16_t *>(wsb + L.at);
   float *part = reinterpret_cast<float *>(wsb + L.part);
+  uint16_t *lb = reinterpret_cast<uint16_t *>(wsb + L.lb);
   const float *t = t_saved;
   cudaError_t e;
   if (!t) {
     float *tw = reinterpret_cast<float *>(wsb + L.t);
-    e = launch_lora_down(x, A, M, K, r, tw, s);
+    e = launch_lora_down(x, M, K, A, r, sc, tw, nullptr, RP, nsm, s);
     if (e != cudaSuccess) return QLORA_ERR_CUDA;
     t = tw;
   }
   e = launch_transposes(A, B, N, K, r, RP, At, Bt, nsm, s);
   if (e != cudaSuccess) return QLORA_ERR_CUDA;
+  // u = dY . B (fp32, for dA) and bf16(s . u) (operand of the dX GEMM's rank-r MMAs)
+  e = launch_lora_down(dY, M, N, Bt, r, sc, u, lb, RP, nsm, s);
+  if (e != cudaSuccess) return QLORA_ERR_CUDA;
   CUtensorMap tmA, tmL1, tmL2;
   if (!make_tmap(&tmA, dY, N, M, (uint64_t)N * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap(&tmL1, Bt, N, RP, (uint64_t)N * 2, 64, RP / 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap(&tmL1, lb, RP, M, (uint64_t)RP * 2, 16, 128, CU_TENSOR_MAP_SWIZZLE_32B) ||
       !make_tmap(&tmL2, At, RP, K, (uint64_t)RP * 2, 16, 128, CU_TENSOR_MAP_SWIZZLE_32B))
     return QLORA_ERR_CUDA;
   GemmArgs g{};
@@ -395,7 +407,6 @@ qlora_status qlora_linear_bwd(const qlora_nf4_weight *w, const uint16_t *x, cons
   g.s = sc;
   g.out = dX;
   g.out_bf16 = dx_dtype == QLORA_BF16;
-  g.aux_out = u;
   g.stages = gemm_pick_stages(RP);
   g.status = reinterpret_cast<int *>(wsb + L.status);
   set_block_constants(g, w);

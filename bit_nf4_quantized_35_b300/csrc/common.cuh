@@ -291,9 +291,10 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t local, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
   return r;
 }
+// Arrive on a barrier of another CTA of the cluster (default semantics; a
+// cluster-scope release here costs a fence per arrive).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
@@ -358,6 +359,18 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
 __device__ __forceinline__ uint2 ldg_nc_v2(const void *p) {
   uint2 v;
   asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+// Scalar read-only loads kept in program order (asm volatile): a prefetch
+// issued early must not be sunk by the compiler to the point of use.
+__device__ __forceinline__ int ldg_nc_s8(const int8_t *p) {
+  int v;
+  asm volatile("ld.global.nc.s8 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float ldg_nc_f32(const float *p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
   return v;
 }
 __device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,

@@ -3,12 +3,10 @@
 // One kernel serves both dense contractions of the QLoRA linear layer
 // ("QLoRA and 4bit Quantization | QLoRA 与 4-bit 量化", Step 3 formula and the
 // gradient routing of Step 4's frozen-base test):
-//   forward  (kDx = false): out[M, N] = x[M, K] . W_hat[N, K]^T
-//                           aux[M, r] = x . A^T                 (t, saved)
-//                           out     += (s . aux) . B^T          (LoRA, s = alpha/r)
-//   backward (kDx = true) : out[M, K] = dY[M, N] . W_hat[N, K]
-//                           aux[M, r] = dY . B                  (u, saved)
-//                           out     += (s . aux) . A
+//   forward  (kDx = false): out[M, N] = (s.t)[M, r] . B[N, r]^T + x[M, K] . W_hat[N, K]^T
+//   backward (kDx = true) : out[M, K] = (s.u)[M, r] . A^T[K, r]^T + dY[M, N] . W_hat[N, K]
+// where t = x A^T (u = dY B) comes in as bf16(s.t) from a small tensor-core
+// pre-pass (lora_grad.cu) and seeds the accumulator before the main loop.
 //
 // CTA pairs (a cluster of 2) share one 256 x 256 output tile through
 // tcgen05 cta_group::2: CTA r owns rows [128r, 128r+128) of the tile and
@@ -21,19 +19,14 @@
 //              values go straight into the 128-byte-swizzled operand layout
 //              the tensor core reads (K-major forward, MN-major dX).  After
 //              the main loop the same warps run the epilogue.
-//   warp 8     TMA: activation rows of this CTA and its half of the LoRA
-//              down-projection operand per stage; its half of the
-//              up-projection operand once.
+//   warp 8     TMA: this CTA's 128 activation rows per stage; its halves of
+//              the two rank-r LoRA operands once.
 //   warp 9     TMEM allocation (both CTAs); in the leader the single MMA
 //              issuer, in the peer a relay that forwards "stage ready" to the
 //              leader's barrier.
-// Per stage the leader issues 4 x (256x256x16) for the base product and
-// 4 x (256 x r_pad x 16) for the LoRA down-projection, both reading the same
-// activation tiles; accumulators live in TMEM columns [0,256) and
-// [256, 256 + r_pad) of both CTAs.  After the contraction each CTA's
-// epilogue scales its down-projection rows by s, rounds them to bf16 into
-// shared memory, and the leader adds the rank-r up-projection with r_pad/16
-// more MMAs before the TMEM -> register -> global store.
+// The leader first issues r_pad/16 MMAs (256 x 256 x 16) for the LoRA term,
+// then 4 per stage for the base product, all into TMEM columns [0, 256) of
+// both CTAs; the epilogue moves TMEM -> registers -> global.
 //
 // Each SM dequantises 128 x 64 weights per stage for 2 x 128 x 256 x 64
 // MMA work, half of what a single-CTA 128 x 256 tile needs; the integer
@@ -55,9 +48,7 @@ constexpr int kGemmThreads = 320;
 constexpr int kABytes = GBM * GBK * 2;     // 16 KB
 constexpr int kBBytes = kHalfN * GBK * 2;  // 16 KB (this CTA's half of B)
 
-__host__ __device__ inline int gemm_stage_bytes(int r_pad) {
-  return kABytes + kBBytes + (r_pad / 2) * 128;
-}
+__host__ __device__ inline int gemm_stage_bytes(int) { return kABytes + kBBytes; }
 __host__ __device__ inline int gemm_upa_bytes(int r_pad) { return (r_pad / 16) * GBM * 32; }
 __host__ __device__ inline int gemm_upb_bytes(int r_pad) { return (r_pad / 16) * kHalfN * 32; }
 __host__ inline int gemm_smem_bytes(int stages, int r_pad) {
@@ -76,14 +67,14 @@ struct Fetch {
 };
 
 // Loads are unconditional (the caller clamps the address into range).
-__device__ __forceinline__ Fetch fetch_half(const GemmArgs &p, int64_t n, int64_t kcol, int half,
+// `qoff` is the byte offset of the 16 packed bytes, `blk` the block index.
+__device__ __forceinline__ Fetch fetch_half(const GemmArgs &p, int64_t qoff, int64_t blk,
                                             bool valid) {
   Fetch f;
   f.valid = valid;
-  f.q = ldg_nc_v4(p.packed + n * (p.wcols >> 1) + (kcol >> 1) + 16 * half);
-  const int64_t blk = n * (p.wcols >> 6) + (kcol >> 6);
-  f.code = __ldg(p.codes + (p.use_code ? blk : 0));
-  f.c = __ldg(p.cvec + blk / p.cdiv);
+  f.q = ldg_nc_v4(p.packed + qoff);
+  f.code = ldg_nc_s8(p.codes + (p.use_code ? blk : 0));
+  f.c = ldg_nc_f32(p.cvec + (blk >> p.cshift));
   return f;
 }
 
@@ -124,12 +115,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const int S = p.stages, RP = p.r_pad, RH = p.r_pad / 2;
+  const int S = p.stages, RP = p.r_pad;
   const int SB = gemm_stage_bytes(RP);
   uint8_t *upa = smem + S * SB;
   uint8_t *upb = upa + gemm_upa_bytes(RP);
   uint64_t *bars = reinterpret_cast<uint64_t *>(upb + gemm_upb_bytes(RP));
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 3);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 2);
   const uint32_t cta_err = smem_u32(tmem_slot + 1);  // shared address of the error flag
 
   const uint32_t smem0 = smem_u32(smem);
@@ -137,7 +128,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
   auto empty_bar = [&](int s) { return smem_u32(bars + S + s); };
   const uint32_t up_bar = smem_u32(bars + 2 * S);
-  const uint32_t acc_bar = smem_u32(bars + 2 * S + 1), acc2_bar = smem_u32(bars + 2 * S + 2);
+  const uint32_t acc_bar = smem_u32(bars + 2 * S + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -153,9 +144,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(full_bar(s), 1 + 8 + (leader ? 1 : 0));
       mbar_init(empty_bar(s), 1);  // multicast tcgen05.commit
     }
-    mbar_init(up_bar, 4 + 1 + (leader ? 1 : 0));
+    mbar_init(up_bar, 1 + (leader ? 1 : 0));  // TMA arrive (+ the peer's relay)
     mbar_init(acc_bar, 1);
-    mbar_init(acc2_bar, 1);
     st_shared_volatile(cta_err, 0u);
     fence_barrier_init();
   }
@@ -164,13 +154,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tmL1);
     tma_prefetch_desc(&tmL2);
   }
-  if (warp == 9) tmem_alloc2(smem_u32(tmem_slot), 512);
+  if (warp == 9) tmem_alloc2(smem_u32(tmem_slot), 256);
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // both CTAs' barriers initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = ld_shared_volatile(smem_u32(tmem_slot));
-  const uint32_t tmem_aux = tmem + 256;
 
   if (warp < 8) {
     // ------------------------------------------------ dequantising producers
@@ -191,21 +180,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       row_off = bsub * 8192 + (nl >> 3) * 1024 + (nl & 7) * 128;
       swz = nl & 7;
     }
+    // Byte offset / block index of this thread's 16 packed bytes at stage 0
+    // and their step per stage (64 contraction elements).
+    const int64_t kbr = p.wcols >> 6;  // blocks per weight row
+    int64_t q0, b0, qstep, bstep;
+    if (!kDx) {
+      q0 = n_fixed * (p.wcols >> 1) + 16 * half;  // row n, columns [0, 64)
+      b0 = n_fixed * kbr;
+      qstep = 32;
+      bstep = 1;
+    } else {
+      q0 = (int64_t)nl * (p.wcols >> 1) + (kcol_fixed >> 1) + 16 * half;
+      b0 = (int64_t)nl * kbr + (kcol_fixed >> 6);
+      qstep = 64 * (p.wcols >> 1);
+      bstep = 64 * kbr;
+    }
     auto fetch_k = [&](int kb) -> Fetch {
       const bool in_k = kb < num_k;
       const int kbc = in_k ? kb : num_k - 1;
-      int64_t n, kcol;
       bool valid;
-      if (!kDx) {
-        n = n_fixed;
-        kcol = (int64_t)kbc * GBK;
-        valid = in_k && n < p.wrows;
-      } else {
-        n = (int64_t)kbc * GBK + nl;
-        kcol = kcol_fixed;
-        valid = in_k && n < p.wrows && kcol < p.wcols;
-      }
-      return fetch_half(p, valid ? n : 0, valid ? kcol : 0, half, valid);
+      if (!kDx)
+        valid = in_k && n_fixed < p.wrows;
+      else
+        valid = in_k && (int64_t)kbc * GBK + nl < p.wrows && kcol_fixed < p.wcols;
+      return fetch_half(p, valid ? q0 + kbc * qstep : 0, valid ? b0 + kbc * bstep : 0, valid);
     };
     // Three-slot ring of prefetched blocks, indexed by compile-time
     // constants only: iteration kb consumes slot kb % 3 and refills slot
@@ -236,37 +234,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     // ---------------------------------------------------------- epilogue
     mbar_wait_bounded(acc_bar, 0, cta_err, p.status);
-    tc_fence_after();
-    if (warp < 4) {
-      // LoRA down-projection (t or u) of this CTA's 128 rows: save fp32,
-      // stage s * aux as bf16 for the up-projection.
-      const int rl = warp * 32 + lane;
-      const int row = m0 + rl;
-      const bool save = p.aux_out != nullptr && blockIdx.y == 0 && row < p.M;
-      for (int cb = 0; cb < RP / 16; ++cb) {
-        uint32_t v[16];
-        tmem_ld16(tmem_aux + ((uint32_t)(warp * 32) << 16) + cb * 16, v);
-        tmem_ld_wait();
-        if (save) {
-          for (int j = 0; j < 16; ++j) {
-            const int col = cb * 16 + j;
-            if (col < p.r) p.aux_out[(int64_t)row * p.r + col] = __uint_as_float(v[j]);
-          }
-        }
-        uint32_t w[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          w[j] = pack_bf16x2(p.s * __uint_as_float(v[2 * j]), p.s * __uint_as_float(v[2 * j + 1]));
-        const uint32_t base = upa_u + cb * (GBM * 32) + (rl >> 3) * 256 + (rl & 7) * 32;
-        const uint32_t x = (rl >> 2) & 1;
-        sts_v4(base + ((0 ^ x) << 4), w[0], w[1], w[2], w[3]);
-        sts_v4(base + ((1 ^ x) << 4), w[4], w[5], w[6], w[7]);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(up_bar);
-    }
-    mbar_wait_bounded(acc2_bar, 0, cta_err, p.status);
     tc_fence_after();
     const int quarter = warp & 3, hcol = warp >> 2;
     const int row = m0 + quarter * 32 + lane;
@@ -306,18 +273,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // --------------------------------------------------------- TMA producer
     if (lane == 0) {
       const int ncb = RP / 16;
-      mbar_arrive_expect_tx(up_bar, ncb * kHalfN * 32);
-      for (int cb = 0; cb < ncb; ++cb)
+      mbar_arrive_expect_tx(up_bar, ncb * (GBM + kHalfN) * 32);
+      for (int cb = 0; cb < ncb; ++cb) {
+        tma_load_2d(upa_u + cb * (GBM * 32), &tmL1, up_bar, cb * 16, m0);
         tma_load_2d(upb_u + cb * (kHalfN * 32), &tmL2, up_bar, cb * 16, cb0);
+      }
       int stage = 0;
       uint32_t ph = 0;
       int issued = 0;
       for (int kb = 0; kb < num_k; ++kb) {
         if (!mbar_wait_bounded(empty_bar(stage), ph ^ 1, cta_err, p.status)) break;
         const uint32_t a_dst = smem0 + stage * SB;
-        mbar_arrive_expect_tx(full_bar(stage), kABytes + RH * 128);
+        mbar_arrive_expect_tx(full_bar(stage), kABytes);
         tma_load_2d(a_dst, &tmA, full_bar(stage), kb * GBK, m0);
-        tma_load_2d(a_dst + kABytes + kBBytes, &tmL1, full_bar(stage), kb * GBK, (int)rank * RH);
         ++issued;
         if (++stage == S) {
           stage = 0;
@@ -336,27 +304,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------- MMA issuer (leader)
     if (lane == 0) {
       constexpr uint32_t idesc_main = make_idesc_bf16(2 * GBM, GBN, kDx);
-      const uint32_t idesc_aux = make_idesc_bf16(2 * GBM, RP, false);
       constexpr uint32_t idesc_up = make_idesc_bf16(2 * GBM, GBN, false);
+      bool ok = mbar_wait_bounded(up_bar, 0, cta_err, p.status);
+      if (ok) {
+        // LoRA term first: D = (s.t) . B^T  (or (s.u) . A for dX)
+        tc_fence_after();
+        for (int cb = 0; cb < RP / 16; ++cb) {
+          const uint64_t ad = make_sdesc(upa_u + cb * (GBM * 32), 16, 256, kSwz32);
+          const uint64_t bd = make_sdesc(upb_u + cb * (kHalfN * 32), 16, 256, kSwz32);
+          tc_mma2(tmem, ad, bd, idesc_up, cb > 0 ? 1u : 0u);
+        }
+      }
       int stage = 0;
       uint32_t ph = 0;
-      bool ok = true;
       for (int kb = 0; kb < num_k && ok; ++kb) {
-        ok = mbar_wait_bounded_cluster(full_bar(stage), ph, cta_err, p.status);
+        ok = mbar_wait_bounded(full_bar(stage), ph, cta_err, p.status);
         if (!ok) break;
         tc_fence_after();
         const uint32_t a_base = smem0 + stage * SB;
         const uint32_t b_base = a_base + kABytes;
-        const uint32_t l_base = b_base + kBBytes;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t ad = make_sdesc(a_base + kk * 32, 16, 1024, kSwz128);
           const uint64_t bd = kDx ? make_sdesc(b_base + kk * 2048, 8192, 1024, kSwz128)
                                   : make_sdesc(b_base + kk * 32, 16, 1024, kSwz128);
-          const uint64_t ld = make_sdesc(l_base + kk * 32, 16, 1024, kSwz128);
-          const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
-          tc_mma2(tmem, ad, bd, idesc_main, accum);
-          tc_mma2(tmem_aux, ad, ld, idesc_aux, accum);
+          tc_mma2(tmem, ad, bd, idesc_main, 1u);
         }
         tc_commit2_mc(empty_bar(stage), 0x3);
         if (++stage == S) {
@@ -365,23 +337,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
       tc_commit2_mc(acc_bar, 0x3);
-      if (ok && mbar_wait_bounded_cluster(up_bar, 0, cta_err, p.status)) {
-        tc_fence_after();
-        for (int cb = 0; cb < RP / 16; ++cb) {
-          const uint64_t ad = make_sdesc(upa_u + cb * (GBM * 32), 16, 256, kSwz32);
-          const uint64_t bd = make_sdesc(upb_u + cb * (kHalfN * 32), 16, 256, kSwz32);
-          tc_mma2(tmem, ad, bd, idesc_up, 1u);
-        }
-      }
-      tc_commit2_mc(acc2_bar, 0x3);
-      if (ld_shared_volatile(cta_err)) mbar_drain(acc2_bar, 0);  // all issued MMAs retired
+      if (ld_shared_volatile(cta_err)) mbar_drain(acc_bar, 0);  // all issued MMAs retired
     }
     __syncwarp();
   } else {
     // ----------------------------------------------- relay (peer CTA)
-    // Forwards "this CTA's half of stage s is ready" (its TMA bytes landed
-    // and its 8 producer warps arrived) to the leader's full barrier.
+    // Forwards "this CTA's LoRA operand halves landed" and then, per stage,
+    // "this CTA's half of stage s is ready" (its TMA bytes landed and its 8
+    // producer warps arrived) to the leader's barriers, in the order the
+    // leader consumes them.
     if (lane == 0) {
+      if (mbar_wait_bounded(up_bar, 0, cta_err, p.status)) mbar_arrive_remote(mapa_shared(up_bar, 0));
       int stage = 0;
       uint32_t ph = 0;
       for (int kb = 0; kb < num_k; ++kb) {
@@ -392,8 +358,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           ph ^= 1;
         }
       }
-      if (mbar_wait_bounded(up_bar, 0, cta_err, p.status))
-        mbar_arrive_remote(mapa_shared(up_bar, 0));
     }
     __syncwarp();
   }
@@ -403,7 +367,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   cluster_sync();  // the pair is done with TMEM and with each other's smem
   if (warp == 9) {
     tc_fence_after();
-    tmem_dealloc2(tmem, 512);
+    tmem_dealloc2(tmem, 256);
   }
 }
 
@@ -444,7 +408,7 @@ cudaError_t launch_gemm(bool dx, const CUtensorMap &tmA, const CUtensorMap &tmL1
 }
 
 int gemm_pick_stages(int r_pad) {
-  for (int st = 6; st >= 2; --st)
+  for (int st = 7; st >= 2; --st)
     if (gemm_smem_bytes(st, r_pad) <= 232448) return st;
   return 0;
 }

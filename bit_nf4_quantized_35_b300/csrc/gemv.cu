@@ -295,9 +295,9 @@ __global__ void __launch_bounds__(GemvWarps<NT>::value * 32, 1) qlora_gemv_kerne
           const int64_t kb = okb ? (kc0 >> 6) + blk : 0;
           P.pk[rt][h][blk] = ldg_nc_v2(p.packed + (int64_t)rowc * (p.K >> 1) + (kb << 5) + tq * 8);
           const int64_t b = (int64_t)rowc * kblocks_row + kb;
-          P.code[rt][h][blk] = __ldg(p.codes + (p.use_code ? b : 0));
+          P.code[rt][h][blk] = ldg_nc_s8(p.codes + (p.use_code ? b : 0));
           P.valid |= okb ? (1u << (rt * 4 + h * 2 + blk)) : 0u;
-          P.cv[rt][h][blk] = __ldg(p.cvec + b / p.cdiv);
+          P.cv[rt][h][blk] = ldg_nc_f32(p.cvec + (b >> p.cshift));
         }
       }
   };
@@ -406,32 +406,6 @@ __global__ void __launch_bounds__(GemvWarps<NT>::value * 32, 1) qlora_gemv_kerne
   cluster_sync_all();  // keep every CTA's shared memory alive until rank 0 has read it
 }
 
-// t[m, j] = sum_k x[m, k] A[j, k]  (fp32 accumulation), one warp per (m, j).
-__global__ void __launch_bounds__(256) lora_down_kernel(const uint16_t *__restrict__ x,
-                                                        const uint16_t *__restrict__ A, int M,
-                                                        int K, int r, float *__restrict__ t) {
-  const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (wid >= (int64_t)M * r) return;
-  const int64_t m = wid / r;
-  const int j = (int)(wid % r);
-  const uint16_t *xr = x + m * K;
-  const uint16_t *ar = A + (int64_t)j * K;
-  float acc = 0.f;
-  for (int k = lane * 8; k < K; k += 256) {
-    const uint4 xv = ldg_nc_v4(xr + k), av = ldg_nc_v4(ar + k);
-    const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, aa[4] = {av.x, av.y, av.z, av.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      acc = fmaf(bf16_lo(xa[e]), bf16_lo(aa[e]), acc);
-      acc = fmaf(bf16_hi(xa[e]), bf16_hi(aa[e]), acc);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) t[m * r + j] = acc;
-}
-
 // ------------------------------------------------------------ launchers
 int gemv_plan(int K, int M, int *warps, int *S) {
   const int maxw = M > 8 ? GemvWarps<2>::value : GemvWarps<1>::value;
@@ -495,13 +469,5 @@ cudaError_t launch_gemv(GemvArgs a, int num_sms, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_lora_down(const uint16_t *x, const uint16_t *A, int64_t M, int K, int r,
-                             float *t, cudaStream_t s) {
-  const int64_t warps = M * r;
-  if (warps == 0) return cudaSuccess;
-  const int64_t blocks = (warps * 32 + 255) / 256;
-  lora_down_kernel<<<(unsigned)blocks, 256, 0, s>>>(x, A, (int)M, K, r, t);
-  return cudaGetLastError();
-}
 
 }  // namespace qlora

@@ -25,7 +25,6 @@ struct GemmArgs {
   float s;
   void *out;
   int out_bf16;
-  float *aux_out;  // t or u, fp32 [M, r]; written by the CTAs of output column tile 0
   int stages;
   int *status;
   // Branch-free block constant: a_hat = use_code ? code[b] * cvec[b / cdiv] : cvec[b / cdiv]
@@ -33,6 +32,7 @@ struct GemmArgs {
   const float *cvec;
   int cdiv;
   int use_code;
+  int cshift;  // log2(cdiv): cdiv is 1 or a power of two
 };
 cudaError_t launch_gemm(bool dx, const CUtensorMap &tmA, const CUtensorMap &tmL1,
                         const CUtensorMap &tmL2, const GemmArgs &args, cudaStream_t s);
@@ -58,14 +58,18 @@ struct GemvArgs {
   const float *cvec;  // as in GemmArgs
   int cdiv;
   int use_code;
+  int cshift;
   int row_tiles;  // ceil(N / 16), set by the launcher
   int clusters;   // gridDim.x, set by the launcher
   int rows_max;   // rows of the largest per-cluster row range, set by the launcher
 };
 int gemv_plan(int K, int M, int *warps, int *S);
 cudaError_t launch_gemv(GemvArgs a, int num_sms, cudaStream_t s);
-cudaError_t launch_lora_down(const uint16_t *x, const uint16_t *A, int64_t M, int K, int r,
-                             float *t, cudaStream_t s);
+// out[m, j] = sum_c G[m, c] H[j, c] (fp32, j < r) and outb[m, j] = bf16(s . out[m, j])
+// (j < r_pad, zero beyond r); either output may be null.  H has r rows of C.
+cudaError_t launch_lora_down(const uint16_t *G, int64_t M, int C, const uint16_t *H, int r,
+                             float s, float *out, uint16_t *outb, int r_pad, int num_sms,
+                             cudaStream_t st);
 
 // Quantise / dequantise (quantize.cu).
 cudaError_t launch_quantize(const void *W, bool bf16_in, int64_t nblocks, int group,

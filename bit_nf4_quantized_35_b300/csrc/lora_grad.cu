@@ -136,7 +136,111 @@ __global__ void transpose_a_kernel(const uint16_t *__restrict__ A, int K, int r,
   }
 }
 
+// ---------------------------------------------------------------------------
+// LoRA down-projection out = G . H^T for a tall, skinny product:
+//   forward  t = x . A^T   (G = x [M, K],  H = A  [r, K])
+//   backward u = dY . B    (G = dY [M, N], H = B^T [r, N])
+// It also writes bf16(s . out), zero-padded to r_pad columns: the operand of
+// the rank-r MMAs that seed the fused GEMM's accumulator.
+// One CTA per 16 rows of G, 8 warps splitting C; bf16 mma.sync m16n8k16 with
+// fp32 accumulation (G streams from memory once, H is a few KB and stays in
+// L1); the 8 warp partials meet in shared memory in a fixed order.
+// Lane (g, q) loads 8 consecutive elements (16 B) of rows g and g+8 per 32
+// columns; the two MMAs of those 32 columns pair their k indices in the same
+// order for G and H, so any consistent assignment is exact.
+constexpr int kDownWarps = 8;
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <int NT>  // n8 tiles: r_pad / 8
+__global__ void __launch_bounds__(kDownWarps * 32) lora_down_kernel(
+    const uint16_t *__restrict__ G, int64_t M, int C, const uint16_t *__restrict__ H, int r,
+    float s, float *__restrict__ out, uint16_t *__restrict__ outb, int r_pad) {
+  __shared__ float red[kDownWarps][16][NT * 8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, q = lane & 3;
+  const int64_t m0 = (int64_t)blockIdx.x * 16;
+  const int64_t rg = m0 + g, rg8 = m0 + g + 8;
+  const bool vg = rg < M, vg8 = rg8 < M;
+  // this warp's share of C, in 32-column chunks
+  const int nch = (C + 31) / 32;
+  const int per = (nch + kDownWarps - 1) / kDownWarps;
+  const int c_lo = warp * per * 32;
+  const int c_hi = min(C, (warp + 1) * per * 32);
+  float d[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
+  const uint16_t *g0p = G + (vg ? rg : 0) * C;
+  const uint16_t *g8p = G + (vg8 ? rg8 : 0) * C;
+  for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+    const int cc = c0 + q * 8;
+    const bool cv = cc < C;  // C % 8 == 0
+    const uint4 a = ldg_nc_v4(g0p + (cv ? cc : 0));
+    const uint4 b = ldg_nc_v4(g8p + (cv ? cc : 0));
+    const uint32_t A0[4] = {vg && cv ? a.x : 0u, vg && cv ? a.y : 0u, vg && cv ? a.z : 0u,
+                            vg && cv ? a.w : 0u};
+    const uint32_t A8[4] = {vg8 && cv ? b.x : 0u, vg8 && cv ? b.y : 0u, vg8 && cv ? b.z : 0u,
+                            vg8 && cv ? b.w : 0u};
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int j = nt * 8 + g;
+      uint4 h = make_uint4(0, 0, 0, 0);
+      if (j < r && cv) h = ldg_nc_v4(H + (int64_t)j * C + cc);
+      // MMA 0: physical columns cc+0..3, MMA 1: cc+4..7
+      mma_bf16_16816(d[nt], A0[0], A8[0], A0[1], A8[1], h.x, h.y);
+      mma_bf16_16816(d[nt], A0[2], A8[2], A0[3], A8[3], h.z, h.w);
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    red[warp][g][nt * 8 + 2 * q] = d[nt][0];
+    red[warp][g][nt * 8 + 2 * q + 1] = d[nt][1];
+    red[warp][g + 8][nt * 8 + 2 * q] = d[nt][2];
+    red[warp][g + 8][nt * 8 + 2 * q + 1] = d[nt][3];
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 16 * NT * 8; i += blockDim.x) {
+    const int row = i / (NT * 8), j = i % (NT * 8);
+    const int64_t m = m0 + row;
+    if (m >= M) continue;
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDownWarps; ++w) v += red[w][row][j];
+    if (out && j < r) out[m * r + j] = v;
+    if (outb && j < r_pad)
+      outb[m * r_pad + j] = j < r ? __bfloat16_as_ushort(__float2bfloat16_rn(s * v)) : (uint16_t)0;
+  }
+}
+
 // ------------------------------------------------------------ launchers
+cudaError_t launch_lora_down(const uint16_t *G, int64_t M, int C, const uint16_t *H, int r,
+                             float s, float *out, uint16_t *outb, int r_pad, int num_sms,
+                             cudaStream_t st) {
+  (void)num_sms;
+  if (M == 0) return cudaSuccess;
+  const unsigned grid = (unsigned)((M + 15) / 16);
+  switch ((r + 7) / 8) {
+    case 1: lora_down_kernel<2><<<grid, kDownWarps * 32, 0, st>>>(G, M, C, H, r, s, out, outb, r_pad); break;
+    case 2: lora_down_kernel<2><<<grid, kDownWarps * 32, 0, st>>>(G, M, C, H, r, s, out, outb, r_pad); break;
+    case 3: lora_down_kernel<4><<<grid, kDownWarps * 32, 0, st>>>(G, M, C, H, r, s, out, outb, r_pad); break;
+    case 4: lora_down_kernel<4><<<grid, kDownWarps * 32, 0, st>>>(G, M, C, H, r, s, out, outb, r_pad); break;
+    case 5: lora_down_kernel<6><<<grid, kDownWarps * 32, 0, st>>>(G, M, C, H, r, s, out, outb, r_pad); break;
+    case 6: lora_down_kernel<6><<<grid, kDownWarps * 32, 0, st>>>(G, M, C, H, r, s, out, outb, r_pad); break;
+    case 7: lora_down_kernel<8><<<grid, kDownWarps * 32, 0, st>>>(G, M, C, H, r, s, out, outb, r_pad); break;
+    case 8: lora_down_kernel<8><<<grid, kDownWarps * 32, 0, st>>>(G, M, C, H, r, s, out, outb, r_pad); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
 int skinny_splits(int64_t M, int C) {
   const int coltiles = (C + kSkinnyCols - 1) / kSkinnyCols;
   int64_t sp = (296 + coltiles - 1) / coltiles;
