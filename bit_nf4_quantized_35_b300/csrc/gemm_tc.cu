@@ -12,16 +12,17 @@
 // tcgen05 cta_group::2: CTA r owns rows [128r, 128r+128) of the tile and
 // half of the B operand (output columns [128r, 128r+128)); one thread of the
 // leader CTA issues every MMA for both.  Contraction step 64.
-// Per CTA, 320 threads:
-//   warps 0-7  dequantising producers: two threads per B row, 32 packed
-//              nibbles each, through the per-block table
-//              T[i] = bf16(c_i * a_hat) indexed with byte permutes; the bf16
+// Per CTA, 576 threads:
+//   warps 0-15 dequantising producers in 4 groups that take the stages
+//              round-robin; a thread owns one B row of its group's stage and
+//              turns its 64 packed nibbles into bf16 through the per-block
+//              table T[i] = bf16(c_i * a_hat) indexed with byte permutes; the
 //              values go straight into the 128-byte-swizzled operand layout
 //              the tensor core reads (K-major forward, MN-major dX).  After
 //              the main loop the same warps run the epilogue.
-//   warp 8     TMA: this CTA's 128 activation rows per stage; its halves of
+//   warp 16    TMA: this CTA's 128 activation rows per stage; its halves of
 //              the two rank-r LoRA operands once.
-//   warp 9     TMEM allocation (both CTAs); in the leader the single MMA
+//   warp 17    TMEM allocation (both CTAs); in the leader the single MMA
 //              issuer, in the peer a relay that forwards "stage ready" to the
 //              leader's barrier.
 // The leader first issues r_pad/16 MMAs (256 x 256 x 16) for the LoRA term,
@@ -44,7 +45,10 @@ constexpr int GBM = 128;  // rows per CTA (the pair covers 256)
 constexpr int GBN = 256;  // output columns per pair tile
 constexpr int GBK = 64;
 constexpr int kHalfN = GBN / 2;
-constexpr int kGemmThreads = 320;
+constexpr int kProdGroups = 4;                     // producer groups, stages round-robin
+constexpr int kProdWarps = 4 * kProdGroups;        // 16 warps: one thread per B row per group
+constexpr int kTmaWarp = kProdWarps, kMmaWarp = kProdWarps + 1;
+constexpr int kGemmThreads = (kProdWarps + 2) * 32;  // 576
 constexpr int kABytes = GBM * GBK * 2;     // 16 KB
 constexpr int kBBytes = kHalfN * GBK * 2;  // 16 KB (this CTA's half of B)
 
@@ -56,45 +60,46 @@ __host__ inline int gemm_smem_bytes(int stages, int r_pad) {
          256;
 }
 
-// Raw packed bytes + block constant of one half (32 weights) of a 64-block.
+// Raw packed bytes + block constant of one 64-block.
 // Loaded values stay raw until use: converting a value right after its load
 // would stall the thread for the whole load latency at prefetch time.
 struct Fetch {
-  uint4 q;   // 16 packed bytes
+  uint4 lo, hi;  // 32 packed bytes
   int code;  // int8 block constant (DQ)
   float c;   // second-level scale s2 (DQ) or fp32 absmax (no DQ)
   bool valid;
 };
 
 // Loads are unconditional (the caller clamps the address into range).
-// `qoff` is the byte offset of the 16 packed bytes, `blk` the block index.
-__device__ __forceinline__ Fetch fetch_half(const GemmArgs &p, int64_t qoff, int64_t blk,
+// `qoff` is the byte offset of the 32 packed bytes, `blk` the block index.
+__device__ __forceinline__ Fetch fetch_block(const GemmArgs &p, int64_t qoff, int64_t blk,
                                             bool valid) {
   Fetch f;
   f.valid = valid;
-  f.q = ldg_nc_v4(p.packed + qoff);
+  f.lo = ldg_nc_v4(p.packed + qoff);
+  f.hi = ldg_nc_v4(p.packed + qoff + 16);
   f.code = ldg_nc_s8(p.codes + (p.use_code ? blk : 0));
   f.c = ldg_nc_f32(p.cvec + (blk >> p.cshift));
   return f;
 }
 
-// Dequantise 32 weights into the 4 16-byte chunks [4*half, 4*half+4) of one
-// 128-byte swizzled row at `row_addr` (chunk c goes to position c ^ swz).
-__device__ __forceinline__ void dequant_store_half(const GemmArgs &p, const Fetch &f,
-                                                   uint32_t row_addr, uint32_t swz, int half) {
+// Dequantise one 64-block into the 8 16-byte chunks of one 128-byte
+// swizzled row at `row_addr` (chunk c goes to position c ^ swz).
+__device__ __forceinline__ void dequant_store_row(const GemmArgs &p, const Fetch &f,
+                                                  uint32_t row_addr, uint32_t swz) {
   if (!f.valid) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) sts_v4(row_addr + (((4 * half + c) ^ swz) << 4), 0, 0, 0, 0);
+    for (int c = 0; c < 8; ++c) sts_v4(row_addr + ((c ^ swz) << 4), 0, 0, 0, 0);
     return;
   }
   const float ahat = p.use_code ? __fmul_rn((float)f.code, f.c) : f.c;
   const Nf4Table t = make_table(ahat);
-  const uint32_t w[4] = {f.q.x, f.q.y, f.q.z, f.q.w};
+  const uint32_t w[8] = {f.lo.x, f.lo.y, f.lo.z, f.lo.w, f.hi.x, f.hi.y, f.hi.z, f.hi.w};
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
+  for (int c = 0; c < 8; ++c) {
     uint32_t o[4];
     lookup8(t, w[c], o);
-    sts_v4(row_addr + (((4 * half + c) ^ swz) << 4), o[0], o[1], o[2], o[3]);
+    sts_v4(row_addr + ((c ^ swz) << 4), o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -140,8 +145,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      // TMA arrive + 8 producer warps (+ the peer's relay in the leader)
-      mbar_init(full_bar(s), 1 + 8 + (leader ? 1 : 0));
+      // TMA arrive + the 4 warps of one producer group (+ the peer's relay)
+      mbar_init(full_bar(s), 1 + 4 + (leader ? 1 : 0));
       mbar_init(empty_bar(s), 1);  // multicast tcgen05.commit
     }
     mbar_init(up_bar, 1 + (leader ? 1 : 0));  // TMA arrive (+ the peer's relay)
@@ -149,23 +154,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     st_shared_volatile(cta_err, 0u);
     fence_barrier_init();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == kTmaWarp && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmL1);
     tma_prefetch_desc(&tmL2);
   }
-  if (warp == 9) tmem_alloc2(smem_u32(tmem_slot), 256);
+  if (warp == kMmaWarp) tmem_alloc2(smem_u32(tmem_slot), 256);
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // both CTAs' barriers initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = ld_shared_volatile(smem_u32(tmem_slot));
 
-  if (warp < 8) {
+  if (warp < kProdWarps) {
     // ------------------------------------------------ dequantising producers
-    const int pid = threadIdx.x;  // 0..255
-    const int half = pid & 1;     // which 32 weights of the 64-block
-    const int rowi = pid >> 1;    // 0..127: row of this CTA's B half
+    // Group `grp` (4 warps) produces stages kb = grp, grp + 4, ...; within a
+    // group thread `rowi` owns one 128-byte row of this CTA's B half.
+    const int grp = threadIdx.x >> 7;
+    const int rowi = threadIdx.x & 127;
     int64_t n_fixed = 0, kcol_fixed = 0;
     uint32_t row_off, swz;
     int nl = 0;
@@ -180,17 +186,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       row_off = bsub * 8192 + (nl >> 3) * 1024 + (nl & 7) * 128;
       swz = nl & 7;
     }
-    // Byte offset / block index of this thread's 16 packed bytes at stage 0
+    // Byte offset / block index of this thread's 32 packed bytes at stage 0
     // and their step per stage (64 contraction elements).
     const int64_t kbr = p.wcols >> 6;  // blocks per weight row
     int64_t q0, b0, qstep, bstep;
     if (!kDx) {
-      q0 = n_fixed * (p.wcols >> 1) + 16 * half;  // row n, columns [0, 64)
+      q0 = n_fixed * (p.wcols >> 1);  // row n, columns [0, 64)
       b0 = n_fixed * kbr;
       qstep = 32;
       bstep = 1;
     } else {
-      q0 = (int64_t)nl * (p.wcols >> 1) + (kcol_fixed >> 1) + 16 * half;
+      q0 = (int64_t)nl * (p.wcols >> 1) + (kcol_fixed >> 1);
       b0 = (int64_t)nl * kbr + (kcol_fixed >> 6);
       qstep = 64 * (p.wcols >> 1);
       bstep = 64 * kbr;
@@ -203,31 +209,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         valid = in_k && n_fixed < p.wrows;
       else
         valid = in_k && (int64_t)kbc * GBK + nl < p.wrows && kcol_fixed < p.wcols;
-      return fetch_half(p, valid ? q0 + kbc * qstep : 0, valid ? b0 + kbc * bstep : 0, valid);
+      return fetch_block(p, valid ? q0 + kbc * qstep : 0, valid ? b0 + kbc * bstep : 0, valid);
     };
     // Three-slot ring of prefetched blocks, indexed by compile-time
-    // constants only: iteration kb consumes slot kb % 3 and refills slot
-    // (kb + 2) % 3, so no register ever copies a load still in flight.
+    // constants only: this group's i-th stage consumes slot i % 3 and
+    // refills slot (i + 2) % 3, so no register ever copies a load in flight.
     Fetch f[3];
-    f[0] = fetch_k(0);
-    f[1] = fetch_k(1);
-    int stage = 0;
-    uint32_t ph = 0;
-    for (int kb0 = 0; kb0 < num_k; kb0 += 3) {
+    f[0] = fetch_k(grp);
+    f[1] = fetch_k(grp + kProdGroups);
+    for (int kb0 = grp; kb0 < num_k; kb0 += 3 * kProdGroups) {
 #pragma unroll
       for (int u = 0; u < 3; ++u) {
-        const int kb = kb0 + u;
+        const int kb = kb0 + u * kProdGroups;
         if (kb < num_k) {
-          f[(u + 2) % 3] = fetch_k(kb + 2);
+          f[(u + 2) % 3] = fetch_k(kb + 2 * kProdGroups);
+          const int stage = kb % S;
+          const uint32_t ph = (uint32_t)(kb / S) & 1u;
           const bool ok = mbar_wait_bounded(empty_bar(stage), ph ^ 1, cta_err, p.status);
-          if (ok) dequant_store_half(p, f[u], smem0 + stage * SB + kABytes + row_off, swz, half);
+          if (ok) dequant_store_row(p, f[u], smem0 + stage * SB + kABytes + row_off, swz);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(full_bar(stage));
-          if (++stage == S) {
-            stage = 0;
-            ph ^= 1;
-          }
         }
       }
     }
@@ -235,10 +237,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ---------------------------------------------------------- epilogue
     mbar_wait_bounded(acc_bar, 0, cta_err, p.status);
     tc_fence_after();
+    // 16 warps: warp w reads TMEM lanes 32*(w%4).. and columns [64*(w/4), +64)
     const int quarter = warp & 3, hcol = warp >> 2;
     const int row = m0 + quarter * 32 + lane;
-    for (int ch = 0; ch < 4; ++ch) {
-      const int col = hcol * 128 + ch * 32;
+    for (int ch = 0; ch < 2; ++ch) {
+      const int col = hcol * 64 + ch * 32;
       uint32_t v[32];
       tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + col, v);
       tmem_ld_wait();
@@ -269,7 +272,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
     }
-  } else if (warp == 8) {
+  } else if (warp == kTmaWarp) {
     // --------------------------------------------------------- TMA producer
     if (lane == 0) {
       const int ncb = RP / 16;
@@ -343,8 +346,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ----------------------------------------------- relay (peer CTA)
     // Forwards "this CTA's LoRA operand halves landed" and then, per stage,
-    // "this CTA's half of stage s is ready" (its TMA bytes landed and its 8
-    // producer warps arrived) to the leader's barriers, in the order the
+    // "this CTA's half of stage s is ready" (its TMA bytes landed and the 4
+    // warps of the producer group arrived) to the leader's barriers, in the order the
     // leader consumes them.
     if (lane == 0) {
       if (mbar_wait_bounded(up_bar, 0, cta_err, p.status)) mbar_arrive_remote(mapa_shared(up_bar, 0));
@@ -365,7 +368,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // the pair is done with TMEM and with each other's smem
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc2(tmem, 256);
   }
