@@ -59,9 +59,12 @@ struct GemvArgs {
   int cdiv;
   int use_code;
   int cshift;
-  int row_tiles;  // ceil(N / 16), set by the launcher
-  int clusters;   // gridDim.x, set by the launcher
-  int rows_max;   // rows of the largest per-cluster row range, set by the launcher
+  // set by the launcher:
+  int slice;      // K columns per CTA of a cluster (multiple of 64)
+  int row_pairs;  // ceil(N / 32)
+  int clusters;   // gridDim.x
+  int rows_max;   // rows of the largest per-cluster row range
+  int kparts;     // k parts per row pair inside a CTA (warps per row pair)
 };
 int gemv_plan(int K, int M, int *warps, int *S);
 cudaError_t launch_gemv(GemvArgs a, int num_sms, cudaStream_t s);
