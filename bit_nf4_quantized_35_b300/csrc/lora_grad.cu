@@ -4,88 +4,167 @@
 // "QLoRA and 4bit Quantization | QLoRA 与 4-bit 量化", Step 3/4 (gradients
 // reach lora_A and lora_B; the NF4 state gets none):
 //   dB = s . dY^T . t     [N, r]   (t = x A^T from the forward, fp32)
-//   dA = s . u^T  . x     [r, K]   (u = dY B from the dX GEMM, fp32)
+//   dA = s . u^T  . x     [r, K]   (u = dY B from the backward pre-pass, fp32)
 // Both are "tall-skinny" products G^T V with G a bf16 [M, C] activation
-// (dY or x) and V an fp32 [M, r] factor, reduced over the M tokens.  They
-// run on the CUDA cores in fp32: the gradients are large sums (|dA|, |dB| of
-// order 10^2 at M = 8192) that must keep ~1e-4 relative accuracy, which a
-// bf16 operand V could not give.  Each thread owns two adjacent columns of G
-// and all r_pad accumulators; V rows are staged in shared memory and read as
-// broadcasts; the M range is split across CTAs and the partial sums are
-// reduced in a fixed order by a second kernel (deterministic).
+// (dY or x) and V an fp32 [M, r] factor, reduced over the M tokens.  The
+// gradients are large sums (|dA|, |dB| of order 10^2 at M = 8192) that must
+// keep ~1e-4 relative accuracy, which a bf16 V could not give: V is split
+// exactly into bf16 hi + lo parts (16 significant bits) and both halves run
+// through bf16 tensor-core MMAs with fp32 accumulation.  The M range is split
+// across CTAs and the partial sums are reduced in a fixed order by a second
+// kernel (deterministic).
 #include "common.cuh"
 #include "kernels.h"
 
 namespace qlora {
 
-constexpr int kSkinnyThreads = 128;
-constexpr int kSkinnyCols = 2 * kSkinnyThreads;  // columns per CTA
-constexpr int kSkinnyRows = 64;                  // V rows staged per pass
+// ---------------------------------------------------------------------------
+// part[split][c][j] = sum_{m in split} G[m][c] . V[m][j]   (j < r_pad)
+// One CTA = 128 columns c x one M split, 8 warps of 16 columns each.  Per
+// 64-row chunk of M: the G tile [64 m][128 c] arrives by cp.async (double
+// buffered, rows padded to 272 B so ldmatrix rows hit distinct banks) and
+// V^T as bf16 hi and lo rows [2 r_pad][64 m] (padded to 144 B).  The MMA
+// A operand (16 c x 16 m) is an ldmatrix.trans of the G tile, the B operand
+// (16 m x 8 j) an ldmatrix of V^T.
+constexpr int kGradThreads = 256;
+constexpr int kGradCols = 128;  // c per CTA
+constexpr int kGradRows = 64;   // m per chunk
+constexpr int kGsPitch = 136;   // halves per G-tile row (128 + 8)
+constexpr int kVtPitch = 72;    // halves per V^T row (64 + 8)
 
-template <int RP>
-__global__ void __launch_bounds__(kSkinnyThreads) skinny_tn_kernel(
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+__host__ __device__ inline int grad_smem_bytes(int RPAD) {
+  return 2 * kGradRows * kGsPitch * 2 + 2 * (2 * RPAD) * kVtPitch * 2;
+}
+
+template <int RPT>  // r_pad / 8
+__global__ void __launch_bounds__(kGradThreads) lora_grad_tc_kernel(
     const uint16_t *__restrict__ G, int64_t M, int C, const float *__restrict__ V, int r,
     int64_t rows_per_split, float *__restrict__ part) {
-  __shared__ __align__(16) float vs[kSkinnyRows][RP];
-  const int c = blockIdx.x * kSkinnyCols + threadIdx.x * 2;
-  const bool cvalid = c < C;
+  constexpr int RPAD = RPT * 8;
+  constexpr int NJ = 2 * RPAD;  // hi rows then lo rows
+  constexpr int NTT = NJ / 8;   // n8 tiles
+  extern __shared__ __align__(16) uint16_t gsm[];
+  uint16_t *gs = gsm;                                 // [2][64][136]
+  uint16_t *vt = gsm + 2 * kGradRows * kGsPitch;      // [2][NJ][72]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, q = lane & 3;
+  const int c0 = blockIdx.x * kGradCols;
   const int64_t m_lo = (int64_t)blockIdx.y * rows_per_split;
-  int64_t m_hi = m_lo + rows_per_split;
-  if (m_hi > M) m_hi = M;
-  float a0[RP], a1[RP];
+  const int64_t m_hi = min(M, m_lo + rows_per_split);
+  const int nchunks = (int)((m_hi - m_lo + kGradRows - 1) / kGradRows);
+
+  auto issue_g = [&](int ch, int buf) {  // 64 x 128 bf16 = 1024 16-byte pieces
+    const int64_t mb = m_lo + (int64_t)ch * kGradRows;
 #pragma unroll
-  for (int j = 0; j < RP; ++j) a0[j] = a1[j] = 0.f;
-  for (int64_t mb = m_lo; mb < m_hi; mb += kSkinnyRows) {
-    const int rows = (int)((m_hi - mb) < kSkinnyRows ? (m_hi - mb) : kSkinnyRows);
+    for (int u = 0; u < 4; ++u) {
+      const int i = threadIdx.x + u * kGradThreads;
+      const int row = i >> 4, cc = (i & 15) * 8;
+      const int64_t m = mb + row;
+      const int c = c0 + cc;
+      const bool ok = m < m_hi && c < C;
+      const uint16_t *src = G + (ok ? m * C + c : 0);
+      cp_async16(smem_u32(gs + (buf * kGradRows + row) * kGsPitch + cc), src, ok ? 16u : 0u);
+    }
+    cp_async_commit();
+  };
+  auto stage_v = [&](int ch, int buf) {  // V rows -> bf16 hi / lo, transposed
+    const int64_t mb = m_lo + (int64_t)ch * kGradRows;
+    for (int i = threadIdx.x; i < kGradRows * RPAD; i += kGradThreads) {
+      const int row = i / RPAD, j = i % RPAD;
+      const int64_t m = mb + row;
+      const float v = (m < m_hi && j < r) ? V[m * r + j] : 0.f;
+      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+      vt[(buf * NJ + j) * kVtPitch + row] = __bfloat16_as_ushort(hi);
+      vt[(buf * NJ + RPAD + j) * kVtPitch + row] = __bfloat16_as_ushort(lo);
+    }
+  };
+
+  float d[NTT][4];
+#pragma unroll
+  for (int nt = 0; nt < NTT; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
+  if (nchunks > 0) {
+    issue_g(0, 0);
+    stage_v(0, 0);
+    cp_async_wait_all();
     __syncthreads();
-    for (int i = threadIdx.x; i < kSkinnyRows * RP; i += kSkinnyThreads) {
-      const int mm = i / RP, j = i % RP;
-      vs[mm][j] = (mm < rows && j < r) ? V[(mb + mm) * r + j] : 0.f;
-    }
-    __syncthreads();
-    const uint16_t *gp = G + mb * C + c;
-    int mm = 0;
-    for (; mm + 8 <= rows; mm += 8) {
-      uint32_t gv[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        gv[q] = cvalid ? __ldg(reinterpret_cast<const uint32_t *>(gp + (int64_t)(mm + q) * C)) : 0u;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float g0 = bf16_lo(gv[q]), g1 = bf16_hi(gv[q]);
-        const float4 *vr = reinterpret_cast<const float4 *>(&vs[mm + q][0]);
-#pragma unroll
-        for (int j4 = 0; j4 < RP / 4; ++j4) {
-          const float4 v = vr[j4];
-          a0[4 * j4 + 0] = fmaf(g0, v.x, a0[4 * j4 + 0]);
-          a0[4 * j4 + 1] = fmaf(g0, v.y, a0[4 * j4 + 1]);
-          a0[4 * j4 + 2] = fmaf(g0, v.z, a0[4 * j4 + 2]);
-          a0[4 * j4 + 3] = fmaf(g0, v.w, a0[4 * j4 + 3]);
-          a1[4 * j4 + 0] = fmaf(g1, v.x, a1[4 * j4 + 0]);
-          a1[4 * j4 + 1] = fmaf(g1, v.y, a1[4 * j4 + 1]);
-          a1[4 * j4 + 2] = fmaf(g1, v.z, a1[4 * j4 + 2]);
-          a1[4 * j4 + 3] = fmaf(g1, v.w, a1[4 * j4 + 3]);
-        }
-      }
-    }
-    for (; mm < rows; ++mm) {
-      const uint32_t gv =
-          cvalid ? __ldg(reinterpret_cast<const uint32_t *>(gp + (int64_t)mm * C)) : 0u;
-      const float g0 = bf16_lo(gv), g1 = bf16_hi(gv);
-#pragma unroll
-      for (int j = 0; j < RP; ++j) {
-        a0[j] = fmaf(g0, vs[mm][j], a0[j]);
-        a1[j] = fmaf(g1, vs[mm][j], a1[j]);
-      }
-    }
   }
-  if (cvalid) {
-    float4 *d0 = reinterpret_cast<float4 *>(part + ((int64_t)blockIdx.y * C + c) * RP);
-    float4 *d1 = d0 + RP / 4;
+  const int cw = warp * 16;  // this warp's 16 columns inside the tile
+  // ldmatrix lane roles: matrix mi = lane >> 3, row within it lane & 7
+  const int mi = lane >> 3, lr = lane & 7;
+  for (int ch = 0; ch < nchunks; ++ch) {
+    const int cur = ch & 1;
+    if (ch + 1 < nchunks) issue_g(ch + 1, cur ^ 1);
 #pragma unroll
-    for (int j4 = 0; j4 < RP / 4; ++j4) {
-      d0[j4] = make_float4(a0[4 * j4], a0[4 * j4 + 1], a0[4 * j4 + 2], a0[4 * j4 + 3]);
-      d1[j4] = make_float4(a1[4 * j4], a1[4 * j4 + 1], a1[4 * j4 + 2], a1[4 * j4 + 3]);
+    for (int kk = 0; kk < kGradRows / 16; ++kk) {
+      const int m0 = kk * 16;
+      // A = G^T (16 c x 16 m): matrices (m0.., cw), (m0.., cw+8), (m0+8.., cw), (m0+8.., cw+8)
+      uint32_t a0, a1, a2, a3;
+      {
+        const int row = m0 + lr + ((mi >> 1) << 3);
+        const int col = cw + ((mi & 1) << 3);
+        ldsm_x4_t(smem_u32(gs + (cur * kGradRows + row) * kGsPitch + col), a0, a1, a2, a3);
+      }
+#pragma unroll
+      for (int np = 0; np < NTT / 2; ++np) {
+        // B = V^T rows (j') x m: matrices (rows 16np.., m0), (16np.., m0+8),
+        // (16np+8.., m0), (16np+8.., m0+8)
+        uint32_t b0, b1, b2, b3;
+        const int row = np * 16 + lr + ((mi >> 1) << 3);
+        const int col = m0 + ((mi & 1) << 3);
+        ldsm_x4(smem_u32(vt + (cur * NJ + row) * kVtPitch + col), b0, b1, b2, b3);
+        mma_bf16_16816(d[2 * np], a0, a1, a2, a3, b0, b1);
+        mma_bf16_16816(d[2 * np + 1], a0, a1, a2, a3, b2, b3);
+      }
+    }
+    if (ch + 1 < nchunks) stage_v(ch + 1, cur ^ 1);
+    cp_async_wait_all();
+    __syncthreads();
+  }
+  // hi + lo, then the partial of this split: rows c0+cw+g (+8), columns j
+#pragma unroll
+  for (int nt = 0; nt < RPT; ++nt) {
+    const int j = nt * 8 + 2 * q;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int c = c0 + cw + g + 8 * h;
+      if (c < C) {
+        float *dst = part + ((int64_t)blockIdx.y * C + c) * RPAD + j;
+        dst[0] = d[nt][2 * h] + d[RPT + nt][2 * h];
+        dst[1] = d[nt][2 * h + 1] + d[RPT + nt][2 * h + 1];
+      }
     }
   }
 }
@@ -150,15 +229,6 @@ __global__ void transpose_a_kernel(const uint16_t *__restrict__ A, int K, int r,
 // order for G and H, so any consistent assignment is exact.
 constexpr int kDownWarps = 8;
 
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
-                                               uint32_t a2, uint32_t a3, uint32_t b0,
-                                               uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
 
 template <int NT>  // n8 tiles: r_pad / 8
 __global__ void __launch_bounds__(kDownWarps * 32) lora_down_kernel(
@@ -242,27 +312,40 @@ cudaError_t launch_lora_down(const uint16_t *G, int64_t M, int C, const uint16_t
 }
 
 int skinny_splits(int64_t M, int C) {
-  const int coltiles = (C + kSkinnyCols - 1) / kSkinnyCols;
+  const int coltiles = (C + kGradCols - 1) / kGradCols;
   int64_t sp = (296 + coltiles - 1) / coltiles;
-  int64_t maxsp = M / 64;
-  if (maxsp < 1) maxsp = 1;
+  int64_t maxsp = (M + kGradRows - 1) / kGradRows;
   if (sp > maxsp) sp = maxsp;
   if (sp < 1) sp = 1;
   return (int)sp;
 }
 
+template <int RPT>
+static cudaError_t launch_grad(dim3 grid, const uint16_t *G, int64_t M, int C, const float *V,
+                               int r, int64_t rps, float *part, cudaStream_t s) {
+  const int smem = grad_smem_bytes(RPT * 8);
+  static bool set = false;
+  if (!set) {
+    cudaError_t e = cudaFuncSetAttribute(lora_grad_tc_kernel<RPT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    set = true;
+  }
+  lora_grad_tc_kernel<RPT><<<grid, kGradThreads, smem, s>>>(G, M, C, V, r, rps, part);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_skinny(const uint16_t *G, int64_t M, int C, const float *V, int r, int RP,
                           float *part, int splits, cudaStream_t s) {
-  const int64_t rps = (M + splits - 1) / splits;
-  dim3 grid((C + kSkinnyCols - 1) / kSkinnyCols, splits);
+  const int64_t rps = ((M + splits - 1) / splits + kGradRows - 1) / kGradRows * kGradRows;
+  dim3 grid((C + kGradCols - 1) / kGradCols, splits);
   switch (RP) {
-    case 16: skinny_tn_kernel<16><<<grid, kSkinnyThreads, 0, s>>>(G, M, C, V, r, rps, part); break;
-    case 32: skinny_tn_kernel<32><<<grid, kSkinnyThreads, 0, s>>>(G, M, C, V, r, rps, part); break;
-    case 48: skinny_tn_kernel<48><<<grid, kSkinnyThreads, 0, s>>>(G, M, C, V, r, rps, part); break;
-    case 64: skinny_tn_kernel<64><<<grid, kSkinnyThreads, 0, s>>>(G, M, C, V, r, rps, part); break;
+    case 16: return launch_grad<2>(grid, G, M, C, V, r, rps, part, s);
+    case 32: return launch_grad<4>(grid, G, M, C, V, r, rps, part, s);
+    case 48: return launch_grad<6>(grid, G, M, C, V, r, rps, part, s);
+    case 64: return launch_grad<8>(grid, G, M, C, V, r, rps, part, s);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_reduce_parts(const float *part, int splits, int C, int RP, int r, float sc,
