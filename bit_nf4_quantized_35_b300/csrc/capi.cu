@@ -318,13 +318,14 @@ qlora_status qlora_linear_fwd(const qlora_nf4_weight *w, const uint16_t *x, int6
     return cuda_status(launch_gemv(a, num_sms_current(), s));
   }
   const int RP = round_up(r, 16);
+  const int bn = gemm_pick_bn((int)M, N, false, num_sms_current());
   uint16_t *lb = reinterpret_cast<uint16_t *>(wsb + L.lb);
   cudaError_t e = launch_lora_down(x, M, K, A, r, sc, t_save, lb, RP, num_sms_current(), s);
   if (e != cudaSuccess) return QLORA_ERR_CUDA;
   CUtensorMap tmA, tmL1, tmL2;
   if (!make_tmap(&tmA, x, K, M, (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tmap(&tmL1, lb, RP, M, (uint64_t)RP * 2, 16, 128, CU_TENSOR_MAP_SWIZZLE_32B) ||
-      !make_tmap(&tmL2, B, r, N, (uint64_t)r * 2, 16, 128, CU_TENSOR_MAP_SWIZZLE_32B))
+      !make_tmap(&tmL2, B, r, N, (uint64_t)r * 2, 16, bn / 2, CU_TENSOR_MAP_SWIZZLE_32B))
     return QLORA_ERR_CUDA;
   GemmArgs g{};
   g.packed = w->packed;
@@ -344,6 +345,7 @@ qlora_status qlora_linear_fwd(const qlora_nf4_weight *w, const uint16_t *x, int6
   g.out_bf16 = y_dtype == QLORA_BF16;
   g.stages = gemm_pick_stages(RP);
   g.status = reinterpret_cast<int *>(wsb + L.status);
+  g.bn = bn;
   set_block_constants(g, w);
   return cuda_status(launch_gemm(false, tmA, tmL1, tmL2, g, s));
 }
@@ -386,10 +388,11 @@ qlora_status qlora_linear_bwd(const qlora_nf4_weight *w, const uint16_t *x, cons
   // u = dY . B (fp32, for dA) and bf16(s . u) (operand of the dX GEMM's rank-r MMAs)
   e = launch_lora_down(dY, M, N, Bt, r, sc, u, lb, RP, nsm, s);
   if (e != cudaSuccess) return QLORA_ERR_CUDA;
+  const int bn = gemm_pick_bn((int)M, K, true, nsm);
   CUtensorMap tmA, tmL1, tmL2;
   if (!make_tmap(&tmA, dY, N, M, (uint64_t)N * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tmap(&tmL1, lb, RP, M, (uint64_t)RP * 2, 16, 128, CU_TENSOR_MAP_SWIZZLE_32B) ||
-      !make_tmap(&tmL2, At, RP, K, (uint64_t)RP * 2, 16, 128, CU_TENSOR_MAP_SWIZZLE_32B))
+      !make_tmap(&tmL2, At, RP, K, (uint64_t)RP * 2, 16, bn / 2, CU_TENSOR_MAP_SWIZZLE_32B))
     return QLORA_ERR_CUDA;
   GemmArgs g{};
   g.packed = w->packed;
@@ -409,6 +412,7 @@ qlora_status qlora_linear_bwd(const qlora_nf4_weight *w, const uint16_t *x, cons
   g.out_bf16 = dx_dtype == QLORA_BF16;
   g.stages = gemm_pick_stages(RP);
   g.status = reinterpret_cast<int *>(wsb + L.status);
+  g.bn = bn;
   set_block_constants(g, w);
   e = launch_gemm(true, tmA, tmL1, tmL2, g, s);
   if (e != cudaSuccess) return QLORA_ERR_CUDA;

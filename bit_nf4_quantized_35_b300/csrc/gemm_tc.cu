@@ -139,8 +139,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t rank = cluster_rank();
   const bool leader = rank == 0;
   const int m0 = (blockIdx.x >> 1) * (2 * GBM) + (int)rank * GBM;  // this CTA's rows
-  const int c0 = blockIdx.y * GBN;                                 // pair's output columns
-  const int cb0 = c0 + (int)rank * kHalfN;                         // this CTA's B half
+  const int BN = p.bn, HN = p.bn / 2;  // pair tile columns / this CTA's B rows
+  const int c0 = blockIdx.y * BN;                                  // pair's output columns
+  const int cb0 = c0 + (int)rank * HN;                             // this CTA's B half
   const int num_k = (p.kdim + GBK - 1) / GBK;
 
   if (threadIdx.x == 0) {
@@ -201,14 +202,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       qstep = 64 * (p.wcols >> 1);
       bstep = 64 * kbr;
     }
+    const bool row_used = rowi < HN;  // rows past the pair tile's half are not read
     auto fetch_k = [&](int kb) -> Fetch {
       const bool in_k = kb < num_k;
       const int kbc = in_k ? kb : num_k - 1;
       bool valid;
       if (!kDx)
-        valid = in_k && n_fixed < p.wrows;
+        valid = in_k && row_used && n_fixed < p.wrows;
       else
-        valid = in_k && (int64_t)kbc * GBK + nl < p.wrows && kcol_fixed < p.wcols;
+        valid = in_k && row_used && (int64_t)kbc * GBK + nl < p.wrows && kcol_fixed < p.wcols;
       return fetch_block(p, valid ? q0 + kbc * qstep : 0, valid ? b0 + kbc * bstep : 0, valid);
     };
     // Three-slot ring of prefetched blocks, indexed by compile-time
@@ -226,7 +228,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const int stage = kb % S;
           const uint32_t ph = (uint32_t)(kb / S) & 1u;
           const bool ok = mbar_wait_bounded(empty_bar(stage), ph ^ 1, cta_err, p.status);
-          if (ok) dequant_store_row(p, f[u], smem0 + stage * SB + kABytes + row_off, swz);
+          if (ok && row_used) dequant_store_row(p, f[u], smem0 + stage * SB + kABytes + row_off, swz);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(full_bar(stage));
@@ -237,11 +239,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ---------------------------------------------------------- epilogue
     mbar_wait_bounded(acc_bar, 0, cta_err, p.status);
     tc_fence_after();
-    // 16 warps: warp w reads TMEM lanes 32*(w%4).. and columns [64*(w/4), +64)
+    // 16 warps: warp w reads TMEM lanes 32*(w%4).. and columns [64*(w/4), +64) of BN
     const int quarter = warp & 3, hcol = warp >> 2;
     const int row = m0 + quarter * 32 + lane;
     for (int ch = 0; ch < 2; ++ch) {
       const int col = hcol * 64 + ch * 32;
+      if (col >= BN) break;  // warp-uniform
       uint32_t v[32];
       tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + col, v);
       tmem_ld_wait();
@@ -276,7 +279,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // --------------------------------------------------------- TMA producer
     if (lane == 0) {
       const int ncb = RP / 16;
-      mbar_arrive_expect_tx(up_bar, ncb * (GBM + kHalfN) * 32);
+      mbar_arrive_expect_tx(up_bar, ncb * (GBM + HN) * 32);
       for (int cb = 0; cb < ncb; ++cb) {
         tma_load_2d(upa_u + cb * (GBM * 32), &tmL1, up_bar, cb * 16, m0);
         tma_load_2d(upb_u + cb * (kHalfN * 32), &tmL2, up_bar, cb * 16, cb0);
@@ -306,8 +309,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (leader) {
     // ------------------------------------------------- MMA issuer (leader)
     if (lane == 0) {
-      constexpr uint32_t idesc_main = make_idesc_bf16(2 * GBM, GBN, kDx);
-      constexpr uint32_t idesc_up = make_idesc_bf16(2 * GBM, GBN, false);
+      const uint32_t idesc_main = make_idesc_bf16(2 * GBM, BN, kDx);
+      const uint32_t idesc_up = make_idesc_bf16(2 * GBM, BN, false);
       bool ok = mbar_wait_bounded(up_bar, 0, cta_err, p.status);
       if (ok) {
         // LoRA term first: D = (s.t) . B^T  (or (s.u) . A for dX)
@@ -391,7 +394,7 @@ cudaError_t launch_gemm(bool dx, const CUtensorMap &tmA, const CUtensorMap &tmL1
     attr_set[dx] = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * ((args.M + 2 * GBM - 1) / (2 * GBM)), (args.out_cols + GBN - 1) / GBN, 1);
+  cfg.gridDim = dim3(2 * ((args.M + 2 * GBM - 1) / (2 * GBM)), (args.out_cols + args.bn - 1) / args.bn, 1);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -408,6 +411,30 @@ cudaError_t launch_gemm(bool dx, const CUtensorMap &tmA, const CUtensorMap &tmL1
     e = cudaLaunchKernelEx(&cfg, qlora_gemm_kernel<false>, tmA, tmL1, tmL2, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+// Pair-tile width: the candidate minimising (waves of tiles over the CTA
+// pairs) x (tile width + a fixed per-tile cost of ~40 columns).  The dX
+// operand is MN-major in 64-column atoms per CTA, so there only 128 or 256.
+int gemm_pick_bn(int M, int out_cols, bool dx, int num_sms) {
+  static const int fwd_c[] = {256, 224, 192, 160, 128};
+  static const int dx_c[] = {256, 128};
+  const int *c = dx ? dx_c : fwd_c;
+  const int nc = dx ? 2 : 5;
+  const int pairs = num_sms / 2 > 0 ? num_sms / 2 : 1;
+  const int mp = (M + 2 * GBM - 1) / (2 * GBM);
+  int best = 256;
+  long best_cost = -1;
+  for (int i = 0; i < nc; ++i) {
+    const long tiles = (long)mp * ((out_cols + c[i] - 1) / c[i]);
+    const long waves = (tiles + pairs - 1) / pairs;
+    const long cost = waves * (c[i] + 40);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = c[i];
+    }
+  }
+  return best;
 }
 
 int gemm_pick_stages(int r_pad) {

@@ -33,10 +33,12 @@ struct GemmArgs {
   int cdiv;
   int use_code;
   int cshift;  // log2(cdiv): cdiv is 1 or a power of two
+  int bn;      // output columns per CTA pair: 128..256, multiple of 32 (set by the launcher)
 };
 cudaError_t launch_gemm(bool dx, const CUtensorMap &tmA, const CUtensorMap &tmL1,
                         const CUtensorMap &tmL2, const GemmArgs &args, cudaStream_t s);
 int gemm_pick_stages(int r_pad);
+int gemm_pick_bn(int M, int out_cols, bool dx, int num_sms);
 
 // Split-K decode GEMV (gemv.cu).
 struct GemvArgs {

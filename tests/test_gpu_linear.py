@@ -173,3 +173,36 @@ def test_gate_decode_gemv_full_size(M):
     y_ref, _ = oracle.linear_fwd(d["x"].float().numpy(), w_hat, d["A"].float().numpy(),
                                  d["B"].float().numpy(), shape.alpha)
     assert_close(to_np_f32(y), y_ref, f"y gate decode M={M}")
+
+
+def test_gate_prefill_forward_full_size():
+    """gate_proj 14336x4096 at 2048 tokens: the widest layer of the layer set
+    (its pair tiles are 224 columns wide), y checked on sampled rows."""
+    shape = inputs.LinearShape("gate_proj_14336x4096_M2048_r16", N=14336, K=4096, M=2048, r=16,
+                               alpha=32.0)
+    d, g, q, w_hat = _prep(shape, with_dy=False)
+    ws = _ws(shape)
+    y, t = _fwd(shape, g, q, ws)
+    rows = _sample_rows(shape.M, n=16, seed=3)
+    y_ref, t_ref = oracle.linear_fwd(d["x"].float().numpy(), w_hat, d["A"].float().numpy(),
+                                     d["B"].float().numpy(), shape.alpha, rows=rows)
+    assert_close(to_np_f32(y)[rows], y_ref, "y gate sampled rows")
+
+
+def test_kproj_backward_full_size():
+    """k_proj 1024x4096 at 2048 tokens: dX on sampled rows, dA and dB in full."""
+    shape = inputs.LinearShape("k_proj_1024x4096_M2048_r16", N=1024, K=4096, M=2048, r=16,
+                               alpha=32.0)
+    d, g, q, w_hat = _prep(shape)
+    ws = _ws(shape)
+    y, t = _fwd(shape, g, q, ws)
+    dX, dA, dB = capi.linear_bwd(q, g["x"], g["dY"], g["A"], g["B"], shape.alpha, ws, t_saved=t)
+    torch.cuda.synchronize()
+    assert ws.device_status() == 0
+    rows = _sample_rows(shape.M, n=16, seed=4)
+    ref = oracle.linear_bwd(d["x"].float().numpy(), d["dY"].float().numpy(), w_hat,
+                            d["A"].float().numpy(), d["B"].float().numpy(), shape.alpha,
+                            rows=rows)
+    assert_close(to_np_f32(dX)[rows], ref["dX"], "dX k_proj sampled rows")
+    assert_close(to_np_f32(dA), ref["dA"], "dA k_proj")
+    assert_close(to_np_f32(dB), ref["dB"], "dB k_proj")
