@@ -8,26 +8,32 @@
 // where t = x A^T (u = dY B) comes in as bf16(s.t) from a small tensor-core
 // pre-pass (lora_grad.cu) and seeds the accumulator before the main loop.
 //
-// CTA pairs (a cluster of 2) share one 256 x 256 output tile through
+// CTA pairs (a cluster of 2) share one 256 x BN output tile through
 // tcgen05 cta_group::2: CTA r owns rows [128r, 128r+128) of the tile and
-// half of the B operand (output columns [128r, 128r+128)); one thread of the
-// leader CTA issues every MMA for both.  Contraction step 64.
-// Per CTA, 576 threads:
+// half of the B operand (BN/2 output columns); one thread of the leader CTA
+// issues every MMA for both.  Contraction step 64.
+//
+// The kernel is persistent: one cluster per SM pair walks the output tiles
+// cid, cid + clusters, ... (row tiles fastest, so the clusters that run at
+// the same time share weight columns in L2).  Stage ring positions and
+// barrier phases run on across tiles, and TMEM holds two accumulators, so
+// the epilogue of one tile overlaps the main loop of the next.
+// Per CTA, 704 threads:
 //   warps 0-15 dequantising producers in 4 groups that take the stages
 //              round-robin; a thread owns one B row of its group's stage and
 //              turns its 64 packed nibbles into bf16 through the per-block
 //              table T[i] = bf16(c_i * a_hat) indexed with byte permutes; the
 //              values go straight into the 128-byte-swizzled operand layout
-//              the tensor core reads (K-major forward, MN-major dX).  After
-//              the main loop the same warps run the epilogue.
-//   warp 16    TMA: this CTA's 128 activation rows per stage; its halves of
-//              the two rank-r LoRA operands once.
-//   warp 17    TMEM allocation (both CTAs); in the leader the single MMA
+//              the tensor core reads (K-major forward, MN-major dX).
+//   warps 16-19 epilogue: TMEM -> registers -> global, one row per thread.
+//   warp 20    TMA: this CTA's 128 activation rows per stage; its halves of
+//              the two rank-r LoRA operands once per tile (double-buffered).
+//   warp 21    TMEM allocation (both CTAs); in the leader the single MMA
 //              issuer, in the peer a relay that forwards "stage ready" to the
-//              leader's barrier.
-// The leader first issues r_pad/16 MMAs (256 x 256 x 16) for the LoRA term,
-// then 4 per stage for the base product, all into TMEM columns [0, 256) of
-// both CTAs; the epilogue moves TMEM -> registers -> global.
+//              leader's barriers.
+// Per tile the leader first issues r_pad/16 MMAs (256 x BN x 16) for the
+// LoRA term, then 4 per stage for the base product, into TMEM columns
+// [256 b, 256 b + BN) of both CTAs, b alternating between tiles.
 //
 // Each SM dequantises 128 x 64 weights per stage for 2 x 128 x 256 x 64
 // MMA work, half of what a single-CTA 128 x 256 tile needs; the integer
@@ -47,8 +53,11 @@ constexpr int GBK = 64;
 constexpr int kHalfN = GBN / 2;
 constexpr int kProdGroups = 4;                     // producer groups, stages round-robin
 constexpr int kProdWarps = 4 * kProdGroups;        // 16 warps: one thread per B row per group
-constexpr int kTmaWarp = kProdWarps, kMmaWarp = kProdWarps + 1;
-constexpr int kGemmThreads = (kProdWarps + 2) * 32;  // 576
+constexpr int kEpiWarp0 = kProdWarps;               // 4 epilogue warps (TMEM lane quarters)
+constexpr int kTmaWarp = kProdWarps + 4, kMmaWarp = kProdWarps + 5;
+constexpr int kGemmThreads = (kProdWarps + 6) * 32;  // 704
+constexpr int kAccCols = 256;                        // TMEM columns per accumulator
+static_assert(kEpiWarp0 % 4 == 0, "epilogue warp q must own TMEM lane quarter q");
 constexpr int kABytes = GBM * GBK * 2;     // 16 KB
 constexpr int kBBytes = kHalfN * GBK * 2;  // 16 KB (this CTA's half of B)
 
@@ -56,8 +65,8 @@ __host__ __device__ inline int gemm_stage_bytes(int) { return kABytes + kBBytes;
 __host__ __device__ inline int gemm_upa_bytes(int r_pad) { return (r_pad / 16) * GBM * 32; }
 __host__ __device__ inline int gemm_upb_bytes(int r_pad) { return (r_pad / 16) * kHalfN * 32; }
 __host__ inline int gemm_smem_bytes(int stages, int r_pad) {
-  return 1024 + stages * gemm_stage_bytes(r_pad) + gemm_upa_bytes(r_pad) + gemm_upb_bytes(r_pad) +
-         256;
+  return 1024 + stages * gemm_stage_bytes(r_pad) +
+         2 * (gemm_upa_bytes(r_pad) + gemm_upb_bytes(r_pad)) + 256;
 }
 
 // Raw packed bytes + block constant of one 64-block.
@@ -112,6 +121,32 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Output tile `tile` of the (row tiles) x (column tiles) grid, row tiles
+// fastest.
+struct TileSched {
+  int mp, total, cid, ncl, count;  // row tiles, tiles, this cluster, clusters, my tiles
+  __device__ TileSched(const GemmArgs &p) {
+    mp = (p.M + 2 * GBM - 1) / (2 * GBM);
+    total = mp * ((p.out_cols + p.bn - 1) / p.bn);
+    cid = (int)(blockIdx.x >> 1);
+    ncl = (int)(gridDim.x >> 1);
+    count = cid < total ? (total - cid + ncl - 1) / ncl : 0;
+  }
+  __device__ void coords(int it, int &mt, int &nt) const {
+    const int tile = cid + it * ncl;
+    nt = tile / mp;
+    mt = tile - nt * mp;
+  }
+};
+
+// One producer thread's walk over its group's stages: every 4th position
+// of the cluster's stage sequence (tile it, contraction block kb).
+struct ProdCursor {
+  int it, kb;
+  bool live, rowok;
+  int64_t q0, b0;  // packed-byte offset / block index of this row's stage 0
+};
+
 template <bool kDx>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     qlora_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -122,27 +157,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int S = p.stages, RP = p.r_pad;
   const int SB = gemm_stage_bytes(RP);
-  uint8_t *upa = smem + S * SB;
-  uint8_t *upb = upa + gemm_upa_bytes(RP);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(upb + gemm_upb_bytes(RP));
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 2);
+  const int UPA = gemm_upa_bytes(RP), UPB = gemm_upb_bytes(RP);
+  uint8_t *upa = smem + S * SB;           // 2 buffers
+  uint8_t *upb = upa + 2 * UPA;           // 2 buffers
+  uint64_t *bars = reinterpret_cast<uint64_t *>(upb + 2 * UPB);
+  // bars: full[S], empty[S], up_full[2], up_empty[2], acc_full[2], acc_empty[2]
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 8);
   const uint32_t cta_err = smem_u32(tmem_slot + 1);  // shared address of the error flag
 
   const uint32_t smem0 = smem_u32(smem);
   const uint32_t upa_u = smem_u32(upa), upb_u = smem_u32(upb);
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
   auto empty_bar = [&](int s) { return smem_u32(bars + S + s); };
-  const uint32_t up_bar = smem_u32(bars + 2 * S);
-  const uint32_t acc_bar = smem_u32(bars + 2 * S + 1);
+  auto up_full = [&](int b) { return smem_u32(bars + 2 * S + b); };
+  auto up_empty = [&](int b) { return smem_u32(bars + 2 * S + 2 + b); };
+  auto acc_full = [&](int b) { return smem_u32(bars + 2 * S + 4 + b); };
+  auto acc_empty = [&](int b) { return smem_u32(bars + 2 * S + 6 + b); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
   const bool leader = rank == 0;
-  const int m0 = (blockIdx.x >> 1) * (2 * GBM) + (int)rank * GBM;  // this CTA's rows
   const int BN = p.bn, HN = p.bn / 2;  // pair tile columns / this CTA's B rows
-  const int c0 = blockIdx.y * BN;                                  // pair's output columns
-  const int cb0 = c0 + (int)rank * HN;                             // this CTA's B half
   const int num_k = (p.kdim + GBK - 1) / GBK;
+  const TileSched ts(p);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -150,8 +187,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(full_bar(s), 1 + 4 + (leader ? 1 : 0));
       mbar_init(empty_bar(s), 1);  // multicast tcgen05.commit
     }
-    mbar_init(up_bar, 1 + (leader ? 1 : 0));  // TMA arrive (+ the peer's relay)
-    mbar_init(acc_bar, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(up_full(b), 1 + (leader ? 1 : 0));  // TMA arrive (+ the peer's relay)
+      mbar_init(up_empty(b), 1);                     // multicast tcgen05.commit
+      mbar_init(acc_full(b), 1);                     // multicast tcgen05.commit
+      mbar_init(acc_empty(b), leader ? 8 : 1);       // 4 epilogue warps of each CTA
+    }
     st_shared_volatile(cta_err, 0u);
     fence_barrier_init();
   }
@@ -160,147 +201,218 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tmL1);
     tma_prefetch_desc(&tmL2);
   }
-  if (warp == kMmaWarp) tmem_alloc2(smem_u32(tmem_slot), 256);
+  if (warp == kMmaWarp) tmem_alloc2(smem_u32(tmem_slot), 2 * kAccCols);
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // both CTAs' barriers initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = ld_shared_volatile(smem_u32(tmem_slot));
+  const int total_stages = ts.count * num_k;
 
   if (warp < kProdWarps) {
     // ------------------------------------------------ dequantising producers
-    // Group `grp` (4 warps) produces stages kb = grp, grp + 4, ...; within a
-    // group thread `rowi` owns one 128-byte row of this CTA's B half.
+    // Group `grp` (4 warps) produces the cluster's stages g = grp, grp + 4,
+    // ...; within a group thread `rowi` owns one 128-byte row of this CTA's
+    // B half.
     const int grp = threadIdx.x >> 7;
     const int rowi = threadIdx.x & 127;
-    int64_t n_fixed = 0, kcol_fixed = 0;
+    const bool row_used = rowi < HN;  // rows past the pair tile's half are not read
     uint32_t row_off, swz;
-    int nl = 0;
+    int nl = 0, bsub = 0;
     if (!kDx) {
-      n_fixed = (int64_t)cb0 + rowi;  // weight row = output column
       row_off = (rowi >> 3) * 1024 + (rowi & 7) * 128;
       swz = rowi & 7;
     } else {
-      const int bsub = rowi >> 6;  // which 64-column atom of this CTA's 128 outputs
-      nl = rowi & 63;              // contraction row inside the stage
-      kcol_fixed = (int64_t)cb0 + 64 * bsub;
+      bsub = rowi >> 6;  // which 64-column atom of this CTA's outputs
+      nl = rowi & 63;    // contraction row inside the stage
       row_off = bsub * 8192 + (nl >> 3) * 1024 + (nl & 7) * 128;
       swz = nl & 7;
     }
-    // Byte offset / block index of this thread's 32 packed bytes at stage 0
-    // and their step per stage (64 contraction elements).
+    // Step per stage (64 contraction elements) of the packed-byte offset and
+    // of the block index.
     const int64_t kbr = p.wcols >> 6;  // blocks per weight row
-    int64_t q0, b0, qstep, bstep;
-    if (!kDx) {
-      q0 = n_fixed * (p.wcols >> 1);  // row n, columns [0, 64)
-      b0 = n_fixed * kbr;
-      qstep = 32;
-      bstep = 1;
-    } else {
-      q0 = (int64_t)nl * (p.wcols >> 1) + (kcol_fixed >> 1);
-      b0 = (int64_t)nl * kbr + (kcol_fixed >> 6);
-      qstep = 64 * (p.wcols >> 1);
-      bstep = 64 * kbr;
-    }
-    const bool row_used = rowi < HN;  // rows past the pair tile's half are not read
-    auto fetch_k = [&](int kb) -> Fetch {
-      const bool in_k = kb < num_k;
-      const int kbc = in_k ? kb : num_k - 1;
-      bool valid;
-      if (!kDx)
-        valid = in_k && row_used && n_fixed < p.wrows;
-      else
-        valid = in_k && row_used && (int64_t)kbc * GBK + nl < p.wrows && kcol_fixed < p.wcols;
-      return fetch_block(p, valid ? q0 + kbc * qstep : 0, valid ? b0 + kbc * bstep : 0, valid);
+    const int64_t qstep = kDx ? 64 * (p.wcols >> 1) : 32;
+    const int64_t bstep = kDx ? 64 * kbr : 1;
+    auto set_tile = [&](ProdCursor &c) {
+      c.live = c.it < ts.count;
+      int mt, nt;
+      ts.coords(c.live ? c.it : 0, mt, nt);
+      const int64_t cb0 = (int64_t)nt * BN + (int64_t)rank * HN;
+      if (!kDx) {
+        const int64_t n = cb0 + rowi;  // weight row = output column
+        c.rowok = row_used && n < p.wrows;
+        c.q0 = n * (p.wcols >> 1);
+        c.b0 = n * kbr;
+      } else {
+        const int64_t kcol = cb0 + 64 * bsub;
+        c.rowok = row_used && kcol < p.wcols;
+        c.q0 = (int64_t)nl * (p.wcols >> 1) + (kcol >> 1);
+        c.b0 = (int64_t)nl * kbr + (kcol >> 6);
+      }
     };
+    auto advance = [&](ProdCursor &c) {
+      c.kb += kProdGroups;
+      if (c.kb >= num_k) {
+        while (c.kb >= num_k) {
+          c.kb -= num_k;
+          ++c.it;
+        }
+        set_tile(c);
+      }
+    };
+    auto fetch = [&](const ProdCursor &c) -> Fetch {
+      bool valid = c.live && c.rowok;
+      if (kDx) valid = valid && (int64_t)c.kb * GBK + nl < p.wrows;
+      return fetch_block(p, valid ? c.q0 + c.kb * qstep : 0, valid ? c.b0 + c.kb * bstep : 0,
+                         valid);
+    };
+    ProdCursor cf;
+    cf.it = 0;
+    cf.kb = grp;
+    while (cf.kb >= num_k) {
+      cf.kb -= num_k;
+      ++cf.it;
+    }
+    set_tile(cf);
     // Three-slot ring of prefetched blocks, indexed by compile-time
     // constants only: this group's i-th stage consumes slot i % 3 and
     // refills slot (i + 2) % 3, so no register ever copies a load in flight.
     Fetch f[3];
-    f[0] = fetch_k(grp);
-    f[1] = fetch_k(grp + kProdGroups);
-    for (int kb0 = grp; kb0 < num_k; kb0 += 3 * kProdGroups) {
+    f[0] = fetch(cf);
+    advance(cf);
+    f[1] = fetch(cf);
+    advance(cf);
+    int stage = grp;
+    uint32_t ph = 0;
+    while (stage >= S) {
+      stage -= S;
+      ph ^= 1u;
+    }
+    for (int g0 = grp; g0 < total_stages; g0 += 3 * kProdGroups) {
 #pragma unroll
       for (int u = 0; u < 3; ++u) {
-        const int kb = kb0 + u * kProdGroups;
-        if (kb < num_k) {
-          f[(u + 2) % 3] = fetch_k(kb + 2 * kProdGroups);
-          const int stage = kb % S;
-          const uint32_t ph = (uint32_t)(kb / S) & 1u;
+        if (g0 + u * kProdGroups < total_stages) {
+          f[(u + 2) % 3] = fetch(cf);
+          advance(cf);
           const bool ok = mbar_wait_bounded(empty_bar(stage), ph ^ 1, cta_err, p.status);
           if (ok && row_used) dequant_store_row(p, f[u], smem0 + stage * SB + kABytes + row_off, swz);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(full_bar(stage));
+          stage += kProdGroups;
+          while (stage >= S) {
+            stage -= S;
+            ph ^= 1u;
+          }
         }
       }
     }
-
+  } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
     // ---------------------------------------------------------- epilogue
-    mbar_wait_bounded(acc_bar, 0, cta_err, p.status);
-    tc_fence_after();
-    // 16 warps: warp w reads TMEM lanes 32*(w%4).. and columns [64*(w/4), +64) of BN
-    const int quarter = warp & 3, hcol = warp >> 2;
-    const int row = m0 + quarter * 32 + lane;
-    for (int ch = 0; ch < 2; ++ch) {
-      const int col = hcol * 64 + ch * 32;
-      if (col >= BN) break;  // warp-uniform
-      uint32_t v[32];
-      tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + col, v);
-      tmem_ld_wait();
-      const int gcol = c0 + col;
-      if (row < p.M && gcol < p.out_cols) {
-        const bool full = gcol + 32 <= p.out_cols;
-        if (p.out_bf16) {
-          uint16_t *dst = reinterpret_cast<uint16_t *>(p.out) + (int64_t)row * p.out_cols + gcol;
+    // Warp q reads TMEM lanes [32q, 32q + 32): one output row per thread.
+    const int quarter = warp & 3;
+    for (int it = 0; it < ts.count; ++it) {
+      const int b = it & 1;
+      const bool ok = mbar_wait_bounded(acc_full(b), (uint32_t)(it >> 1) & 1u, cta_err, p.status);
+      tc_fence_after();
+      int mt, nt;
+      ts.coords(it, mt, nt);
+      const int row = mt * (2 * GBM) + (int)rank * GBM + quarter * 32 + lane;
+      const int c0 = nt * BN;
+      const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * kAccCols);
+      for (int col = 0; col < BN && ok; col += 32) {
+        uint32_t v[32];
+        tmem_ld32(tbase + col, v);
+        tmem_ld_wait();
+        const int gcol = c0 + col;
+        if (row < p.M && gcol < p.out_cols) {
+          const bool full = gcol + 32 <= p.out_cols;
+          if (p.out_bf16) {
+            uint16_t *dst = reinterpret_cast<uint16_t *>(p.out) + (int64_t)row * p.out_cols + gcol;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            if (full || gcol + 8 * q < p.out_cols) {
-              uint4 o;
-              o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
-              o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
-              o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
-              o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
-              *reinterpret_cast<uint4 *>(dst + 8 * q) = o;
+            for (int q = 0; q < 4; ++q) {
+              if (full || gcol + 8 * q < p.out_cols) {
+                uint4 o;
+                o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
+                o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
+                o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
+                o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
+                *reinterpret_cast<uint4 *>(dst + 8 * q) = o;
+              }
+            }
+          } else {
+            float *dst = reinterpret_cast<float *>(p.out) + (int64_t)row * p.out_cols + gcol;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              if (full || gcol + 4 * q < p.out_cols)
+                *reinterpret_cast<uint4 *>(dst + 4 * q) =
+                    make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
             }
           }
-        } else {
-          float *dst = reinterpret_cast<float *>(p.out) + (int64_t)row * p.out_cols + gcol;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            if (full || gcol + 4 * q < p.out_cols)
-              *reinterpret_cast<uint4 *>(dst + 4 * q) =
-                  make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-          }
         }
+      }
+      // This warp is done reading accumulator b: free it for tile it + 2.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader)
+          mbar_arrive(acc_empty(b));
+        else
+          mbar_arrive_remote(mapa_shared(acc_empty(b), 0));
       }
     }
   } else if (warp == kTmaWarp) {
     // --------------------------------------------------------- TMA producer
     if (lane == 0) {
       const int ncb = RP / 16;
-      mbar_arrive_expect_tx(up_bar, ncb * (GBM + HN) * 32);
-      for (int cb = 0; cb < ncb; ++cb) {
-        tma_load_2d(upa_u + cb * (GBM * 32), &tmL1, up_bar, cb * 16, m0);
-        tma_load_2d(upb_u + cb * (kHalfN * 32), &tmL2, up_bar, cb * 16, cb0);
-      }
+      // LoRA operand halves of tile j into buffer j & 1, one tile ahead.
+      auto issue_up = [&](int j) {
+        const int b = j & 1;
+        if (!mbar_wait_bounded(up_empty(b), ((uint32_t)(j >> 1) & 1u) ^ 1u, cta_err, p.status))
+          return false;
+        int mt, nt;
+        ts.coords(j, mt, nt);
+        const int m0 = mt * (2 * GBM) + (int)rank * GBM;
+        const int cb0 = nt * BN + (int)rank * HN;
+        mbar_arrive_expect_tx(up_full(b), ncb * (GBM + HN) * 32);
+        for (int cb = 0; cb < ncb; ++cb) {
+          tma_load_2d(upa_u + b * UPA + cb * (GBM * 32), &tmL1, up_full(b), cb * 16, m0);
+          tma_load_2d(upb_u + b * UPB + cb * (kHalfN * 32), &tmL2, up_full(b), cb * 16, cb0);
+        }
+        return true;
+      };
       int stage = 0;
       uint32_t ph = 0;
-      int issued = 0;
-      for (int kb = 0; kb < num_k; ++kb) {
-        if (!mbar_wait_bounded(empty_bar(stage), ph ^ 1, cta_err, p.status)) break;
-        const uint32_t a_dst = smem0 + stage * SB;
-        mbar_arrive_expect_tx(full_bar(stage), kABytes);
-        tma_load_2d(a_dst, &tmA, full_bar(stage), kb * GBK, m0);
-        ++issued;
-        if (++stage == S) {
-          stage = 0;
-          ph ^= 1;
+      int issued = 0, up_issued = 0;
+      bool ok = true;
+      for (int it = 0; it < ts.count && ok; ++it) {
+        if (it == 0) {
+          ok = issue_up(0);
+          up_issued += ok;
+        }
+        if (ok && it + 1 < ts.count) {
+          ok = issue_up(it + 1);
+          up_issued += ok;
+        }
+        int mt, nt;
+        ts.coords(it, mt, nt);
+        const int m0 = mt * (2 * GBM) + (int)rank * GBM;
+        for (int kb = 0; kb < num_k && ok; ++kb) {
+          ok = mbar_wait_bounded(empty_bar(stage), ph ^ 1, cta_err, p.status);
+          if (!ok) break;
+          mbar_arrive_expect_tx(full_bar(stage), kABytes);
+          tma_load_2d(smem0 + stage * SB, &tmA, full_bar(stage), kb * GBK, m0);
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            ph ^= 1;
+          }
         }
       }
       if (ld_shared_volatile(cta_err)) {
         // Error path: let every issued copy land before the CTA exits.
-        mbar_drain(up_bar, 0);
+        for (int j = up_issued > 2 ? up_issued - 2 : 0; j < up_issued; ++j)
+          mbar_drain(up_full(j & 1), (uint32_t)(j >> 1) & 1u);
         const int first = issued > S ? issued - S : 0;
         for (int i = first; i < issued; ++i) mbar_drain(full_bar(i % S), (i / S) & 1);
       }
@@ -311,57 +423,75 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       const uint32_t idesc_main = make_idesc_bf16(2 * GBM, BN, kDx);
       const uint32_t idesc_up = make_idesc_bf16(2 * GBM, BN, false);
-      bool ok = mbar_wait_bounded(up_bar, 0, cta_err, p.status);
-      if (ok) {
-        // LoRA term first: D = (s.t) . B^T  (or (s.u) . A for dX)
-        tc_fence_after();
-        for (int cb = 0; cb < RP / 16; ++cb) {
-          const uint64_t ad = make_sdesc(upa_u + cb * (GBM * 32), 16, 256, kSwz32);
-          const uint64_t bd = make_sdesc(upb_u + cb * (kHalfN * 32), 16, 256, kSwz32);
-          tc_mma2(tmem, ad, bd, idesc_up, cb > 0 ? 1u : 0u);
-        }
-      }
       int stage = 0;
       uint32_t ph = 0;
-      for (int kb = 0; kb < num_k && ok; ++kb) {
-        ok = mbar_wait_bounded(full_bar(stage), ph, cta_err, p.status);
+      bool ok = true;
+      int last_acc = -1;
+      for (int it = 0; it < ts.count && ok; ++it) {
+        const int b = it & 1;
+        const uint32_t use_ph = (uint32_t)(it >> 1) & 1u;
+        ok = mbar_wait_bounded(acc_empty(b), use_ph ^ 1u, cta_err, p.status);
+        if (ok) ok = mbar_wait_bounded(up_full(b), use_ph, cta_err, p.status);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t a_base = smem0 + stage * SB;
-        const uint32_t b_base = a_base + kABytes;
+        const uint32_t d = tmem + (uint32_t)(b * kAccCols);
+        // LoRA term first: D = (s.t) . B^T  (or (s.u) . A for dX)
+        for (int cb = 0; cb < RP / 16; ++cb) {
+          const uint64_t ad = make_sdesc(upa_u + b * UPA + cb * (GBM * 32), 16, 256, kSwz32);
+          const uint64_t bd = make_sdesc(upb_u + b * UPB + cb * (kHalfN * 32), 16, 256, kSwz32);
+          tc_mma2(d, ad, bd, idesc_up, cb > 0 ? 1u : 0u);
+        }
+        tc_commit2_mc(up_empty(b), 0x3);
+        for (int kb = 0; kb < num_k; ++kb) {
+          ok = mbar_wait_bounded(full_bar(stage), ph, cta_err, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t a_base = smem0 + stage * SB;
+          const uint32_t b_base = a_base + kABytes;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t ad = make_sdesc(a_base + kk * 32, 16, 1024, kSwz128);
-          const uint64_t bd = kDx ? make_sdesc(b_base + kk * 2048, 8192, 1024, kSwz128)
-                                  : make_sdesc(b_base + kk * 32, 16, 1024, kSwz128);
-          tc_mma2(tmem, ad, bd, idesc_main, 1u);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = make_sdesc(a_base + kk * 32, 16, 1024, kSwz128);
+            const uint64_t bd = kDx ? make_sdesc(b_base + kk * 2048, 8192, 1024, kSwz128)
+                                    : make_sdesc(b_base + kk * 32, 16, 1024, kSwz128);
+            tc_mma2(d, ad, bd, idesc_main, 1u);
+          }
+          tc_commit2_mc(empty_bar(stage), 0x3);
+          if (++stage == S) {
+            stage = 0;
+            ph ^= 1;
+          }
         }
-        tc_commit2_mc(empty_bar(stage), 0x3);
-        if (++stage == S) {
-          stage = 0;
-          ph ^= 1;
-        }
+        tc_commit2_mc(acc_full(b), 0x3);
+        last_acc = it;
       }
-      tc_commit2_mc(acc_bar, 0x3);
-      if (ld_shared_volatile(cta_err)) mbar_drain(acc_bar, 0);  // all issued MMAs retired
+      // Error path: every issued MMA retired before TMEM is freed.
+      if (ld_shared_volatile(cta_err) && last_acc >= 0)
+        mbar_drain(acc_full(last_acc & 1), (uint32_t)(last_acc >> 1) & 1u);
     }
     __syncwarp();
   } else {
     // ----------------------------------------------- relay (peer CTA)
-    // Forwards "this CTA's LoRA operand halves landed" and then, per stage,
-    // "this CTA's half of stage s is ready" (its TMA bytes landed and the 4
-    // warps of the producer group arrived) to the leader's barriers, in the order the
-    // leader consumes them.
+    // Forwards, per tile, "this CTA's LoRA operand halves landed" and then,
+    // per stage, "this CTA's half of stage s is ready" (its TMA bytes landed
+    // and the 4 warps of the producer group arrived) to the leader's
+    // barriers, in the order the leader consumes them.
     if (lane == 0) {
-      if (mbar_wait_bounded(up_bar, 0, cta_err, p.status)) mbar_arrive_remote(mapa_shared(up_bar, 0));
       int stage = 0;
       uint32_t ph = 0;
-      for (int kb = 0; kb < num_k; ++kb) {
-        if (!mbar_wait_bounded(full_bar(stage), ph, cta_err, p.status)) break;
-        mbar_arrive_remote(mapa_shared(full_bar(stage), 0));
-        if (++stage == S) {
-          stage = 0;
-          ph ^= 1;
+      bool ok = true;
+      for (int it = 0; it < ts.count && ok; ++it) {
+        const int b = it & 1;
+        ok = mbar_wait_bounded(up_full(b), (uint32_t)(it >> 1) & 1u, cta_err, p.status);
+        if (!ok) break;
+        mbar_arrive_remote(mapa_shared(up_full(b), 0));
+        for (int kb = 0; kb < num_k; ++kb) {
+          ok = mbar_wait_bounded(full_bar(stage), ph, cta_err, p.status);
+          if (!ok) break;
+          mbar_arrive_remote(mapa_shared(full_bar(stage), 0));
+          if (++stage == S) {
+            stage = 0;
+            ph ^= 1;
+          }
         }
       }
     }
@@ -373,7 +503,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   cluster_sync();  // the pair is done with TMEM and with each other's smem
   if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc2(tmem, 256);
+    tmem_dealloc2(tmem, 2 * kAccCols);
   }
 }
 
@@ -382,6 +512,8 @@ cudaError_t launch_gemm(bool dx, const CUtensorMap &tmA, const CUtensorMap &tmL1
                         const CUtensorMap &tmL2, const GemmArgs &args, cudaStream_t s) {
   const int smem = gemm_smem_bytes(args.stages, args.r_pad);
   static bool attr_set[2] = {false, false};
+  // Clusters that fit on the device at once, per (kernel, shared memory size).
+  static int cached_clusters[2] = {0, 0}, cached_smem[2] = {-1, -1}, cached_dev[2] = {-1, -1};
   cudaError_t e;
   if (!attr_set[dx]) {
     if (dx)
@@ -394,7 +526,6 @@ cudaError_t launch_gemm(bool dx, const CUtensorMap &tmA, const CUtensorMap &tmL1
     attr_set[dx] = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * ((args.M + 2 * GBM - 1) / (2 * GBM)), (args.out_cols + args.bn - 1) / args.bn, 1);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -405,6 +536,26 @@ cudaError_t launch_gemm(bool dx, const CUtensorMap &tmA, const CUtensorMap &tmL1
   attrs[0].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if (cached_smem[dx] != smem || cached_dev[dx] != dev) {
+    int n = 0;
+    cfg.gridDim = dim3(2, 1, 1);
+    if (dx)
+      e = cudaOccupancyMaxActiveClusters(&n, qlora_gemm_kernel<true>, &cfg);
+    else
+      e = cudaOccupancyMaxActiveClusters(&n, qlora_gemm_kernel<false>, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    cached_clusters[dx] = n;
+    cached_smem[dx] = smem;
+    cached_dev[dx] = dev;
+  }
+  const long tiles = (long)((args.M + 2 * GBM - 1) / (2 * GBM)) *
+                     ((args.out_cols + args.bn - 1) / args.bn);
+  if (tiles == 0) return cudaSuccess;
+  const int clusters = (int)(tiles < cached_clusters[dx] ? tiles : cached_clusters[dx]);
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
   if (dx)
     e = cudaLaunchKernelEx(&cfg, qlora_gemm_kernel<true>, tmA, tmL1, tmL2, args);
   else
