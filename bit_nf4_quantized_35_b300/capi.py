@@ -7,7 +7,7 @@ returns an error status, the binding raises.
 
 The function names follow the C ABI:
   qlora_nf4_sizes, qlora_quantize_nf4, qlora_dequant, qlora_workspace_size,
-  qlora_workspace_init, qlora_device_status, qlora_linear_fwd,
+  qlora_workspace_size_min, qlora_workspace_init, qlora_device_status, qlora_linear_fwd,
   qlora_linear_bwd, qlora_nf4_thresholds, qlora_nf4_codebook.
 """
 from __future__ import annotations
@@ -31,7 +31,7 @@ EXPORTED = (
     "qlora_nf4_sizes", "qlora_quantize_nf4", "qlora_dequant", "qlora_workspace_size",
     "qlora_workspace_init", "qlora_device_status", "qlora_linear_fwd", "qlora_linear_bwd",
     "qlora_nf4_thresholds", "qlora_nf4_codebook", "qlora_status_string",
-    "qlora_linear_bwd_noalloc",
+    "qlora_linear_bwd_noalloc", "qlora_workspace_size_min",
 )
 
 
@@ -68,6 +68,7 @@ def load(path: str = LIB_PATH):
         "qlora_quantize_nf4": [P, st, P, P, P],
         "qlora_dequant": [P, P, P],
         "qlora_workspace_size": [i64, i64, i64, i32, P],
+        "qlora_workspace_size_min": [i64, i64, i64, i32, P],
         "qlora_workspace_init": [P, sz, P],
         "qlora_device_status": [P, P, P],
         "qlora_linear_fwd": [P, P, i64, P, P, i32, f32, P, st, P, P, sz, u32, P],
@@ -127,6 +128,13 @@ def workspace_size(M: int, N: int, K: int, r: int) -> int:
     return b.value
 
 
+def workspace_size_min(M: int, N: int, K: int, r: int) -> int:
+    b = ctypes.c_size_t()
+    _check("qlora_workspace_size_min",
+           load().qlora_workspace_size_min(M, N, K, r, ctypes.byref(b)))
+    return b.value
+
+
 # ---------------------------------------------------------------- device side
 @dataclass
 class NF4Weight:
@@ -183,10 +191,14 @@ def dequant(w: NF4Weight, out: torch.Tensor | None = None, stream=None) -> torch
 
 
 class Workspace:
-    """A zero-initialised device workspace sized for (M, N, K, r)."""
+    """A zero-initialised device workspace sized for (M, N, K, r).
 
-    def __init__(self, M: int, N: int, K: int, r: int, device="cuda", stream=None):
-        self.nbytes = workspace_size(M, N, K, r)
+    ``minimal=True`` sizes it with qlora_workspace_size_min (no split-tile
+    area: the fused GEMM then computes whole output tiles only)."""
+
+    def __init__(self, M: int, N: int, K: int, r: int, device="cuda", stream=None,
+                 minimal: bool = False):
+        self.nbytes = (workspace_size_min if minimal else workspace_size)(M, N, K, r)
         self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
         _check("qlora_workspace_init", load().qlora_workspace_init(
             _ptr(self.buf), self.nbytes, _stream(stream)))

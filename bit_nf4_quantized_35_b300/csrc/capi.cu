@@ -92,8 +92,12 @@ qlora_status check_weight(const qlora_nf4_weight *w, bool need_buffers) {
 }
 
 // Workspace layout for (M, N, K, r).
+// `total_min` is the least a call accepts; `total` adds the split-tile
+// area of the fused GEMM (fp32 partial tiles and their counters, sized for
+// every cluster the device can run), which calls use when it is there.
 struct WsLayout {
-  size_t status, t, u, lb, bt, at, part, total;
+  size_t status, t, u, lb, bt, at, part, total_min, skcnt, skpart, total;
+  int sk_clusters;
 };
 WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int r) {
   const int RP = round_up(r, 16);
@@ -114,6 +118,12 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int r) {
   L.part = off;
   const size_t pn = (size_t)skinny_splits(M, (int)N) * N, pk = (size_t)skinny_splits(M, (int)K) * K;
   off += round_up_sz((pn > pk ? pn : pk) * RP * 4, 256);
+  L.total_min = off;
+  L.sk_clusters = gemm_cluster_bound();
+  L.skcnt = off;
+  off += round_up_sz((size_t)L.sk_clusters * 2 * sizeof(int), 256);
+  L.skpart = off;
+  off += (size_t)L.sk_clusters * 2 * 2 * 128 * 256 * sizeof(float);
   L.total = off;
   return L;
 }
@@ -159,6 +169,16 @@ void set_block_constants(GemmArgs &g, const qlora_nf4_weight *w) {
 
 qlora_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA; }
 
+void set_gemm_plan(GemmArgs &g, const GemmPlan &plan, const WsLayout &L, uint8_t *wsb) {
+  g.sk = plan.sk;
+  g.clusters = plan.clusters;
+  if (plan.sk) {
+    g.sk_count = reinterpret_cast<int *>(wsb + L.skcnt);
+    g.sk_part = reinterpret_cast<float *>(wsb + L.skpart);
+    g.sk_slots_clusters = L.sk_clusters;
+  }
+}
+
 qlora_status check_linear_common(const qlora_nf4_weight *w, const uint16_t *x, int64_t M,
                                  const uint16_t *A, const uint16_t *B, int32_t r, void *ws,
                                  size_t ws_bytes) {
@@ -173,7 +193,7 @@ qlora_status check_linear_common(const qlora_nf4_weight *w, const uint16_t *x, i
   if (!aligned16(x) || !aligned16(A) || !aligned16(B)) return QLORA_ERR_ALIGN;
   if (!ws) return QLORA_ERR_WORKSPACE;
   if (!aligned16(ws)) return QLORA_ERR_ALIGN;
-  if (ws_bytes < ws_layout(M, w->rows, w->cols, r).total) return QLORA_ERR_WORKSPACE;
+  if (ws_bytes < ws_layout(M, w->rows, w->cols, r).total_min) return QLORA_ERR_WORKSPACE;
   return QLORA_OK;
 }
 
@@ -253,6 +273,13 @@ qlora_status qlora_workspace_size(int64_t M, int64_t N, int64_t K, int32_t r, si
   return QLORA_OK;
 }
 
+qlora_status qlora_workspace_size_min(int64_t M, int64_t N, int64_t K, int32_t r, size_t *bytes) {
+  if (!bytes) return QLORA_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || r < 1 || r > 64) return QLORA_ERR_SHAPE;
+  *bytes = ws_layout(M, N, K, r).total_min;
+  return QLORA_OK;
+}
+
 qlora_status qlora_workspace_init(void *ws, size_t ws_bytes, void *stream) {
   if (!ws) return QLORA_ERR_INVALID_ARG;
   return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream)));
@@ -318,9 +345,14 @@ qlora_status qlora_linear_fwd(const qlora_nf4_weight *w, const uint16_t *x, int6
     return cuda_status(launch_gemv(a, num_sms_current(), s));
   }
   const int RP = round_up(r, 16);
-  const int bn = gemm_pick_bn((int)M, N, false, num_sms_current());
+  const bool sk_ws = ws_bytes >= L.total;
+  GemmPlan plan;
+  cudaError_t e = gemm_plan(false, (int)M, N, K, RP, sk_ws ? L.sk_clusters : 0, &plan);
+  if (e == cudaErrorInvalidValue) return QLORA_ERR_SHAPE;
+  if (e != cudaSuccess) return QLORA_ERR_CUDA;
+  const int bn = plan.bn;
   uint16_t *lb = reinterpret_cast<uint16_t *>(wsb + L.lb);
-  cudaError_t e = launch_lora_down(x, M, K, A, r, sc, t_save, lb, RP, num_sms_current(), s);
+  e = launch_lora_down(x, M, K, A, r, sc, t_save, lb, RP, num_sms_current(), s);
   if (e != cudaSuccess) return QLORA_ERR_CUDA;
   CUtensorMap tmA, tmL1, tmL2;
   if (!make_tmap(&tmA, x, K, M, (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -346,6 +378,7 @@ qlora_status qlora_linear_fwd(const qlora_nf4_weight *w, const uint16_t *x, int6
   g.stages = gemm_pick_stages(RP);
   g.status = reinterpret_cast<int *>(wsb + L.status);
   g.bn = bn;
+  set_gemm_plan(g, plan, L, wsb);
   set_block_constants(g, w);
   return cuda_status(launch_gemm(false, tmA, tmL1, tmL2, g, s));
 }
@@ -388,7 +421,11 @@ qlora_status qlora_linear_bwd(const qlora_nf4_weight *w, const uint16_t *x, cons
   // u = dY . B (fp32, for dA) and bf16(s . u) (operand of the dX GEMM's rank-r MMAs)
   e = launch_lora_down(dY, M, N, Bt, r, sc, u, lb, RP, nsm, s);
   if (e != cudaSuccess) return QLORA_ERR_CUDA;
-  const int bn = gemm_pick_bn((int)M, K, true, nsm);
+  GemmPlan plan;
+  e = gemm_plan(true, (int)M, K, N, RP, ws_bytes >= L.total ? L.sk_clusters : 0, &plan);
+  if (e == cudaErrorInvalidValue) return QLORA_ERR_SHAPE;
+  if (e != cudaSuccess) return QLORA_ERR_CUDA;
+  const int bn = plan.bn;
   CUtensorMap tmA, tmL1, tmL2;
   if (!make_tmap(&tmA, dY, N, M, (uint64_t)N * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tmap(&tmL1, lb, RP, M, (uint64_t)RP * 2, 16, 128, CU_TENSOR_MAP_SWIZZLE_32B) ||
@@ -413,6 +450,7 @@ qlora_status qlora_linear_bwd(const qlora_nf4_weight *w, const uint16_t *x, cons
   g.stages = gemm_pick_stages(RP);
   g.status = reinterpret_cast<int *>(wsb + L.status);
   g.bn = bn;
+  set_gemm_plan(g, plan, L, wsb);
   set_block_constants(g, w);
   e = launch_gemm(true, tmA, tmL1, tmL2, g, s);
   if (e != cudaSuccess) return QLORA_ERR_CUDA;

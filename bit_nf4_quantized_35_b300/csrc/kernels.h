@@ -34,11 +34,30 @@ struct GemmArgs {
   int use_code;
   int cshift;  // log2(cdiv): cdiv is 1 or a power of two
   int bn;      // output columns per CTA pair: 128..256, multiple of 32 (set by the launcher)
+  // Split tiles (stream-K).  With sk_part set, each cluster takes an equal
+  // share of the (tile, 64-wide contraction block) units and a tile shared by
+  // several clusters is summed from fp32 partials by the last one to finish.
+  // sk_part: 2 * sk_slots_clusters * 2 * 128 * 256 floats; sk_count:
+  // 2 * sk_slots_clusters ints, zero between calls.  Null: whole tiles only.
+  float *sk_part;
+  int *sk_count;
+  int sk_slots_clusters;
+  int sk;        // 1 when this launch splits tiles (from gemm_plan)
+  int clusters;  // CTA pairs launched (from gemm_plan)
 };
+// Launch shape of the fused GEMM for one call: pair-tile width, split mode
+// and cluster count.  sk_slots_clusters = 0 means no split-tile area.
+struct GemmPlan {
+  int bn, sk, clusters;
+};
+cudaError_t gemm_plan(bool dx, int M, int out_cols, int kdim, int r_pad, int sk_slots_clusters,
+                      GemmPlan *plan);
+// Upper bound on the clusters any launch uses on the current device (sizes
+// the split-tile area).
+int gemm_cluster_bound();
 cudaError_t launch_gemm(bool dx, const CUtensorMap &tmA, const CUtensorMap &tmL1,
                         const CUtensorMap &tmL2, const GemmArgs &args, cudaStream_t s);
 int gemm_pick_stages(int r_pad);
-int gemm_pick_bn(int M, int out_cols, bool dx, int num_sms);
 
 // Split-K decode GEMV (gemv.cu).
 struct GemvArgs {

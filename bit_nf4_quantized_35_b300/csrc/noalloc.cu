@@ -13,8 +13,6 @@
 
 #include "common.cuh"
 
-extern "C" qlora_status qlora_workspace_size(int64_t M, int64_t N, int64_t K, int32_t r,
-                                             size_t *bytes);
 
 namespace {
 
@@ -52,7 +50,7 @@ extern "C" qlora_status qlora_linear_bwd_noalloc(const qlora_nf4_weight *w, cons
                                                  uint32_t flags, void *stream) {
   if (!w) return QLORA_ERR_INVALID_ARG;
   size_t need = 0;
-  qlora_status st = qlora_workspace_size(M, w->rows, w->cols, r, &need);
+  qlora_status st = qlora_workspace_size_min(M, w->rows, w->cols, r, &need);
   if (st != QLORA_OK) return st;
   if (need > (size_t)QLORA_NOALLOC_SCRATCH_BYTES) return QLORA_ERR_WORKSPACE;
   void *ws = nullptr;

@@ -126,14 +126,24 @@ qlora_status qlora_quantize_nf4(const void *W, qlora_dtype w_dtype, const qlora_
  * Errors as for qlora_quantize_nf4. */
 qlora_status qlora_dequant(const qlora_nf4_weight *w, uint16_t *W_out, void *stream);
 
-/* Workspace bytes needed by qlora_linear_fwd / qlora_linear_bwd for these
- * sizes (M tokens, N out features, K in features, LoRA rank r).  One
- * workspace sized this way serves both calls.  Host only. */
+/* Workspace bytes for qlora_linear_fwd / qlora_linear_bwd at these sizes
+ * (M tokens, N out features, K in features, LoRA rank r) on the current
+ * device.  One workspace sized this way serves both calls.  It includes a
+ * split-tile area (fp32 partial tiles, 512 KiB per pair of SMs: 37 MiB on a
+ * 148-SM device) that lets the fused GEMM spread a layer whose output tiles
+ * do not fill the SMs' waves over all of them.  Host only. */
 qlora_status qlora_workspace_size(int64_t M, int64_t N, int64_t K, int32_t r, size_t *bytes);
+
+/* The least workspace the calls accept: qlora_workspace_size without the
+ * split-tile area.  With less than qlora_workspace_size bytes the fused GEMM
+ * computes whole output tiles only (same results, fewer busy SMs on some
+ * shapes).  Host only. */
+qlora_status qlora_workspace_size_min(int64_t M, int64_t N, int64_t K, int32_t r, size_t *bytes);
 
 /* Zero a freshly allocated workspace (device).  Must be called once before
  * the first forward/backward call that uses it; the library keeps the parts
- * that must start at zero at zero after every call. */
+ * that must start at zero at zero after every call that completes.  After a
+ * call whose device status is QLORA_ERR_TIMEOUT, zero it again. */
 qlora_status qlora_workspace_init(void *ws, size_t ws_bytes, void *stream);
 
 /* Read (and clear) the device status word of a workspace: synchronises
@@ -196,9 +206,10 @@ qlora_status qlora_linear_bwd(const qlora_nf4_weight *w, const uint16_t *x, cons
  * ws_bytes.  Its workspace is a fixed array of QLORA_NOALLOC_SCRATCH_BYTES
  * in the library's device memory, held by every GPU that loads the library
  * until the process exits; the call allocates and frees nothing.
- *   - Sizes whose qlora_workspace_size exceeds QLORA_NOALLOC_SCRATCH_BYTES
- *     return QLORA_ERR_WORKSPACE (16 MiB covers the Llama-3-8B projection
- *     shapes at r = 16 up to 8192 tokens).
+ *   - Sizes whose qlora_workspace_size_min exceeds
+ *     QLORA_NOALLOC_SCRATCH_BYTES return QLORA_ERR_WORKSPACE (16 MiB covers
+ *     the Llama-3-8B projection shapes at r = 16 up to 8192 tokens).  The
+ *     array has no split-tile area, so the dX GEMM computes whole tiles.
  *   - The first call on a device looks up the array's device address (a
  *     CUDA runtime query, no allocation) and caches it; make that first call
  *     before any stream capture.
