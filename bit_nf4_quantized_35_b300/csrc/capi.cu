@@ -96,7 +96,7 @@ qlora_status check_weight(const qlora_nf4_weight *w, bool need_buffers) {
 // area of the fused GEMM (fp32 partial tiles and their counters, sized for
 // every cluster the device can run), which calls use when it is there.
 struct WsLayout {
-  size_t status, t, u, lb, bt, at, part, total_min, skcnt, skpart, total;
+  size_t status, t, u, lb, bt, at, part, gcnt, total_min, skcnt, skpart, total;
   int sk_clusters;
 };
 WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int r) {
@@ -118,6 +118,9 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int r) {
   L.part = off;
   const size_t pn = (size_t)skinny_splits(M, (int)N) * N, pk = (size_t)skinny_splits(M, (int)K) * K;
   off += round_up_sz((pn > pk ? pn : pk) * RP * 4, 256);
+  L.gcnt = off;  // column-tile counters of the dA / dB kernel (zero between calls)
+  const int tn = skinny_tiles((int)N), tk = skinny_tiles((int)K);
+  off += round_up_sz((size_t)(tn > tk ? tn : tk) * sizeof(int), 256);
   L.total_min = off;
   L.sk_clusters = gemm_cluster_bound();
   L.skcnt = off;
@@ -455,14 +458,11 @@ qlora_status qlora_linear_bwd(const qlora_nf4_weight *w, const uint16_t *x, cons
   e = launch_gemm(true, tmA, tmL1, tmL2, g, s);
   if (e != cudaSuccess) return QLORA_ERR_CUDA;
   // dB = s . dY^T . t
-  const int spN = skinny_splits(M, N);
-  e = launch_skinny(dY, M, N, t, r, RP, part, spN, s);
-  if (e == cudaSuccess) e = launch_reduce_parts(part, spN, N, RP, r, sc, false, dB, nsm, s);
+  int *gcnt = reinterpret_cast<int *>(wsb + L.gcnt);
+  e = launch_skinny(dY, M, N, t, r, RP, part, gcnt, skinny_splits(M, N), sc, false, dB, s);
   if (e != cudaSuccess) return QLORA_ERR_CUDA;
   // dA = s . u^T . x
-  const int spK = skinny_splits(M, K);
-  e = launch_skinny(x, M, K, u, r, RP, part, spK, s);
-  if (e == cudaSuccess) e = launch_reduce_parts(part, spK, K, RP, r, sc, true, dA, nsm, s);
+  e = launch_skinny(x, M, K, u, r, RP, part, gcnt, skinny_splits(M, K), sc, true, dA, s);
   return cuda_status(e);
 }
 

@@ -105,10 +105,13 @@ cudaError_t launch_dequant(const uint8_t *packed, const int8_t *codes, const flo
 
 // Rank-r gradient contractions and layout helpers (lora_grad.cu).
 int skinny_splits(int64_t M, int C);
+int skinny_tiles(int C);
+// dst = sc . G^T V for G [M, C] bf16, V [M, r] fp32: dst[c * r + j], or
+// dst[j * C + c] with transpose.  part: splits * C * RP floats of scratch;
+// tile_count: skinny_tiles(C) ints, zero before the call and after it.
 cudaError_t launch_skinny(const uint16_t *G, int64_t M, int C, const float *V, int r, int RP,
-                          float *part, int splits, cudaStream_t s);
-cudaError_t launch_reduce_parts(const float *part, int splits, int C, int RP, int r, float sc,
-                                bool transpose, float *dst, int num_sms, cudaStream_t s);
+                          float *part, int *tile_count, int splits, float sc, bool transpose,
+                          float *dst, cudaStream_t s);
 cudaError_t launch_transposes(const uint16_t *A, const uint16_t *B, int N, int K, int r, int RP,
                               uint16_t *At, uint16_t *Bt, int num_sms, cudaStream_t s);
 

@@ -19,16 +19,22 @@
 namespace qlora {
 
 // ---------------------------------------------------------------------------
-// part[split][c][j] = sum_{m in split} G[m][c] . V[m][j]   (j < r_pad)
-// One CTA = 128 columns c x one M split, 8 warps of 16 columns each.  Per
-// 64-row chunk of M: the G tile [64 m][128 c] arrives by cp.async (double
-// buffered, rows padded to 272 B so ldmatrix rows hit distinct banks) and
-// V^T as bf16 hi and lo rows [2 r_pad][64 m] (padded to 144 B).  The MMA
-// A operand (16 c x 16 m) is an ldmatrix.trans of the G tile, the B operand
-// (16 m x 8 j) an ldmatrix of V^T.
+// dst = s . G^T V  (transpose = 0: dst[c * r + j], the dB layout [N, r];
+//                   transpose = 1: dst[j * C + c], the dA layout [r, K])
+// One CTA = 128 columns c x one M split, 8 warps of 16 columns each.  The M
+// range streams in 64-row chunks through a 4-deep cp.async ring holding the
+// G tile [64 m][128 c] (rows padded to 272 B so ldmatrix rows hit distinct
+// banks) and the raw fp32 V rows [64 m][r_pad]; before its MMAs a chunk's V
+// is split into bf16 hi and lo rows of V^T [2 r_pad][64 m] (padded to
+// 144 B).  The MMA A operand (16 c x 16 m) is an ldmatrix.trans of the G
+// tile, the B operand (16 m x 8 j) an ldmatrix of V^T.
+// Each split stores its fp32 partial sums part[split][c][j]; the last CTA of
+// a column tile to finish (a counter per tile, left at zero) adds the splits
+// in split order and writes dst, so the result does not depend on timing.
 constexpr int kGradThreads = 256;
 constexpr int kGradCols = 128;  // c per CTA
 constexpr int kGradRows = 64;   // m per chunk
+constexpr int kGradStages = 4;  // cp.async ring depth
 constexpr int kGsPitch = 136;   // halves per G-tile row (128 + 8)
 constexpr int kVtPitch = 72;    // halves per V^T row (64 + 8)
 
@@ -60,73 +66,87 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __host__ __device__ inline int grad_smem_bytes(int RPAD) {
-  return 2 * kGradRows * kGsPitch * 2 + 2 * (2 * RPAD) * kVtPitch * 2;
+  return kGradStages * (kGradRows * kGsPitch * 2 + kGradRows * RPAD * 4) +
+         (2 * RPAD) * kVtPitch * 2 + 16;
 }
 
 template <int RPT>  // r_pad / 8
 __global__ void __launch_bounds__(kGradThreads) lora_grad_tc_kernel(
     const uint16_t *__restrict__ G, int64_t M, int C, const float *__restrict__ V, int r,
-    int64_t rows_per_split, float *__restrict__ part) {
+    int64_t rows_per_split, float *__restrict__ part, int *__restrict__ tile_count, float sc,
+    int transpose, float *__restrict__ dst) {
   constexpr int RPAD = RPT * 8;
   constexpr int NJ = 2 * RPAD;  // hi rows then lo rows
   constexpr int NTT = NJ / 8;   // n8 tiles
-  extern __shared__ __align__(16) uint16_t gsm[];
-  uint16_t *gs = gsm;                                 // [2][64][136]
-  uint16_t *vt = gsm + 2 * kGradRows * kGsPitch;      // [2][NJ][72]
+  extern __shared__ __align__(16) uint8_t grad_smem[];
+  uint16_t *gs = reinterpret_cast<uint16_t *>(grad_smem);  // [S][64][136]
+  float *vraw = reinterpret_cast<float *>(gs + kGradStages * kGradRows * kGsPitch);  // [S][64][RPAD]
+  uint16_t *vt = reinterpret_cast<uint16_t *>(vraw + kGradStages * kGradRows * RPAD);  // [NJ][72]
+  int *last_flag = reinterpret_cast<int *>(vt + NJ * kVtPitch);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
   const int c0 = blockIdx.x * kGradCols;
   const int64_t m_lo = (int64_t)blockIdx.y * rows_per_split;
   const int64_t m_hi = min(M, m_lo + rows_per_split);
-  const int nchunks = (int)((m_hi - m_lo + kGradRows - 1) / kGradRows);
+  const int nchunks = m_hi > m_lo ? (int)((m_hi - m_lo + kGradRows - 1) / kGradRows) : 0;
 
-  auto issue_g = [&](int ch, int buf) {  // 64 x 128 bf16 = 1024 16-byte pieces
-    const int64_t mb = m_lo + (int64_t)ch * kGradRows;
+  // One chunk: 64 x 128 bf16 of G (1024 16-byte pieces) and 64 x r fp32 of
+  // V (r / 4 pieces per row, r % 8 == 0); rows past the split read nothing
+  // and land as zeros.  One commit group per call, empty past the end.
+  auto issue = [&](int ch) {
+    if (ch < nchunks) {
+      const int buf = ch % kGradStages;
+      const int64_t mb = m_lo + (int64_t)ch * kGradRows;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = threadIdx.x + u * kGradThreads;
-      const int row = i >> 4, cc = (i & 15) * 8;
-      const int64_t m = mb + row;
-      const int c = c0 + cc;
-      const bool ok = m < m_hi && c < C;
-      const uint16_t *src = G + (ok ? m * C + c : 0);
-      cp_async16(smem_u32(gs + (buf * kGradRows + row) * kGsPitch + cc), src, ok ? 16u : 0u);
+      for (int u = 0; u < 4; ++u) {
+        const int i = threadIdx.x + u * kGradThreads;
+        const int row = i >> 4, cc = (i & 15) * 8;
+        const int64_t m = mb + row;
+        const int c = c0 + cc;
+        const bool ok = m < m_hi && c < C;
+        cp_async16(smem_u32(gs + (buf * kGradRows + row) * kGsPitch + cc),
+                   G + (ok ? m * C + c : 0), ok ? 16u : 0u);
+      }
+      for (int i = threadIdx.x; i < kGradRows * (RPAD / 4); i += kGradThreads) {
+        const int row = i / (RPAD / 4), j4 = (i % (RPAD / 4)) * 4;
+        const int64_t m = mb + row;
+        const bool ok = m < m_hi && j4 < r;
+        cp_async16(smem_u32(vraw + (buf * kGradRows + row) * RPAD + j4),
+                   V + (ok ? m * r + j4 : 0), ok ? 16u : 0u);
+      }
     }
     cp_async_commit();
-  };
-  auto stage_v = [&](int ch, int buf) {  // V rows -> bf16 hi / lo, transposed
-    const int64_t mb = m_lo + (int64_t)ch * kGradRows;
-    for (int i = threadIdx.x; i < kGradRows * RPAD; i += kGradThreads) {
-      const int row = i / RPAD, j = i % RPAD;
-      const int64_t m = mb + row;
-      const float v = (m < m_hi && j < r) ? V[m * r + j] : 0.f;
-      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-      const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-      vt[(buf * NJ + j) * kVtPitch + row] = __bfloat16_as_ushort(hi);
-      vt[(buf * NJ + RPAD + j) * kVtPitch + row] = __bfloat16_as_ushort(lo);
-    }
   };
 
   float d[NTT][4];
 #pragma unroll
   for (int nt = 0; nt < NTT; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
-  if (nchunks > 0) {
-    issue_g(0, 0);
-    stage_v(0, 0);
-    cp_async_wait_all();
-    __syncthreads();
-  }
+#pragma unroll
+  for (int ch = 0; ch < kGradStages - 1; ++ch) issue(ch);
   const int cw = warp * 16;  // this warp's 16 columns inside the tile
   // ldmatrix lane roles: matrix mi = lane >> 3, row within it lane & 7
   const int mi = lane >> 3, lr = lane & 7;
   for (int ch = 0; ch < nchunks; ++ch) {
-    const int cur = ch & 1;
-    if (ch + 1 < nchunks) issue_g(ch + 1, cur ^ 1);
+    const int cur = ch % kGradStages;
+    cp_async_wait<kGradStages - 2>();  // this thread's copies of chunk ch have landed
+    __syncthreads();                   // everyone's; chunk ch - 1 is fully consumed
+    issue(ch + kGradStages - 1);       // into the buffer chunk ch - 1 used
+    // V rows of chunk ch -> bf16 hi / lo, transposed
+    for (int i = threadIdx.x; i < kGradRows * RPAD; i += kGradThreads) {
+      const int row = i / RPAD, j = i % RPAD;
+      const float v = vraw[(cur * kGradRows + row) * RPAD + j];
+      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+      vt[j * kVtPitch + row] = __bfloat16_as_ushort(hi);
+      vt[(RPAD + j) * kVtPitch + row] = __bfloat16_as_ushort(lo);
+    }
+    __syncthreads();
 #pragma unroll
     for (int kk = 0; kk < kGradRows / 16; ++kk) {
       const int m0 = kk * 16;
@@ -144,15 +164,13 @@ __global__ void __launch_bounds__(kGradThreads) lora_grad_tc_kernel(
         uint32_t b0, b1, b2, b3;
         const int row = np * 16 + lr + ((mi >> 1) << 3);
         const int col = m0 + ((mi & 1) << 3);
-        ldsm_x4(smem_u32(vt + (cur * NJ + row) * kVtPitch + col), b0, b1, b2, b3);
+        ldsm_x4(smem_u32(vt + row * kVtPitch + col), b0, b1, b2, b3);
         mma_bf16_16816(d[2 * np], a0, a1, a2, a3, b0, b1);
         mma_bf16_16816(d[2 * np + 1], a0, a1, a2, a3, b2, b3);
       }
     }
-    if (ch + 1 < nchunks) stage_v(ch + 1, cur ^ 1);
-    cp_async_wait_all();
-    __syncthreads();
   }
+  cp_async_wait<0>();
   // hi + lo, then the partial of this split: rows c0+cw+g (+8), columns j
 #pragma unroll
   for (int nt = 0; nt < RPT; ++nt) {
@@ -161,35 +179,65 @@ __global__ void __launch_bounds__(kGradThreads) lora_grad_tc_kernel(
     for (int h = 0; h < 2; ++h) {
       const int c = c0 + cw + g + 8 * h;
       if (c < C) {
-        float *dst = part + ((int64_t)blockIdx.y * C + c) * RPAD + j;
-        dst[0] = d[nt][2 * h] + d[RPT + nt][2 * h];
-        dst[1] = d[nt][2 * h + 1] + d[RPT + nt][2 * h + 1];
+        float *p = part + ((int64_t)blockIdx.y * C + c) * RPAD + j;
+        __stcg(p, d[nt][2 * h] + d[RPT + nt][2 * h]);
+        __stcg(p + 1, d[nt][2 * h + 1] + d[RPT + nt][2 * h + 1]);
       }
     }
   }
-}
-
-// dst = s * sum over splits (fixed order) of part[split][c][j], j < r.
-// transpose == 0: dst[c * r + j] (dB layout [N, r]);
-// transpose == 1: dst[j * C + c] (dA layout [r, K]).
-__global__ void __launch_bounds__(256) reduce_parts_kernel(const float *__restrict__ part,
-                                                           int splits, int C, int RP, int r,
-                                                           float s, int transpose,
-                                                           float *__restrict__ dst) {
-  const int64_t total = (int64_t)C * r;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    int c, j;
-    if (transpose) {
-      j = (int)(i / C);
-      c = (int)(i % C);
-    } else {
-      c = (int)(i / r);
-      j = (int)(i % r);
+  // Count this split in; the last one for the tile adds the splits in order.
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int prev = atomicAdd(tile_count + blockIdx.x, 1);
+    const bool last = prev == (int)gridDim.y - 1;
+    if (last) atomicExch(tile_count + blockIdx.x, 0);
+    *last_flag = last ? 1 : 0;
+  }
+  __syncthreads();
+  if (*last_flag == 0) return;
+  __threadfence();
+  // 4 consecutive j per thread (r % 8 == 0), 8 split loads in flight; the
+  // sum runs in split order.
+  const int ncols = min(kGradCols, C - c0);
+  const int r4 = r / 4;
+  const float4 *pbase = reinterpret_cast<const float4 *>(part);
+  const int64_t sp_stride = (int64_t)C * (RPAD / 4);  // float4s per split
+  for (int i = threadIdx.x; i < ncols * r4; i += kGradThreads) {
+    // transposed (dA) output: consecutive threads along c, coalesced rows
+    const int c = transpose ? c0 + i % ncols : c0 + i / r4;
+    const int j4 = transpose ? (i / ncols) * 4 : (i % r4) * 4;
+    const float4 *src = pbase + (int64_t)c * (RPAD / 4) + j4 / 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int sp = 0;
+    for (; sp + 8 <= (int)gridDim.y; sp += 8) {
+      float4 w[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) w[k] = __ldcg(src + (int64_t)(sp + k) * sp_stride);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        acc.x += w[k].x;
+        acc.y += w[k].y;
+        acc.z += w[k].z;
+        acc.w += w[k].w;
+      }
     }
-    float v = 0.f;
-    for (int sp = 0; sp < splits; ++sp) v += part[((int64_t)sp * C + c) * RP + j];
-    dst[i] = s * v;
+    for (; sp < (int)gridDim.y; ++sp) {
+      const float4 w = __ldcg(src + (int64_t)sp * sp_stride);
+      acc.x += w.x;
+      acc.y += w.y;
+      acc.z += w.z;
+      acc.w += w.w;
+    }
+    if (transpose) {
+      dst[(int64_t)(j4 + 0) * C + c] = sc * acc.x;
+      dst[(int64_t)(j4 + 1) * C + c] = sc * acc.y;
+      dst[(int64_t)(j4 + 2) * C + c] = sc * acc.z;
+      dst[(int64_t)(j4 + 3) * C + c] = sc * acc.w;
+    } else {
+      *reinterpret_cast<float4 *>(dst + (int64_t)c * r + j4) =
+          make_float4(sc * acc.x, sc * acc.y, sc * acc.z, sc * acc.w);
+    }
   }
 }
 
@@ -221,20 +269,24 @@ __global__ void transpose_a_kernel(const uint16_t *__restrict__ A, int K, int r,
 //   backward u = dY . B    (G = dY [M, N], H = B^T [r, N])
 // It also writes bf16(s . out), zero-padded to r_pad columns: the operand of
 // the rank-r MMAs that seed the fused GEMM's accumulator.
-// One CTA per 16 rows of G, 8 warps splitting C; bf16 mma.sync m16n8k16 with
-// fp32 accumulation (G streams from memory once, H is a few KB and stays in
-// L1); the 8 warp partials meet in shared memory in a fixed order.
+// One CTA per 16 rows of G, 16 warps splitting C; bf16 mma.sync m16n8k16
+// with fp32 accumulation (G streams from memory once, H is a few KB and
+// stays in L1/L2).  The kernel is bound by HBM: each lane issues the loads
+// of U 32-column chunks before the first MMA that needs them, so
+// 16 warps x 32 lanes x 2U x 16 B of G are in flight per CTA.  The warp
+// partials meet in shared memory in a fixed order (w + 8 first, then the
+// 8 sums in warp order).
 // Lane (g, q) loads 8 consecutive elements (16 B) of rows g and g+8 per 32
 // columns; the two MMAs of those 32 columns pair their k indices in the same
 // order for G and H, so any consistent assignment is exact.
-constexpr int kDownWarps = 8;
-
+constexpr int kDownWarps = 16;
 
 template <int NT>  // n8 tiles: r_pad / 8
 __global__ void __launch_bounds__(kDownWarps * 32) lora_down_kernel(
     const uint16_t *__restrict__ G, int64_t M, int C, const uint16_t *__restrict__ H, int r,
     float s, float *__restrict__ out, uint16_t *__restrict__ outb, int r_pad) {
-  __shared__ float red[kDownWarps][16][NT * 8];
+  constexpr int U = NT <= 2 ? 4 : (NT <= 4 ? 2 : 1);  // chunks in flight per lane
+  __shared__ float red[kDownWarps / 2][16][NT * 8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
   const int64_t m0 = (int64_t)blockIdx.x * 16;
@@ -250,40 +302,68 @@ __global__ void __launch_bounds__(kDownWarps * 32) lora_down_kernel(
   for (int nt = 0; nt < NT; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
   const uint16_t *g0p = G + (vg ? rg : 0) * C;
   const uint16_t *g8p = G + (vg8 ? rg8 : 0) * C;
-  for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
-    const int cc = c0 + q * 8;
-    const bool cv = cc < C;  // C % 8 == 0
-    const uint4 a = ldg_nc_v4(g0p + (cv ? cc : 0));
-    const uint4 b = ldg_nc_v4(g8p + (cv ? cc : 0));
-    const uint32_t A0[4] = {vg && cv ? a.x : 0u, vg && cv ? a.y : 0u, vg && cv ? a.z : 0u,
-                            vg && cv ? a.w : 0u};
-    const uint32_t A8[4] = {vg8 && cv ? b.x : 0u, vg8 && cv ? b.y : 0u, vg8 && cv ? b.z : 0u,
-                            vg8 && cv ? b.w : 0u};
+  for (int c0 = c_lo; c0 < c_hi; c0 += 32 * U) {
+    uint4 a[U], b[U], h[U][NT];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int j = nt * 8 + g;
-      uint4 h = make_uint4(0, 0, 0, 0);
-      if (j < r && cv) h = ldg_nc_v4(H + (int64_t)j * C + cc);
-      // MMA 0: physical columns cc+0..3, MMA 1: cc+4..7
-      mma_bf16_16816(d[nt], A0[0], A8[0], A0[1], A8[1], h.x, h.y);
-      mma_bf16_16816(d[nt], A0[2], A8[2], A0[3], A8[3], h.z, h.w);
+    for (int u = 0; u < U; ++u) {
+      const int cc = c0 + u * 32 + q * 8;
+      const bool cv = cc < c_hi;  // C % 8 == 0
+      a[u] = ldg_nc_v4(g0p + (cv ? cc : 0));
+      b[u] = ldg_nc_v4(g8p + (cv ? cc : 0));
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int j = nt * 8 + g;
+        h[u][nt] = ldg_nc_v4(H + (int64_t)(j < r ? j : 0) * C + (cv ? cc : 0));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const bool cv = c0 + u * 32 + q * 8 < c_hi;
+      const bool k0 = vg && cv, k8 = vg8 && cv;
+      const uint32_t A0[4] = {k0 ? a[u].x : 0u, k0 ? a[u].y : 0u, k0 ? a[u].z : 0u,
+                              k0 ? a[u].w : 0u};
+      const uint32_t A8[4] = {k8 ? b[u].x : 0u, k8 ? b[u].y : 0u, k8 ? b[u].z : 0u,
+                              k8 ? b[u].w : 0u};
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const bool hv = nt * 8 + g < r && cv;
+        const uint4 hh = hv ? h[u][nt] : make_uint4(0, 0, 0, 0);
+        // MMA 0: physical columns cc+0..3, MMA 1: cc+4..7
+        mma_bf16_16816(d[nt], A0[0], A8[0], A0[1], A8[1], hh.x, hh.y);
+        mma_bf16_16816(d[nt], A0[2], A8[2], A0[3], A8[3], hh.z, hh.w);
+      }
     }
   }
+  // Warps 8..15 store, warps 0..7 add theirs, then the 8 sums in warp order.
+  const int wslot = warp & (kDownWarps / 2 - 1);
+  for (int pass = 0; pass < 2; ++pass) {
+    if ((warp >= kDownWarps / 2) == (pass == 0)) {
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    red[warp][g][nt * 8 + 2 * q] = d[nt][0];
-    red[warp][g][nt * 8 + 2 * q + 1] = d[nt][1];
-    red[warp][g + 8][nt * 8 + 2 * q] = d[nt][2];
-    red[warp][g + 8][nt * 8 + 2 * q + 1] = d[nt][3];
+      for (int nt = 0; nt < NT; ++nt) {
+        float *r0 = &red[wslot][g][nt * 8 + 2 * q];
+        float *r8 = &red[wslot][g + 8][nt * 8 + 2 * q];
+        if (pass == 0) {
+          r0[0] = d[nt][0];
+          r0[1] = d[nt][1];
+          r8[0] = d[nt][2];
+          r8[1] = d[nt][3];
+        } else {
+          r0[0] = d[nt][0] + r0[0];
+          r0[1] = d[nt][1] + r0[1];
+          r8[0] = d[nt][2] + r8[0];
+          r8[1] = d[nt][3] + r8[1];
+        }
+      }
+    }
+    __syncthreads();
   }
-  __syncthreads();
   for (int i = threadIdx.x; i < 16 * NT * 8; i += blockDim.x) {
     const int row = i / (NT * 8), j = i % (NT * 8);
     const int64_t m = m0 + row;
     if (m >= M) continue;
     float v = 0.f;
 #pragma unroll
-    for (int w = 0; w < kDownWarps; ++w) v += red[w][row][j];
+    for (int w = 0; w < kDownWarps / 2; ++w) v += red[w][row][j];
     if (out && j < r) out[m * r + j] = v;
     if (outb && j < r_pad)
       outb[m * r_pad + j] = j < r ? __bfloat16_as_ushort(__float2bfloat16_rn(s * v)) : (uint16_t)0;
@@ -311,18 +391,23 @@ cudaError_t launch_lora_down(const uint16_t *G, int64_t M, int C, const uint16_t
   return cudaGetLastError();
 }
 
+// M splits per column tile: about two CTAs per SM, but at least 4 chunks of
+// 64 rows per split so that the cp.async ring streams.
 int skinny_splits(int64_t M, int C) {
   const int coltiles = (C + kGradCols - 1) / kGradCols;
   int64_t sp = (296 + coltiles - 1) / coltiles;
-  int64_t maxsp = (M + kGradRows - 1) / kGradRows;
+  int64_t maxsp = (M + 4 * kGradRows - 1) / (4 * kGradRows);
   if (sp > maxsp) sp = maxsp;
   if (sp < 1) sp = 1;
   return (int)sp;
 }
 
+int skinny_tiles(int C) { return (C + kGradCols - 1) / kGradCols; }
+
 template <int RPT>
 static cudaError_t launch_grad(dim3 grid, const uint16_t *G, int64_t M, int C, const float *V,
-                               int r, int64_t rps, float *part, cudaStream_t s) {
+                               int r, int64_t rps, float *part, int *tile_count, float sc,
+                               bool transpose, float *dst, cudaStream_t s) {
   const int smem = grad_smem_bytes(RPT * 8);
   static bool set = false;
   if (!set) {
@@ -331,32 +416,24 @@ static cudaError_t launch_grad(dim3 grid, const uint16_t *G, int64_t M, int C, c
     if (e != cudaSuccess) return e;
     set = true;
   }
-  lora_grad_tc_kernel<RPT><<<grid, kGradThreads, smem, s>>>(G, M, C, V, r, rps, part);
+  lora_grad_tc_kernel<RPT><<<grid, kGradThreads, smem, s>>>(G, M, C, V, r, rps, part, tile_count,
+                                                             sc, transpose ? 1 : 0, dst);
   return cudaGetLastError();
 }
 
 cudaError_t launch_skinny(const uint16_t *G, int64_t M, int C, const float *V, int r, int RP,
-                          float *part, int splits, cudaStream_t s) {
+                          float *part, int *tile_count, int splits, float sc, bool transpose,
+                          float *dst, cudaStream_t s) {
+  if (C == 0) return cudaSuccess;
   const int64_t rps = ((M + splits - 1) / splits + kGradRows - 1) / kGradRows * kGradRows;
   dim3 grid((C + kGradCols - 1) / kGradCols, splits);
   switch (RP) {
-    case 16: return launch_grad<2>(grid, G, M, C, V, r, rps, part, s);
-    case 32: return launch_grad<4>(grid, G, M, C, V, r, rps, part, s);
-    case 48: return launch_grad<6>(grid, G, M, C, V, r, rps, part, s);
-    case 64: return launch_grad<8>(grid, G, M, C, V, r, rps, part, s);
+    case 16: return launch_grad<2>(grid, G, M, C, V, r, rps, part, tile_count, sc, transpose, dst, s);
+    case 32: return launch_grad<4>(grid, G, M, C, V, r, rps, part, tile_count, sc, transpose, dst, s);
+    case 48: return launch_grad<6>(grid, G, M, C, V, r, rps, part, tile_count, sc, transpose, dst, s);
+    case 64: return launch_grad<8>(grid, G, M, C, V, r, rps, part, tile_count, sc, transpose, dst, s);
     default: return cudaErrorInvalidValue;
   }
-}
-
-cudaError_t launch_reduce_parts(const float *part, int splits, int C, int RP, int r, float sc,
-                                bool transpose, float *dst, int num_sms, cudaStream_t s) {
-  const int64_t total = (int64_t)C * r;
-  int64_t blocks = (total + 255) / 256;
-  if (blocks > (int64_t)num_sms * 8) blocks = (int64_t)num_sms * 8;
-  if (blocks < 1) blocks = 1;
-  reduce_parts_kernel<<<(unsigned)blocks, 256, 0, s>>>(part, splits, C, RP, r, sc,
-                                                       transpose ? 1 : 0, dst);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_transposes(const uint16_t *A, const uint16_t *B, int N, int K, int r, int RP,

@@ -213,9 +213,11 @@ qlora_status qlora_linear_bwd(const qlora_nf4_weight *w, const uint16_t *x, cons
  *   - The first call on a device looks up the array's device address (a
  *     CUDA runtime query, no allocation) and caches it; make that first call
  *     before any stream capture.
- *   - Every call on a device shares the one array and nothing in it needs to
- *     start at zero.  Calls that overlap on the GPU (different streams, no
- *     ordering between them) race on it and give undefined results.
+ *   - Every call on a device shares the one array.  The few counters in it
+ *     that must start at zero are zero when the library loads and every call
+ *     that completes leaves them at zero.  Calls that overlap on the GPU
+ *     (different streams, no ordering between them) race on it and give
+ *     undefined results.
  *   - A device-side timeout is not reported by this entry point (it has no
  *     workspace the caller could read). */
 #define QLORA_NOALLOC_SCRATCH_BYTES (16u << 20)
