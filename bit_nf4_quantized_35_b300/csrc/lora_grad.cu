@@ -241,25 +241,24 @@ __global__ void __launch_bounds__(kGradThreads) lora_grad_tc_kernel(
   }
 }
 
-// Bt[j][n] = B[n][j] (j < r), 0 for r <= j < RP.
-__global__ void transpose_b_kernel(const uint16_t *__restrict__ B, int N, int r, int RP,
-                                   uint16_t *__restrict__ Bt) {
-  const int64_t total = (int64_t)RP * N;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int j = (int)(i / N), n = (int)(i % N);
-    Bt[i] = j < r ? B[(int64_t)n * r + j] : (uint16_t)0;
-  }
-}
-
-// At[k][j] = A[j][k] (j < r), 0 for r <= j < RP.
-__global__ void transpose_a_kernel(const uint16_t *__restrict__ A, int K, int r, int RP,
-                                   uint16_t *__restrict__ At) {
-  const int64_t total = (int64_t)K * RP;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int k = (int)(i / RP), j = (int)(i % RP);
-    At[i] = j < r ? A[(int64_t)j * K + k] : (uint16_t)0;
+// Both transposes of the LoRA factors in one launch (blocks [0, nb) do B,
+// the rest A):
+//   Bt[j][n] = B[n][j] and At[k][j] = A[j][k] for j < r; 0 for r <= j < RP.
+__global__ void transpose_ab_kernel(const uint16_t *__restrict__ A, const uint16_t *__restrict__ B,
+                                    int N, int K, int r, int RP, int nb, uint16_t *__restrict__ At,
+                                    uint16_t *__restrict__ Bt) {
+  const bool doB = (int)blockIdx.x < nb;
+  const int64_t total = doB ? (int64_t)RP * N : (int64_t)K * RP;
+  const int64_t b0 = doB ? blockIdx.x : blockIdx.x - nb;
+  const int64_t nblk = doB ? nb : gridDim.x - nb;
+  for (int64_t i = b0 * blockDim.x + threadIdx.x; i < total; i += nblk * blockDim.x) {
+    if (doB) {
+      const int j = (int)(i / N), n = (int)(i % N);
+      Bt[i] = j < r ? B[(int64_t)n * r + j] : (uint16_t)0;
+    } else {
+      const int k = (int)(i / RP), j = (int)(i % RP);
+      At[i] = j < r ? A[(int64_t)j * K + k] : (uint16_t)0;
+    }
   }
 }
 
@@ -440,11 +439,12 @@ cudaError_t launch_transposes(const uint16_t *A, const uint16_t *B, int N, int K
                               uint16_t *At, uint16_t *Bt, int num_sms, cudaStream_t s) {
   const int64_t tb = (int64_t)RP * N, ta = (int64_t)K * RP;
   int64_t gb = (tb + 255) / 256, ga = (ta + 255) / 256;
-  const int64_t cap = (int64_t)num_sms * 8;
+  const int64_t cap = (int64_t)num_sms * 4;
   if (gb > cap) gb = cap;
   if (ga > cap) ga = cap;
-  transpose_b_kernel<<<(unsigned)gb, 256, 0, s>>>(B, N, r, RP, Bt);
-  transpose_a_kernel<<<(unsigned)ga, 256, 0, s>>>(A, K, r, RP, At);
+  if (gb < 1) gb = 1;
+  if (ga < 1) ga = 1;
+  transpose_ab_kernel<<<(unsigned)(gb + ga), 256, 0, s>>>(A, B, N, K, r, RP, (int)gb, At, Bt);
   return cudaGetLastError();
 }
 
