@@ -186,17 +186,20 @@ __global__ void __launch_bounds__(kGradThreads) lora_grad_tc_kernel(
     }
   }
   // Count this split in; the last one for the tile adds the splits in order.
-  __threadfence();
+  // The block barrier orders every thread's partial stores before thread
+  // 0's fence and count (one release per CTA); the reading threads are
+  // ordered after thread 0's count by the next barrier.
   __syncthreads();
   if (threadIdx.x == 0) {
+    __threadfence();
     const int prev = atomicAdd(tile_count + blockIdx.x, 1);
     const bool last = prev == (int)gridDim.y - 1;
     if (last) atomicExch(tile_count + blockIdx.x, 0);
+    __threadfence();
     *last_flag = last ? 1 : 0;
   }
   __syncthreads();
   if (*last_flag == 0) return;
-  __threadfence();
   // 4 consecutive j per thread (r % 8 == 0), 8 split loads in flight; the
   // sum runs in split order.
   const int ncols = min(kGradCols, C - c0);
@@ -390,12 +393,12 @@ cudaError_t launch_lora_down(const uint16_t *G, int64_t M, int C, const uint16_t
   return cudaGetLastError();
 }
 
-// M splits per column tile: about two CTAs per SM, but at least 4 chunks of
-// 64 rows per split so that the cp.async ring streams.
+// M splits per column tile: as many as keep all CTAs in one wave of two
+// CTAs per SM (148 SMs), with at least 2 chunks of 64 rows per split.
 int skinny_splits(int64_t M, int C) {
   const int coltiles = (C + kGradCols - 1) / kGradCols;
-  int64_t sp = (296 + coltiles - 1) / coltiles;
-  int64_t maxsp = (M + 4 * kGradRows - 1) / (4 * kGradRows);
+  int64_t sp = 296 / coltiles;
+  int64_t maxsp = (M + 2 * kGradRows - 1) / (2 * kGradRows);
   if (sp > maxsp) sp = maxsp;
   if (sp < 1) sp = 1;
   return (int)sp;
