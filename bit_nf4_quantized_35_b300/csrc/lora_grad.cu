@@ -271,13 +271,15 @@ __global__ void transpose_ab_kernel(const uint16_t *__restrict__ A, const uint16
 //   backward u = dY . B    (G = dY [M, N], H = B^T [r, N])
 // It also writes bf16(s . out), zero-padded to r_pad columns: the operand of
 // the rank-r MMAs that seed the fused GEMM's accumulator.
-// One CTA per 16 rows of G, 16 warps splitting C; bf16 mma.sync m16n8k16
-// with fp32 accumulation (G streams from memory once, H is a few KB and
-// stays in L1/L2).  The kernel is bound by HBM: each lane issues the loads
+// One CTA per 16 rows of G (C < 8192), or a cluster of 2 CTAs per 16 rows,
+// each CTA one half of C; a CTA's columns are split among its 16 warps;
+// bf16 mma.sync m16n8k16 with fp32 accumulation (G streams from memory once,
+// H is a few KB and stays in L1/L2).  The kernel is bound by HBM: each lane issues the loads
 // of U 32-column chunks before the first MMA that needs them, so
 // 16 warps x 32 lanes x 2U x 16 B of G are in flight per CTA.  The warp
 // partials meet in shared memory in a fixed order (w + 8 first, then the
-// 8 sums in warp order).
+// 8 sums in warp order), then the two CTAs' sums in CTA 0 through
+// distributed shared memory (CTA 0's half first).
 // Lane (g, q) loads 8 consecutive elements (16 B) of rows g and g+8 per 32
 // columns; the two MMAs of those 32 columns pair their k indices in the same
 // order for G and H, so any consistent assignment is exact.
@@ -289,16 +291,20 @@ __global__ void __launch_bounds__(kDownWarps * 32) lora_down_kernel(
     float s, float *__restrict__ out, uint16_t *__restrict__ outb, int r_pad) {
   constexpr int U = NT <= 2 ? 4 : (NT <= 4 ? 2 : 1);  // chunks in flight per lane
   __shared__ float red[kDownWarps / 2][16][NT * 8];
+  __shared__ float fin[16][NT * 8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
   const int64_t m0 = (int64_t)blockIdx.x * 16;
   const int64_t rg = m0 + g, rg8 = m0 + g + 8;
   const bool vg = rg < M, vg8 = rg8 < M;
-  // this warp's share of C, in 32-column chunks
+  // this CTA's part of C (all of it, or half: blockIdx.y = rank in the
+  // cluster), then this warp's share of it, in 32-column chunks
   const int nch = (C + 31) / 32;
-  const int per = (nch + kDownWarps - 1) / kDownWarps;
-  const int c_lo = warp * per * 32;
-  const int c_hi = min(C, (warp + 1) * per * 32);
+  const int h0 = gridDim.y == 2 ? (nch + 1) / 2 : nch;
+  const int ch_lo = blockIdx.y == 0 ? 0 : h0, ch_n = blockIdx.y == 0 ? h0 : nch - h0;
+  const int per = (ch_n + kDownWarps - 1) / kDownWarps;
+  const int c_lo = (ch_lo + min(ch_n, warp * per)) * 32;
+  const int c_hi = min(C, (ch_lo + min(ch_n, (warp + 1) * per)) * 32);
   float d[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
@@ -361,36 +367,72 @@ __global__ void __launch_bounds__(kDownWarps * 32) lora_down_kernel(
   }
   for (int i = threadIdx.x; i < 16 * NT * 8; i += blockDim.x) {
     const int row = i / (NT * 8), j = i % (NT * 8);
-    const int64_t m = m0 + row;
-    if (m >= M) continue;
     float v = 0.f;
 #pragma unroll
     for (int w = 0; w < kDownWarps / 2; ++w) v += red[w][row][j];
-    if (out && j < r) out[m * r + j] = v;
-    if (outb && j < r_pad)
-      outb[m * r_pad + j] = j < r ? __bfloat16_as_ushort(__float2bfloat16_rn(s * v)) : (uint16_t)0;
+    fin[row][j] = v;
   }
+  if (gridDim.y == 2) cluster_sync();  // both halves' sums are in shared memory
+  if (blockIdx.y == 0) {
+    for (int i = threadIdx.x; i < 16 * NT * 8; i += blockDim.x) {
+      const int row = i / (NT * 8), j = i % (NT * 8);
+      const int64_t m = m0 + row;
+      if (m >= M) continue;
+      float peer = 0.f;
+      if (gridDim.y == 2)
+        asm volatile("ld.shared::cluster.f32 %0, [%1];"
+                     : "=f"(peer)
+                     : "r"(mapa_shared(smem_u32(&fin[row][j]), 1))
+                     : "memory");
+      const float v = fin[row][j] + peer;
+      if (out && j < r) out[m * r + j] = v;
+      if (outb && j < r_pad)
+        outb[m * r_pad + j] = j < r ? __bfloat16_as_ushort(__float2bfloat16_rn(s * v)) : (uint16_t)0;
+    }
+  }
+  if (gridDim.y == 2) cluster_sync();  // the peer's sums are read before it exits
 }
 
 // ------------------------------------------------------------ launchers
+template <int NT>
+static cudaError_t launch_down(unsigned gx, const uint16_t *G, int64_t M, int C,
+                               const uint16_t *H, int r, float s, float *out, uint16_t *outb,
+                               int r_pad, cudaStream_t st) {
+  // Wide inputs: two CTAs per row block (a cluster), so that more SMs stream.
+  const bool split = C >= 8192;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(gx, split ? 2 : 1, 1);
+  cfg.blockDim = dim3(kDownWarps * 32, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = 1;
+  attrs[0].val.clusterDim.y = 2;
+  attrs[0].val.clusterDim.z = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = split ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, lora_down_kernel<NT>, G, M, C, H, r, s, out, outb, r_pad);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_lora_down(const uint16_t *G, int64_t M, int C, const uint16_t *H, int r,
                              float s, float *out, uint16_t *outb, int r_pad, int num_sms,
                              cudaStream_t st) {
   (void)num_sms;
   if (M == 0) return cudaSuccess;
-  const unsigned grid = (unsigned)((M + 15) / 16);
+  const unsigned gx = (unsigned)((M + 15) / 16);
   switch ((r + 7) / 8) {
-    case 1: lora_down_kernel<2><<<grid, kDownWarps * 32, 0, st>>>(G, M, C, H, r, s, out, outb, r_pad); break;
-    case 2: lora_down_kernel<2><<<grid, kDownWarps * 32, 0, st>>>(G, M, C, H, r, s, out, outb, r_pad); break;
-    case 3: lora_down_kernel<4><<<grid, kDownWarps * 32, 0, st>>>(G, M, C, H, r, s, out, outb, r_pad); break;
-    case 4: lora_down_kernel<4><<<grid, kDownWarps * 32, 0, st>>>(G, M, C, H, r, s, out, outb, r_pad); break;
-    case 5: lora_down_kernel<6><<<grid, kDownWarps * 32, 0, st>>>(G, M, C, H, r, s, out, outb, r_pad); break;
-    case 6: lora_down_kernel<6><<<grid, kDownWarps * 32, 0, st>>>(G, M, C, H, r, s, out, outb, r_pad); break;
-    case 7: lora_down_kernel<8><<<grid, kDownWarps * 32, 0, st>>>(G, M, C, H, r, s, out, outb, r_pad); break;
-    case 8: lora_down_kernel<8><<<grid, kDownWarps * 32, 0, st>>>(G, M, C, H, r, s, out, outb, r_pad); break;
+    case 1:
+    case 2: return launch_down<2>(gx, G, M, C, H, r, s, out, outb, r_pad, st);
+    case 3:
+    case 4: return launch_down<4>(gx, G, M, C, H, r, s, out, outb, r_pad, st);
+    case 5:
+    case 6: return launch_down<6>(gx, G, M, C, H, r, s, out, outb, r_pad, st);
+    case 7:
+    case 8: return launch_down<8>(gx, G, M, C, H, r, s, out, outb, r_pad, st);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 // M splits per column tile: as many as keep all CTAs in one wave of two
