@@ -50,7 +50,7 @@ RANK_R, ALPHA = 16, 32.0
 LAYERS = [("q_proj", 4096, 4096), ("k_proj", 1024, 4096), ("v_proj", 1024, 4096),
           ("o_proj", 4096, 4096), ("gate_proj", 14336, 4096), ("up_proj", 14336, 4096),
           ("down_proj", 4096, 14336)]
-KERNELS_PER_LAYER_STEP = 8  # fwd: GEMM; bwd: 2 transposes, dX GEMM, 2 skinny, 2 reduces
+KERNELS_PER_LAYER_STEP = 7  # fwd: LoRA pre-pass, GEMM; bwd: transposes, dY pre-pass, dX GEMM, dB, dA
 
 
 def fwd_flops(M, N, K, r):
