@@ -21,10 +21,15 @@
 //     operands, f32 accumulation): the 4-bit indices become f16 codepoint
 //     pairs through a 256-entry byte table in shared memory, replicated per
 //     lane so that 32 random bytes never collide on a bank.
-//   - One warp also computes the CTA's slice of t = x A^T on the same x
-//     fragments.  The S partial sums meet once, in CTA 0 of the cluster, in
-//     rank order (deterministic, no workspace, no atomics), which adds the
-//     LoRA term s . t . B^T and writes y.
+//   - All warps share the CTA's slice of t = x A^T (same x fragments, one
+//     16-wide j tile and every (16 / tiles)-th 64-block each) before their
+//     main loop.  After it, every CTA of the cluster sums t over the ranks
+//     and finishes its own share of the cluster's rows: the S partial sums
+//     of a row meet in rank order (deterministic, no workspace, no atomics),
+//     plus the LoRA term s . t . B^T from B rows staged by cp.async.
+//   - The codepoint-pair table is built from immediates (no memory reads),
+//     and the ring's position advances by adds (a division only when a warp
+//     starts its next task).
 // The codepoints enter as f16 (error <= 2^-12 relative) and the product
 // with a_hat stays in fp32, so the result is within the documented
 // tolerance of x . W_hat^T with the bf16-rounded W_hat.
@@ -32,8 +37,6 @@
 #include "kernels.h"
 
 namespace qlora {
-
-__constant__ float kNf4Const[16] = {QLORA_NF4_VALUES};
 
 constexpr int kGemvWarps = 16;
 constexpr int kGemvMaxSlice = 2048;  // K columns per CTA
@@ -46,6 +49,16 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Same with a zero accumulator in.
+__device__ __forceinline__ void mma_f16_16816_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                                uint32_t b1) {
+  asm(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
 }
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -83,24 +96,42 @@ __device__ __forceinline__ uint32_t lut(uint32_t lanebase, uint32_t w) {
   return v;
 }
 
+// Codepoint idx (0..15) as a chain of selects between immediates.
+template <int I>
+__device__ __forceinline__ float nf4_select(int idx, float acc) {
+  constexpr float kv[16] = {QLORA_NF4_VALUES};
+  constexpr float v = kv[I];
+  acc = idx == I ? v : acc;
+  if constexpr (I + 1 < 16)
+    return nf4_select<I + 1>(idx, acc);
+  else
+    return acc;
+}
+
 // bf16 pair -> f16 pair (both halves), round to nearest.
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return pack_f16x2(bf16_lo(w), bf16_hi(w));
 }
 
+// Bytes per staged row of B (r bf16 plus 16 bytes of padding, so that lanes
+// reading consecutive rows spread over the banks).
+__host__ __device__ inline int gemv_bpitch(int r) { return r * 2 + 16; }
+
 // Shared-memory layout of the GEMV kernel (bytes).
 struct GemvSmem {
-  int tab, xs, part, tpart, tfull, bsm, amax, total;
+  int tab, xs, part, tpw, tpart, tfull, bsm, amax, total;
 };
-__host__ __device__ inline GemvSmem gemv_smem_layout(int nblk, int MT, int rows_max, int G) {
+__host__ __device__ inline GemvSmem gemv_smem_layout(int nblk, int MT, int rows_max, int G, int S,
+                                                     int r) {
   GemvSmem L;
   L.tab = 0;  // 32 KB slack, then the 256 x 32 lanes x u32 table at a 32 KB-aligned address
-  L.xs = 65536;                                         // nblk x MT x 72 f16
-  L.part = L.xs + nblk * MT * kXRowHalves * 2;          // G x rows_max x 16 f32: partial y
-  L.tpart = L.part + G * rows_max * 16 * 4;             // 64 j x 16 tok f32: partial t
-  L.tfull = L.tpart + 64 * 16 * 4;                      // 16 tok x 64 j f32 (rank 0)
-  L.bsm = L.tfull + 16 * 64 * 4;                        // rows_max x 64 bf16 (rank 0)
-  L.amax = L.bsm + rows_max * 64 * 2;                   // 16 ints: per-token max |x| bits
+  L.xs = 65536;                                   // nblk x MT x 72 f16
+  L.part = L.xs + nblk * MT * kXRowHalves * 2;    // G x rows_max x 16 f32: partial y
+  L.tpw = L.part + G * rows_max * 16 * 4;         // 16 warps x 16 j x 16 tok f32: per-warp t
+  L.tpart = L.tpw + kGemvWarps * 16 * 16 * 4;     // 64 j x 16 tok f32: t over this CTA's slice
+  L.tfull = L.tpart + 64 * 16 * 4;                // 64 j x 16 tok f32: t over the whole K
+  L.bsm = L.tfull + 64 * 16 * 4;                  // this CTA's share of rows x B row
+  L.amax = L.bsm + ((rows_max + S - 1) / S) * gemv_bpitch(r);  // 16 ints: max |x| bits
   L.total = L.amax + 16 * 4;
   return L;
 }
@@ -119,19 +150,20 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(const Ge
   extern __shared__ __align__(16) uint8_t smem[];
   const int MT = NT * 8;
   const int nblk = p.slice >> 6;
-  const GemvSmem SL = gemv_smem_layout(nblk, MT, p.rows_max, p.kparts);
+  const int S = gridDim.y;
+  const GemvSmem SL = gemv_smem_layout(nblk, MT, p.rows_max, p.kparts, S, p.r);
   const uint32_t tab_u = (smem_u32(smem) + 0x7fffu) & ~0x7fffu;  // 32 KB aligned
   uint16_t *xs = reinterpret_cast<uint16_t *>(smem + SL.xs);
   float *part = reinterpret_cast<float *>(smem + SL.part);
+  float *tpw = reinterpret_cast<float *>(smem + SL.tpw);
   float *tpart = reinterpret_cast<float *>(smem + SL.tpart);
   float *tfull = reinterpret_cast<float *>(smem + SL.tfull);
-  uint16_t *bsm = reinterpret_cast<uint16_t *>(smem + SL.bsm);
   int *amax_bits = reinterpret_cast<int *>(smem + SL.amax);
+  const uint32_t bsm_u = smem_u32(smem + SL.bsm);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tq = lane & 3;
   const uint32_t rank = cluster_ctarank();
-  const int S = gridDim.y;
   const int RP = (p.r + 15) & ~15;
   const int kc0 = (int)rank * p.slice;
   const int kb0 = kc0 >> 6;
@@ -140,37 +172,83 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(const Ge
   const int rp_end = (int)((int64_t)p.row_pairs * (blockIdx.x + 1) / p.clusters);
   const int row_lo = rp_begin * 32;
   const int row_hi = min(rp_end * 32, p.N);
+  // This CTA's share of the cluster's rows in the final reduction.
+  const int share = (row_hi - row_lo + S - 1) / S;
+  const int sh_lo = min(row_lo + (int)rank * share, row_hi);
+  const int sh_hi = min(sh_lo + share, row_hi);
+  const int bpitch = gemv_bpitch(p.r);
 
-  // ---- prologue: codepoint-pair table, B rows (rank 0), x slice as f16
-  for (int i = threadIdx.x; i < 256 * 32; i += blockDim.x) {
-    const int b = i >> 5;  // uniform across a warp
-    const uint32_t v = pack_f16x2(kNf4Const[b >> 4], kNf4Const[b & 15]);
-    asm volatile("st.shared.u32 [%0], %1;" ::"r"(tab_u + i * 4), "r"(v) : "memory");
-  }
-  if (threadIdx.x < 16) amax_bits[threadIdx.x] = 0;
-  if (rank == 0) {
-    const int per_row = p.r >> 3;
-    const int npieces = (row_hi - row_lo) * per_row;
-    for (int i0 = threadIdx.x; i0 < npieces; i0 += 4 * blockDim.x) {
-      uint4 v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u * blockDim.x;
-        const int ic = i < npieces ? i : 0;
-        v[u] = ldg_nc_v4(p.B + (int64_t)(row_lo + ic / per_row) * p.r + (ic % per_row) * 8);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u * blockDim.x;
-        if (i < npieces)
-          *reinterpret_cast<uint4 *>(bsm + (i / per_row) * 64 + (i % per_row) * 8) = v[u];
-      }
+  // ---- 1. B rows of this CTA's row share go to shared memory (cp.async,
+  // waited for before the final reduction).
+  {
+    const int pieces = p.r >> 3;  // 16-byte pieces per B row
+    const int nb = (sh_hi - sh_lo) * pieces;
+    for (int i = threadIdx.x; i < nb; i += blockDim.x) {
+      const int rl = i / pieces, c = i - rl * pieces;
+      cp_async16(bsm_u + rl * bpitch + c * 16, p.B + (int64_t)(sh_lo + rl) * p.r + c * 8, 16);
     }
+    cp_async_commit();
   }
-  __syncthreads();
+
+  // Main-loop work.  A task is (row pair, k part): the CTA's K slice is cut
+  // into G = p.kparts parts so that P row pairs x G parts keep all warps
+  // busy; task t = rp_local * G + part, warp w runs tasks w, w + 16, ...
+  // Step = one 64-block of a task.
+  const int G = p.kparts;
+  const int bpp = (nblk + G - 1) / G;  // blocks per part
+  const int ntask = (rp_end - rp_begin) * G;
+  const int my_tasks = (ntask - warp + kGemvWarps - 1) / kGemvWarps;
+  const int steps = my_tasks > 0 ? my_tasks * bpp : 0;
+  // Position of a step, advanced by adds: a runtime division only when a
+  // warp moves to its next task.  Byte offsets into the packed weight and
+  // block indices are 32-bit (the launcher checks N * K / 2 < 2^32).
+  const uint32_t rs8 = 8u * (uint32_t)(p.K >> 1);  // bytes of 8 packed rows
+  const uint32_t cs8 = 8u * (uint32_t)kbr;         // blocks of 8 rows
+  struct Cursor {
+    int task, bi, blk;  // task index, block within the task, block within the slice
+    uint32_t pko;       // byte offset of (row pair row g, block, lane quarter)
+    uint32_t cbi;       // block index of (row pair row g, block)
+    uint32_t rowok;     // bit q: row pair row g + 8q is < N
+  };
+  auto set_task = [&](Cursor &c) {
+    const int rpl = c.task / G;
+    c.bi = 0;
+    c.blk = (c.task - rpl * G) * bpp;
+    const int row0 = (rp_begin + rpl) * 32 + g;
+    c.pko = (uint32_t)row0 * (uint32_t)(p.K >> 1) + (uint32_t)(kb0 + c.blk) * 32u + tq * 8;
+    c.cbi = (uint32_t)row0 * (uint32_t)kbr + (uint32_t)(kb0 + c.blk);
+    c.rowok = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) c.rowok |= row0 + 8 * q < p.N ? 1u << q : 0u;
+  };
+  auto advance = [&](Cursor &c) {
+    if (++c.bi == bpp) {
+      c.task += kGemvWarps;
+      if (c.task < ntask) set_task(c);
+    } else {
+      ++c.blk;
+      c.pko += 32;
+      ++c.cbi;
+    }
+  };
+  auto load_step = [&](const Cursor &c, GemvStep &P) {
+    const bool kok = c.task < ntask && c.blk < nblk && kb0 + c.blk < kbr;
+    P.valid = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // q = rt * 2 + h: row g + 8q of the pair
+      const bool ok = kok && ((c.rowok >> q) & 1u);
+      const uint32_t po = ok ? c.pko + q * rs8 : 0u;
+      const uint32_t bi = ok ? c.cbi + q * cs8 : 0u;
+      P.pk[q >> 1][q & 1] = ldg_nc_v2(p.packed + po);
+      P.code[q >> 1][q & 1] = ldg_nc_s8(p.codes + (p.use_code ? bi : 0u));
+      P.cv[q >> 1][q & 1] = ldg_nc_f32(p.cvec + (bi >> p.cshift));
+      P.valid |= ok ? (1u << q) : 0u;
+    }
+  };
+
   // x slice: MT tokens x nblk*64 columns, 8 columns per piece.
   const int xpieces = MT * nblk * 8;
-  constexpr int kMaxXp = (16 * (kGemvMaxSlice / 8)) / (kGemvWarps * 32);  // 8
+  constexpr int kMaxXp = NT * 4;  // MT x (2048 / 8) pieces over 512 threads
   uint4 xv[kMaxXp];
 #pragma unroll
   for (int u = 0; u < kMaxXp; ++u) {
@@ -179,6 +257,20 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(const Ge
     xv[u] = make_uint4(0, 0, 0, 0);
     if (i < xpieces && tok < p.M && col < p.K) xv[u] = ldg_nc_v4(p.x + (int64_t)tok * p.K + col);
   }
+
+  // ---- 2. codepoint-pair table, from immediates (no memory reads)
+  {
+    const float mine = nf4_select<0>(lane & 15, 0.f);  // lane l holds codepoint l & 15
+    for (int b = warp; b < 256; b += kGemvWarps) {
+      // low half: codepoint of the byte's high nibble, high half: low nibble
+      const uint32_t v = pack_f16x2(__shfl_sync(0xffffffffu, mine, b >> 4),
+                                    __shfl_sync(0xffffffffu, mine, b & 15));
+      asm volatile("st.shared.u32 [%0], %1;" ::"r"(tab_u + (b * 32 + lane) * 4), "r"(v) : "memory");
+    }
+  }
+  if (threadIdx.x < 16) amax_bits[threadIdx.x] = 0;
+  __syncthreads();
+  // ---- 3. x as f16 MMA fragments, each token scaled by 2^-e (exact)
 #pragma unroll
   for (int u = 0; u < kMaxXp; ++u) {
     const int i = threadIdx.x + u * blockDim.x;
@@ -233,89 +325,88 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(const Ge
     }
   };
 
-  // ---- t = x A^T over this CTA's slice (the last warp, before its rows)
-  if (warp == kGemvWarps - 1) {
-    for (int jt = 0; jt < RP / 16; ++jt) {
+  // first two slots of the main loop's register ring
+  constexpr int kRing = 3;  // ring slots (kRing - 1 steps in flight)
+  GemvStep P[kRing];
+  Cursor cl = {warp, 0, 0, 0u, 0u, 0u};  // load position
+  if (cl.task < ntask) set_task(cl);
+  struct CCursor {
+    int task, bi, blk;
+  } cc = {cl.task, 0, cl.blk};  // compute position
+#pragma unroll
+  for (int u = 0; u + 1 < kRing; ++u) {
+    load_step(cl, P[u]);
+    advance(cl);
+  }
+
+  // ---- 4. t = x A^T over this CTA's slice.  Warps with no main-loop task
+  // (a CTA with fewer than 16 tasks) compute it while the others stream W;
+  // otherwise all warps do, before their main loop.  Work unit = (16-wide j
+  // tile jt, block group grp): the blocks grp, grp + gpj, ... of the slice;
+  // unit u = jt + grp * JT goes to t-warp u, u + Tw, ...  Each unit's sum is
+  // parked in its own slot and the slots are added in group order after the
+  // main loop (fixed order).
+  const int JT = RP >> 4;
+  const int t_first = ntask < kGemvWarps ? ntask : 0;  // first t-warp
+  const int Tw = kGemvWarps - t_first;                 // t-warps
+  const int gpj = max(1, Tw / JT);                     // block groups per j tile
+  if (warp >= t_first) {
+    auto load_a = [&](int jt, int blk, uint4 (&av)[2][2]) {
+      const int col = kc0 + blk * 64 + tq * 16;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int j = jt * 16 + g + 8 * h;
+        const bool ok = blk < nblk && j < p.r && col < p.K;
+        const uint16_t *src = p.A + (ok ? (int64_t)j * p.K + col : 0);
+        av[h][0] = ok ? ldg_nc_v4(src) : make_uint4(0, 0, 0, 0);
+        av[h][1] = ok ? ldg_nc_v4(src + 8) : make_uint4(0, 0, 0, 0);
+      }
+    };
+    auto mma_a = [&](int blk, const uint4 (&av)[2][2], float (&d)[NT][4]) {
+      const uint32_t a0w[8] = {av[0][0].x, av[0][0].y, av[0][0].z, av[0][0].w,
+                               av[0][1].x, av[0][1].y, av[0][1].z, av[0][1].w};
+      const uint32_t a8w[8] = {av[1][0].x, av[1][0].y, av[1][0].z, av[1][0].w,
+                               av[1][1].x, av[1][1].y, av[1][1].z, av[1][1].w};
+      uint32_t xf[4][NT][2];
+      load_xf(blk, xf);
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const uint32_t a[4] = {bf16x2_to_f16x2(a0w[2 * jj]), bf16x2_to_f16x2(a8w[2 * jj]),
+                               bf16x2_to_f16x2(a0w[2 * jj + 1]), bf16x2_to_f16x2(a8w[2 * jj + 1])};
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_f16_16816(d[nt], a, xf[jj][nt][0], xf[jj][nt][1]);
+      }
+    };
+    for (int u = warp - t_first; u < JT * gpj; u += Tw) {
+      const int jt = u % JT, grp = u / JT;
       float d[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
-      for (int blk = 0; blk < nblk; ++blk) {
-        const int col = kc0 + blk * 64 + tq * 16;
-        uint32_t a0w[8] = {0, 0, 0, 0, 0, 0, 0, 0}, a8w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int j = jt * 16 + g + 8 * h;
-          if (j < p.r && col < p.K) {
-            const uint4 u0 = ldg_nc_v4(p.A + (int64_t)j * p.K + col);
-            const uint4 u1 = ldg_nc_v4(p.A + (int64_t)j * p.K + col + 8);
-            uint32_t *dst = h ? a8w : a0w;
-            dst[0] = u0.x, dst[1] = u0.y, dst[2] = u0.z, dst[3] = u0.w;
-            dst[4] = u1.x, dst[5] = u1.y, dst[6] = u1.z, dst[7] = u1.w;
-          }
-        }
-        uint32_t xf[4][NT][2];
-        load_xf(blk, xf);
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const uint32_t a[4] = {bf16x2_to_f16x2(a0w[2 * jj]), bf16x2_to_f16x2(a8w[2 * jj]),
-                                 bf16x2_to_f16x2(a0w[2 * jj + 1]), bf16x2_to_f16x2(a8w[2 * jj + 1])};
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_f16_16816(d[nt], a, xf[jj][nt][0], xf[jj][nt][1]);
+      // two blocks in flight: load the next while the current one multiplies
+      uint4 av0[2][2], av1[2][2];
+      load_a(jt, grp, av0);
+      for (int blk = grp; blk < nblk; blk += 2 * gpj) {
+        load_a(jt, blk + gpj, av1);
+        mma_a(blk, av0, d);
+        if (blk + gpj < nblk) {
+          load_a(jt, blk + 2 * gpj, av0);
+          mma_a(blk + gpj, av1, d);
         }
       }
+      float *tw = tpw + u * 256;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int tok = nt * 8 + 2 * tq;
-        tpart[(jt * 16 + g) * 16 + tok] = d[nt][0] * csc[nt][0];
-        tpart[(jt * 16 + g) * 16 + tok + 1] = d[nt][1] * csc[nt][1];
-        tpart[(jt * 16 + g + 8) * 16 + tok] = d[nt][2] * csc[nt][0];
-        tpart[(jt * 16 + g + 8) * 16 + tok + 1] = d[nt][3] * csc[nt][1];
+        tw[g * 16 + tok] = d[nt][0] * csc[nt][0];
+        tw[g * 16 + tok + 1] = d[nt][1] * csc[nt][1];
+        tw[(g + 8) * 16 + tok] = d[nt][2] * csc[nt][0];
+        tw[(g + 8) * 16 + tok + 1] = d[nt][3] * csc[nt][1];
       }
     }
   }
 
-  // ---- main loop.  A task is (row pair, k part): the CTA's K slice is cut
-  // into G = p.kparts parts so that P row pairs x G parts keep all warps
-  // busy; task t = rp_local * G + part, warp w runs tasks w, w + 16, ...
-  // Step = one 64-block of a task.
+  // ---- 5. main loop over the register ring
   const uint32_t lanebase = tab_u | (lane * 4);
-  const int G = p.kparts;
-  const int bpp = (nblk + G - 1) / G;  // blocks per part
-  const int ntask = (rp_end - rp_begin) * G;
-  const int my_tasks = (ntask - warp + kGemvWarps - 1) / kGemvWarps;
-  const int steps = my_tasks > 0 ? my_tasks * bpp : 0;
-  // Position of a step (task, block within the task), advanced by adds
-  // (no runtime divisions in the loop).
-  struct Cursor {
-    int task, bi;  // task index, block index within the task's part
-  };
-  auto advance = [&](Cursor &c) {
-    if (++c.bi == bpp) {
-      c.bi = 0;
-      c.task += kGemvWarps;
-    }
-  };
-  auto load_step = [&](const Cursor &c, GemvStep &P) {
-    const bool in = c.task < ntask;
-    const int rpl = in ? c.task / G : 0;  // once per block, G is small
-    const int blk = in ? (c.task - rpl * G) * bpp + c.bi : 0;
-    const int rp = rp_begin + rpl;
-    const int kb = kb0 + blk;
-    const bool kok = in && blk < nblk && kb < kbr;
-    P.valid = 0;
-#pragma unroll
-    for (int rt = 0; rt < 2; ++rt)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int row = rp * 32 + rt * 16 + 8 * h + g;
-        const bool ok = kok && row < p.N;
-        const int64_t b = ok ? (int64_t)row * kbr + kb : 0;
-        P.pk[rt][h] = ldg_nc_v2(p.packed + (ok ? (b << 5) + tq * 8 : 0));
-        P.code[rt][h] = ldg_nc_s8(p.codes + (p.use_code ? b : 0));
-        P.cv[rt][h] = ldg_nc_f32(p.cvec + (b >> p.cshift));
-        P.valid |= ok ? (1u << (rt * 2 + h)) : 0u;
-      }
-  };
   float acc[2][NT][4];
   auto zero_acc = [&]() {
 #pragma unroll
@@ -323,17 +414,22 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(const Ge
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) acc[rt][nt][0] = acc[rt][nt][1] = acc[rt][nt][2] = acc[rt][nt][3] = 0.f;
   };
-  auto compute_step = [&](const Cursor &c, const GemvStep &P) {
-    const int rpl = c.task / G;
-    const int part_i = c.task - rpl * G;
-    const int blk = min(part_i * bpp + c.bi, nblk - 1);
+  auto advance_c = [&](CCursor &c) {
+    if (++c.bi == bpp) {
+      c.bi = 0;
+      c.task += kGemvWarps;
+      c.blk = (c.task % G) * bpp;
+    } else {
+      ++c.blk;
+    }
+  };
+  auto compute_step = [&](const CCursor &c, const GemvStep &P) {
+    const int blk = min(c.blk, nblk - 1);
     uint32_t xf[4][NT][2];
     load_xf(blk, xf);
 #pragma unroll
     for (int rt = 0; rt < 2; ++rt) {
       float tmp[NT][4];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) tmp[nt][0] = tmp[nt][1] = tmp[nt][2] = tmp[nt][3] = 0.f;
       const uint32_t w0[2] = {P.pk[rt][0].x, P.pk[rt][0].y};
       const uint32_t w8[2] = {P.pk[rt][1].x, P.pk[rt][1].y};
 #pragma unroll
@@ -352,7 +448,12 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(const Ge
           a[3] = lut<3>(lanebase, w8[wi]);
         }
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_f16_16816(tmp[nt], a, xf[j][nt][0], xf[j][nt][1]);
+        for (int nt = 0; nt < NT; ++nt) {
+          if (j == 0)
+            mma_f16_16816_z(tmp[nt], a, xf[j][nt][0], xf[j][nt][1]);
+          else
+            mma_f16_16816(tmp[nt], a, xf[j][nt][0], xf[j][nt][1]);
+        }
       }
       const float ah0 = ((P.valid >> (rt * 2)) & 1u)
                             ? (p.use_code ? __fmul_rn((float)P.code[rt][0], P.cv[rt][0]) : P.cv[rt][0])
@@ -369,6 +470,8 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(const Ge
       }
     }
     if (c.bi == bpp - 1) {  // end of a task: scale by 2^e and park in its smem slab
+      const int rpl = c.task / G;
+      const int part_i = c.task - rpl * G;
 #pragma unroll
       for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
@@ -384,25 +487,20 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(const Ge
     }
   };
   zero_acc();
-  GemvStep P[3];
-  Cursor cc = {warp, 0}, cl = {warp, 0};  // compute / load positions
-  load_step(cl, P[0]);
-  advance(cl);
-  load_step(cl, P[1]);
-  advance(cl);
-  for (int st0 = 0; st0 < steps; st0 += 3) {
+  for (int st0 = 0; st0 < steps; st0 += kRing) {
 #pragma unroll
-    for (int u = 0; u < 3; ++u) {
+    for (int u = 0; u < kRing; ++u) {
       if (st0 + u < steps) {
-        load_step(cl, P[(u + 2) % 3]);
+        load_step(cl, P[(u + kRing - 1) % kRing]);
         advance(cl);
         compute_step(cc, P[u]);
-        advance(cc);
+        advance_c(cc);
       }
     }
   }
 
-  // ---- the G k-part slabs of each row meet in slab 0 (fixed order)
+  // ---- 6. within the CTA: the G k-part slabs of each row meet in slab 0,
+  // and the per-warp t sums in tpart (fixed orders)
   __syncthreads();
   if (G > 1) {
     const int nrows_l = (rp_end - rp_begin) * 32;
@@ -412,55 +510,87 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(const Ge
       part[i] = v;
     }
   }
-  // ---- cluster reduction in CTA 0: t first, then y (+ LoRA), rank order
+  {
+    for (int i = threadIdx.x; i < RP * 16; i += blockDim.x) {
+      const int j = i >> 4, tok = i & 15;
+      float v = 0.f;
+      if (tok < MT)
+        for (int grp = 0; grp < gpj; ++grp) v += tpw[((j >> 4) + grp * JT) * 256 + (j & 15) * 16 + tok];
+      tpart[i] = v;
+    }
+  }
+  // ---- 7. across the cluster (rank order): every CTA forms the whole-K t,
+  // then finishes its share of the rows, y = sum of the ranks' partials + s t B^T
   __syncthreads();
   cluster_sync_all();
-  if (rank == 0) {
-    for (int i = threadIdx.x; i < 16 * RP; i += blockDim.x) {
-      const int tok = i / RP, j = i % RP;
-      float v = 0.f;
-      for (int q = 0; q < S; ++q) v += ld_dsmem_f32(tpart + j * 16 + tok, (uint32_t)q);
-      tfull[tok * 64 + j] = v;
-      if (p.t_save && blockIdx.x == 0 && tok < p.M && j < p.r) p.t_save[tok * p.r + j] = v;
-    }
-    __syncthreads();
-    const int nrows = row_hi - row_lo;
-    const int nout = nrows * p.M;
+  for (int i = threadIdx.x; i < RP * 16; i += blockDim.x) {
+    float v = 0.f;
+    for (int q = 0; q < S; ++q) v += ld_dsmem_f32(tpart + i, (uint32_t)q);
+    tfull[i] = v;
+    const int j = i >> 4, tok = i & 15;
+    if (p.t_save && rank == 0 && blockIdx.x == 0 && tok < p.M && j < p.r) p.t_save[tok * p.r + j] = v;
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  {
+    const int nsh = sh_hi - sh_lo;
+    const int nout = nsh * p.M;
+    const int pieces = p.r >> 3;
     for (int i0 = threadIdx.x; i0 < nout; i0 += 4 * blockDim.x) {
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      int row[4], tok[4];
+      float v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * blockDim.x;
+        const int ic = i < nout ? i : 0;
+        row[u] = ic / p.M;
+        tok[u] = ic - row[u] * p.M;
+        v[u] = 0.f;
+      }
       for (int q = 0; q < S; ++q) {
 #pragma unroll
+        for (int u = 0; u < 4; ++u)
+          v[u] += ld_dsmem_f32(part + (sh_lo - row_lo + row[u]) * 16 + tok[u], (uint32_t)q);
+      }
+      float l[4] = {0.f, 0.f, 0.f, 0.f};  // LoRA term t . B^T
+      for (int c = 0; c < pieces; ++c) {
+#pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int i = i0 + u * blockDim.x;
-          const int ic = i < nout ? i : 0;
-          v[u] += ld_dsmem_f32(part + (ic % nrows) * 16 + ic / nrows, (uint32_t)q);
+          const uint4 bw = lds_v4(bsm_u + row[u] * bpitch + c * 16);
+          const float *tc = tfull + c * 8 * 16 + tok[u];
+          l[u] = fmaf(tc[0 * 16], bf16_lo(bw.x), l[u]);
+          l[u] = fmaf(tc[1 * 16], bf16_hi(bw.x), l[u]);
+          l[u] = fmaf(tc[2 * 16], bf16_lo(bw.y), l[u]);
+          l[u] = fmaf(tc[3 * 16], bf16_hi(bw.y), l[u]);
+          l[u] = fmaf(tc[4 * 16], bf16_lo(bw.z), l[u]);
+          l[u] = fmaf(tc[5 * 16], bf16_hi(bw.z), l[u]);
+          l[u] = fmaf(tc[6 * 16], bf16_lo(bw.w), l[u]);
+          l[u] = fmaf(tc[7 * 16], bf16_hi(bw.w), l[u]);
         }
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int i = i0 + u * blockDim.x;
-        if (i >= nout) continue;
-        const int tok = i / nrows, row = i % nrows;
-        float l = 0.f;  // LoRA term s . t . B^T
-        for (int j = 0; j < p.r; ++j)
-          l = fmaf(tfull[tok * 64 + j], __uint_as_float((uint32_t)bsm[row * 64 + j] << 16), l);
-        const float y = fmaf(p.s, l, v[u]);
-        const int n = row_lo + row;
-        if (p.y_bf16)
-          reinterpret_cast<__nv_bfloat16 *>(p.y)[(int64_t)tok * p.N + n] = __float2bfloat16_rn(y);
-        else
-          reinterpret_cast<float *>(p.y)[(int64_t)tok * p.N + n] = y;
+        if (i < nout) {
+          const float y = fmaf(p.s, l[u], v[u]);
+          const int64_t o = (int64_t)tok[u] * p.N + sh_lo + row[u];
+          if (p.y_bf16)
+            reinterpret_cast<__nv_bfloat16 *>(p.y)[o] = __float2bfloat16_rn(y);
+          else
+            reinterpret_cast<float *>(p.y)[o] = y;
+        }
       }
     }
   }
-  cluster_sync_all();  // keep every CTA's shared memory alive until rank 0 has read it
+  cluster_sync_all();  // keep every CTA's shared memory alive until the others have read it
 }
 
 // ------------------------------------------------------------ launchers
 // Cluster size S = ceil(K / 2048): the x slice of a CTA fits shared memory.
 // (Larger clusters would leave SMs idle: a cluster must fit in one GPC.)
-int gemv_plan(int K, int M, int *warps, int *S) {
+int gemv_plan(int N, int K, int M, int *warps, int *S) {
   if (M < 1 || M > 16) return -1;
+  if ((uint64_t)N * (uint64_t)K / 2 >= (1ull << 32)) return -1;  // 32-bit byte offsets
   int smin = (K + kGemvMaxSlice - 1) / kGemvMaxSlice;
   if (smin < 1) smin = 1;
   if (smin > 8) return -1;
@@ -471,7 +601,7 @@ int gemv_plan(int K, int M, int *warps, int *S) {
 
 cudaError_t launch_gemv(GemvArgs a, int num_sms, cudaStream_t s) {
   int warps, S;
-  if (gemv_plan(a.K, a.M, &warps, &S) != 0) return cudaErrorInvalidValue;
+  if (gemv_plan(a.N, a.K, a.M, &warps, &S) != 0) return cudaErrorInvalidValue;
   a.slice = ((a.K + S - 1) / S + 63) / 64 * 64;
   a.row_pairs = (a.N + 31) / 32;
   int clusters = num_sms / S;
@@ -485,7 +615,7 @@ cudaError_t launch_gemv(GemvArgs a, int num_sms, cudaStream_t s) {
   if (G > a.slice / 64) G = a.slice / 64;
   a.kparts = G;
   const int nt = a.M > 8 ? 2 : 1;
-  const size_t smem = gemv_smem_layout(a.slice / 64, nt * 8, a.rows_max, G).total;
+  const size_t smem = gemv_smem_layout(a.slice / 64, nt * 8, a.rows_max, G, S, a.r).total;
   if (smem > 232448) return cudaErrorInvalidValue;
   // Dynamic shared memory limit raised to what this launch needs (once per
   // new maximum), cluster sizes above 8 never requested.

@@ -175,6 +175,29 @@ def test_gate_decode_gemv_full_size(M):
     assert_close(to_np_f32(y), y_ref, f"y gate decode M={M}")
 
 
+GEMV_WIDE_K = [
+    # K = 14336: the K slices of one row range spread over a cluster of 7 CTAs
+    inputs.LinearShape("down_proj_4096x14336_M3_r16", N=4096, K=14336, M=3, r=16, alpha=32.0),
+    # K = 4160 = 65 x 64 over 3 CTAs (the last slice shorter than the others),
+    # r = 40 (three 16-wide tiles of t, the last one ragged), N = 1032 (a
+    # ragged last row pair), 9 tokens (two 8-token tiles)
+    inputs.LinearShape("ragged_N1032_K4160_M9_r40", N=1032, K=4160, M=9, r=40, alpha=80.0),
+]
+
+
+@pytest.mark.parametrize("shape", GEMV_WIDE_K, ids=lambda s: s.name)
+def test_decode_gemv_wide_k(shape):
+    d, g, q, w_hat = _prep(shape, with_dy=False)
+    ws = _ws(shape)
+    y, t = _fwd(shape, g, q, ws, FORCE_GEMV)
+    y_ref, t_ref = oracle.linear_fwd(d["x"].float().numpy(), w_hat, d["A"].float().numpy(),
+                                     d["B"].float().numpy(), shape.alpha)
+    assert_close(to_np_f32(y), y_ref, f"y {shape.name}")
+    assert_close(to_np_f32(t), t_ref, f"t {shape.name}", max_abs=1e-3, rel_fro=1e-5)
+    y16, _ = _fwd(shape, g, q, ws, FORCE_GEMV, y_dtype=torch.bfloat16)
+    assert torch.equal(y16, y.to(torch.bfloat16)), "bf16 output is not the rounded fp32 result"
+
+
 def test_gate_prefill_forward_full_size():
     """gate_proj 14336x4096 at 2048 tokens: the widest layer of the layer set
     (its pair tiles are 224 columns wide), y checked on sampled rows."""
