@@ -316,8 +316,7 @@ qlora_status qlora_linear_fwd(const qlora_nf4_weight *w, const uint16_t *x, int6
   const float sc = alpha / (float)r;
   const WsLayout L = ws_layout(M, N, K, r);
   uint8_t *wsb = static_cast<uint8_t *>(ws);
-  int gw, gS;
-  const bool gemv_ok = M <= 16 && gemv_plan(N, K, (int)M, &gw, &gS) == 0;
+  const bool gemv_ok = M <= 16 && gemv_plan(N, K, (int)M, r, num_sms_current()) == 0;
   const bool use_gemv =
       (flags & QLORA_FLAG_FORCE_GEMV) || (M <= 16 && gemv_ok && !(flags & QLORA_FLAG_FORCE_GEMM));
   if (use_gemv) {

@@ -119,8 +119,12 @@ __host__ __device__ inline int gemv_bpitch(int r) { return r * 2 + 16; }
 
 // Shared-memory layout of the GEMV kernel (bytes).
 struct GemvSmem {
-  int tab, xs, part, tpw, tpart, tfull, bsm, amax, total;
+  int tab, xs, part, tpw, tpart, tfull, bsm, amax, ah, total;
 };
+// Pitch (floats) of the block-constant array: one padded row of the CTA's
+// rows per 64-block, so that lanes storing consecutive blocks of one row
+// land in different banks.
+__host__ __device__ inline int gemv_ah_pitch(int rows_max) { return rows_max + 1; }
 __host__ __device__ inline GemvSmem gemv_smem_layout(int nblk, int MT, int rows_max, int G, int S,
                                                      int r) {
   GemvSmem L;
@@ -132,18 +136,10 @@ __host__ __device__ inline GemvSmem gemv_smem_layout(int nblk, int MT, int rows_
   L.tfull = L.tpart + 64 * 16 * 4;                // 64 j x 16 tok f32: t over the whole K
   L.bsm = L.tfull + 64 * 16 * 4;                  // this CTA's share of rows x B row
   L.amax = L.bsm + ((rows_max + S - 1) / S) * gemv_bpitch(r);  // 16 ints: max |x| bits
-  L.total = L.amax + 16 * 4;
+  L.ah = L.amax + 16 * 4;  // nblk x pitch f32: a_hat of (block, row) of this CTA's range
+  L.total = L.ah + nblk * gemv_ah_pitch(rows_max) * 4;
   return L;
 }
-
-// Packed bytes and block constants of rows (g, g+8) of the two row tiles of
-// one 32-row pair, one 64-block.  Raw until use (see the GEMM producer).
-struct GemvStep {
-  uint2 pk[2][2];
-  int code[2][2];
-  float cv[2][2];
-  uint32_t valid;  // bit (rt * 2 + h)
-};
 
 template <int NT>
 __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(const GemvArgs p) {
@@ -159,6 +155,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(const Ge
   float *tpart = reinterpret_cast<float *>(smem + SL.tpart);
   float *tfull = reinterpret_cast<float *>(smem + SL.tfull);
   int *amax_bits = reinterpret_cast<int *>(smem + SL.amax);
+  float *ah = reinterpret_cast<float *>(smem + SL.ah);
   const uint32_t bsm_u = smem_u32(smem + SL.bsm);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -197,55 +194,6 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(const Ge
   const int G = p.kparts;
   const int bpp = (nblk + G - 1) / G;  // blocks per part
   const int ntask = (rp_end - rp_begin) * G;
-  const int my_tasks = (ntask - warp + kGemvWarps - 1) / kGemvWarps;
-  const int steps = my_tasks > 0 ? my_tasks * bpp : 0;
-  // Position of a step, advanced by adds: a runtime division only when a
-  // warp moves to its next task.  Byte offsets into the packed weight and
-  // block indices are 32-bit (the launcher checks N * K / 2 < 2^32).
-  const uint32_t rs8 = 8u * (uint32_t)(p.K >> 1);  // bytes of 8 packed rows
-  const uint32_t cs8 = 8u * (uint32_t)kbr;         // blocks of 8 rows
-  struct Cursor {
-    int task, bi, blk;  // task index, block within the task, block within the slice
-    uint32_t pko;       // byte offset of (row pair row g, block, lane quarter)
-    uint32_t cbi;       // block index of (row pair row g, block)
-    uint32_t rowok;     // bit q: row pair row g + 8q is < N
-  };
-  auto set_task = [&](Cursor &c) {
-    const int rpl = c.task / G;
-    c.bi = 0;
-    c.blk = (c.task - rpl * G) * bpp;
-    const int row0 = (rp_begin + rpl) * 32 + g;
-    c.pko = (uint32_t)row0 * (uint32_t)(p.K >> 1) + (uint32_t)(kb0 + c.blk) * 32u + tq * 8;
-    c.cbi = (uint32_t)row0 * (uint32_t)kbr + (uint32_t)(kb0 + c.blk);
-    c.rowok = 0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) c.rowok |= row0 + 8 * q < p.N ? 1u << q : 0u;
-  };
-  auto advance = [&](Cursor &c) {
-    if (++c.bi == bpp) {
-      c.task += kGemvWarps;
-      if (c.task < ntask) set_task(c);
-    } else {
-      ++c.blk;
-      c.pko += 32;
-      ++c.cbi;
-    }
-  };
-  auto load_step = [&](const Cursor &c, GemvStep &P) {
-    const bool kok = c.task < ntask && c.blk < nblk && kb0 + c.blk < kbr;
-    P.valid = 0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {  // q = rt * 2 + h: row g + 8q of the pair
-      const bool ok = kok && ((c.rowok >> q) & 1u);
-      const uint32_t po = ok ? c.pko + q * rs8 : 0u;
-      const uint32_t bi = ok ? c.cbi + q * cs8 : 0u;
-      P.pk[q >> 1][q & 1] = ldg_nc_v2(p.packed + po);
-      P.code[q >> 1][q & 1] = ldg_nc_s8(p.codes + (p.use_code ? bi : 0u));
-      P.cv[q >> 1][q & 1] = ldg_nc_f32(p.cvec + (bi >> p.cshift));
-      P.valid |= ok ? (1u << q) : 0u;
-    }
-  };
-
   // x slice: MT tokens x nblk*64 columns, 8 columns per piece.
   const int xpieces = MT * nblk * 8;
   constexpr int kMaxXp = NT * 4;  // MT x (2048 / 8) pieces over 512 threads
@@ -269,6 +217,32 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(const Ge
     }
   }
   if (threadIdx.x < 16) amax_bits[threadIdx.x] = 0;
+  // block constants a_hat of the CTA's rows x slice blocks (0 outside W):
+  // lane = block, warp + 16 i = row, all loads of a thread in one batch
+  const int nrows_l = (rp_end - rp_begin) * 32;
+  const int ah_pitch = gemv_ah_pitch(p.rows_max);
+  if (lane < nblk) {
+    constexpr int kAhBatch = 14;
+    const bool kin = kb0 + lane < kbr;
+    for (int rl0 = warp; rl0 < nrows_l; rl0 += kGemvWarps * kAhBatch) {
+      int code[kAhBatch];
+      float cv[kAhBatch];
+#pragma unroll
+      for (int i = 0; i < kAhBatch; ++i) {
+        const int row = row_lo + rl0 + kGemvWarps * i;
+        const bool ok = kin && rl0 + kGemvWarps * i < nrows_l && row < p.N;
+        const int64_t b = ok ? (int64_t)row * kbr + kb0 + lane : 0;
+        code[i] = ldg_nc_s8(p.codes + (p.use_code ? b : 0));
+        cv[i] = ok ? ldg_nc_f32(p.cvec + (b >> p.cshift)) : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < kAhBatch; ++i) {
+        const int rl = rl0 + kGemvWarps * i;
+        if (rl < nrows_l)
+          ah[lane * ah_pitch + rl] = p.use_code ? __fmul_rn((float)code[i], cv[i]) : cv[i];
+      }
+    }
+  }
   __syncthreads();
   // ---- 3. x as f16 MMA fragments, each token scaled by 2^-e (exact)
 #pragma unroll
@@ -324,20 +298,6 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(const Ge
       xf[2][nt][0] = b.x, xf[2][nt][1] = b.y, xf[3][nt][0] = b.z, xf[3][nt][1] = b.w;
     }
   };
-
-  // first two slots of the main loop's register ring
-  constexpr int kRing = 3;  // ring slots (kRing - 1 steps in flight)
-  GemvStep P[kRing];
-  Cursor cl = {warp, 0, 0, 0u, 0u, 0u};  // load position
-  if (cl.task < ntask) set_task(cl);
-  struct CCursor {
-    int task, bi, blk;
-  } cc = {cl.task, 0, cl.blk};  // compute position
-#pragma unroll
-  for (int u = 0; u + 1 < kRing; ++u) {
-    load_step(cl, P[u]);
-    advance(cl);
-  }
 
   // ---- 4. t = x A^T over this CTA's slice.  Warps with no main-loop task
   // (a CTA with fewer than 16 tasks) compute it while the others stream W;
@@ -405,98 +365,108 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(const Ge
     }
   }
 
-  // ---- 5. main loop over the register ring
+  // ---- 5. main loop.  A task is (row pair, k part): the CTA's K slice is
+  // cut into G = p.kparts parts so that P row pairs x G parts keep all warps
+  // busy; task t = rp_local * G + part, warp w runs tasks w, w + 16, ...
+  // Step = one 64-block: the packed bytes of rows g + 8q (q = rt * 2 + h)
+  // come through a register ring from one pointer per row (a whole ring
+  // turn's loads are pointer + immediate); a_hat comes from shared memory.
   const uint32_t lanebase = tab_u | (lane * 4);
-  float acc[2][NT][4];
-  auto zero_acc = [&]() {
+  constexpr int kRing = 4;  // ring slots (kRing - 1 blocks in flight)
+  for (int task = warp; task < ntask; task += kGemvWarps) {
+    const int rpl = task / G;
+    const int part_i = task - rpl * G;
+    const int blk0 = part_i * bpp;
+    // blocks of the task inside the slice and inside K (warp-uniform)
+    const int nv = max(0, min(min(bpp, nblk - blk0), (int)kbr - (kb0 + blk0)));
+    const int row0 = row_lo + rpl * 32 + g;
+    const uint8_t *pr[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int row = row0 + 8 * q;
+      const int rr = row < p.N ? row : row_lo;  // a_hat is 0 for rows past N
+      pr[q] = p.packed + (size_t)rr * (size_t)(p.K >> 1) + (size_t)(kb0 + blk0) * 32 + tq * 8;
+    }
+    float acc[2][NT][4];
 #pragma unroll
     for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) acc[rt][nt][0] = acc[rt][nt][1] = acc[rt][nt][2] = acc[rt][nt][3] = 0.f;
-  };
-  auto advance_c = [&](CCursor &c) {
-    if (++c.bi == bpp) {
-      c.bi = 0;
-      c.task += kGemvWarps;
-      c.blk = (c.task % G) * bpp;
-    } else {
-      ++c.blk;
-    }
-  };
-  auto compute_step = [&](const CCursor &c, const GemvStep &P) {
-    const int blk = min(c.blk, nblk - 1);
-    uint32_t xf[4][NT][2];
-    load_xf(blk, xf);
+    uint2 P[kRing][4];
 #pragma unroll
-    for (int rt = 0; rt < 2; ++rt) {
-      float tmp[NT][4];
-      const uint32_t w0[2] = {P.pk[rt][0].x, P.pk[rt][0].y};
-      const uint32_t w8[2] = {P.pk[rt][1].x, P.pk[rt][1].y};
+    for (int u = 0; u + 1 < kRing; ++u)
+      if (u < nv) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int wi = j >> 1;
-        uint32_t a[4];
-        if ((j & 1) == 0) {
-          a[0] = lut<0>(lanebase, w0[wi]);
-          a[1] = lut<0>(lanebase, w8[wi]);
-          a[2] = lut<1>(lanebase, w0[wi]);
-          a[3] = lut<1>(lanebase, w8[wi]);
-        } else {
-          a[0] = lut<2>(lanebase, w0[wi]);
-          a[1] = lut<2>(lanebase, w8[wi]);
-          a[2] = lut<3>(lanebase, w0[wi]);
-          a[3] = lut<3>(lanebase, w8[wi]);
-        }
+        for (int q = 0; q < 4; ++q) P[u][q] = ldg_nc_v2(pr[q] + u * 32);
+      }
+    const float *ahr = ah + blk0 * ah_pitch + rpl * 32 + g;  // a_hat of (block, row g)
+    for (int b0 = 0; b0 < nv; b0 += kRing) {
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          if (j == 0)
-            mma_f16_16816_z(tmp[nt], a, xf[j][nt][0], xf[j][nt][1]);
-          else
-            mma_f16_16816(tmp[nt], a, xf[j][nt][0], xf[j][nt][1]);
+      for (int u = 0; u < kRing; ++u) {
+        const int b = b0 + u;
+        if (b < nv) {
+          if (b + kRing - 1 < nv) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              P[(u + kRing - 1) % kRing][q] = ldg_nc_v2(pr[q] + (u + kRing - 1) * 32);
+          }
+          uint32_t xf[4][NT][2];
+          load_xf(blk0 + b, xf);
+          const float *ahb = ahr + b * ah_pitch;
+#pragma unroll
+          for (int rt = 0; rt < 2; ++rt) {
+            float tmp[NT][4];
+            const uint32_t w0[2] = {P[u][rt * 2].x, P[u][rt * 2].y};
+            const uint32_t w8[2] = {P[u][rt * 2 + 1].x, P[u][rt * 2 + 1].y};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int wi = j >> 1;
+              uint32_t a[4];
+              if ((j & 1) == 0) {
+                a[0] = lut<0>(lanebase, w0[wi]);
+                a[1] = lut<0>(lanebase, w8[wi]);
+                a[2] = lut<1>(lanebase, w0[wi]);
+                a[3] = lut<1>(lanebase, w8[wi]);
+              } else {
+                a[0] = lut<2>(lanebase, w0[wi]);
+                a[1] = lut<2>(lanebase, w8[wi]);
+                a[2] = lut<3>(lanebase, w0[wi]);
+                a[3] = lut<3>(lanebase, w8[wi]);
+              }
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                if (j == 0)
+                  mma_f16_16816_z(tmp[nt], a, xf[j][nt][0], xf[j][nt][1]);
+                else
+                  mma_f16_16816(tmp[nt], a, xf[j][nt][0], xf[j][nt][1]);
+              }
+            }
+            const float ah0 = ahb[rt * 16], ah8 = ahb[rt * 16 + 8];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              acc[rt][nt][0] = fmaf(ah0, tmp[nt][0], acc[rt][nt][0]);
+              acc[rt][nt][1] = fmaf(ah0, tmp[nt][1], acc[rt][nt][1]);
+              acc[rt][nt][2] = fmaf(ah8, tmp[nt][2], acc[rt][nt][2]);
+              acc[rt][nt][3] = fmaf(ah8, tmp[nt][3], acc[rt][nt][3]);
+            }
+          }
         }
       }
-      const float ah0 = ((P.valid >> (rt * 2)) & 1u)
-                            ? (p.use_code ? __fmul_rn((float)P.code[rt][0], P.cv[rt][0]) : P.cv[rt][0])
-                            : 0.f;
-      const float ah8 = ((P.valid >> (rt * 2 + 1)) & 1u)
-                            ? (p.use_code ? __fmul_rn((float)P.code[rt][1], P.cv[rt][1]) : P.cv[rt][1])
-                            : 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) pr[q] += kRing * 32;
+    }
+    // the task's sum, scaled by 2^e, parked in its k part's slab
+#pragma unroll
+    for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        acc[rt][nt][0] = fmaf(ah0, tmp[nt][0], acc[rt][nt][0]);
-        acc[rt][nt][1] = fmaf(ah0, tmp[nt][1], acc[rt][nt][1]);
-        acc[rt][nt][2] = fmaf(ah8, tmp[nt][2], acc[rt][nt][2]);
-        acc[rt][nt][3] = fmaf(ah8, tmp[nt][3], acc[rt][nt][3]);
+        const int tok = nt * 8 + 2 * tq;
+        float *r0 = part + (part_i * p.rows_max + rpl * 32 + rt * 16 + g) * 16 + tok;
+        *reinterpret_cast<float2 *>(r0) =
+            make_float2(acc[rt][nt][0] * csc[nt][0], acc[rt][nt][1] * csc[nt][1]);
+        *reinterpret_cast<float2 *>(r0 + 8 * 16) =
+            make_float2(acc[rt][nt][2] * csc[nt][0], acc[rt][nt][3] * csc[nt][1]);
       }
-    }
-    if (c.bi == bpp - 1) {  // end of a task: scale by 2^e and park in its smem slab
-      const int rpl = c.task / G;
-      const int part_i = c.task - rpl * G;
-#pragma unroll
-      for (int rt = 0; rt < 2; ++rt)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const int tok = nt * 8 + 2 * tq;
-          float *r0 = part + (part_i * p.rows_max + rpl * 32 + rt * 16 + g) * 16 + tok;
-          *reinterpret_cast<float2 *>(r0) =
-              make_float2(acc[rt][nt][0] * csc[nt][0], acc[rt][nt][1] * csc[nt][1]);
-          *reinterpret_cast<float2 *>(r0 + 8 * 16) =
-              make_float2(acc[rt][nt][2] * csc[nt][0], acc[rt][nt][3] * csc[nt][1]);
-        }
-      zero_acc();
-    }
-  };
-  zero_acc();
-  for (int st0 = 0; st0 < steps; st0 += kRing) {
-#pragma unroll
-    for (int u = 0; u < kRing; ++u) {
-      if (st0 + u < steps) {
-        load_step(cl, P[(u + kRing - 1) % kRing]);
-        advance(cl);
-        compute_step(cc, P[u]);
-        advance_c(cc);
-      }
-    }
   }
 
   // ---- 6. within the CTA: the G k-part slabs of each row meet in slab 0,
@@ -588,20 +558,15 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(const Ge
 // ------------------------------------------------------------ launchers
 // Cluster size S = ceil(K / 2048): the x slice of a CTA fits shared memory.
 // (Larger clusters would leave SMs idle: a cluster must fit in one GPC.)
-int gemv_plan(int N, int K, int M, int *warps, int *S) {
-  if (M < 1 || M > 16) return -1;
-  if ((uint64_t)N * (uint64_t)K / 2 >= (1ull << 32)) return -1;  // 32-bit byte offsets
-  int smin = (K + kGemvMaxSlice - 1) / kGemvMaxSlice;
-  if (smin < 1) smin = 1;
-  if (smin > 8) return -1;
-  *warps = kGemvWarps;
-  *S = smin;
-  return 0;
-}
-
-cudaError_t launch_gemv(GemvArgs a, int num_sms, cudaStream_t s) {
-  int warps, S;
-  if (gemv_plan(a.N, a.K, a.M, &warps, &S) != 0) return cudaErrorInvalidValue;
+// Fills the launcher's fields of `a`; -1 when the shape does not fit the
+// kernel (more than 16 tokens, K beyond 8 slices, byte offsets past 32 bits,
+// or more shared memory than a CTA may have).
+static int gemv_config(GemvArgs &a, int num_sms, int *S_out, size_t *smem_out) {
+  if (a.M < 1 || a.M > 16) return -1;
+  if ((uint64_t)a.N * (uint64_t)a.K / 2 >= (1ull << 32)) return -1;  // 32-bit byte offsets
+  int S = (a.K + kGemvMaxSlice - 1) / kGemvMaxSlice;
+  if (S < 1) S = 1;
+  if (S > 8) return -1;
   a.slice = ((a.K + S - 1) / S + 63) / 64 * 64;
   a.row_pairs = (a.N + 31) / 32;
   int clusters = num_sms / S;
@@ -616,7 +581,30 @@ cudaError_t launch_gemv(GemvArgs a, int num_sms, cudaStream_t s) {
   a.kparts = G;
   const int nt = a.M > 8 ? 2 : 1;
   const size_t smem = gemv_smem_layout(a.slice / 64, nt * 8, a.rows_max, G, S, a.r).total;
-  if (smem > 232448) return cudaErrorInvalidValue;
+  if (smem > 232448) return -1;
+  *S_out = S;
+  *smem_out = smem;
+  return 0;
+}
+
+int gemv_plan(int N, int K, int M, int r, int num_sms) {
+  GemvArgs a{};
+  a.N = N;
+  a.K = K;
+  a.M = M;
+  a.r = r;
+  int S;
+  size_t smem;
+  return gemv_config(a, num_sms, &S, &smem);
+}
+
+cudaError_t launch_gemv(GemvArgs a, int num_sms, cudaStream_t s) {
+  int S;
+  size_t smem;
+  if (gemv_config(a, num_sms, &S, &smem) != 0) return cudaErrorInvalidValue;
+  const int nt = a.M > 8 ? 2 : 1;
+  const int clusters = a.clusters;
+  const int warps = kGemvWarps;
   // Dynamic shared memory limit raised to what this launch needs (once per
   // new maximum), cluster sizes above 8 never requested.
   static size_t smem_set[2] = {0, 0};

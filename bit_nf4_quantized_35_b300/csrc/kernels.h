@@ -87,7 +87,8 @@ struct GemvArgs {
   int rows_max;   // rows of the largest per-cluster row range
   int kparts;     // k parts per row pair inside a CTA (warps per row pair)
 };
-int gemv_plan(int N, int K, int M, int *warps, int *S);
+// 0 when the decode kernel takes this shape on num_sms SMs, else -1.
+int gemv_plan(int N, int K, int M, int r, int num_sms);
 cudaError_t launch_gemv(GemvArgs a, int num_sms, cudaStream_t s);
 // out[m, j] = sum_c G[m, c] H[j, c] (fp32, j < r) and outb[m, j] = bf16(s . out[m, j])
 // (j < r_pad, zero beyond r); either output may be null.  H has r rows of C.
