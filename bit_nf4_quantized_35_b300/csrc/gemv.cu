@@ -165,8 +165,9 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(const Ge
   const int kc0 = (int)rank * p.slice;
   const int kb0 = kc0 >> 6;
   const int64_t kbr = p.K >> 6;
-  const int rp_begin = (int)((int64_t)p.row_pairs * blockIdx.x / p.clusters);
-  const int rp_end = (int)((int64_t)p.row_pairs * (blockIdx.x + 1) / p.clusters);
+  // (row_pairs * clusters < 2^31 for any N the launcher accepts)
+  const int rp_begin = (int)((uint32_t)p.row_pairs * blockIdx.x / (uint32_t)p.clusters);
+  const int rp_end = (int)((uint32_t)p.row_pairs * (blockIdx.x + 1) / (uint32_t)p.clusters);
   const int row_lo = rp_begin * 32;
   const int row_hi = min(rp_end * 32, p.N);
   // This CTA's share of the cluster's rows in the final reduction.
@@ -197,13 +198,18 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(const Ge
   // x slice: MT tokens x nblk*64 columns, 8 columns per piece.
   const int xpieces = MT * nblk * 8;
   constexpr int kMaxXp = NT * 4;  // MT x (2048 / 8) pieces over 512 threads
+  const int ppt = nblk * 8;  // pieces per token
   uint4 xv[kMaxXp];
+  int xtok[kMaxXp], xc8[kMaxXp];  // (token, piece within the token) of piece u
 #pragma unroll
   for (int u = 0; u < kMaxXp; ++u) {
     const int i = threadIdx.x + u * blockDim.x;
-    const int tok = i / (nblk * 8), col = (i % (nblk * 8)) * 8 + kc0;
+    xtok[u] = i / ppt;
+    xc8[u] = i - xtok[u] * ppt;
+    const int col = xc8[u] * 8 + kc0;
     xv[u] = make_uint4(0, 0, 0, 0);
-    if (i < xpieces && tok < p.M && col < p.K) xv[u] = ldg_nc_v4(p.x + (int64_t)tok * p.K + col);
+    if (i < xpieces && xtok[u] < p.M && col < p.K)
+      xv[u] = ldg_nc_v4(p.x + (int64_t)xtok[u] * p.K + col);
   }
 
   // ---- 2. codepoint-pair table, from immediates (no memory reads)
@@ -245,23 +251,27 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(const Ge
   }
   __syncthreads();
   // ---- 3. x as f16 MMA fragments, each token scaled by 2^-e (exact)
+  // per-token max |x|: all 32 lanes reduce over the lanes of the same token
+  // (|x| bits order like the magnitudes), then one shared-memory atomic per
+  // (warp, token)
 #pragma unroll
   for (int u = 0; u < kMaxXp; ++u) {
     const int i = threadIdx.x + u * blockDim.x;
-    if (i < xpieces) {
-      const uint32_t w[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
-      float m = 0.f;
+    const uint32_t w[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+    float m = 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[e])), fabsf(bf16_hi(w[e]))));
-      atomicMax(&amax_bits[i / (nblk * 8)], __float_as_int(m));
-    }
+    for (int e = 0; e < 4; ++e) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[e])), fabsf(bf16_hi(w[e]))));
+    const int key = i < xpieces ? xtok[u] : -1;
+    const unsigned same = __match_any_sync(0xffffffffu, key);
+    const unsigned mx = __reduce_max_sync(same, __float_as_uint(m));
+    if (key >= 0 && lane == __ffs(same) - 1) atomicMax(&amax_bits[key], (int)mx);
   }
   __syncthreads();
 #pragma unroll
   for (int u = 0; u < kMaxXp; ++u) {
     const int i = threadIdx.x + u * blockDim.x;
     if (i < xpieces) {
-      const int tok = i / (nblk * 8), c8 = i % (nblk * 8);
+      const int tok = xtok[u], c8 = xc8[u];
       const int E = ((amax_bits[tok] >> 23) & 0xff) - 127;
       const int e = E >= 15 ? E - 14 : 0;
       const float sc = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
