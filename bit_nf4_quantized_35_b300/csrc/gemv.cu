@@ -176,8 +176,33 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(const Ge
   const int sh_hi = min(sh_lo + share, row_hi);
   const int bpitch = gemv_bpitch(p.r);
 
-  // ---- 1. B rows of this CTA's row share go to shared memory (cp.async,
-  // waited for before the final reduction).
+  // Main-loop work.  A task is (row pair, k part): the CTA's K slice is cut
+  // into G = p.kparts parts so that P row pairs x G parts keep all warps
+  // busy; task t = rp_local * G + part, warp w runs tasks w, w + 16, ...
+  // Step = one 64-block of a task.
+  const int G = p.kparts;
+  const int bpp = (nblk + G - 1) / G;  // blocks per part
+  const int ntask = (rp_end - rp_begin) * G;
+
+  // ---- 1. work that reads no global memory: with programmatic dependent
+  // launch it overlaps the tail of the kernel before this one (which may
+  // have written any input, the NF4 buffers included).  Codepoint-pair
+  // table, from immediates:
+  {
+    const float mine = nf4_select<0>(lane & 15, 0.f);  // lane l holds codepoint l & 15
+    for (int b = warp; b < 256; b += kGemvWarps) {
+      // low half: codepoint of the byte's high nibble, high half: low nibble
+      const uint32_t v = pack_f16x2(__shfl_sync(0xffffffffu, mine, b >> 4),
+                                    __shfl_sync(0xffffffffu, mine, b & 15));
+      asm volatile("st.shared.u32 [%0], %1;" ::"r"(tab_u + (b * 32 + lane) * 4), "r"(v) : "memory");
+    }
+  }
+  if (threadIdx.x < 16) amax_bits[threadIdx.x] = 0;
+  // ---- 2. wait for the kernel before this one (no-op without programmatic
+  // dependent launch), then read the inputs: B rows of this CTA's row share
+  // to shared memory (cp.async, waited for before the final reduction), the
+  // x slice, and the block constants.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   {
     const int pieces = p.r >> 3;  // 16-byte pieces per B row
     const int nb = (sh_hi - sh_lo) * pieces;
@@ -188,13 +213,6 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(const Ge
     cp_async_commit();
   }
 
-  // Main-loop work.  A task is (row pair, k part): the CTA's K slice is cut
-  // into G = p.kparts parts so that P row pairs x G parts keep all warps
-  // busy; task t = rp_local * G + part, warp w runs tasks w, w + 16, ...
-  // Step = one 64-block of a task.
-  const int G = p.kparts;
-  const int bpp = (nblk + G - 1) / G;  // blocks per part
-  const int ntask = (rp_end - rp_begin) * G;
   // x slice: MT tokens x nblk*64 columns, 8 columns per piece.
   const int xpieces = MT * nblk * 8;
   constexpr int kMaxXp = NT * 4;  // MT x (2048 / 8) pieces over 512 threads
@@ -212,23 +230,12 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(const Ge
       xv[u] = ldg_nc_v4(p.x + (int64_t)xtok[u] * p.K + col);
   }
 
-  // ---- 2. codepoint-pair table, from immediates (no memory reads)
-  {
-    const float mine = nf4_select<0>(lane & 15, 0.f);  // lane l holds codepoint l & 15
-    for (int b = warp; b < 256; b += kGemvWarps) {
-      // low half: codepoint of the byte's high nibble, high half: low nibble
-      const uint32_t v = pack_f16x2(__shfl_sync(0xffffffffu, mine, b >> 4),
-                                    __shfl_sync(0xffffffffu, mine, b & 15));
-      asm volatile("st.shared.u32 [%0], %1;" ::"r"(tab_u + (b * 32 + lane) * 4), "r"(v) : "memory");
-    }
-  }
-  if (threadIdx.x < 16) amax_bits[threadIdx.x] = 0;
   // block constants a_hat of the CTA's rows x slice blocks (0 outside W):
   // lane = block, warp + 16 i = row, all loads of a thread in one batch
   const int nrows_l = (rp_end - rp_begin) * 32;
   const int ah_pitch = gemv_ah_pitch(p.rows_max);
   if (lane < nblk) {
-    constexpr int kAhBatch = 14;
+    constexpr int kAhBatch = NT == 1 ? 14 : 7;  // rows per load batch (registers)
     const bool kin = kb0 + lane < kbr;
     for (int rl0 = warp; rl0 < nrows_l; rl0 += kGemvWarps * kAhBatch) {
       int code[kAhBatch];
@@ -479,6 +486,9 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(const Ge
       }
   }
 
+  // the next kernel may start its own frozen-buffer work on SMs as they free up
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   // ---- 6. within the CTA: the G k-part slabs of each row meet in slab 0,
   // and the per-warp t sums in tpart (fixed orders)
   __syncthreads();
@@ -634,13 +644,17 @@ cudaError_t launch_gemv(GemvArgs a, int num_sms, cudaStream_t s) {
   cfg.blockDim = dim3(warps * 32, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attrs[1];
+  cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeClusterDimension;
   attrs[0].val.clusterDim.x = 1;
   attrs[0].val.clusterDim.y = S;
   attrs[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: the kernel waits (griddepcontrol.wait)
+  // before reading x, A or B or writing anything
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (nt == 2)
     e = cudaLaunchKernelEx(&cfg, qlora_gemv_kernel<2>, a);
   else
