@@ -182,6 +182,9 @@ GEMV_WIDE_K = [
     # r = 40 (three 16-wide tiles of t, the last one ragged), N = 1032 (a
     # ragged last row pair), 9 tokens (two 8-token tiles)
     inputs.LinearShape("ragged_N1032_K4160_M9_r40", N=1032, K=4160, M=9, r=40, alpha=80.0),
+    # 448 rows per cluster: the shared ring slots do not fit next to the
+    # per-row arrays, so the register-only main loop runs
+    inputs.LinearShape("tall_N32000_K4096_M1_r16", N=32000, K=4096, M=1, r=16, alpha=32.0),
 ]
 
 
