@@ -413,6 +413,22 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
+// Programmatic dependent launch.  A kernel launched with the attribute may
+// start while the kernel before it on the stream is finishing; it does only
+// on-chip set-up before pdl_wait_release(), which waits until that kernel has
+// completed and its writes are visible, so every global read and write after
+// it keeps stream order.  The release lets the next kernel start the same way.
+__device__ __forceinline__ void pdl_wait_release() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+inline cudaLaunchAttribute pdl_attr() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
 __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"

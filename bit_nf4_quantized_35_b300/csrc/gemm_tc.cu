@@ -274,6 +274,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem = ld_shared_volatile(smem_u32(tmem_slot));
   const int total_stages = sc.u1 - sc.u0;
+  pdl_wait_release();  // everything above is on-chip set-up
 
   if (is_prod_warp(warp)) {
     // ------------------------------------------------ dequantising producers
@@ -826,13 +827,14 @@ cudaError_t launch_gemm(bool dx, const CUtensorMap &tmA, const CUtensorMap &tmL1
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attrs[1];
+  cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeClusterDimension;
   attrs[0].val.clusterDim.x = 2;
   attrs[0].val.clusterDim.y = 1;
   attrs[0].val.clusterDim.z = 1;
+  attrs[1] = pdl_attr();
   cfg.attrs = attrs;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (dx)
     e = cudaLaunchKernelEx(&cfg, qlora_gemm_kernel<true>, tmA, tmL1, tmL2, args);
   else

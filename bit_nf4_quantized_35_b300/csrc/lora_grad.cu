@@ -70,6 +70,7 @@ __global__ void __launch_bounds__(kGradThreads) lora_grad_tc_kernel(
     const uint16_t *__restrict__ G, int64_t M, int C, const float *__restrict__ V, int r,
     int64_t rows_per_split, float *__restrict__ part, int *__restrict__ tile_count, float sc,
     int transpose, float *__restrict__ dst) {
+  pdl_wait_release();
   constexpr int RPAD = RPT * 8;
   constexpr int NJ = 2 * RPAD;  // hi rows then lo rows
   constexpr int NTT = NJ / 8;   // n8 tiles
@@ -239,6 +240,7 @@ __global__ void __launch_bounds__(kGradThreads) lora_grad_tc_kernel(
 __global__ void transpose_ab_kernel(const uint16_t *__restrict__ A, const uint16_t *__restrict__ B,
                                     int N, int K, int r, int RP, int nb, uint16_t *__restrict__ At,
                                     uint16_t *__restrict__ Bt) {
+  pdl_wait_release();
   const bool doB = (int)blockIdx.x < nb;
   const int64_t total = doB ? (int64_t)RP * N : (int64_t)K * RP;
   const int64_t b0 = doB ? blockIdx.x : blockIdx.x - nb;
@@ -278,6 +280,7 @@ template <int NT>  // n8 tiles: r_pad / 8
 __global__ void __launch_bounds__(kDownWarps * 32) lora_down_kernel(
     const uint16_t *__restrict__ G, int64_t M, int C, const uint16_t *__restrict__ H, int r,
     float s, float *__restrict__ out, uint16_t *__restrict__ outb, int r_pad) {
+  pdl_wait_release();
   constexpr int U = NT <= 2 ? 4 : (NT <= 4 ? 2 : 1);  // chunks in flight per lane
   __shared__ float red[kDownWarps / 2][16][NT * 8];
   __shared__ float fin[16][NT * 8];
@@ -393,13 +396,14 @@ static cudaError_t launch_down(unsigned gx, const uint16_t *G, int64_t M, int C,
   cfg.gridDim = dim3(gx, split ? 2 : 1, 1);
   cfg.blockDim = dim3(kDownWarps * 32, 1, 1);
   cfg.stream = st;
-  cudaLaunchAttribute attrs[1];
-  attrs[0].id = cudaLaunchAttributeClusterDimension;
-  attrs[0].val.clusterDim.x = 1;
-  attrs[0].val.clusterDim.y = 2;
-  attrs[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attrs[2];
+  attrs[0] = pdl_attr();
+  attrs[1].id = cudaLaunchAttributeClusterDimension;
+  attrs[1].val.clusterDim.x = 1;
+  attrs[1].val.clusterDim.y = 2;
+  attrs[1].val.clusterDim.z = 1;
   cfg.attrs = attrs;
-  cfg.numAttrs = split ? 1 : 0;
+  cfg.numAttrs = split ? 2 : 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, lora_down_kernel<NT>, G, M, C, H, r, s, out, outb, r_pad);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -449,8 +453,17 @@ static cudaError_t launch_grad(dim3 grid, const uint16_t *G, int64_t M, int C, c
     if (e != cudaSuccess) return e;
     set = true;
   }
-  lora_grad_tc_kernel<RPT><<<grid, kGradThreads, smem, s>>>(G, M, C, V, r, rps, part, tile_count,
-                                                             sc, transpose ? 1 : 0, dst);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kGradThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attrs[1] = {pdl_attr()};
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, lora_grad_tc_kernel<RPT>, G, M, C, V, r, rps, part,
+                                     tile_count, sc, transpose ? 1 : 0, dst);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -478,7 +491,15 @@ cudaError_t launch_transposes(const uint16_t *A, const uint16_t *B, int N, int K
   if (ga > cap) ga = cap;
   if (gb < 1) gb = 1;
   if (ga < 1) ga = 1;
-  transpose_ab_kernel<<<(unsigned)(gb + ga), 256, 0, s>>>(A, B, N, K, r, RP, (int)gb, At, Bt);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(gb + ga), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attrs[1] = {pdl_attr()};
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, transpose_ab_kernel, A, B, N, K, r, RP, (int)gb, At, Bt);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
