@@ -29,6 +29,10 @@
  *     detected on the device (a pipeline wait that ran out, non-finite
  *     weights) are written to device words and read after synchronising
  *     (qlora_device_status, the quantiser's nonfinite flag).
+ *   - Stream order holds as usual.  The forward and backward kernels are
+ *     launched with programmatic dependent launch: one may start while the
+ *     work before it on the stream finishes, but it touches no global memory
+ *     until that work has completed and its writes are visible.
  *   - Device pointers must be 16-byte aligned.
  *   - The NF4 buffers are const in the forward and backward calls: that is
  *     the frozen-base contract ([QLoRA-26] Step 4 "frozen base gradient
