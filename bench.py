@@ -18,7 +18,7 @@ GEMV on the 14336x4096 gate projection at 1/4/16 tokens (GB/s of packed
 bulk NF4+DQ quantisation of 136 4096x14336 matrices (GB/s), and
 dequantisation (GB/s).
 
---impl reference times the CPU oracle (the reference arm of this build):
+--impl reference times the CPU oracle (the reference arm):
 each step runs the oracle's forward + backward on a 4-token sample of one
 projection of the same workload, cycling over the seven shapes.
 
