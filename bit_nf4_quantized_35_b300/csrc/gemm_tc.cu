@@ -274,7 +274,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem = ld_shared_volatile(smem_u32(tmem_slot));
   const int total_stages = sc.u1 - sc.u0;
-  pdl_wait_release();  // everything above is on-chip set-up
+  // Everything above is on-chip set-up; every global access comes after the
+  // previous kernel on the stream has completed (programmatic dependent
+  // launch).  Dependents are released when this CTA's work is done.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (is_prod_warp(warp)) {
     // ------------------------------------------------ dequantising producers
@@ -688,6 +691,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncwarp();
   }
 
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // the pair is done with TMEM and with each other's smem
