@@ -11,25 +11,28 @@
 //     2048 wide).  The slice of x is staged once in shared memory as f16
 //     MMA fragments, each token scaled by an exact power of two so any bf16
 //     magnitude fits f16.
-//   - Every warp owns whole 32-row pairs of tiles over the CTA's K slice and
-//     keeps their partial sums in registers: the main loop has no block-wide
-//     synchronisation.  A three-slot register ring prefetches the packed
-//     bytes and block constants of the next blocks.
+//   - A task is (32-row pair, part of the K slice); warp w runs tasks w,
+//     w + 16, ... and keeps a task's partial sums in registers, so the main
+//     loop has no block-wide synchronisation.  A four-slot register ring
+//     brings the packed bytes of the next blocks from one pointer per row
+//     (every load of a ring turn is pointer + immediate).
 //   - Per 64-weight block the block constant a_hat is factored out:
 //       sum_{k in block} w_hat x = a_hat . sum_{k in block} c_idx(k) x_k,
 //     and the inner sum runs on the tensor cores (mma.sync m16n8k16, f16
 //     operands, f32 accumulation): the 4-bit indices become f16 codepoint
 //     pairs through a 256-entry byte table in shared memory, replicated per
-//     lane so that 32 random bytes never collide on a bank.
-//   - All warps share the CTA's slice of t = x A^T (same x fragments, one
-//     16-wide j tile and every (16 / tiles)-th 64-block each) before their
-//     main loop.  After it, every CTA of the cluster sums t over the ranks
-//     and finishes its own share of the cluster's rows: the S partial sums
-//     of a row meet in rank order (deterministic, no workspace, no atomics),
-//     plus the LoRA term s . t . B^T from B rows staged by cp.async.
-//   - The codepoint-pair table is built from immediates (no memory reads),
-//     and the ring's position advances by adds (a division only when a warp
-//     starts its next task).
+//     lane so that 32 random bytes never collide on a bank.  a_hat of the
+//     CTA's rows x blocks is computed once, into shared memory.
+//   - t = x A^T over the CTA's slice is computed by the warps that have no
+//     main-loop task (in parallel with the others' weight stream), else by
+//     all warps before their loop.  After the loop every CTA of the cluster
+//     sums t over the ranks and finishes its own share of the cluster's
+//     rows: the S partial sums of a row meet in rank order (deterministic,
+//     no workspace, no atomics), plus the LoRA term s . t . B^T from B rows
+//     staged by cp.async.
+//   - The codepoint-pair table is built from immediates before the grid
+//     dependency wait (programmatic dependent launch); every global access
+//     comes after it.
 // The codepoints enter as f16 (error <= 2^-12 relative) and the product
 // with a_hat stays in fp32, so the result is within the documented
 // tolerance of x . W_hat^T with the bf16-rounded W_hat.
