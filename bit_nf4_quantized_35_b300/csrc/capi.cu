@@ -202,6 +202,13 @@ qlora_status check_linear_common(const qlora_nf4_weight *w, const uint16_t *x, i
 
 }  // namespace
 
+void qlora::ws_counter_range(int64_t M, int64_t N, int64_t K, int r, size_t *off,
+                             size_t *bytes) {
+  const WsLayout L = ws_layout(M, N, K, r);
+  *off = L.gcnt;
+  *bytes = L.total_min - L.gcnt;
+}
+
 extern "C" {
 
 const char *qlora_status_string(qlora_status s) {

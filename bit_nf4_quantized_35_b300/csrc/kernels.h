@@ -116,4 +116,9 @@ cudaError_t launch_skinny(const uint16_t *G, int64_t M, int C, const float *V, i
 cudaError_t launch_transposes(const uint16_t *A, const uint16_t *B, int N, int K, int r, int RP,
                               uint16_t *At, uint16_t *Bt, int num_sms, cudaStream_t s);
 
+// Byte range [*off, *off + *bytes) of a (M, N, K, r) workspace holding the
+// dA/dB column-tile counters, which must be zero when a backward call starts
+// (capi.cu).  The device status word is the first 256 bytes.
+void ws_counter_range(int64_t M, int64_t N, int64_t K, int r, size_t *off, size_t *bytes);
+
 }  // namespace qlora

@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "kernels.h"
 
 
 namespace {
@@ -56,9 +57,20 @@ extern "C" qlora_status qlora_linear_bwd_noalloc(const qlora_nf4_weight *w, cons
   void *ws = nullptr;
   st = scratch_address(&ws);
   if (st != QLORA_OK) return st;
-  // Nothing in the scratch has to start at zero: the backward writes every
-  // byte it reads, and the device status word is only ever set, never read,
-  // on this path.
-  return qlora_linear_bwd(w, x, dY, M, A, B, r, alpha, t_saved, dX, dx_dtype, dA, dB, ws,
-                          (size_t)QLORA_NOALLOC_SCRATCH_BYTES, flags, stream);
+  // Two parts of the workspace are read before this call writes them: the
+  // device status word (first 256 bytes) and the dA/dB column-tile counters,
+  // which must start at zero.  The counters' place depends on the sizes, so
+  // an earlier call of other sizes (or one that timed out) may have left
+  // other data there.  Both are zeroed on the caller's stream first; every
+  // other byte the backward reads it has written itself.
+  size_t cnt_off = 0, cnt_bytes = 0;
+  qlora::ws_counter_range(M, w->rows, w->cols, r, &cnt_off, &cnt_bytes);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t *wsb = static_cast<uint8_t *>(ws);
+  if (cudaMemsetAsync(wsb, 0, 256, s) != cudaSuccess ||
+      cudaMemsetAsync(wsb + cnt_off, 0, cnt_bytes, s) != cudaSuccess)
+    return QLORA_ERR_CUDA;
+  // `need` bytes (no split-tile area): the dX GEMM computes whole tiles.
+  return qlora_linear_bwd(w, x, dY, M, A, B, r, alpha, t_saved, dX, dx_dtype, dA, dB, ws, need,
+                          flags, stream);
 }

@@ -217,10 +217,13 @@ qlora_status qlora_linear_bwd(const qlora_nf4_weight *w, const uint16_t *x, cons
  *   - The first call on a device looks up the array's device address (a
  *     CUDA runtime query, no allocation) and caches it; make that first call
  *     before any stream capture.
- *   - Every call on a device shares the one array.  The few counters in it
- *     that must start at zero are zero when the library loads and every call
- *     that completes leaves them at zero.  Calls that overlap on the GPU
- *     (different streams, no ordering between them) race on it and give
+ *   - Every call on a device shares the one array, which keeps what the
+ *     last call left in it.  The parts a call reads before writing (the
+ *     device status word and the dA/dB tile counters, which must start at
+ *     zero) are zeroed on `stream` at the start of each call (two memsets,
+ *     no allocation), so calls of different sizes, or a call after one that
+ *     timed out, start clean.  Calls that overlap on the GPU (different
+ *     streams, no ordering between them) race on the array and give
  *     undefined results.
  *   - A device-side timeout is not reported by this entry point (it has no
  *     workspace the caller could read). */
