@@ -74,6 +74,8 @@ def _declare(lib):
     lib.oracle_nf4_storage_bytes.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = ctypes.c_int
+    lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+    lib.oracle_set_num_threads.restype = None
     return lib
 
 
@@ -104,6 +106,11 @@ def _f32(a) -> np.ndarray:
 
 def num_threads() -> int:
     return _load().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    """Thread count of the oracle's OpenMP loops (results do not depend on it)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def codebook() -> np.ndarray:

@@ -301,34 +301,56 @@ void oracle_linear_bwd(const float *x, const float *dY, int64_t M, int64_t K, in
       u_out[m * r + j] = acc2;
     }
   }
+  /* dX: one row of dY at a time.  Each dX[m, k] is still one sum over n in
+   * ascending order; the loops only run n outside k so that W_hat is read
+   * row by row. */
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t ri = 0; ri < nrows; ++ri) {
     const int64_t m = rows[ri];
     const float *gm = dY + m * N;
     const double *um = u_out + m * r;
+    double *base = dX + ri * K;
+    for (int64_t k = 0; k < K; ++k) base[k] = 0.0;
+    for (int64_t n = 0; n < N; ++n) {
+      const double g = (double)gm[n];
+      const float *wn = w + n * K;
+      for (int64_t k = 0; k < K; ++k) base[k] += g * (double)wn[k];
+    }
     for (int64_t k = 0; k < K; ++k) {
-      double base = 0.0;
-      for (int64_t n = 0; n < N; ++n) base += (double)gm[n] * (double)w[n * K + k];
       double lora = 0.0;
       for (int32_t j = 0; j < r; ++j) lora += um[j] * (double)A[j * K + k];
-      dX[ri * K + k] = base + s * lora;
+      base[k] = base[k] + s * lora;
     }
   }
-#pragma omp parallel for schedule(static)
-  for (int64_t k = 0; k < K; ++k) {
-    for (int32_t j = 0; j < r; ++j) {
-      double acc = 0.0;
-      for (int64_t m = 0; m < M; ++m) acc += u_out[m * r + j] * (double)x[m * K + k];
-      dA[j * K + k] = s * acc;
-    }
+  /* dA[j, k] = s * sum_m u[m, j] x[m, k] and dB[n, j] = s * sum_m dY[m, n] t[m, j]:
+   * each a sum over m in ascending order, kept in a binary64 accumulator per
+   * element while the rows of x (of dY) are read one after another. */
+  const int64_t kChunk = 256;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t k0 = 0; k0 < K; k0 += kChunk) {
+    const int64_t k1 = k0 + kChunk < K ? k0 + kChunk : K;
+    double *acc = (double *)calloc((size_t)(k1 - k0) * (size_t)r, sizeof(double));
+    for (int64_t m = 0; m < M; ++m)
+      for (int32_t j = 0; j < r; ++j) {
+        const double uj = u_out[m * r + j];
+        for (int64_t k = k0; k < k1; ++k) acc[j * (k1 - k0) + (k - k0)] += uj * (double)x[m * K + k];
+      }
+    for (int32_t j = 0; j < r; ++j)
+      for (int64_t k = k0; k < k1; ++k) dA[j * K + k] = s * acc[j * (k1 - k0) + (k - k0)];
+    free(acc);
   }
-#pragma omp parallel for schedule(static)
-  for (int64_t n = 0; n < N; ++n) {
-    for (int32_t j = 0; j < r; ++j) {
-      double acc = 0.0;
-      for (int64_t m = 0; m < M; ++m) acc += (double)dY[m * N + n] * t_out[m * r + j];
-      dB[n * r + j] = s * acc;
-    }
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t n0 = 0; n0 < N; n0 += kChunk) {
+    const int64_t n1 = n0 + kChunk < N ? n0 + kChunk : N;
+    double *acc = (double *)calloc((size_t)(n1 - n0) * (size_t)r, sizeof(double));
+    for (int64_t m = 0; m < M; ++m)
+      for (int64_t n = n0; n < n1; ++n) {
+        const double g = (double)dY[m * N + n];
+        for (int32_t j = 0; j < r; ++j) acc[(n - n0) * r + j] += g * t_out[m * r + j];
+      }
+    for (int64_t n = n0; n < n1; ++n)
+      for (int32_t j = 0; j < r; ++j) dB[n * r + j] = s * acc[(n - n0) * r + j];
+    free(acc);
   }
 }
 
@@ -357,5 +379,15 @@ int oracle_num_threads(void) {
   return omp_get_max_threads();
 #else
   return 1;
+#endif
+}
+
+/* Thread count of the OpenMP loops above (timing only: every result is
+ * independent of it, each output element being one sequential sum). */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
 #endif
 }

@@ -34,10 +34,11 @@ MUTANTS = {
                             "ahat = (float)absmax_code[b] * scale2[0];"),
     "fwd_lora_sign": ("y[ri * N + n] = base + s * lora;", "y[ri * N + n] = base - s * lora;"),
     "fwd_drops_scaling": ("y[ri * N + n] = base + s * lora;", "y[ri * N + n] = base + lora;"),
-    "bwd_dA_drops_scaling": ("dA[j * K + k] = s * acc;", "dA[j * K + k] = acc;"),
-    "bwd_dB_uses_u": ("acc += (double)dY[m * N + n] * t_out[m * r + j];",
-                      "acc += (double)dY[m * N + n] * u_out[m * r + j];"),
-    "bwd_dX_drops_lora": ("dX[ri * K + k] = base + s * lora;", "dX[ri * K + k] = base;"),
+    "bwd_dA_drops_scaling": ("dA[j * K + k] = s * acc[j * (k1 - k0) + (k - k0)];",
+                             "dA[j * K + k] = acc[j * (k1 - k0) + (k - k0)];"),
+    "bwd_dB_uses_u": ("acc[(n - n0) * r + j] += g * t_out[m * r + j];",
+                      "acc[(n - n0) * r + j] += g * u_out[m * r + j];"),
+    "bwd_dX_drops_lora": ("base[k] = base[k] + s * lora;", "base[k] = base[k];"),
     "bwd_u_transposed_B": ("acc2 += (double)gm[n] * (double)B[n * r + j];",
                            "acc2 += (double)gm[n] * (double)B[(j * N + n) % (N * r)];"),
     "bf16_round_half_up": ("u += 0x7fffu + lsb;", "u += 0x8000u + 0 * lsb;"),
