@@ -214,23 +214,32 @@ def measured_peaks():
 
 
 def profile_traffic(kernel_tag: str, source_file: str):
-    """DRAM bytes per launch of a kernel from the committed ncu summary
-    profiles/traffic.md (lines: `tag bytes_per_launch source_sha256`), or None
-    when absent or when the kernel source changed since the capture."""
-    p = os.path.join(ROOT, "profiles", "traffic.md")
+    """DRAM bytes per launch of a kernel from the committed ncu figures in
+    profiles/traffic.json ({tag: {"bytes_per_launch", "source_sha16", ...}}),
+    or None when absent or when the kernel source changed since the capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
+    entry = json.load(open(p)).get(kernel_tag)
+    if not entry:
+        return None
     sha = hashlib.sha256(open(source_file, "rb").read()).hexdigest()[:16]
-    for line in open(p):
-        parts = line.strip().strip("|").split("|") if "|" in line else line.split()
-        parts = [x.strip() for x in parts if x.strip()]
-        if len(parts) >= 3 and parts[0] == kernel_tag:
-            try:
-                val = float(parts[1])
-            except ValueError:
-                continue
-            return val if parts[2] == sha else None
-    return None
+    return float(entry["bytes_per_launch"]) if entry.get("source_sha16") == sha else None
+
+
+def pick_tensor_peak(peaks: dict, clocks: dict):
+    """Dense bf16 peak for a kernel timed in this run: the sustained figure
+    when the run's own clock record shows the power cap (or SM clocks well
+    below max), else the burst figure."""
+    reasons = set(clocks.get("reasons") or [])
+    mhz, mx = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    low = mhz is not None and mx and mhz < 0.95 * float(mx)
+    if "sw_power_cap" in reasons or low:
+        why = "sw_power_cap seen" if "sw_power_cap" in reasons else f"SM clock {mhz} of {mx} MHz"
+        return peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]), \
+            f"bf16_tflops_sustained ({why} during the timed region)"
+    return peaks["bf16_tflops"], (f"bf16_tflops burst (SM clock {mhz} of {mx} MHz, no power cap "
+                                  "during the timed region)")
 
 
 def gen_bf16(shape, std, seed, device):
@@ -328,36 +337,48 @@ def run_ours(args, ws_n, rank, device):
     for L in layers:
         host.append({
             "x": L["x"].cpu().pin_memory(), "dY": L["dY"].cpu().pin_memory(),
+            "y": torch.empty_like(L["y"], device="cpu").pin_memory(),
+            "dX": torch.empty_like(L["dX"], device="cpu").pin_memory(),
             "dA": torch.empty_like(L["dA"], device="cpu").pin_memory(),
             "dB": torch.empty_like(L["dB"], device="cpu").pin_memory(),
         })
     h2d = sum(h["x"].numel() * 2 + h["dY"].numel() * 2 for h in host)
-    d2h = sum(h["dA"].numel() * 4 + h["dB"].numel() * 4 for h in host)
+    d2h = sum(h["y"].numel() * 2 + h["dX"].numel() * 2 + h["dA"].numel() * 4 +
+              h["dB"].numel() * 4 for h in host)
 
-    # Inputs go up on a copy stream while earlier layers compute (a training
-    # loop prefetching its next batch): layer i's compute waits for its
-    # copies, and the next step's copies into layer i's buffers wait until
-    # this step's layer i is done with them.
-    copy_stream = torch.cuda.Stream(device=device)
+    # Inputs go up on one copy stream while earlier layers compute (a training
+    # loop prefetching its next batch) and every result (y, dX, dA, dB) comes
+    # back on another: layer i's compute waits for its inputs and for the
+    # previous step's read-back of its outputs; the next step's copies into
+    # layer i's input buffers wait until this step's layer i is done with them.
+    up_stream = torch.cuda.Stream(device=device)
+    down_stream = torch.cuda.Stream(device=device)
     ready = [torch.cuda.Event() for _ in layers]
-    freed = [torch.cuda.Event() for _ in layers]
+    inputs_free = [torch.cuda.Event() for _ in layers]
+    computed = [torch.cuda.Event() for _ in layers]
+    outputs_free = [torch.cuda.Event() for _ in layers]
 
     def e2e_step(start=None):
         if start is not None:
-            copy_stream.wait_event(start)  # the timed region opens before the first copy
+            up_stream.wait_event(start)  # the timed region opens before the first copy
         for i, (L, h) in enumerate(zip(layers, host)):
-            copy_stream.wait_event(freed[i])
-            with torch.cuda.stream(copy_stream):
+            up_stream.wait_event(inputs_free[i])
+            with torch.cuda.stream(up_stream):
                 L["x"].copy_(h["x"], non_blocking=True)
                 L["dY"].copy_(h["dY"], non_blocking=True)
-            ready[i].record(copy_stream)
+            ready[i].record(up_stream)
         for i, (L, h) in enumerate(zip(layers, host)):
             stream.wait_event(ready[i])
+            stream.wait_event(outputs_free[i])
             layer_fwd(L)
             layer_bwd(L)
-            freed[i].record(stream)
-            h["dA"].copy_(L["dA"], non_blocking=True)
-            h["dB"].copy_(L["dB"], non_blocking=True)
+            inputs_free[i].record(stream)
+            computed[i].record(stream)
+            down_stream.wait_event(computed[i])
+            with torch.cuda.stream(down_stream):
+                for k in ("y", "dX", "dA", "dB"):
+                    h[k].copy_(L[k], non_blocking=True)
+            outputs_free[i].record(down_stream)
 
     e2e_step()
     torch.cuda.synchronize()
@@ -366,6 +387,7 @@ def run_ours(args, ws_n, rank, device):
     s0.record(stream)
     for k in range(e2e_steps):
         e2e_step(s0 if k == 0 else None)
+    stream.wait_stream(down_stream)
     s1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(s0.elapsed_time(s1), ws_n, device)
@@ -373,8 +395,8 @@ def run_ours(args, ws_n, rank, device):
 
     rows = sub_benchmarks(capi, layers, device, stream, args) if not args.no_rows else {}
 
-    peaks, peak_kind = measured_peaks()
-    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    peaks, peak_src = measured_peaks()
+    peak, peak_kind = pick_tensor_peak(peaks, clocks)
     traffic = profile_traffic("qlora_gemm_kernel<false>:gate_proj_14336x4096_M2048",
                               os.path.join(ROOT, "bit_nf4_quantized_35_b300", "csrc",
                                             "gemm_tc.cu"))
@@ -409,13 +431,16 @@ def run_ours(args, ws_n, rank, device):
             "bound": "tensor",
             "achieved": round(gemm_achieved, 2),
             "peak": peak,
-            "peak_kind": f"{peak_kind} bf16_tflops_sustained (kernel timed inside a long step)",
+            "peak_kind": f"{peak_src} {peak_kind}",
             "unit": "TFLOP/s",
             "frac": round(gemm_achieved / peak, 4),
             "traffic": traffic,
         },
         "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "copies": "x, dY up from pinned host buffers; y, dX (bf16), dA, dB (fp32) "
+                          "back to pinned host buffers, on two copy streams overlapped with "
+                          "compute"},
         "gpu_launches": KERNELS_PER_LAYER_STEP * len(layers) * args.steps,
         "fwd_gemm_per_layer": {L["name"]: {"ms": round(ms, 4), "tflops": round(
             fwd_flops(M, L["N"], L["K"], RANK_R) / (ms * 1e-3) / 1e12, 1)}
@@ -426,6 +451,8 @@ def run_ours(args, ws_n, rank, device):
     }
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(tokens=16, layers_subset=None)
+        if not args.no_rows:
+            out["cpu_baseline"]["rows"] = oracle_rows()
     return out
 
 
@@ -520,7 +547,146 @@ def sub_benchmarks(capi, layers, device, stream, args):
     rows["dequant_4096x14336"] = {"us": round(dms * 1e3, 1),
                                   "GBps": round(db / (dms * 1e-3) / 1e9, 1),
                                   "frac_of_hbm": round(db / (dms * 1e-3) / 1e9 / hbm, 4)}
+    del mats, outs, outw
+    torch.cuda.empty_cache()
+    rows["llama3_7proj_fwd_bwd_M8192"] = layer_set_at(capi, layers, 8192, device, stream,
+                                                      steps=3 if args.quick else 6)
     return rows
+
+
+def layer_set_at(capi, layers, M, device, stream, steps):
+    """Forward + backward of the seven projections at M tokens (the layer set
+    as its workload states it: 4 x 2048 tokens), per layer and in total."""
+    bufs = []
+    for li, L in enumerate(layers):
+        N, K = L["N"], L["K"]
+        bufs.append({
+            "x": gen_bf16((M, K), 1.0, 900 + li, device),
+            "dY": gen_bf16((M, N), 1.0, 950 + li, device),
+            "t": torch.empty((M, RANK_R), dtype=torch.float32, device=device),
+            "y": torch.empty((M, N), dtype=torch.bfloat16, device=device),
+            "dX": torch.empty((M, K), dtype=torch.bfloat16, device=device),
+            "dA": torch.empty((RANK_R, K), dtype=torch.float32, device=device),
+            "dB": torch.empty((N, RANK_R), dtype=torch.float32, device=device),
+            "ws": capi.Workspace(M, N, K, RANK_R, device=device),
+        })
+
+    def run(L, b, ev=None):
+        if ev:
+            ev[0].record(stream)
+        capi.linear_fwd(L["q"], b["x"], L["A"], L["B"], ALPHA, b["ws"], y=b["y"], t_save=b["t"])
+        if ev:
+            ev[1].record(stream)
+        capi.linear_bwd(L["q"], b["x"], b["dY"], L["A"], L["B"], ALPHA, b["ws"], t_saved=b["t"],
+                        dX=b["dX"], dA=b["dA"], dB=b["dB"])
+        if ev:
+            ev[2].record(stream)
+
+    for _ in range(3):
+        for L, b in zip(layers, bufs):
+            run(L, b)
+    torch.cuda.synchronize()
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in layers]
+           for _ in range(steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for st in range(steps):
+        for li, (L, b) in enumerate(zip(layers, bufs)):
+            run(L, b, evs[st][li])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_step = e0.elapsed_time(e1) / steps
+    total = sum(fwd_flops(M, L["N"], L["K"], RANK_R) + bwd_flops(M, L["N"], L["K"], RANK_R)
+                for L in layers)
+    per = {}
+    for li, L in enumerate(layers):
+        f = sum(evs[st][li][0].elapsed_time(evs[st][li][1]) for st in range(steps)) / steps
+        bw = sum(evs[st][li][1].elapsed_time(evs[st][li][2]) for st in range(steps)) / steps
+        per[L["name"]] = {
+            "fwd_ms": round(f, 4), "bwd_ms": round(bw, 4),
+            "fwd_tflops": round(fwd_flops(M, L["N"], L["K"], RANK_R) / (f * 1e-3) / 1e12, 1),
+            "bwd_tflops": round(bwd_flops(M, L["N"], L["K"], RANK_R) / (bw * 1e-3) / 1e12, 1)}
+    del bufs
+    torch.cuda.empty_cache()
+    return {"tokens": M, "steps": steps, "ms_per_step": round(ms_step, 4),
+            "tflops": round(total / (ms_step * 1e-3) / 1e12, 2), "per_layer": per}
+
+
+def oracle_rows():
+    """The oracle, as it stands, timed on the host cores for the other rows
+    of the line: with one thread and with all of them, on the workloads the
+    GPU rows run (samples where stated)."""
+    import numpy as np
+    from bit_nf4_quantized_35_b300 import inputs
+    from oracle import oracle
+
+    oracle.build()
+    ncores = oracle.num_threads()
+    out = {"cores_all": ncores}
+
+    def timed(fn):
+        res = {}
+        for tag, n in (("1_thread", 1), ("all_cores", ncores)):
+            oracle.set_num_threads(n)
+            t0 = time.perf_counter()
+            fn()
+            res[tag] = time.perf_counter() - t0
+        oracle.set_num_threads(ncores)
+        return res
+
+    # decode GEMV on gate 14336x4096: the oracle dequantises the packed weight
+    # and runs the fp64 forward (GB/s of packed weights, as the GPU row)
+    N, K = 14336, 4096
+    W = inputs.normal((N, K), inputs.STD_W, inputs.SEED_W).float().numpy()
+    q = oracle.quantize_nf4(W, 64, 256, want_idx=False)
+    A = inputs.normal((RANK_R, K), inputs.STD_LORA, inputs.SEED_A).float().numpy()
+    B = inputs.normal((N, RANK_R), inputs.STD_LORA, inputs.SEED_B).float().numpy()
+    for Mg in (1, 4, 16):
+        x = inputs.normal((Mg, K), 1.0, inputs.SEED_X).float().numpy()
+        t = timed(lambda: oracle.linear_fwd(x, oracle.dequant_f32(q), A, B, ALPHA))
+        out[f"gemv_gate_M{Mg}"] = {k: {"s": round(v, 3), "packed_GBps": round(
+            N * K / 2 / v / 1e9, 3)} for k, v in t.items()}
+    # dequantisation of one 4096x14336 matrix
+    Wb = inputs.bulk_matrix(0).float().numpy()
+    qb = oracle.quantize_nf4(Wb, 64, 256, want_idx=False)
+    db = 4096 * 14336 * (0.5 + 1 / 64 + 4 / 16384 + 2)
+    t = timed(lambda: oracle.dequant_bf16(qb))
+    out["dequant_4096x14336"] = {k: {"s": round(v, 3), "GBps": round(db / v / 1e9, 3)}
+                                 for k, v in t.items()}
+    # bulk quantisation: one of the 136 matrices (with its outliers)
+    qbytes = 4096 * 14336 * (2 + 0.5 + 1 / 64 + 4 / 16384)
+    t = timed(lambda: oracle.quantize_nf4(Wb, 64, 256, want_idx=False))
+    out["quantize_bulk"] = {k: {"s": round(v, 3), "GBps": round(qbytes / v / 1e9, 3)}
+                            for k, v in t.items()}
+    out["quantize_bulk"]["sample"] = "1 of the 136 4096x14336 matrices (bulk matrix 0)"
+    # q_proj 4096x4096 forward at 2048 tokens: in full on all cores; on one
+    # thread 64 of the tokens (rows are independent), the full time scaled x32
+    shape = inputs.QPROJ_2048
+    d = inputs.linear_inputs(shape, with_dy=False)
+    wq = oracle.dequant_f32(oracle.quantize_nf4(d["W"].float().numpy(), 64, 256, want_idx=False))
+    xq, Aq, Bq = d["x"].float().numpy(), d["A"].float().numpy(), d["B"].float().numpy()
+    fl = fwd_flops(2048, 4096, 4096, RANK_R)
+    oracle.set_num_threads(1)
+    t0 = time.perf_counter()
+    oracle.linear_fwd(xq, wq, Aq, Bq, shape.alpha, rows=np.arange(64, dtype=np.int64))
+    t1 = (time.perf_counter() - t0) * 2048 / 64
+    oracle.set_num_threads(ncores)
+    t0 = time.perf_counter()
+    oracle.linear_fwd(xq, wq, Aq, Bq, shape.alpha)
+    ta = time.perf_counter() - t0
+    out["qproj_fwd_M2048"] = {
+        "1_thread": {"s": round(t1, 2), "tflops": round(fl / t1 / 1e12, 6),
+                     "sample": "64 of the 2048 tokens, time scaled x32"},
+        "all_cores": {"s": round(ta, 2), "tflops": round(fl / ta / 1e12, 6),
+                      "sample": "all 2048 tokens"}}
+    # the 256x256 single layer (r = 8, 4 tokens), forward + backward in full
+    s1 = inputs.SINGLE_256
+    d1 = {k: v.float().numpy() for k, v in inputs.linear_inputs(s1).items()}
+    w1 = oracle.dequant_f32(oracle.quantize_nf4(d1["W"], 64, 256, want_idx=False))
+    t = timed(lambda: (oracle.linear_fwd(d1["x"], w1, d1["A"], d1["B"], s1.alpha),
+                       oracle.linear_bwd(d1["x"], d1["dY"], w1, d1["A"], d1["B"], s1.alpha)))
+    out["single_256_fwd_bwd"] = {k: {"s": round(v, 5)} for k, v in t.items()}
+    return out
 
 
 # ------------------------------------------------------- oracle (CPU) arm

@@ -168,13 +168,14 @@ class NF4Weight:
 
 
 def quantize_nf4(W: torch.Tensor, group: int = 256, out: NF4Weight | None = None,
-                 nonfinite_flag: torch.Tensor | None = None, stream=None) -> NF4Weight:
+                 nonfinite_flag: torch.Tensor | None = None, stream=None,
+                 block: int = 64) -> NF4Weight:
     """qlora_quantize_nf4 on a contiguous fp32 or bf16 CUDA matrix [rows, cols]."""
     assert W.is_cuda and W.is_contiguous() and W.dim() == 2
     dt = {torch.float32: QLORA_F32, torch.bfloat16: QLORA_BF16}[W.dtype]
     rows, cols = W.shape
     if out is None:
-        out = NF4Weight.empty(rows, cols, W.device, group=group)
+        out = NF4Weight.empty(rows, cols, W.device, block=block, group=group)
     s = out.struct()
     _check("qlora_quantize_nf4", load().qlora_quantize_nf4(
         _ptr(W), dt, ctypes.byref(s), _ptr(nonfinite_flag), _stream(stream)))
