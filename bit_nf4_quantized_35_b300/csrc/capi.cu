@@ -76,11 +76,11 @@ const float *thresholds() {
 qlora_status check_weight(const qlora_nf4_weight *w, bool need_buffers) {
   if (!w) return QLORA_ERR_INVALID_ARG;
   if (w->rows < 0 || w->cols < 0) return QLORA_ERR_SHAPE;
-  if (w->block != kBlock) return QLORA_ERR_SHAPE;
+  if (w->block != 64 && w->block != 128) return QLORA_ERR_SHAPE;
   if (!(w->group == 0 || w->group == 32 || w->group == 64 || w->group == 128 ||
         w->group == 256))
     return QLORA_ERR_SHAPE;
-  if (w->cols % kBlock) return QLORA_ERR_SHAPE;
+  if (w->cols % w->block) return QLORA_ERR_SHAPE;
   if (!need_buffers) return QLORA_OK;
   if (!w->packed) return QLORA_ERR_INVALID_ARG;
   if (w->group > 0 && (!w->absmax_code || !w->scale2)) return QLORA_ERR_INVALID_ARG;
@@ -148,16 +148,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 bool make_tmap(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
                uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer,
-               CUtensorMapSwizzle swz) {
+               CUtensorMapSwizzle swz,
+               CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {pitch_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -167,6 +168,7 @@ void set_block_constants(GemmArgs &g, const qlora_nf4_weight *w) {
   g.cdiv = w->group > 0 ? w->group : 1;
   g.cshift = 0;
   while ((1 << g.cshift) < g.cdiv) ++g.cshift;
+  g.bshift = w->block == 128 ? 1 : 0;
   if (!g.use_code) g.codes = reinterpret_cast<const int8_t *>(w->packed);
 }
 
@@ -258,8 +260,9 @@ qlora_status qlora_quantize_nf4(const void *W, qlora_dtype w_dtype, const qlora_
   if (!W) return QLORA_ERR_INVALID_ARG;
   if (w_dtype != QLORA_F32 && w_dtype != QLORA_BF16) return QLORA_ERR_DTYPE;
   if (!aligned16(W)) return QLORA_ERR_ALIGN;
-  const int64_t nblocks = out->rows * out->cols / kBlock;
-  return cuda_status(launch_quantize(W, w_dtype == QLORA_BF16, nblocks, out->group, out->packed,
+  const int64_t nblocks = out->rows * out->cols / out->block;
+  return cuda_status(launch_quantize(W, w_dtype == QLORA_BF16, out->block, nblocks, out->group,
+                                     out->packed,
                                      out->absmax_code, out->absmax_f32, out->scale2,
                                      nonfinite_flag, thresholds(),
                                      static_cast<cudaStream_t>(stream)));
@@ -270,9 +273,9 @@ qlora_status qlora_dequant(const qlora_nf4_weight *w, uint16_t *W_out, void *str
   if (st != QLORA_OK) return st;
   if (!W_out) return QLORA_ERR_INVALID_ARG;
   if (!aligned16(W_out)) return QLORA_ERR_ALIGN;
-  const int64_t nblocks = w->rows * w->cols / kBlock;
+  const int64_t nblocks = w->rows * w->cols / w->block;
   return cuda_status(launch_dequant(w->packed, w->absmax_code, w->absmax_f32, w->scale2, w->group,
-                                    nblocks, W_out, num_sms_current(),
+                                    w->block, nblocks, W_out, num_sms_current(),
                                     static_cast<cudaStream_t>(stream)));
 }
 
@@ -323,35 +326,39 @@ qlora_status qlora_linear_fwd(const qlora_nf4_weight *w, const uint16_t *x, int6
   const float sc = alpha / (float)r;
   const WsLayout L = ws_layout(M, N, K, r);
   uint8_t *wsb = static_cast<uint8_t *>(ws);
-  const bool gemv_ok = M <= 16 && gemv_plan(N, K, (int)M, r, num_sms_current()) == 0;
+  GemvPlan gplan{};
+  const bool gemv_ok = M <= 16 && gemv_plan(N, K, (int)M, r, num_sms_current(), &gplan) == 0;
   const bool use_gemv =
       (flags & QLORA_FLAG_FORCE_GEMV) || (M <= 16 && gemv_ok && !(flags & QLORA_FLAG_FORCE_GEMM));
   if (use_gemv) {
     if (!gemv_ok) return QLORA_ERR_SHAPE;
+    CUtensorMap tmW;
+    if (!make_tmap(&tmW, w->packed, (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2, 128, 16,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_UINT8))
+      return QLORA_ERR_CUDA;
     GemvArgs a{};
     a.packed = w->packed;
-    a.codes = w->absmax_code;
-    a.absf = w->absmax_f32;
-    a.scale2 = w->scale2;
-    a.group = w->group;
+    a.use_code = w->group > 0;
+    a.codes = a.use_code ? w->absmax_code : reinterpret_cast<const int8_t *>(w->packed);
+    a.cvec = a.use_code ? w->scale2 : w->absmax_f32;
+    const int cdiv = w->group > 0 ? w->group : 1;
+    a.cshift = 0;
+    while ((1 << a.cshift) < cdiv) ++a.cshift;
+    a.bshift = w->block == 128 ? 1 : 0;
     a.N = N;
     a.K = K;
     a.x = x;
     a.M = (int)M;
-    a.A = A;
     a.B = B;
-    a.t_save = t_save;
-    a.use_code = w->group > 0;
-    a.cvec = w->group > 0 ? w->scale2 : w->absmax_f32;
-    a.cdiv = w->group > 0 ? w->group : 1;
-    a.cshift = 0;
-    while ((1 << a.cshift) < a.cdiv) ++a.cshift;
-    if (!a.use_code) a.codes = reinterpret_cast<const int8_t *>(w->packed);
     a.r = r;
+    a.RP = round_up(r, 16);
     a.s = sc;
     a.y = y;
     a.y_bf16 = y_dtype == QLORA_BF16;
-    return cuda_status(launch_gemv(a, num_sms_current(), s));
+    a.t = reinterpret_cast<const float *>(wsb + L.t);
+    a.status = reinterpret_cast<int *>(wsb + L.status);
+    return cuda_status(launch_gemv(tmW, a, gplan, A, reinterpret_cast<float *>(wsb + L.part),
+                                   reinterpret_cast<int *>(wsb + L.gcnt), t_save, s));
   }
   const int RP = round_up(r, 16);
   const bool sk_ws = ws_bytes >= L.total;

@@ -195,6 +195,15 @@ __device__ __forceinline__ bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t
   return mbar_wait_bounded_t<true>(bar, parity, err, status);
 }
 
+// Bounded drain used only on the error path: waits for a phase regardless
+// of the CTA error flag, for at most ~0.1 s.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > (1ll << 28)) return;
+  }
+}
+
 // ------------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
                                             int32_t c0, int32_t c1) {

@@ -103,13 +103,16 @@ struct Fetch {
 };
 
 // Loads are unconditional (the caller clamps the address into range).
-// `qoff` is the byte offset of the 32 packed bytes, `blk` the block index.
-__device__ __forceinline__ Fetch fetch_block(const GemmArgs &p, int64_t qoff, int64_t blk,
+// `qoff` is the byte offset of the 32 packed bytes, `chunk` the index of
+// their 64-element chunk of the flattened weight; the chunk lies in block
+// chunk >> bshift (block = 64 << bshift elements).
+__device__ __forceinline__ Fetch fetch_block(const GemmArgs &p, int64_t qoff, int64_t chunk,
                                             bool valid) {
   Fetch f;
   f.valid = valid;
   f.lo = ldg_nc_v4(p.packed + qoff);
   f.hi = ldg_nc_v4(p.packed + qoff + 16);
+  const int64_t blk = chunk >> p.bshift;
   f.code = ldg_nc_s8(p.codes + (p.use_code ? blk : 0));
   f.c = ldg_nc_f32(p.cvec + (blk >> p.cshift));
   return f;
@@ -132,15 +135,6 @@ __device__ __forceinline__ void dequant_store_row(const GemmArgs &p, const Fetch
     uint32_t o[4];
     lookup8(t, w[c], o);
     sts_v4(row_addr + ((c ^ swz) << 4), o[0], o[1], o[2], o[3]);
-  }
-}
-
-// Bounded drain used only on the error path: waits for a phase regardless
-// of the CTA error flag, for at most ~0.1 s.
-__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > (1ll << 28)) return;
   }
 }
 

@@ -1,667 +1,484 @@
-// gemv.cu -- memory-bound split-K QLoRA forward for decode-sized M (<= 16
-// tokens), sm_103a.
+// gemv.cu -- memory-bound QLoRA forward for decode-sized M (<= 16 tokens),
+// sm_103a.
 //
 // y[m, n] = sum_k x[m, k] w_hat[n, k] + s . sum_j t[m, j] B[n, j],  t = x A^T
-// ("QLoRA and 4bit Quantization | QLoRA 与 4-bit 量化", Step 3 formula).
+// ("QLoRA and 4bit Quantization | QLoRA 与 4-bit 量化", Step 3 formula), with
+// w_hat = bf16(c_idx . a_hat) exactly as the dequantiser produces it.
 //
-// The packed 4-bit weight is the only large operand (N*K/2 bytes), so the
-// kernel is built to stream it from HBM once:
-//   - A cluster of S CTAs (S <= 8) owns a contiguous range of 32-row pairs
-//     of tiles of W; CTA s of the cluster covers one slice of K (at most
-//     2048 wide).  The slice of x is staged once in shared memory as f16
-//     MMA fragments, each token scaled by an exact power of two so any bf16
-//     magnitude fits f16.
-//   - A task is (32-row pair, part of the K slice); warp w runs tasks w,
-//     w + 16, ... and keeps a task's partial sums in registers, so the main
-//     loop has no block-wide synchronisation.  A four-slot register ring
-//     brings the packed bytes of the next blocks from one pointer per row
-//     (every load of a ring turn is pointer + immediate).
-//   - Per 64-weight block the block constant a_hat is factored out:
-//       sum_{k in block} w_hat x = a_hat . sum_{k in block} c_idx(k) x_k,
-//     and the inner sum runs on the tensor cores (mma.sync m16n8k16, f16
-//     operands, f32 accumulation): the 4-bit indices become f16 codepoint
-//     pairs through a 256-entry byte table in shared memory, replicated per
-//     lane so that 32 random bytes never collide on a bank.  a_hat of the
-//     CTA's rows x blocks is computed once, into shared memory.
-//   - t = x A^T over the CTA's slice is computed by the warps that have no
-//     main-loop task (in parallel with the others' weight stream), else by
-//     all warps before their loop.  After the loop every CTA of the cluster
-//     sums t over the ranks and finishes its own share of the cluster's
-//     rows: the S partial sums of a row meet in rank order (deterministic,
-//     no workspace, no atomics), plus the LoRA term s . t . B^T from B rows
-//     staged by cp.async.
-//   - The codepoint-pair table is built from immediates before the grid
-//     dependency wait (programmatic dependent launch); every global access
-//     comes after it.
-// The codepoints enter as f16 (error <= 2^-12 relative) and the product
-// with a_hat stays in fp32, so the result is within the documented
-// tolerance of x . W_hat^T with the bf16-rounded W_hat.
+// Two kernels, launched back to back with programmatic dependent launch:
+//   lora_t_decode_kernel  t = x A^T.  CTA kt covers 256 columns of K; its
+//     warps (one per 16 rows of A) run bf16 mma.sync with fp32 accumulation
+//     and store a partial t; the last CTA to finish (a counter in the
+//     workspace, reset afterwards) adds the partials in CTA order.
+//   qlora_gemv_kernel     the base product and the LoRA epilogue.  It streams
+//     the packed weights as soon as it starts (everything before the t kernel
+//     on the stream has completed by then: the t kernel releases its
+//     dependents only after its own grid-dependency wait), and waits for the
+//     t kernel only before its epilogue reads t.
+//
+// The weight stream.  The packed weight [N, K/2 bytes] is cut into units of
+// 16 rows x 256 columns (a 2 KB tile: 16 rows x 4 blocks of 64).  A cluster
+// of S CTAs owns a contiguous range of 16-row tiles; CTA q of the cluster
+// covers the q-th slice of the 256-column chunks of K (S and the split are
+// chosen on the host to even out the units per SM).  Inside a CTA the units
+// (tile major, chunk minor) are shared out as 16 contiguous ranges, one per
+// warp; each warp brings its units into its own ring of 2 KB slots with
+// tiled TMA loads (128-byte swizzle, one mbarrier per slot), so up to
+// 16 x kGemvDepth units are in flight per SM with no register cost.
+//
+// The arithmetic of a unit (one warp): mma.sync m16n8k16 bf16, A = 16 weight
+// rows, B = up to 8 tokens per n-tile, fp32 accumulation.  The contraction
+// order inside a unit is free, so lane (g, tq) takes whole 64-blocks: lane
+// group tq owns block tq of the unit, and MMA j covers positions 4j .. 4j+3
+// of every lane group's block.  A lane therefore dequantises rows g and g+8
+// of one block (64 + 64 weights) with two per-block tables
+// T[i] = bf16(c_i . a_hat) indexed by byte permutes (the dequantiser's
+// routine, so the MMA operands are the exact bf16 W_hat), and reads the
+// matching x values from shared memory, where x is stored with a 16-byte
+// XOR swizzle that keeps every fragment load free of bank conflicts.
+//
+// Reduction (fixed order, deterministic, no atomics): a warp's sum over one
+// tile's chunks goes to the CTA's tile sums when the warp covered the whole
+// tile, else to one of two partial slots of the warp; the slots of a tile
+// are added in warp order.  The S CTAs of a cluster then add their tile sums
+// in rank order through distributed shared memory, each finishing its share
+// of the cluster's rows with the LoRA term s . t . B^T.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace qlora {
 
 constexpr int kGemvWarps = 16;
-constexpr int kGemvMaxSlice = 2048;  // K columns per CTA
-constexpr int kXRowHalves = 72;      // padded f16 row of one token in one 64-block
+constexpr int kGemvDepth = 3;        // TMA ring slots per warp
+constexpr int kUnitBytes = 2048;     // 16 rows x 128 packed bytes
+constexpr int kChunk = 256;          // columns of K per unit
+constexpr int kTWarps = 4;           // t kernel: one warp per 16 rows of A (r <= 64)
 
-__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                              uint32_t b1) {
-  asm(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Same with a zero accumulator in.
-__device__ __forceinline__ void mma_f16_16816_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                                uint32_t b1) {
-  asm(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%10,%10,%10,%10};"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
-}
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-__device__ __forceinline__ float ld_dsmem_f32(const float *local, uint32_t rank) {
-  uint32_t la = smem_u32(local), ra;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(la), "r"(rank));
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_addr), "r"(rank));
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
   return v;
 }
 
-// Codepoint pair of one packed byte: byte kByte (0..3) of word w.  The
-// table starts at a 32 KB-aligned shared address `lanebase & ~0x7fff`; entry
-// b of lane l is at + b * 128 + l * 4, and `lanebase` = table | l * 4, so the
-// address is one shift and one AND-OR.
-template <int kByte>
-__device__ __forceinline__ uint32_t lut(uint32_t lanebase, uint32_t w) {
-  uint32_t off;
-  if constexpr (kByte == 0)
-    off = ((w << 7) & 0x7f80u) | lanebase;
-  else
-    off = ((w >> (8 * kByte - 7)) & 0x7f80u) | lanebase;
-  // Not volatile: a pure function of its address (the table is written
-  // once, before a block barrier), so the compiler may schedule it freely.
-  uint32_t v;
-  asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(off));
-  return v;
+__device__ __forceinline__ uint4 ldg_v4_or_zero(const uint16_t *p, bool ok) {
+  return ok ? ldg_nc_v4(p) : make_uint4(0, 0, 0, 0);
 }
 
-// Codepoint idx (0..15) as a chain of selects between immediates.
-template <int I>
-__device__ __forceinline__ float nf4_select(int idx, float acc) {
-  constexpr float kv[16] = {QLORA_NF4_VALUES};
-  constexpr float v = kv[I];
-  acc = idx == I ? v : acc;
-  if constexpr (I + 1 < 16)
-    return nf4_select<I + 1>(idx, acc);
-  else
-    return acc;
+// ------------------------------------------------------------- t = x A^T
+// Grid: ceil(K / 256) CTAs of kTWarps warps.  tpart [gridDim.x][M][RP],
+// tfin [M][RP] (fp32, workspace), counter: one int, zero between calls.
+__global__ void __launch_bounds__(kTWarps * 32) lora_t_decode_kernel(
+    const uint16_t *__restrict__ x, int M, int K, const uint16_t *__restrict__ A, int r, int RP,
+    float *__restrict__ tpart, float *__restrict__ tfin, int *__restrict__ counter,
+    float *__restrict__ t_save) {
+  __shared__ int last_s;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, tq = lane & 3;
+  const int kt = blockIdx.x;
+  if (warp * 16 < RP) {
+    const int blk = kt * 4 + tq;  // this lane group's 64-block of K
+    const bool kin = blk * 64 < K;
+    const int j0 = warp * 16 + g, j1 = j0 + 8;
+    const uint16_t *a0p = A + (int64_t)(j0 < r ? j0 : 0) * K + (int64_t)(kin ? blk : 0) * 64;
+    const uint16_t *a1p = A + (int64_t)(j1 < r ? j1 : 0) * K + (int64_t)(kin ? blk : 0) * 64;
+    const bool ok0 = kin && j0 < r, ok1 = kin && j1 < r;
+    float d[2][4] = {};
+#pragma unroll
+    for (int wi = 0; wi < 8; ++wi) {
+      const uint4 ag = ldg_v4_or_zero(a0p + 8 * wi, ok0);
+      const uint4 ah = ldg_v4_or_zero(a1p + 8 * wi, ok1);
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int tok = nt * 8 + g;
+        const bool okx = kin && tok < M;
+        const uint4 xv = ldg_v4_or_zero(
+            x + (int64_t)(okx ? tok : 0) * K + (int64_t)(kin ? blk : 0) * 64 + 8 * wi, okx);
+        mma_bf16(d[nt], ag.x, ah.x, ag.y, ah.y, xv.x, xv.y);
+        mma_bf16(d[nt], ag.z, ah.z, ag.w, ah.w, xv.z, xv.w);
+      }
+    }
+    float *tp = tpart + (int64_t)kt * M * RP;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int tok = nt * 8 + 2 * tq;
+      if (tok < M) {
+        tp[tok * RP + j0] = d[nt][0];
+        tp[tok * RP + j1] = d[nt][2];
+      }
+      if (tok + 1 < M) {
+        tp[(tok + 1) * RP + j0] = d[nt][1];
+        tp[(tok + 1) * RP + j1] = d[nt][3];
+      }
+    }
+  }
+  // The last CTA to finish adds the partials in CTA order.
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    last_s = atomicAdd(counter, 1) == (int)gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!last_s) return;
+  __threadfence();
+  for (int i = threadIdx.x; i < M * RP; i += blockDim.x) {
+    float v = 0.f;
+    for (int q = 0; q < (int)gridDim.x; ++q) v += __ldcg(tpart + (int64_t)q * M * RP + i);
+    tfin[i] = v;
+    const int tok = i / RP, j = i - tok * RP;
+    if (t_save && j < r) t_save[tok * r + j] = v;
+  }
+  if (threadIdx.x == 0) *counter = 0;
 }
 
-// bf16 pair -> f16 pair (both halves), round to nearest.
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
-  return pack_f16x2(bf16_lo(w), bf16_hi(w));
-}
-
-// Bytes per staged row of B (r bf16 plus 16 bytes of padding, so that lanes
-// reading consecutive rows spread over the banks).
-__host__ __device__ inline int gemv_bpitch(int r) { return r * 2 + 16; }
-
-// Shared-memory layout of the GEMV kernel (bytes).
+// ------------------------------------------------------------ main kernel
 struct GemvSmem {
-  int tab, xs, part, tpw, tpart, tfull, bsm, amax, ah, total;
+  int ring, xs, part, tsum, tfin, bars, err, total;
 };
-// Pitch (floats) of the block-constant array: one padded row of the CTA's
-// rows per 64-block, so that lanes storing consecutive blocks of one row
-// land in different banks.
-__host__ __device__ inline int gemv_ah_pitch(int rows_max) { return rows_max + 1; }
-__host__ __device__ inline GemvSmem gemv_smem_layout(int nblk, int MT, int rows_max, int G, int S,
-                                                     int r) {
+__host__ __device__ inline GemvSmem gemv_smem(int M, int MT, int slice_chunks, int tiles_max,
+                                              int RP) {
   GemvSmem L;
-  L.tab = 0;  // 32 KB slack, then the 256 x 32 lanes x u32 table at a 32 KB-aligned address
-  L.xs = 65536;                                   // nblk x MT x 72 f16
-  L.part = L.xs + nblk * MT * kXRowHalves * 2;    // G x rows_max x 16 f32: partial y
-  L.tpw = L.part + G * rows_max * 16 * 4;         // 16 warps x 16 j x 16 tok f32: per-warp t
-  L.tpart = L.tpw + kGemvWarps * 16 * 16 * 4;     // 64 j x 16 tok f32: t over this CTA's slice
-  L.tfull = L.tpart + 64 * 16 * 4;                // 64 j x 16 tok f32: t over the whole K
-  L.bsm = L.tfull + 64 * 16 * 4;                  // this CTA's share of rows x B row
-  L.amax = L.bsm + ((rows_max + S - 1) / S) * gemv_bpitch(r);  // 16 ints: max |x| bits
-  L.ah = L.amax + 16 * 4;  // nblk x pitch f32: a_hat of (block, row) of this CTA's range
-  L.total = L.ah + nblk * gemv_ah_pitch(rows_max) * 4;
+  L.ring = 0;  // 16 warps x kGemvDepth slots x 2 KB, 1024-byte aligned
+  L.xs = L.ring + kGemvWarps * kGemvDepth * kUnitBytes;
+  L.part = L.xs + M * slice_chunks * kChunk * 2;       // [16 warps][2][16 rows][MT] f32
+  L.tsum = L.part + kGemvWarps * 2 * 16 * MT * 4;      // [tiles_max][16 rows][MT] f32
+  L.tfin = L.tsum + tiles_max * 16 * MT * 4;           // [M][RP] f32
+  L.bars = L.tfin + M * RP * 4;                        // [16][kGemvDepth] mbarriers
+  L.bars = (L.bars + 7) & ~7;
+  L.err = L.bars + kGemvWarps * kGemvDepth * 8;
+  L.total = L.err + 16 + 1024;                         // + alignment slack of the base
   return L;
 }
 
+// Physical 16-byte slot of logical slot s of token row tok in the x tile.
+__device__ __forceinline__ int xswz(int tok, int s) {
+  return s ^ (((s >> 3) & 3) | ((tok & 1) << 2));
+}
+
 template <int NT>
-__global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(const GemvArgs p) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  const int MT = NT * 8;
-  const int nblk = p.slice >> 6;
-  const int S = gridDim.y;
-  const GemvSmem SL = gemv_smem_layout(nblk, MT, p.rows_max, p.kparts, S, p.r);
-  const uint32_t tab_u = (smem_u32(smem) + 0x7fffu) & ~0x7fffu;  // 32 KB aligned
-  uint16_t *xs = reinterpret_cast<uint16_t *>(smem + SL.xs);
+__global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
+    const __grid_constant__ CUtensorMap tmW, const GemvArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  constexpr int MT = NT * 8;
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t *smem = smem_raw + (base - smem_u32(smem_raw));
+  const GemvSmem SL = gemv_smem(p.M, MT, p.slice_chunks, p.tiles_max, p.RP);
+  const uint32_t ring_u = base + SL.ring;
+  const uint32_t xs_u = base + SL.xs;
   float *part = reinterpret_cast<float *>(smem + SL.part);
-  float *tpw = reinterpret_cast<float *>(smem + SL.tpw);
-  float *tpart = reinterpret_cast<float *>(smem + SL.tpart);
-  float *tfull = reinterpret_cast<float *>(smem + SL.tfull);
-  int *amax_bits = reinterpret_cast<int *>(smem + SL.amax);
-  float *ah = reinterpret_cast<float *>(smem + SL.ah);
-  const uint32_t bsm_u = smem_u32(smem + SL.bsm);
+  float *tsum = reinterpret_cast<float *>(smem + SL.tsum);
+  float *tfin = reinterpret_cast<float *>(smem + SL.tfin);
+  const uint32_t bars_u = base + SL.bars;
+  const uint32_t err_u = base + SL.err;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tq = lane & 3;
-  const uint32_t rank = cluster_ctarank();
-  const int RP = (p.r + 15) & ~15;
-  const int kc0 = (int)rank * p.slice;
-  const int kb0 = kc0 >> 6;
-  const int64_t kbr = p.K >> 6;
-  // (row_pairs * clusters < 2^31 for any N the launcher accepts)
-  const int rp_begin = (int)((uint32_t)p.row_pairs * blockIdx.x / (uint32_t)p.clusters);
-  const int rp_end = (int)((uint32_t)p.row_pairs * (blockIdx.x + 1) / (uint32_t)p.clusters);
-  const int row_lo = rp_begin * 32;
-  const int row_hi = min(rp_end * 32, p.N);
-  // This CTA's share of the cluster's rows in the final reduction.
-  const int share = (row_hi - row_lo + S - 1) / S;
-  const int sh_lo = min(row_lo + (int)rank * share, row_hi);
-  const int sh_hi = min(sh_lo + share, row_hi);
-  const int bpitch = gemv_bpitch(p.r);
+  const int S = p.S;
+  const uint32_t rank = cluster_rank();
+  const int cl = blockIdx.x / S;
+  // tiles of this cluster, chunks (of 256 columns) of this CTA
+  const int t0 = (int)((int64_t)p.tiles_total * cl / p.clusters);
+  const int t1 = (int)((int64_t)p.tiles_total * (cl + 1) / p.clusters);
+  const int Tc = t1 - t0;
+  const int Ctot = (p.K + kChunk - 1) / kChunk;
+  const int c0 = (int)rank * p.slice_chunks;
+  const int Cc = max(0, min(p.slice_chunks, Ctot - c0));
+  const int U = Tc * Cc;
+  const int u0 = U * warp / kGemvWarps, u1 = U * (warp + 1) / kGemvWarps;
+  const int kbr = p.K >> 6;  // 64-chunks per weight row
 
-  // Main-loop work.  A task is (row pair, k part): the CTA's K slice is cut
-  // into G = p.kparts parts so that P row pairs x G parts keep all warps
-  // busy; task t = rp_local * G + part, warp w runs tasks w, w + 16, ...
-  // Step = one 64-block of a task.
-  const int G = p.kparts;
-  const int bpp = (nblk + G - 1) / G;  // blocks per part
-  const int ntask = (rp_end - rp_begin) * G;
+  if (threadIdx.x < kGemvWarps * kGemvDepth) mbar_init(bars_u + threadIdx.x * 8, 1);
+  if (threadIdx.x == 0) st_shared_volatile(err_u, 0u);
+  fence_barrier_init();
+  __syncthreads();
 
-  // ---- 1. work that reads no global memory: with programmatic dependent
-  // launch it overlaps the tail of the kernel before this one (which may
-  // have written any input, the NF4 buffers included).  Codepoint-pair
-  // table, from immediates:
+  // ---- 1. the first units of every warp's ring (the weights were written
+  // before the t kernel, which has passed its own dependency wait)
+  auto issue = [&](int u, int slot) {
+    const int tile = t0 + u / Cc, chunk = c0 + u % Cc;
+    const uint32_t bar = bars_u + (warp * kGemvDepth + slot) * 8;
+    mbar_arrive_expect_tx(bar, kUnitBytes);
+    tma_load_2d(ring_u + (warp * kGemvDepth + slot) * kUnitBytes, &tmW, bar, chunk * 128,
+                tile * 16);
+  };
+  if (lane == 0) {
+    tma_prefetch_desc(&tmW);
+    for (int i = 0; i < kGemvDepth && u0 + i < u1; ++i) issue(u0 + i, i);
+  }
+
+  // ---- 2. x slice -> shared memory (tokens < M; zero past K), swizzled
+  const int spr = p.slice_chunks * (kChunk / 8);  // 16-byte slots per token row
   {
-    const float mine = nf4_select<0>(lane & 15, 0.f);  // lane l holds codepoint l & 15
-    for (int b = warp; b < 256; b += kGemvWarps) {
-      // low half: codepoint of the byte's high nibble, high half: low nibble
-      const uint32_t v = pack_f16x2(__shfl_sync(0xffffffffu, mine, b >> 4),
-                                    __shfl_sync(0xffffffffu, mine, b & 15));
-      asm volatile("st.shared.u32 [%0], %1;" ::"r"(tab_u + (b * 32 + lane) * 4), "r"(v) : "memory");
+    const int kc0 = c0 * kChunk;
+    for (int i = threadIdx.x; i < p.M * spr; i += blockDim.x) {
+      const int tok = i / spr, s = i - tok * spr;
+      const int col = kc0 + s * 8;
+      const uint4 v =
+          col < p.K ? ldg_nc_v4(p.x + (int64_t)tok * p.K + col) : make_uint4(0, 0, 0, 0);
+      sts_v4(xs_u + (tok * spr + xswz(tok, s)) * 16, v.x, v.y, v.z, v.w);
     }
-  }
-  if (threadIdx.x < 16) amax_bits[threadIdx.x] = 0;
-  // ---- 2. wait for the kernel before this one (no-op without programmatic
-  // dependent launch), then read the inputs: B rows of this CTA's row share
-  // to shared memory (cp.async, waited for before the final reduction), the
-  // x slice, and the block constants.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  {
-    const int pieces = p.r >> 3;  // 16-byte pieces per B row
-    const int nb = (sh_hi - sh_lo) * pieces;
-    for (int i = threadIdx.x; i < nb; i += blockDim.x) {
-      const int rl = i / pieces, c = i - rl * pieces;
-      cp_async16(bsm_u + rl * bpitch + c * 16, p.B + (int64_t)(sh_lo + rl) * p.r + c * 8, 16);
-    }
-    cp_async_commit();
   }
 
-  // x slice: MT tokens x nblk*64 columns, 8 columns per piece.
-  const int xpieces = MT * nblk * 8;
-  constexpr int kMaxXp = NT * 4;  // MT x (2048 / 8) pieces over 512 threads
-  const int ppt = nblk * 8;  // pieces per token
-  uint4 xv[kMaxXp];
-  int xtok[kMaxXp], xc8[kMaxXp];  // (token, piece within the token) of piece u
-#pragma unroll
-  for (int u = 0; u < kMaxXp; ++u) {
-    const int i = threadIdx.x + u * blockDim.x;
-    xtok[u] = i / ppt;
-    xc8[u] = i - xtok[u] * ppt;
-    const int col = xc8[u] * 8 + kc0;
-    xv[u] = make_uint4(0, 0, 0, 0);
-    if (i < xpieces && xtok[u] < p.M && col < p.K)
-      xv[u] = ldg_nc_v4(p.x + (int64_t)xtok[u] * p.K + col);
-  }
+  // block constant a_hat of weight row n, 64-chunk kc of that row (0 outside W)
+  auto ahat_of = [&](int n, int kc) -> float {
+    if (n >= p.N || kc >= kbr) return 0.f;
+    const int64_t b = ((int64_t)n * kbr + kc) >> p.bshift;
+    const float cv = ldg_nc_f32(p.cvec + (b >> p.cshift));
+    return p.use_code ? __fmul_rn((float)ldg_nc_s8(p.codes + b), cv) : cv;
+  };
+  __syncthreads();  // x staged
 
-  // block constants a_hat of the CTA's rows x slice blocks (0 outside W):
-  // lane = block, warp + 16 i = row, all loads of a thread in one batch
-  const int nrows_l = (rp_end - rp_begin) * 32;
-  const int ah_pitch = gemv_ah_pitch(p.rows_max);
-  if (lane < nblk) {
-    constexpr int kAhBatch = NT == 1 ? 14 : 7;  // rows per load batch (registers)
-    const bool kin = kb0 + lane < kbr;
-    for (int rl0 = warp; rl0 < nrows_l; rl0 += kGemvWarps * kAhBatch) {
-      int code[kAhBatch];
-      float cv[kAhBatch];
-#pragma unroll
-      for (int i = 0; i < kAhBatch; ++i) {
-        const int row = row_lo + rl0 + kGemvWarps * i;
-        const bool ok = kin && rl0 + kGemvWarps * i < nrows_l && row < p.N;
-        const int64_t b = ok ? (int64_t)row * kbr + kb0 + lane : 0;
-        code[i] = ldg_nc_s8(p.codes + (p.use_code ? b : 0));
-        cv[i] = ok ? ldg_nc_f32(p.cvec + (b >> p.cshift)) : 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < kAhBatch; ++i) {
-        const int rl = rl0 + kGemvWarps * i;
-        if (rl < nrows_l)
-          ah[lane * ah_pitch + rl] = p.use_code ? __fmul_rn((float)code[i], cv[i]) : cv[i];
-      }
-    }
-  }
-  __syncthreads();
-  // ---- 3. x as f16 MMA fragments, each token scaled by 2^-e (exact)
-  // per-token max |x|: all 32 lanes reduce over the lanes of the same token
-  // (|x| bits order like the magnitudes), then one shared-memory atomic per
-  // (warp, token)
-#pragma unroll
-  for (int u = 0; u < kMaxXp; ++u) {
-    const int i = threadIdx.x + u * blockDim.x;
-    const uint32_t w[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
-    float m = 0.f;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[e])), fabsf(bf16_hi(w[e]))));
-    const int key = i < xpieces ? xtok[u] : -1;
-    const unsigned same = __match_any_sync(0xffffffffu, key);
-    const unsigned mx = __reduce_max_sync(same, __float_as_uint(m));
-    if (key >= 0 && lane == __ffs(same) - 1) atomicMax(&amax_bits[key], (int)mx);
-  }
-  __syncthreads();
-#pragma unroll
-  for (int u = 0; u < kMaxXp; ++u) {
-    const int i = threadIdx.x + u * blockDim.x;
-    if (i < xpieces) {
-      const int tok = xtok[u], c8 = xc8[u];
-      const int E = ((amax_bits[tok] >> 23) & 0xff) - 127;
-      const int e = E >= 15 ? E - 14 : 0;
-      const float sc = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
-      const uint32_t w[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
-      uint4 o;
-      o.x = pack_f16x2(bf16_lo(w[0]) * sc, bf16_hi(w[0]) * sc);
-      o.y = pack_f16x2(bf16_lo(w[1]) * sc, bf16_hi(w[1]) * sc);
-      o.z = pack_f16x2(bf16_lo(w[2]) * sc, bf16_hi(w[2]) * sc);
-      o.w = pack_f16x2(bf16_lo(w[3]) * sc, bf16_hi(w[3]) * sc);
-      const int blk = c8 >> 3, c = (c8 & 7) * 8;
-      *reinterpret_cast<uint4 *>(xs + (blk * MT + tok) * kXRowHalves + c) = o;
-    }
-  }
-  __syncthreads();
-  // 2^e of the two tokens (nt*8 + 2tq, +1) whose accumulator columns this lane holds
-  float csc[NT][2];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int E = ((amax_bits[nt * 8 + 2 * tq + i] >> 23) & 0xff) - 127;
-      const int e = E >= 15 ? E - 14 : 0;
-      csc[nt][i] = __uint_as_float((uint32_t)(127 + e) << 23);
-    }
-
-  // B fragments of block `blk` for token tile nt: words (4j,4j+1), (4j+2,4j+3)
-  auto load_xf = [&](int blk, uint32_t (&xf)[4][NT][2]) {
+  // ---- 3. main loop
+  const int tok_lo = g, tok_hi = 8 + g;  // this lane's tokens in n-tiles 0 and 1
+  float acc[NT][4];
+  int cur = -1, seg = 0;
+  bool ok = true;
+  auto flush = [&](int tile) {
+    const bool whole = tile * Cc >= u0 && (tile + 1) * Cc <= u1;
+    float *dst = whole ? tsum + tile * 16 * MT : part + (warp * 2 + (seg == 0 ? 0 : 1)) * 16 * MT;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const uint16_t *src = xs + (blk * MT + nt * 8 + g) * kXRowHalves + tq * 16;
-      const uint4 a = *reinterpret_cast<const uint4 *>(src);
-      const uint4 b = *reinterpret_cast<const uint4 *>(src + 8);
-      xf[0][nt][0] = a.x, xf[0][nt][1] = a.y, xf[1][nt][0] = a.z, xf[1][nt][1] = a.w;
-      xf[2][nt][0] = b.x, xf[2][nt][1] = b.y, xf[3][nt][0] = b.z, xf[3][nt][1] = b.w;
+      const int tok = nt * 8 + 2 * tq;
+      dst[g * MT + tok] = acc[nt][0];
+      dst[g * MT + tok + 1] = acc[nt][1];
+      dst[(g + 8) * MT + tok] = acc[nt][2];
+      dst[(g + 8) * MT + tok + 1] = acc[nt][3];
     }
+    ++seg;
   };
-
-  // ---- 4. t = x A^T over this CTA's slice.  Warps with no main-loop task
-  // (a CTA with fewer than 16 tasks) compute it while the others stream W;
-  // otherwise all warps do, before their main loop.  Work unit = (16-wide j
-  // tile jt, block group grp): the blocks grp, grp + gpj, ... of the slice;
-  // unit u = jt + grp * JT goes to t-warp u, u + Tw, ...  Each unit's sum is
-  // parked in its own slot and the slots are added in group order after the
-  // main loop (fixed order).
-  const int JT = RP >> 4;
-  const int t_first = ntask < kGemvWarps ? ntask : 0;  // first t-warp
-  const int Tw = kGemvWarps - t_first;                 // t-warps
-  const int gpj = max(1, Tw / JT);                     // block groups per j tile
-  if (warp >= t_first) {
-    auto load_a = [&](int jt, int blk, uint4 (&av)[2][2]) {
-      const int col = kc0 + blk * 64 + tq * 16;
+  // a_hat of the lane's two rows, loaded one unit ahead
+  auto ahat_unit = [&](int u, float &a, float &b) {
+    const int tile = t0 + u / Cc, chunk = c0 + u % Cc;
+    const int kc = chunk * 4 + tq;
+    a = ahat_of(tile * 16 + g, kc);
+    b = ahat_of(tile * 16 + g + 8, kc);
+  };
+  float ah_g = 0.f, ah_h = 0.f;
+  if (u0 < u1) ahat_unit(u0, ah_g, ah_h);
+  int done = 0;  // units consumed
+  for (int u = u0; u < u1; ++u) {
+    const int i = u - u0;
+    const int slot = i % kGemvDepth;
+    const int tile = u / Cc, chunk = u % Cc;
+    if (tile != cur) {
+      if (cur >= 0) flush(cur);
+      cur = tile;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int j = jt * 16 + g + 8 * h;
-        const bool ok = blk < nblk && j < p.r && col < p.K;
-        const uint16_t *src = p.A + (ok ? (int64_t)j * p.K + col : 0);
-        av[h][0] = ok ? ldg_nc_v4(src) : make_uint4(0, 0, 0, 0);
-        av[h][1] = ok ? ldg_nc_v4(src + 8) : make_uint4(0, 0, 0, 0);
-      }
-    };
-    auto mma_a = [&](int blk, const uint4 (&av)[2][2], float (&d)[NT][4]) {
-      const uint32_t a0w[8] = {av[0][0].x, av[0][0].y, av[0][0].z, av[0][0].w,
-                               av[0][1].x, av[0][1].y, av[0][1].z, av[0][1].w};
-      const uint32_t a8w[8] = {av[1][0].x, av[1][0].y, av[1][0].z, av[1][0].w,
-                               av[1][1].x, av[1][1].y, av[1][1].z, av[1][1].w};
-      uint32_t xf[4][NT][2];
-      load_xf(blk, xf);
+      for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    }
+    float nah_g = 0.f, nah_h = 0.f;
+    if (u + 1 < u1) ahat_unit(u + 1, nah_g, nah_h);
+    const uint32_t bar = bars_u + (warp * kGemvDepth + slot) * 8;
+    if (!mbar_wait_bounded(bar, (uint32_t)(i / kGemvDepth) & 1u, err_u, p.status)) {
+      ok = false;
+      break;
+    }
+    // this lane's 32 packed bytes of rows g and g + 8, block tq (128-byte swizzle)
+    const uint32_t sb = ring_u + (warp * kGemvDepth + slot) * kUnitBytes;
+    const uint4 w0 = lds_v4(sb + g * 128 + (((2 * tq) ^ g) << 4));
+    const uint4 w1 = lds_v4(sb + g * 128 + (((2 * tq + 1) ^ g) << 4));
+    const uint4 v0 = lds_v4(sb + (g + 8) * 128 + (((2 * tq) ^ g) << 4));
+    const uint4 v1 = lds_v4(sb + (g + 8) * 128 + (((2 * tq + 1) ^ g) << 4));
+    ++done;
+    __syncwarp();
+    if (lane == 0 && u + kGemvDepth < u1) {
+      fence_proxy_async_smem();
+      issue(u + kGemvDepth, slot);
+    }
+    const Nf4Table tg = make_table(ah_g), th = make_table(ah_h);
+    const uint32_t wg[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    const uint32_t wh[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    // x slot of (token, block tq, positions 8 wi .. 8 wi + 7)
+    const int s_base = chunk * 32 + tq * 8;
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const uint32_t a[4] = {bf16x2_to_f16x2(a0w[2 * jj]), bf16x2_to_f16x2(a8w[2 * jj]),
-                               bf16x2_to_f16x2(a0w[2 * jj + 1]), bf16x2_to_f16x2(a8w[2 * jj + 1])};
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_f16_16816(d[nt], a, xf[jj][nt][0], xf[jj][nt][1]);
-      }
-    };
-    for (int u = warp - t_first; u < JT * gpj; u += Tw) {
-      const int jt = u % JT, grp = u / JT;
-      float d[NT][4];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
-      // two blocks in flight: load the next while the current one multiplies
-      uint4 av0[2][2], av1[2][2];
-      load_a(jt, grp, av0);
-      for (int blk = grp; blk < nblk; blk += 2 * gpj) {
-        load_a(jt, blk + gpj, av1);
-        mma_a(blk, av0, d);
-        if (blk + gpj < nblk) {
-          load_a(jt, blk + 2 * gpj, av0);
-          mma_a(blk + gpj, av1, d);
-        }
-      }
-      float *tw = tpw + u * 256;
+    for (int wi = 0; wi < 8; ++wi) {
+      uint32_t og[4], oh[4];
+      lookup8(tg, wg[wi], og);
+      lookup8(th, wh[wi], oh);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const int tok = nt * 8 + 2 * tq;
-        tw[g * 16 + tok] = d[nt][0] * csc[nt][0];
-        tw[g * 16 + tok + 1] = d[nt][1] * csc[nt][1];
-        tw[(g + 8) * 16 + tok] = d[nt][2] * csc[nt][0];
-        tw[(g + 8) * 16 + tok + 1] = d[nt][3] * csc[nt][1];
+        const int tok = nt == 0 ? tok_lo : tok_hi;
+        uint4 xv = make_uint4(0, 0, 0, 0);
+        if (tok < p.M) xv = lds_v4(xs_u + (tok * spr + xswz(tok, s_base + wi)) * 16);
+        mma_bf16(acc[nt], og[0], oh[0], og[1], oh[1], xv.x, xv.y);
+        mma_bf16(acc[nt], og[2], oh[2], og[3], oh[3], xv.z, xv.w);
       }
     }
+    ah_g = nah_g;
+    ah_h = nah_h;
   }
-
-  // ---- 5. main loop.  A task is (row pair, k part): the CTA's K slice is
-  // cut into G = p.kparts parts so that P row pairs x G parts keep all warps
-  // busy; task t = rp_local * G + part, warp w runs tasks w, w + 16, ...
-  // Step = one 64-block: the packed bytes of rows g + 8q (q = rt * 2 + h)
-  // come through a register ring from one pointer per row (a whole ring
-  // turn's loads are pointer + immediate); a_hat comes from shared memory.
-  const uint32_t lanebase = tab_u | (lane * 4);
-  constexpr int kRing = 4;  // ring slots (kRing - 1 blocks in flight)
-  for (int task = warp; task < ntask; task += kGemvWarps) {
-    const int rpl = task / G;
-    const int part_i = task - rpl * G;
-    const int blk0 = part_i * bpp;
-    // blocks of the task inside the slice and inside K (warp-uniform)
-    const int nv = max(0, min(min(bpp, nblk - blk0), (int)kbr - (kb0 + blk0)));
-    const int row0 = row_lo + rpl * 32 + g;
-    const uint8_t *pr[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int row = row0 + 8 * q;
-      const int rr = row < p.N ? row : row_lo;  // a_hat is 0 for rows past N
-      pr[q] = p.packed + (size_t)rr * (size_t)(p.K >> 1) + (size_t)(kb0 + blk0) * 32 + tq * 8;
-    }
-    float acc[2][NT][4];
-#pragma unroll
-    for (int rt = 0; rt < 2; ++rt)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) acc[rt][nt][0] = acc[rt][nt][1] = acc[rt][nt][2] = acc[rt][nt][3] = 0.f;
-    uint2 P[kRing][4];
-#pragma unroll
-    for (int u = 0; u + 1 < kRing; ++u)
-      if (u < nv) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) P[u][q] = ldg_nc_v2(pr[q] + u * 32);
-      }
-    const float *ahr = ah + blk0 * ah_pitch + rpl * 32 + g;  // a_hat of (block, row g)
-    for (int b0 = 0; b0 < nv; b0 += kRing) {
-#pragma unroll
-      for (int u = 0; u < kRing; ++u) {
-        const int b = b0 + u;
-        if (b < nv) {
-          if (b + kRing - 1 < nv) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              P[(u + kRing - 1) % kRing][q] = ldg_nc_v2(pr[q] + (u + kRing - 1) * 32);
-          }
-          uint32_t xf[4][NT][2];
-          load_xf(blk0 + b, xf);
-          const float *ahb = ahr + b * ah_pitch;
-#pragma unroll
-          for (int rt = 0; rt < 2; ++rt) {
-            float tmp[NT][4];
-            const uint32_t w0[2] = {P[u][rt * 2].x, P[u][rt * 2].y};
-            const uint32_t w8[2] = {P[u][rt * 2 + 1].x, P[u][rt * 2 + 1].y};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int wi = j >> 1;
-              uint32_t a[4];
-              if ((j & 1) == 0) {
-                a[0] = lut<0>(lanebase, w0[wi]);
-                a[1] = lut<0>(lanebase, w8[wi]);
-                a[2] = lut<1>(lanebase, w0[wi]);
-                a[3] = lut<1>(lanebase, w8[wi]);
-              } else {
-                a[0] = lut<2>(lanebase, w0[wi]);
-                a[1] = lut<2>(lanebase, w8[wi]);
-                a[2] = lut<3>(lanebase, w0[wi]);
-                a[3] = lut<3>(lanebase, w8[wi]);
-              }
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                if (j == 0)
-                  mma_f16_16816_z(tmp[nt], a, xf[j][nt][0], xf[j][nt][1]);
-                else
-                  mma_f16_16816(tmp[nt], a, xf[j][nt][0], xf[j][nt][1]);
-              }
-            }
-            const float ah0 = ahb[rt * 16], ah8 = ahb[rt * 16 + 8];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              acc[rt][nt][0] = fmaf(ah0, tmp[nt][0], acc[rt][nt][0]);
-              acc[rt][nt][1] = fmaf(ah0, tmp[nt][1], acc[rt][nt][1]);
-              acc[rt][nt][2] = fmaf(ah8, tmp[nt][2], acc[rt][nt][2]);
-              acc[rt][nt][3] = fmaf(ah8, tmp[nt][3], acc[rt][nt][3]);
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) pr[q] += kRing * 32;
-    }
-    // the task's sum, scaled by 2^e, parked in its k part's slab
-#pragma unroll
-    for (int rt = 0; rt < 2; ++rt)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int tok = nt * 8 + 2 * tq;
-        float *r0 = part + (part_i * p.rows_max + rpl * 32 + rt * 16 + g) * 16 + tok;
-        *reinterpret_cast<float2 *>(r0) =
-            make_float2(acc[rt][nt][0] * csc[nt][0], acc[rt][nt][1] * csc[nt][1]);
-        *reinterpret_cast<float2 *>(r0 + 8 * 16) =
-            make_float2(acc[rt][nt][2] * csc[nt][0], acc[rt][nt][3] * csc[nt][1]);
-      }
+  if (ok && cur >= 0) flush(cur);
+  if (!ok && lane == 0) {
+    // error path: wait (bounded) for this warp's copies still in flight,
+    // units done .. min(done + kGemvDepth, count) - 1
+    const int cnt = u1 - u0;
+    for (int i = done; i < cnt && i < done + kGemvDepth; ++i)
+      mbar_drain(bars_u + (warp * kGemvDepth + i % kGemvDepth) * 8,
+                 (uint32_t)(i / kGemvDepth) & 1u);
   }
+  __syncthreads();
 
-  // the next kernel may start its own frozen-buffer work on SMs as they free up
+  // ---- 4. partial segments of each tile, added in warp order
+  auto warp_of = [&](int uu) { return (kGemvWarps * (uu + 1) - 1) / U; };
+  for (int i = threadIdx.x; i < Tc * 16 * MT; i += blockDim.x) {
+    const int tile = i / (16 * MT), e = i - tile * 16 * MT;
+    const int wa = warp_of(tile * Cc), wb = warp_of((tile + 1) * Cc - 1);
+    if (wa == wb) continue;  // one warp covered the whole tile
+    float v = 0.f;
+    for (int w = wa; w <= wb; ++w) {
+      const int sw = (U * w / kGemvWarps) / Cc;  // first tile of warp w
+      v += part[(w * 2 + (sw == tile ? 0 : 1)) * 16 * MT + e];
+    }
+    tsum[tile * 16 * MT + e] = v;
+  }
+  __syncthreads();
+  cluster_sync();  // every CTA's tile sums are complete
+
+  // ---- 5. t from the t kernel (the only input written by the kernel before)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  for (int i = threadIdx.x; i < p.M * p.RP; i += blockDim.x) tfin[i] = __ldcg(p.t + i);
+  __syncthreads();
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  // ---- 6. within the CTA: the G k-part slabs of each row meet in slab 0,
-  // and the per-warp t sums in tpart (fixed orders)
-  __syncthreads();
-  if (G > 1) {
-    const int nrows_l = (rp_end - rp_begin) * 32;
-    for (int i = threadIdx.x; i < nrows_l * 16; i += blockDim.x) {
-      float v = part[i];
-      for (int q = 1; q < G; ++q) v += part[q * p.rows_max * 16 + i];
-      part[i] = v;
-    }
-  }
+  // ---- 6. this CTA's share of the cluster's rows: y = sum over ranks + s t B^T
   {
-    for (int i = threadIdx.x; i < RP * 16; i += blockDim.x) {
-      const int j = i >> 4, tok = i & 15;
-      float v = 0.f;
-      if (tok < MT)
-        for (int grp = 0; grp < gpj; ++grp) v += tpw[((j >> 4) + grp * JT) * 256 + (j & 15) * 16 + tok];
-      tpart[i] = v;
-    }
-  }
-  // ---- 7. across the cluster (rank order): every CTA forms the whole-K t,
-  // then finishes its share of the rows, y = sum of the ranks' partials + s t B^T
-  __syncthreads();
-  cluster_sync_all();
-  for (int i = threadIdx.x; i < RP * 16; i += blockDim.x) {
-    float v = 0.f;
-    for (int q = 0; q < S; ++q) v += ld_dsmem_f32(tpart + i, (uint32_t)q);
-    tfull[i] = v;
-    const int j = i >> 4, tok = i & 15;
-    if (p.t_save && rank == 0 && blockIdx.x == 0 && tok < p.M && j < p.r) p.t_save[tok * p.r + j] = v;
-  }
-  cp_async_wait<0>();
-  __syncthreads();
-  {
-    const int nsh = sh_hi - sh_lo;
-    const int nout = nsh * p.M;
-    const int pieces = p.r >> 3;
-    for (int i0 = threadIdx.x; i0 < nout; i0 += 4 * blockDim.x) {
-      int row[4], tok[4];
-      float v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u * blockDim.x;
-        const int ic = i < nout ? i : 0;
-        row[u] = ic / p.M;
-        tok[u] = ic - row[u] * p.M;
-        v[u] = 0.f;
-      }
-      for (int q = 0; q < S; ++q) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          v[u] += ld_dsmem_f32(part + (sh_lo - row_lo + row[u]) * 16 + tok[u], (uint32_t)q);
-      }
-      float l[4] = {0.f, 0.f, 0.f, 0.f};  // LoRA term t . B^T
-      for (int c = 0; c < pieces; ++c) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint4 bw = lds_v4(bsm_u + row[u] * bpitch + c * 16);
-          const float *tc = tfull + c * 8 * 16 + tok[u];
-          l[u] = fmaf(tc[0 * 16], bf16_lo(bw.x), l[u]);
-          l[u] = fmaf(tc[1 * 16], bf16_hi(bw.x), l[u]);
-          l[u] = fmaf(tc[2 * 16], bf16_lo(bw.y), l[u]);
-          l[u] = fmaf(tc[3 * 16], bf16_hi(bw.y), l[u]);
-          l[u] = fmaf(tc[4 * 16], bf16_lo(bw.z), l[u]);
-          l[u] = fmaf(tc[5 * 16], bf16_hi(bw.z), l[u]);
-          l[u] = fmaf(tc[6 * 16], bf16_lo(bw.w), l[u]);
-          l[u] = fmaf(tc[7 * 16], bf16_hi(bw.w), l[u]);
+    const int row0 = t0 * 16;
+    const int nrows = min(t1 * 16, p.N) - row0;
+    const int share = (nrows + S - 1) / S;
+    const int r_lo = min((int)rank * share, nrows), r_hi = min(r_lo + share, nrows);
+    const uint32_t tsum_u = base + SL.tsum;
+    for (int rl = r_lo + (int)threadIdx.x; rl < r_hi; rl += blockDim.x) {
+      const int n = row0 + rl;
+      const uint16_t *brow = p.B + (int64_t)n * p.r;
+      const uint32_t off = tsum_u + ((rl >> 4) * 16 * MT + (rl & 15) * MT) * 4;
+      for (int m = 0; m < p.M; ++m) {
+        float v = 0.f;
+        for (int q = 0; q < S; ++q) v += ld_dsmem_f32(off + m * 4, (uint32_t)q);
+        float l = 0.f;
+        for (int c = 0; c < p.r; c += 8) {
+          const uint4 bw = ldg_nc_v4(brow + c);
+          const float *tc = tfin + m * p.RP + c;
+          l = fmaf(tc[0], bf16_lo(bw.x), l);
+          l = fmaf(tc[1], bf16_hi(bw.x), l);
+          l = fmaf(tc[2], bf16_lo(bw.y), l);
+          l = fmaf(tc[3], bf16_hi(bw.y), l);
+          l = fmaf(tc[4], bf16_lo(bw.z), l);
+          l = fmaf(tc[5], bf16_hi(bw.z), l);
+          l = fmaf(tc[6], bf16_lo(bw.w), l);
+          l = fmaf(tc[7], bf16_hi(bw.w), l);
         }
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u * blockDim.x;
-        if (i < nout) {
-          const float y = fmaf(p.s, l[u], v[u]);
-          const int64_t o = (int64_t)tok[u] * p.N + sh_lo + row[u];
-          if (p.y_bf16)
-            reinterpret_cast<__nv_bfloat16 *>(p.y)[o] = __float2bfloat16_rn(y);
-          else
-            reinterpret_cast<float *>(p.y)[o] = y;
-        }
+        const float y = fmaf(p.s, l, v);
+        const int64_t o = (int64_t)m * p.N + n;
+        if (p.y_bf16)
+          reinterpret_cast<__nv_bfloat16 *>(p.y)[o] = __float2bfloat16_rn(y);
+        else
+          reinterpret_cast<float *>(p.y)[o] = y;
       }
     }
   }
-  cluster_sync_all();  // keep every CTA's shared memory alive until the others have read it
+  cluster_sync();  // keep this CTA's tile sums alive until the peers have read them
 }
 
 // ------------------------------------------------------------ launchers
-// Cluster size S = ceil(K / 2048): the x slice of a CTA fits shared memory.
-// (Larger clusters would leave SMs idle: a cluster must fit in one GPC.)
-// Fills the launcher's fields of `a`; -1 when the shape does not fit the
-// kernel (more than 16 tokens, K beyond 8 slices, byte offsets past 32 bits,
-// or more shared memory than a CTA may have).
-static int gemv_config(GemvArgs &a, int num_sms, int *S_out, size_t *smem_out) {
-  if (a.M < 1 || a.M > 16) return -1;
-  if ((uint64_t)a.N * (uint64_t)a.K / 2 >= (1ull << 32)) return -1;  // 32-bit byte offsets
-  int S = (a.K + kGemvMaxSlice - 1) / kGemvMaxSlice;
-  if (S < 1) S = 1;
-  if (S > 8) return -1;
-  a.slice = ((a.K + S - 1) / S + 63) / 64 * 64;
-  a.row_pairs = (a.N + 31) / 32;
-  int clusters = num_sms / S;
-  if (clusters > a.row_pairs) clusters = a.row_pairs;
-  if (clusters < 1) clusters = 1;
-  a.clusters = clusters;
-  const int pairs_max = (a.row_pairs + clusters - 1) / clusters;
-  a.rows_max = pairs_max * 32;
-  int G = kGemvWarps / (pairs_max > 0 ? pairs_max : 1);
-  if (G < 1) G = 1;
-  if (G > a.slice / 64) G = a.slice / 64;
-  a.kparts = G;
-  const int nt = a.M > 8 ? 2 : 1;
-  const size_t smem = gemv_smem_layout(a.slice / 64, nt * 8, a.rows_max, G, S, a.r).total;
-  if (smem > 232448) return -1;
-  *S_out = S;
-  *smem_out = smem;
+// Cluster size S (K slices) and the split: S minimises the 2 KB units per SM,
+// ceil(tiles / clusters) x ceil(chunks / S), among the S whose shared memory
+// fits; ties go to the smaller S.
+int gemv_plan(int N, int K, int M, int r, int num_sms, GemvPlan *out) {
+  if (M < 1 || M > 16 || N < 1 || K < 64 || r < 1 || r > 64) return -1;
+  const int RP = (r + 15) & ~15;
+  const int MT = M > 8 ? 16 : 8;
+  const int T = (N + 15) / 16;
+  const int C = (K + kChunk - 1) / kChunk;
+  GemvPlan best{};
+  int64_t best_load = -1;
+  for (int S = 1; S <= 8; ++S) {
+    const int sc = (C + S - 1) / S;
+    if ((S - 1) * sc >= C) continue;  // every rank gets chunks
+    int clusters = num_sms / S;
+    if (clusters > T) clusters = T;
+    if (clusters < 1) continue;
+    const int tiles_max = (T + clusters - 1) / clusters;
+    const int64_t load = (int64_t)tiles_max * sc;
+    const GemvSmem L = gemv_smem(M, MT, sc, tiles_max, RP);
+    if (L.total > 232448) continue;
+    if (best_load < 0 || load < best_load) {
+      best_load = load;
+      best.S = S;
+      best.slice_chunks = sc;
+      best.clusters = clusters;
+      best.tiles_total = T;
+      best.tiles_max = tiles_max;
+      best.smem = L.total;
+    }
+  }
+  if (best_load < 0) return -1;
+  if (out) *out = best;
   return 0;
 }
 
-int gemv_plan(int N, int K, int M, int r, int num_sms) {
-  GemvArgs a{};
-  a.N = N;
-  a.K = K;
-  a.M = M;
-  a.r = r;
-  int S;
-  size_t smem;
-  return gemv_config(a, num_sms, &S, &smem);
-}
-
-cudaError_t launch_gemv(GemvArgs a, int num_sms, cudaStream_t s) {
-  int S;
-  size_t smem;
-  if (gemv_config(a, num_sms, &S, &smem) != 0) return cudaErrorInvalidValue;
+cudaError_t launch_gemv(const CUtensorMap &tmW, GemvArgs a, const GemvPlan &plan,
+                        const uint16_t *A, float *tpart, int *counter, float *t_save,
+                        cudaStream_t s) {
+  a.S = plan.S;
+  a.slice_chunks = plan.slice_chunks;
+  a.clusters = plan.clusters;
+  a.tiles_total = plan.tiles_total;
+  a.tiles_max = plan.tiles_max;
+  // t = x A^T into the workspace (a.t), partials in tpart
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((a.K + kChunk - 1) / kChunk, 1, 1);
+    cfg.blockDim = dim3(kTWarps * 32, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute at[1] = {pdl_attr()};
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, lora_t_decode_kernel, a.x, a.M, a.K, A, a.r, a.RP,
+                                       tpart, const_cast<float *>(a.t), counter, t_save);
+    if (e != cudaSuccess) return e;
+  }
   const int nt = a.M > 8 ? 2 : 1;
-  const int clusters = a.clusters;
-  const int warps = kGemvWarps;
-  // Dynamic shared memory limit raised to what this launch needs (once per
-  // new maximum), cluster sizes above 8 never requested.
   static size_t smem_set[2] = {0, 0};
   cudaError_t e;
-  if (smem > smem_set[nt - 1]) {
+  if ((size_t)plan.smem > smem_set[nt - 1]) {
     if (nt == 2)
       e = cudaFuncSetAttribute(qlora_gemv_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem);
+                               plan.smem);
     else
       e = cudaFuncSetAttribute(qlora_gemv_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem);
+                               plan.smem);
     if (e != cudaSuccess) return e;
-    smem_set[nt - 1] = smem;
+    smem_set[nt - 1] = plan.smem;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(clusters, S, 1);
-  cfg.blockDim = dim3(warps * 32, 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.gridDim = dim3(plan.clusters * plan.S, 1, 1);
+  cfg.blockDim = dim3(kGemvWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = plan.smem;
   cfg.stream = s;
   cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeClusterDimension;
-  attrs[0].val.clusterDim.x = 1;
-  attrs[0].val.clusterDim.y = S;
+  attrs[0].val.clusterDim.x = plan.S;
+  attrs[0].val.clusterDim.y = 1;
   attrs[0].val.clusterDim.z = 1;
-  // programmatic dependent launch: the kernel waits (griddepcontrol.wait)
-  // before reading x, A or B or writing anything
-  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  attrs[1] = pdl_attr();
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
   if (nt == 2)
-    e = cudaLaunchKernelEx(&cfg, qlora_gemv_kernel<2>, a);
+    e = cudaLaunchKernelEx(&cfg, qlora_gemv_kernel<2>, tmW, a);
   else
-    e = cudaLaunchKernelEx(&cfg, qlora_gemv_kernel<1>, a);
+    e = cudaLaunchKernelEx(&cfg, qlora_gemv_kernel<1>, tmW, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

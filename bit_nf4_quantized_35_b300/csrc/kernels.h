@@ -33,6 +33,7 @@ struct GemmArgs {
   int cdiv;
   int use_code;
   int cshift;  // log2(cdiv): cdiv is 1 or a power of two
+  int bshift;  // log2(block / 64): a 64-element chunk c lies in block c >> bshift
   int bn;      // output columns per CTA pair: 128..256, multiple of 32 (set by the launcher)
   // Split tiles (stream-K).  With sk_part set, each cluster takes an equal
   // share of the (tile, 64-wide contraction block) units and a tile shared by
@@ -59,37 +60,38 @@ cudaError_t launch_gemm(bool dx, const CUtensorMap &tmA, const CUtensorMap &tmL1
                         const CUtensorMap &tmL2, const GemmArgs &args, cudaStream_t s);
 int gemm_pick_stages(int r_pad);
 
-// Split-K decode GEMV (gemv.cu).
+// Decode GEMV (gemv.cu): t kernel + weight-streaming kernel.
 struct GemvArgs {
   const uint8_t *packed;
-  const int8_t *codes;
-  const float *absf;
-  const float *scale2;
-  int group;
+  const int8_t *codes;  // readable memory even without DQ (use_code = 0)
+  const float *cvec;    // s2 (DQ) or fp32 absmax: a_hat = use_code ? code[b] * cvec[b >> cshift] : cvec[b]
+  int use_code, cshift, bshift;
   int N, K;
-  const uint16_t *x;
+  const uint16_t *x;  // [M, K] bf16
   int M;
-  const uint16_t *A;  // [r, K] bf16
   const uint16_t *B;  // [N, r] bf16
-  float *t_save;      // [M, r] fp32 or null
-  int r;
+  int r, RP;
   float s;
   void *y;
   int y_bf16;
-  const float *cvec;  // as in GemmArgs
-  int cdiv;
-  int use_code;
-  int cshift;
-  // set by the launcher:
-  int slice;      // K columns per CTA of a cluster (multiple of 64)
-  int row_pairs;  // ceil(N / 32)
-  int clusters;   // gridDim.x
-  int rows_max;   // rows of the largest per-cluster row range
-  int kparts;     // k parts per row pair inside a CTA (warps per row pair)
+  const float *t;  // [M, RP] fp32 in the workspace, written by the t kernel
+  int *status;     // device status word
+  // set by the launcher from the plan:
+  int S, slice_chunks, clusters, tiles_total, tiles_max;
 };
-// 0 when the decode kernel takes this shape on num_sms SMs, else -1.
-int gemv_plan(int N, int K, int M, int r, int num_sms);
-cudaError_t launch_gemv(GemvArgs a, int num_sms, cudaStream_t s);
+// Launch shape of the decode GEMV: S CTAs per cluster (K slices of
+// slice_chunks x 256 columns), clusters owning ranges of 16-row tiles.
+struct GemvPlan {
+  int S, slice_chunks, clusters, tiles_total, tiles_max, smem;
+};
+// 0 when the decode kernel takes this shape on num_sms SMs (plan filled), else -1.
+int gemv_plan(int N, int K, int M, int r, int num_sms, GemvPlan *plan);
+// tmW: 2-D uint8 tensor map of the packed weight [N, K/2], box 128 x 16,
+// 128-byte swizzle.  tpart: ceil(K/256) x M x RP floats of scratch; counter:
+// one int, zero before the call and after it.
+cudaError_t launch_gemv(const CUtensorMap &tmW, GemvArgs a, const GemvPlan &plan,
+                        const uint16_t *A, float *tpart, int *counter, float *t_save,
+                        cudaStream_t s);
 // out[m, j] = sum_c G[m, c] H[j, c] (fp32, j < r) and outb[m, j] = bf16(s . out[m, j])
 // (j < r_pad, zero beyond r); either output may be null.  H has r rows of C.
 cudaError_t launch_lora_down(const uint16_t *G, int64_t M, int C, const uint16_t *H, int r,
@@ -97,12 +99,12 @@ cudaError_t launch_lora_down(const uint16_t *G, int64_t M, int C, const uint16_t
                              cudaStream_t st);
 
 // Quantise / dequantise (quantize.cu).
-cudaError_t launch_quantize(const void *W, bool bf16_in, int64_t nblocks, int group,
+cudaError_t launch_quantize(const void *W, bool bf16_in, int block, int64_t nblocks, int group,
                             uint8_t *packed, int8_t *codes, float *absf, float *scale2,
                             int *nonfinite_flag, const float th[15], cudaStream_t s);
 cudaError_t launch_dequant(const uint8_t *packed, const int8_t *codes, const float *absf,
-                           const float *scale2, int group, int64_t nblocks, uint16_t *out,
-                           int num_sms, cudaStream_t s);
+                           const float *scale2, int group, int block, int64_t nblocks,
+                           uint16_t *out, int num_sms, cudaStream_t s);
 
 // Rank-r gradient contractions and layout helpers (lora_grad.cu).
 int skinny_splits(int64_t M, int C);

@@ -20,13 +20,26 @@
 //     scaled table T[i] = bf16(c_i * a_hat) is built once per lane and
 //     indexed with byte permutes (the same routine the fused GEMM producer
 //     uses), 32-byte stores.
+#include <cmath>
+
 #include "common.cuh"
 #include "kernels.h"
 
 namespace qlora {
 
-struct Thresholds {
-  float th[16];  // 15 used: index = #{k : x >= th[k]}
+// Decision tables of the nearest-codepoint rule (built on the host from the
+// 15 thresholds; see launch_quantize):
+//   th[k]     the thresholds: index = #{k : x >= th[k]} (th[15] = 2)
+//   bth[j]    for the 1/16-wide bucket j of [-1, 1] (x in [-1 + j/16,
+//             -1 + (j+1)/16)), the one threshold inside it, or 2 when none
+//   bbase[j]  #{k : th[k] < -1 + j/16}
+// Entries 32 and 63 repeat buckets 31 and 0: the bucket arithmetic below
+// yields them for x just above 1 and just below -1.
+struct QuantTables {
+  float th[16];
+  float bth[64];
+  int bbase[64];
+  int exact_only;  // 1: the tables do not fit the bucket rule; divide every element
 };
 
 // Number of thresholds <= x, by bisection over the sorted thresholds.
@@ -38,45 +51,63 @@ __device__ __forceinline__ int nf4_index(float x, const float *th) {
   return i;
 }
 
-template <bool kBf16In>
-__global__ void __launch_bounds__(256) quantize_nf4_kernel(const void *__restrict__ W,
+// Byte offset of element e (0..7) of a lane's 8 consecutive elements in its
+// packed 32-bit word: byte e/2, element 2j in the high nibble.
+__device__ __forceinline__ constexpr int nib_shift(int e) { return 8 * (e >> 1) + ((e & 1) ? 0 : 4); }
+
+// Band (absolute, in normalised units) around each threshold inside which
+// the reciprocal-based value may fall on the other side of the threshold
+// than the IEEE quotient.  With y = RN(1/a) and xn' = RN(w . y):
+//   xn' = (w/a)(1 + d1)(1 + d2),  RN(w/a) = (w/a)(1 + d3),  |di| <= 2^-24,
+// so |xn' - RN(w/a)| < 2^-22 |w/a| <= 2^-22 (normal range; a subnormal xn'
+// is at most 2^-126 from it, far from every threshold).  Outside a band of
+// 2^-20 both lie on the same side of the threshold.
+constexpr float kQuantBand = 9.5367431640625e-07f;  // 2^-20
+
+// kR = block / 64: a CTA of 256 kR threads quantises 256 consecutive blocks
+// (one double-quantisation group of 256, or several smaller groups); the
+// 8 kR lanes of a block reduce its maximum with shuffles.
+template <bool kBf16In, int kR>
+__global__ void __launch_bounds__(256 * kR) quantize_nf4_kernel(const void *__restrict__ W,
                                                            int64_t nblocks, int group,
                                                            uint8_t *__restrict__ packed,
                                                            int8_t *__restrict__ codes,
                                                            float *__restrict__ absf,
                                                            float *__restrict__ scale2,
                                                            int *__restrict__ nonfinite_flag,
-                                                           Thresholds thr) {
+                                                           const QuantTables tab) {
   __shared__ float th_s[16];
+  __shared__ float bth_s[64];
+  __shared__ int bbase_s[64];
   __shared__ float amax_s[256];
   __shared__ float wmax_s[8];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sub = lane >> 3, li = lane & 7;
-  if (tid == 0) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) th_s[i] = thr.th[i];
+  const int64_t nchunks = nblocks * kR;  // 64-element chunks
+  if (tid < 16) th_s[tid] = tab.th[tid];
+  if (tid < 64) {
+    bth_s[tid] = tab.bth[tid];
+    bbase_s[tid] = tab.bbase[tid];
   }
 
-  const int64_t blk0 = (int64_t)blockIdx.x * 256;
+  const int64_t blk0 = (int64_t)blockIdx.x * 256;  // first block of the CTA
+  const int64_t ch0 = blk0 * kR;                   // its first 64-element chunk
 
-  // Issue every load of this thread first (8 passes x 8 elements).
-  float v[8][8];
+  // Issue every load of this thread first (8 passes x 8 elements), kept raw.
+  // Pass p, warp w, lane group `sub` covers chunk p * 32 kR + 4 w + sub.
+  constexpr int kWords = kBf16In ? 4 : 8;  // 32-bit words per pass
+  uint32_t raw[8][kWords];
   bool inb[8];
 #pragma unroll
   for (int p = 0; p < 8; ++p) {
-    const int b = p * 32 + warp * 4 + sub;
-    const int64_t gb = blk0 + b;
-    inb[p] = gb < nblocks;
+    const int c = p * 32 * kR + warp * 4 + sub;
+    const int64_t gb = ch0 + c;  // global chunk
+    inb[p] = gb < nchunks;
     if (kBf16In) {
       uint4 u = make_uint4(0, 0, 0, 0);
       if (inb[p])
         u = ldg_nc_v4(reinterpret_cast<const uint16_t *>(W) + gb * kBlock + li * 8);
-      const uint32_t ww[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        v[p][2 * e] = bf16_lo(ww[e]);
-        v[p][2 * e + 1] = bf16_hi(ww[e]);
-      }
+      raw[p][0] = u.x, raw[p][1] = u.y, raw[p][2] = u.z, raw[p][3] = u.w;
     } else {
       uint4 u0 = make_uint4(0, 0, 0, 0), u1 = u0;
       if (inb[p]) {
@@ -84,46 +115,89 @@ __global__ void __launch_bounds__(256) quantize_nf4_kernel(const void *__restric
         u0 = ldg_nc_v4(src);
         u1 = ldg_nc_v4(src + 4);
       }
-      v[p][0] = __uint_as_float(u0.x), v[p][1] = __uint_as_float(u0.y);
-      v[p][2] = __uint_as_float(u0.z), v[p][3] = __uint_as_float(u0.w);
-      v[p][4] = __uint_as_float(u1.x), v[p][5] = __uint_as_float(u1.y);
-      v[p][6] = __uint_as_float(u1.z), v[p][7] = __uint_as_float(u1.w);
+      raw[p][0] = u0.x, raw[p][1] = u0.y, raw[p][2] = u0.z, raw[p][3] = u0.w;
+      raw[p][4] = u1.x, raw[p][5] = u1.y, raw[p][6] = u1.z, raw[p][7] = u1.w;
     }
   }
-  __syncthreads();  // th_s visible
+  __syncthreads();  // tables visible
+
+  auto elem = [&](int p, int e) -> float {
+    if (kBf16In) return (e & 1) ? bf16_hi(raw[p][e >> 1]) : bf16_lo(raw[p][e >> 1]);
+    return __uint_as_float(raw[p][e]);
+  };
 
   int nonfinite = 0;
 #pragma unroll
   for (int p = 0; p < 8; ++p) {
-    const int b = p * 32 + warp * 4 + sub;
-    float amax = 0.0f;
+    const int c = p * 32 * kR + warp * 4 + sub;
+    // Block absmax as the largest magnitude bit pattern (the order of
+    // non-negative floats); a pattern >= 0x7f800000 means an infinite or NaN
+    // element, and the maximum is then taken over the finite ones only.
+    uint32_t mb;
+    if (kBf16In) {
+      uint32_t m2 = 0;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float x = v[p][e];
-      if (isfinite(x)) {
-        amax = fmaxf(amax, fabsf(x));
-      } else {
+      for (int q = 0; q < 4; ++q) m2 = __vmaxu2(m2, raw[p][q] & 0x7fff7fffu);
+      mb = max(m2 << 16, m2 & 0xffff0000u);
+    } else {
+      mb = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) mb = max(mb, raw[p][q] & 0x7fffffffu);
+    }
+    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
+    if (kR == 2) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
+    const bool nf = mb >= 0x7f800000u;
+    if (__any_sync(0xffffffffu, nf)) {  // rare: some block of the warp is not finite
+      uint32_t mf = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t bits = __float_as_uint(elem(p, e)) & 0x7fffffffu;
+        if (bits < 0x7f800000u) mf = max(mf, bits);
+      }
+      mf = max(mf, __shfl_xor_sync(0xffffffffu, mf, 1));
+      mf = max(mf, __shfl_xor_sync(0xffffffffu, mf, 2));
+      mf = max(mf, __shfl_xor_sync(0xffffffffu, mf, 4));
+      if (kR == 2) mf = max(mf, __shfl_xor_sync(0xffffffffu, mf, 8));
+      if (nf) {
+        mb = mf;
         ++nonfinite;
       }
     }
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-    if (li == 0) amax_s[b] = amax;  // 0 for blocks past the end
+    const float amax = __uint_as_float(mb);
+    if (li == 0 && (sub % kR) == 0) amax_s[c / kR] = amax;  // 0 for blocks past the end
+    // Fast path: xn' = w . RN(1/a) and the bucket tables; an element whose
+    // xn' lies within the band of a threshold is decided again with the
+    // IEEE quotient.  Block constants outside [2^-126, 2^126] (reciprocal
+    // out of the normal range) take the IEEE path for every element.
+    const bool fast = !tab.exact_only && amax >= 1.17549435e-38f && amax <= 8.50705917e+37f;
+    const float y = __frcp_rn(amax);
     uint32_t word = 0;
+    bool risky = false;
 #pragma unroll
-    for (int e = 0; e < 8; e += 2) {
-      int q0 = kZeroIndex, q1 = kZeroIndex;
-      if (amax != 0.0f) {
-        q0 = nf4_index(__fdiv_rn(v[p][e], amax), th_s);
-        q1 = nf4_index(__fdiv_rn(v[p][e + 1], amax), th_s);
+    for (int e = 0; e < 8; ++e) {
+      const float xn = __fmul_rn(elem(p, e), y);
+      // nearest integer of 16 xn + 15.5, i.e. the bucket floor(16 xn + 16),
+      // in the low mantissa bits (1.5 * 2^23 puts the unit at bit 0)
+      const float u = __fmaf_rn(xn, 16.0f, 12582927.5f);
+      const int j = __float_as_int(u) & 63;
+      const float d = __fsub_rn(xn, bth_s[j]);
+      risky |= fabsf(d) < kQuantBand;
+      const uint32_t q = (uint32_t)(bbase_s[j] + (d >= 0.0f ? 1 : 0));
+      word |= q << nib_shift(e);
+    }
+    if (amax == 0.0f) {
+      word = 0x77777777u;  // every index is the exact-zero codepoint
+    } else if (__any_sync(0xffffffffu, risky || !fast)) {
+      if (risky || !fast) {
+        word = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          word |= (uint32_t)nf4_index(__fdiv_rn(elem(p, e), amax), th_s) << nib_shift(e);
       }
-      word |= (uint32_t)((q0 << 4) | q1) << (4 * e);  // byte e/2
     }
-    if (inb[p]) {
-      const int64_t gb = blk0 + b;
-      *reinterpret_cast<uint32_t *>(packed + gb * (kBlock / 2) + li * 4) = word;
-    }
+    if (inb[p]) *reinterpret_cast<uint32_t *>(packed + (ch0 + c) * 32 + li * 4) = word;
   }
   if (nonfinite_flag) {
     nonfinite = __any_sync(0xffffffffu, nonfinite != 0);
@@ -131,18 +205,21 @@ __global__ void __launch_bounds__(256) quantize_nf4_kernel(const void *__restric
   }
   __syncthreads();
 
-  // Second level: one scale per `group` consecutive block constants.
-  const float a = amax_s[tid];
+  // Second level: one scale per `group` consecutive block constants, by
+  // threads 0..255 (warps 0..7); the others only take the block barrier.
+  const bool dq = tid < 256;
+  const float a = dq ? amax_s[tid] : 0.0f;
   const int64_t gb = blk0 + tid;
   if (group == 0) {
-    if (gb < nblocks) absf[gb] = a;
+    if (dq && gb < nblocks) absf[gb] = a;
     return;
   }
   float m = a;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if (lane == 0) wmax_s[warp] = m;
+  if (lane == 0 && dq) wmax_s[warp] = m;
   __syncthreads();
+  if (!dq) return;
   const int wpg = group >> 5;  // warps per group (group >= 32)
   const int w0 = (warp / wpg) * wpg;
   float gmax = 0.0f;
@@ -162,12 +239,13 @@ __global__ void __launch_bounds__(256) dequant_nf4_kernel(const uint8_t *__restr
                                                           const int8_t *__restrict__ codes,
                                                           const float *__restrict__ absf,
                                                           const float *__restrict__ scale2,
-                                                          int group, int64_t nblocks,
+                                                          int group, int64_t npieces,
+                                                          int piece_shift,
                                                           uint16_t *__restrict__ out) {
-  const int64_t nquads = nblocks * 4;  // 16-element pieces
-  for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < nquads;
+  // piece q (16 elements) lies in block q >> piece_shift (block / 16 pieces)
+  for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < npieces;
        q += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t b = q >> 2;
+    const int64_t b = q >> piece_shift;
     const uint2 pk = ldg_nc_v2(packed + q * 8);
     float ahat;
     if (group > 0)
@@ -185,33 +263,77 @@ __global__ void __launch_bounds__(256) dequant_nf4_kernel(const uint8_t *__restr
 }
 
 // ----------------------------------------------------------- host launchers
-cudaError_t launch_quantize(const void *W, bool bf16_in, int64_t nblocks, int group,
+// Bucket tables for the fast decision path, from the 15 sorted thresholds.
+// Valid when every 1/16-wide bucket of [-1, 1] holds at most one threshold
+// and no threshold lies within 2^-10 of a bucket edge (an element whose
+// bucket is computed from the reciprocal-based value, up to 2^-22 off, then
+// still gets the bucket's answer); otherwise every element is divided.
+static void build_quant_tables(const float th[15], QuantTables &t) {
+  for (int i = 0; i < 15; ++i) t.th[i] = th[i];
+  t.th[15] = 2.0f;
+  t.exact_only = 0;
+  for (int j = 0; j < 32; ++j) {
+    const double lo = -1.0 + j / 16.0, hi = -1.0 + (j + 1) / 16.0;
+    int base = 0, inside = 0;
+    float th_in = 2.0f;
+    for (int k = 0; k < 15; ++k) {
+      const double v = th[k];
+      if (v < lo) ++base;
+      if (v >= lo && v < hi) {
+        ++inside;
+        th_in = th[k];
+      }
+      if (std::fabs(v - lo) < 1.0 / 1024 || std::fabs(v - hi) < 1.0 / 1024) t.exact_only = 1;
+    }
+    if (inside > 1) t.exact_only = 1;
+    t.bth[j] = th_in;
+    t.bbase[j] = base;
+  }
+  for (int j = 32; j < 64; ++j) {  // never produced, except 32 (x just above 1) and 63 (just below -1)
+    t.bth[j] = j == 63 ? t.bth[0] : t.bth[31];
+    t.bbase[j] = j == 63 ? t.bbase[0] : t.bbase[31];
+  }
+}
+
+cudaError_t launch_quantize(const void *W, bool bf16_in, int block, int64_t nblocks, int group,
                             uint8_t *packed, int8_t *codes, float *absf, float *scale2,
                             int *nonfinite_flag, const float th[15], cudaStream_t s) {
   if (nblocks == 0) return cudaSuccess;
-  Thresholds thr;
-  for (int i = 0; i < 15; ++i) thr.th[i] = th[i];
-  thr.th[15] = 2.0f;
+  QuantTables tab;
+  build_quant_tables(th, tab);
   const int64_t grid = (nblocks + 255) / 256;
-  if (bf16_in)
-    quantize_nf4_kernel<true><<<(unsigned)grid, 256, 0, s>>>(W, nblocks, group, packed, codes,
-                                                             absf, scale2, nonfinite_flag, thr);
-  else
-    quantize_nf4_kernel<false><<<(unsigned)grid, 256, 0, s>>>(W, nblocks, group, packed, codes,
-                                                              absf, scale2, nonfinite_flag, thr);
+  const unsigned g = (unsigned)grid;
+  if (block == 64) {
+    if (bf16_in)
+      quantize_nf4_kernel<true, 1><<<g, 256, 0, s>>>(W, nblocks, group, packed, codes, absf,
+                                                      scale2, nonfinite_flag, tab);
+    else
+      quantize_nf4_kernel<false, 1><<<g, 256, 0, s>>>(W, nblocks, group, packed, codes, absf,
+                                                       scale2, nonfinite_flag, tab);
+  } else if (block == 128) {
+    if (bf16_in)
+      quantize_nf4_kernel<true, 2><<<g, 512, 0, s>>>(W, nblocks, group, packed, codes, absf,
+                                                      scale2, nonfinite_flag, tab);
+    else
+      quantize_nf4_kernel<false, 2><<<g, 512, 0, s>>>(W, nblocks, group, packed, codes, absf,
+                                                       scale2, nonfinite_flag, tab);
+  } else {
+    return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_dequant(const uint8_t *packed, const int8_t *codes, const float *absf,
-                           const float *scale2, int group, int64_t nblocks, uint16_t *out,
-                           int num_sms, cudaStream_t s) {
+                           const float *scale2, int group, int block, int64_t nblocks,
+                           uint16_t *out, int num_sms, cudaStream_t s) {
   if (nblocks == 0) return cudaSuccess;
-  const int64_t work = nblocks * 4;
+  if (block != 64 && block != 128) return cudaErrorInvalidValue;
+  const int64_t work = nblocks * (block / 16);
   int64_t grid = (work + 255) / 256;
   const int64_t cap = (int64_t)num_sms * 8 * 4;
   if (grid > cap) grid = cap;
-  dequant_nf4_kernel<<<(unsigned)grid, 256, 0, s>>>(packed, codes, absf, scale2, group, nblocks,
-                                                    out);
+  dequant_nf4_kernel<<<(unsigned)grid, 256, 0, s>>>(packed, codes, absf, scale2, group, work,
+                                                    block == 64 ? 2 : 3, out);
   return cudaGetLastError();
 }
 

@@ -7,7 +7,8 @@
  *   - dequantisation of that weight to bf16,
  *   - the forward pass  y = x . W_hat^T + (x . A^T) . B^T . alpha / r
  *     (a fused dequantise + tensor-core GEMM for M > 16 tokens, a
- *     memory-bound split-K GEMV for M <= 16),
+ *     memory-bound decode GEMV streaming the packed weights for M <= 16;
+ *     both compute with the exact bf16 W_hat the dequantiser produces),
  *   - the backward pass dX, dA and dB with the NF4 buffers frozen.
  *
  * Sources of each operation (page title -- section):
@@ -83,7 +84,8 @@ typedef enum { QLORA_F32 = 0, QLORA_BF16 = 1 } qlora_dtype;
  * Sizes (qlora_nf4_sizes): packed rows*cols/2 bytes; absmax_code nblocks
  * bytes (group > 0); absmax_f32 nblocks floats (group == 0); scale2
  * ceil(nblocks/group) floats (group > 0); nblocks = rows*cols/block.
- * Supported: block == 64; group in {0, 32, 64, 128, 256}.
+ * Supported: block in {64, 128} ([QLoRA-22] engineering notes: 64 or 128
+ * weights share one scale); group in {0, 32, 64, 128, 256}.
  * All pointers are device pointers owned by the caller; unused ones are NULL. */
 typedef struct {
   int64_t rows;
@@ -116,8 +118,9 @@ qlora_status qlora_nf4_sizes(int64_t rows, int64_t cols, int32_t block, int32_t 
  * nonfinite_flag: NULL, or a device int32 that the kernel sets to 1 when it
  * meets a NaN or infinite weight (the caller zeroes it first); indices of
  * such blocks are unspecified.
- * Errors: QLORA_ERR_INVALID_ARG (null buffers), QLORA_ERR_SHAPE (block != 64,
- * unsupported group, cols % 64), QLORA_ERR_DTYPE, QLORA_ERR_ALIGN, QLORA_ERR_CUDA. */
+ * Errors: QLORA_ERR_INVALID_ARG (null buffers), QLORA_ERR_SHAPE (block not 64
+ * or 128, unsupported group, cols % block), QLORA_ERR_DTYPE, QLORA_ERR_ALIGN,
+ * QLORA_ERR_CUDA. */
 qlora_status qlora_quantize_nf4(const void *W, qlora_dtype w_dtype, const qlora_nf4_weight *out,
                                 int32_t *nonfinite_flag, void *stream);
 
@@ -155,7 +158,9 @@ qlora_status qlora_workspace_init(void *ws, size_t ws_bytes, void *stream);
 qlora_status qlora_device_status(void *ws, int32_t *status, void *stream);
 
 /* Flags of qlora_linear_fwd: select the kernel explicitly (tests only).
- * Default (0): GEMV for M <= 16, tensor-core GEMM otherwise. */
+ * Default (0): GEMV for M <= 16, tensor-core GEMM otherwise.  FORCE_GEMV
+ * returns QLORA_ERR_SHAPE for M > 16 (or a K whose x slice does not fit the
+ * decode kernel's shared memory). */
 #define QLORA_FLAG_FORCE_GEMV 1u
 #define QLORA_FLAG_FORCE_GEMM 2u
 
@@ -174,7 +179,7 @@ qlora_status qlora_device_status(void *ws, int32_t *status, void *stream);
  *   ws     device workspace of qlora_workspace_size(M, N, K, r) bytes,
  *          zeroed once by qlora_workspace_init; it also holds the device
  *          status word
- * Requires K % 64 == 0, N % 8 == 0, M >= 1.  Arithmetic: bf16 operands,
+ * Requires K % block == 0, N % 8 == 0, M >= 1.  Arithmetic: bf16 operands,
  * fp32 accumulation.  Errors: QLORA_ERR_INVALID_ARG, QLORA_ERR_SHAPE,
  * QLORA_ERR_ALIGN, QLORA_ERR_DTYPE, QLORA_ERR_WORKSPACE, QLORA_ERR_CUDA. */
 qlora_status qlora_linear_fwd(const qlora_nf4_weight *w, const uint16_t *x, int64_t M,
@@ -193,7 +198,7 @@ qlora_status qlora_linear_fwd(const qlora_nf4_weight *w, const uint16_t *x, int6
  *   dY      device bf16 [M, N];  x, A, B as in the forward
  *   t_saved device fp32 [M, r] from the forward, or NULL (recomputed)
  *   dX, dA, dB device outputs (overwritten, not accumulated)
- * Requires K % 64 == 0, N % 8 == 0, r % 8 == 0, r <= 64.
+ * Requires K % block == 0, N % 8 == 0, r % 8 == 0, r <= 64.
  * Errors as for qlora_linear_fwd. */
 qlora_status qlora_linear_bwd(const qlora_nf4_weight *w, const uint16_t *x, const uint16_t *dY,
                               int64_t M, const uint16_t *A, const uint16_t *B, int32_t r,

@@ -59,6 +59,8 @@ def _declare(lib):
     lib.oracle_nearest_code.restype = ctypes.c_int
     lib.oracle_nearest_codes_bits.argtypes = [u32, i64, P]
     lib.oracle_nearest_codes_bits.restype = None
+    lib.oracle_nearest_codes_scaled_bits.argtypes = [u32, i64, ctypes.c_float, P]
+    lib.oracle_nearest_codes_scaled_bits.restype = None
     lib.oracle_bf16_rne_array.argtypes = [P, i64, P]
     lib.oracle_bf16_rne_array.restype = None
     lib.oracle_quantize_nf4.argtypes = [P, i64, i64, i32, i32, P, P, P, P, P]
@@ -129,6 +131,15 @@ def nearest_codes_bits(start_bits: int, count: int) -> np.ndarray:
     """Indices for ``count`` consecutive binary32 bit patterns."""
     out = np.empty(count, dtype=np.uint8)
     _load().oracle_nearest_codes_bits(ctypes.c_uint32(start_bits), count, _ptr(out))
+    return out
+
+
+def nearest_codes_scaled_bits(start_bits: int, count: int, absmax: float) -> np.ndarray:
+    """Indices of ``count`` consecutive binary32 weights in a block whose
+    absolute maximum is ``absmax`` (division, then nearest codepoint)."""
+    out = np.empty(count, dtype=np.uint8)
+    _load().oracle_nearest_codes_scaled_bits(ctypes.c_uint32(start_bits), count,
+                                             ctypes.c_float(absmax), _ptr(out))
     return out
 
 

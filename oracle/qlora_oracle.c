@@ -84,6 +84,24 @@ void oracle_nearest_codes_bits(uint32_t start_bits, int64_t count, uint8_t *out)
   }
 }
 
+/* Indices of the weights w with `count` consecutive binary32 bit patterns
+ * starting at `start_bits`, in a block whose absolute maximum is `absmax`
+ * (> 0): the quantiser's two steps for one element, the binary32 division
+ * w / absmax ([Gemma-9] 9.2.1, "normalise to [-1, 1]") and the nearest
+ * codepoint ([QLoRA-26] Step 2).  Used to compare against exhaustive device
+ * sweeps of one block constant. */
+void oracle_nearest_codes_scaled_bits(uint32_t start_bits, int64_t count, float absmax,
+                                      uint8_t *out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < count; ++i) {
+    uint32_t b = start_bits + (uint32_t)i;
+    float w;
+    memcpy(&w, &b, 4);
+    volatile float xn = w / absmax;
+    out[i] = (uint8_t)oracle_nearest_code(xn);
+  }
+}
+
 /* binary32 -> bf16 bits, round to nearest, ties to even, on the bit
  * pattern.  NaN stays NaN (quiet bit set). */
 uint16_t oracle_bf16_rne(float f) {

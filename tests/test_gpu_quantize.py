@@ -19,14 +19,14 @@ def _lib():
     capi.load()
 
 
-def _check_quant(W_cpu: torch.Tensor, group: int):
+def _check_quant(W_cpu: torch.Tensor, group: int, block: int = 64):
     """Quantise on the GPU and with the oracle; compare every output bit."""
     W = W_cpu.cuda().contiguous()
     flag = torch.zeros(1, dtype=torch.int32, device="cuda")
-    q = capi.quantize_nf4(W, group=group, nonfinite_flag=flag)
+    q = capi.quantize_nf4(W, group=group, nonfinite_flag=flag, block=block)
     deq = capi.dequant(q)
     torch.cuda.synchronize()
-    ref = oracle.quantize_nf4(W_cpu.float().numpy(), 64, group)
+    ref = oracle.quantize_nf4(W_cpu.float().numpy(), block, group)
     assert np.array_equal(q.packed.cpu().numpy(), ref.packed), "packed bytes differ"
     if group > 0:
         assert np.array_equal(q.absmax_code.cpu().numpy(), ref.absmax_code), "codes differ"
@@ -50,6 +50,20 @@ def test_groups_and_ragged_tail(group):
     # 37 rows x 192 cols = 111 blocks: one partial CTA, partial last group
     W = inputs.normal((37, 192), inputs.STD_W, 11, torch.bfloat16)
     _check_quant(W, group)
+
+
+@pytest.mark.parametrize("group", [0, 32, 64, 256])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
+def test_block128_groups_and_ragged_tail(group, dtype):
+    """128-weight blocks: 37 x 384 = 111 blocks (one partial CTA, a partial
+    last group), bf16 and fp32 weights, every output bit."""
+    W = inputs.normal((37, 384), inputs.STD_W, 12, dtype)
+    W[5, 128:256] = 0.0  # an all-zero block
+    _check_quant(W, group, block=128)
+
+
+def test_block128_bulk_matrix_full_size():
+    _check_quant(inputs.bulk_matrix(1), 256, block=128)
 
 
 def test_edge_values():
@@ -115,26 +129,78 @@ def test_dequant_deterministic_and_buffers_const():
         assert torch.equal(x, y)
 
 
-@pytest.mark.slow
-def test_exhaustive_decision_rule_all_fp32_in_unit_interval():
-    """Every fp32 x in [-1, 1] (about 2.13e9 values) quantised as the
-    non-maximal element of a block whose absmax is exactly 1 (so w / a == x)
-    gets the oracle's nearest-codepoint index."""
+def _f32_bits(v: float) -> int:
+    return int(np.array([v], dtype=np.float32).view(np.uint32)[0])
+
+
+def _sweep(absmax: float, start: int, count: int, chunk_blocks: int = 1 << 20):
+    """Quantise every binary32 weight with the `count` consecutive bit
+    patterns from `start` as the non-maximal elements of blocks whose first
+    element (the absmax) is `absmax`, and compare each index with the
+    oracle's (IEEE division by absmax, then nearest codepoint)."""
     per_block = 63
-    chunk_blocks = 1 << 20
-    ranges = [(0x00000000, 0x3F800000 + 1), (0x80000000, 0xBF800000 + 1)]
-    for lo, hi in ranges:
-        start = lo
-        while start < hi:
-            n = min(per_block * chunk_blocks, hi - start)
-            nb = (n + per_block - 1) // per_block
-            bits = torch.arange(start, start + nb * per_block, dtype=torch.int64, device="cuda")
-            bits = torch.clamp(bits, max=hi - 1)
-            vals = (bits.to(torch.int32)).view(torch.float32).view(nb, per_block)
-            W = torch.cat([torch.ones(nb, 1, device="cuda"), vals], dim=1).contiguous()
-            q = capi.quantize_nf4(W.view(nb, 64), group=0)
-            p = q.packed.view(nb, 32)
-            idx = torch.stack([p >> 4, p & 15], dim=2).view(nb, 64)[:, 1:].reshape(-1)[:n]
-            ref = oracle.nearest_codes_bits(start, n)
-            assert np.array_equal(idx.cpu().numpy(), ref), hex(start)
-            start += n
+    a = float(np.float32(absmax))
+    end = start + count
+    while start < end:
+        n = min(per_block * chunk_blocks, end - start)
+        nb = (n + per_block - 1) // per_block
+        bits = torch.arange(start, start + nb * per_block, dtype=torch.int64, device="cuda")
+        bits = torch.clamp(bits, max=end - 1)
+        bits = torch.where(bits >= 1 << 31, bits - (1 << 32), bits)  # as signed 32-bit patterns
+        vals = bits.to(torch.int32).view(torch.float32).view(nb, per_block)
+        W = torch.cat([torch.full((nb, 1), a, device="cuda"), vals], dim=1).contiguous()
+        q = capi.quantize_nf4(W.view(nb, 64), group=0)
+        p = q.packed.view(nb, 32)
+        idx = torch.stack([p >> 4, p & 15], dim=2).view(nb, 64)[:, 1:].reshape(-1)[:n]
+        ref = oracle.nearest_codes_scaled_bits(start, n, a)
+        got = idx.cpu().numpy()
+        if not np.array_equal(got, ref):
+            bad = int(np.flatnonzero(got != ref)[0])
+            raise AssertionError(f"absmax {a!r}: weight bits {start + bad:#010x} -> "
+                                 f"{got[bad]} (oracle {ref[bad]})")
+        assert np.all(q.absmax_f32.cpu().numpy() == np.float32(a))
+        start += n
+
+
+def _sweep_all(absmax: float):
+    """Every binary32 w with |w| <= absmax."""
+    top = _f32_bits(absmax)
+    _sweep(absmax, 0, top + 1)
+    _sweep(absmax, 0x80000000, top + 1)
+
+
+def _sweep_windows(absmax: float, half: int = 1 << 14):
+    """Windows of 2 * half consecutive weights around w = th_k * absmax for
+    every decision threshold th_k, plus the ends of the range."""
+    a = float(np.float32(absmax))
+    top = _f32_bits(a)
+    for th in capi.nf4_thresholds():
+        c = _f32_bits(float(np.float32(th) * np.float32(a)))
+        mag, sign = c & 0x7FFFFFFF, c & 0x80000000
+        lo, hi = max(0, mag - half), min(top, mag + half)
+        _sweep(a, sign | lo, hi - lo + 1)
+    for sign in (0, 0x80000000):
+        _sweep(a, sign | max(0, top - half), min(top, half) + 1)
+        _sweep(a, sign, min(top, half) + 1)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("absmax", [1.0, 0.018737793, 1.5 * 2.0 ** -126, 1703.25, 9.1e-41],
+                         ids=["1", "0.0187", "1.5e-126x2", "1703.25", "denormal"])
+def test_exhaustive_decision_rule(absmax):
+    """Every binary32 w in [-absmax, absmax] (about 2.1e9 values for absmax
+    near 1) quantised as a non-maximal element of a block whose absmax is
+    `absmax` gets the oracle's index: the division by the block constant
+    and the nearest-codepoint rule, exactly."""
+    _sweep_all(absmax)
+
+
+@pytest.mark.parametrize("absmax", [2.0 ** -126, 2.0 ** -100, 0.5, 3.0517578e-05, 0.2718,
+                                    2.0 ** 20, 6.02e23, 2.0 ** 126, 1.1e38, 3.4e38],
+                         ids=lambda a: f"{a:.4g}")
+def test_decision_rule_near_every_threshold(absmax):
+    """Windows of 32768 consecutive weights around every decision threshold
+    (scaled by the block constant), for powers of two, random constants and
+    the ends of the binary32 range (where the reciprocal leaves the normal
+    range and every element takes the IEEE quotient)."""
+    _sweep_windows(absmax)

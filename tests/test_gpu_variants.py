@@ -1,9 +1,9 @@
 """GPU parity of the forward / backward for the other storage formats and for
 input ranges beyond N(0, 1), against the fp64 oracle.
 
-- Block constants kept in fp32 (no double quantisation, group 0) and double
-  quantisation with groups of 64 block constants, on both forward kernels
-  (tensor-core GEMM and decode GEMV) and on the backward.
+- Blocks of 64 and of 128 weights, block constants kept in fp32 (no double
+  quantisation, group 0) or double-quantised in groups of 64 or 256, on both
+  forward kernels (tensor-core GEMM and decode GEMV) and on the backward.
 - The decode GEMV at K = 14336 with heavy-tailed activations (N(0, 4) with
   +-30 outliers) and a LoRA factor A holding entries beyond the f16 range
   (|a| > 65504): the GEMV must compute with the exact bf16 W_hat and accept
@@ -32,10 +32,10 @@ def _quantized(d, group, block=64):
     return g, q, oracle.dequant_f32(ref_q)
 
 
-FMT = [(64, 0), (64, 64), (64, 256)]
+FMT = [(64, 0), (64, 64), (64, 256), (128, 0), (128, 64), (128, 256)]
 FWD_SHAPES = [
     inputs.LinearShape("N1032_K1024_M300_r16", N=1032, K=1024, M=300, r=16, alpha=32.0),
-    inputs.LinearShape("N520_K4160_M5_r16", N=520, K=4160, M=5, r=16, alpha=32.0),
+    inputs.LinearShape("N520_K4224_M5_r16", N=520, K=4224, M=5, r=16, alpha=32.0),
 ]
 
 

@@ -146,3 +146,22 @@ def test_nearest_codes_bits_matches_scalar():
     for i in range(0, 1000, 37):
         v = np.uint32(int(start) + i).view(np.float32)
         assert out[i] == orc.nearest_code(v)
+
+
+def test_scaled_sweep_matches_block_quantisation():
+    """The sweep helper (division by a block constant, then nearest code) gives
+    the indices oracle_quantize_nf4 gives the same weights inside a block
+    whose absmax is that constant; with absmax 1 it is the plain rule."""
+    rng = np.random.default_rng(7)
+    for a in (1.0, 0.0173, 3.3e-5, 2.0 ** -100, 1.7e3):
+        a32 = np.float32(a)
+        w = (rng.uniform(-1, 1, 63) * a32).astype(np.float32)
+        start = int(np.float32(w[0]).view(np.uint32))
+        block = np.concatenate([[a32], w]).astype(np.float32)
+        q = orc.quantize_nf4(block.reshape(1, 64), 64, 0)
+        for i in range(63):
+            b = int(w[i].view(np.uint32))
+            assert orc.nearest_codes_scaled_bits(b, 1, float(a32))[0] == q.idx[0, i + 1]
+    bits = 0x3E000000
+    assert np.array_equal(orc.nearest_codes_scaled_bits(bits, 4096, 1.0),
+                          orc.nearest_codes_bits(bits, 4096))

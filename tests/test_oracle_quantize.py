@@ -226,3 +226,51 @@ def test_quantize_rejects_bad_shapes():
         orc.quantize_nf4(np.zeros((2, 65), np.float32))
     with pytest.raises(ValueError):
         orc.quantize_nf4(np.zeros((2, 64), np.float32), block=63)
+
+
+# ------------------------------------------------------------- block 128
+# "QLoRA and 4bit Quantization | QLoRA 与 4-bit NormalFloat 量化核心机制",
+# engineering notes: 64 or 128 parameters share one scale.
+
+def test_block128_storage_closed_forms():
+    """128-weight blocks: 4 + 32/128 = 4.25 bits per parameter with binary32
+    constants, 4 + 8/128 + 32/(128*256) with double quantisation."""
+    for rows, cols in ((4096, 4096), (14336, 4096), (4096, 14336)):
+        n = rows * cols
+        p0, c0, s0 = orc.storage_bytes(rows, cols, 128, 0)
+        assert 8 * (p0 + c0 + s0) / n == 4.25
+        p, c, s = orc.storage_bytes(rows, cols, 128, 256)
+        assert 8 * (p + c + s) / n == 4 + 8 / 128 + 32 / (128 * 256)
+
+
+def test_block128_absmax_and_brute_force_nearest():
+    """Per 128-weight block the constant is numpy's abs-max over the block,
+    and every index is the nearest codepoint of w / a found by brute force
+    over the 16 entries (exact rationals, up to the binary32 rounding of the
+    division)."""
+    w = _rand_w(3, 256, 21)
+    w[1, 128 + 5] = 0.0
+    w[2, :128] = 0.0  # an all-zero block
+    q = orc.quantize_nf4(w, block=128, group=0)
+    blocks = w.reshape(-1, 128)
+    assert np.array_equal(q.absmax_f32, np.abs(blocks).max(axis=1))
+    cb = [Fraction(float(c)) for c in orc.codebook()]
+    idx = q.idx.reshape(-1, 128)
+    for b in range(blocks.shape[0]):
+        a = Fraction(float(np.abs(blocks[b]).max()))
+        for i in range(128):
+            if a == 0:
+                assert idx[b, i] == 7
+                continue
+            xn = Fraction(float(blocks[b, i])) / a
+            d = [abs(xn - c) for c in cb]
+            m = min(d)
+            ok = {k for k, dk in enumerate(d) if dk - m <= Fraction(2) ** -22}
+            assert idx[b, i] in ok
+    # one block of 128 is not two blocks of 64: the halves share one constant
+    w2 = np.zeros((1, 128), np.float32)
+    w2[0, 0], w2[0, 100] = 0.02, 0.2
+    q128 = orc.quantize_nf4(w2, block=128, group=0)
+    q64 = orc.quantize_nf4(w2, block=64, group=0)
+    assert q128.absmax_f32.tolist() == [np.float32(0.2)]
+    assert q128.idx[0, 0] != q64.idx[0, 0]
