@@ -549,6 +549,24 @@ def sub_benchmarks(capi, layers, device, stream, args):
                                   "frac_of_hbm": round(db / (dms * 1e-3) / 1e9 / hbm, 4)}
     del mats, outs, outw
     torch.cuda.empty_cache()
+    # adapter merge bf16(W_hat + alpha/r B A) of the gate and up projections, alternating
+    mg = [L for L in layers if L["name"] in ("gate_proj", "up_proj")]
+    mo = [torch.empty((L["N"], L["K"]), dtype=torch.bfloat16, device=device) for L in mg]
+    for i in range(3):
+        capi.merge_lora(mg[i % 2]["q"], mg[i % 2]["A"], mg[i % 2]["B"], ALPHA, out=mo[i % 2])
+    torch.cuda.synchronize()
+    e0.record()
+    for i in range(20):
+        capi.merge_lora(mg[i % 2]["q"], mg[i % 2]["A"], mg[i % 2]["B"], ALPHA, out=mo[i % 2])
+    e1.record()
+    torch.cuda.synchronize()
+    mms = e0.elapsed_time(e1) / 20
+    Nm, Km = mg[0]["N"], mg[0]["K"]
+    mb = Nm * Km * (0.5 + 1 / 64 + 4 / 16384 + 2) + RANK_R * (Nm + Km) * 2
+    rows["merge_14336x4096"] = {"us": round(mms * 1e3, 1), "GBps": round(mb / (mms * 1e-3) / 1e9, 1),
+                                "frac_of_hbm": round(mb / (mms * 1e-3) / 1e9 / hbm, 4),
+                                "note": "gate and up weights alternated (147 MB per call pair > L2)"}
+    del mo
     rows["llama3_7proj_fwd_bwd_M8192"] = layer_set_at(capi, layers, 8192, device, stream,
                                                       steps=3 if args.quick else 6)
     return rows
@@ -646,6 +664,12 @@ def oracle_rows():
         t = timed(lambda: oracle.linear_fwd(x, oracle.dequant_f32(q), A, B, ALPHA))
         out[f"gemv_gate_M{Mg}"] = {k: {"s": round(v, 3), "packed_GBps": round(
             N * K / 2 / v / 1e9, 3)} for k, v in t.items()}
+    # adapter merge of the gate weight (the bytes of the GPU row)
+    wg = oracle.dequant_f32(q)
+    mbytes = N * K * (0.5 + 1 / 64 + 4 / 16384 + 2) + RANK_R * (N + K) * 2
+    t = timed(lambda: oracle.merge_bf16(wg, A, B, ALPHA))
+    out["merge_14336x4096"] = {k: {"s": round(v, 3), "GBps": round(mbytes / v / 1e9, 3)}
+                               for k, v in t.items()}
     # dequantisation of one 4096x14336 matrix
     Wb = inputs.bulk_matrix(0).float().numpy()
     qb = oracle.quantize_nf4(Wb, 64, 256, want_idx=False)
@@ -792,6 +816,7 @@ def run_case(args):
         "gemv": lambda: capi.linear_fwd(q, x, A, B, ALPHA, ws, y_dtype=torch.bfloat16, t_save=t),
         "quantize": lambda: capi.quantize_nf4(W, out=out_q),
         "dequant": lambda: capi.dequant(q, out=out_w),
+        "merge": lambda: capi.merge_lora(q, A, B, ALPHA, out=out_w),
     }
     capi.linear_fwd(q, x, A, B, ALPHA, ws, t_save=t)
     fn = fns[args.only]
@@ -817,7 +842,8 @@ def main(argv=None):
     ap.add_argument("--quick", action="store_true", help="smaller sub-benchmarks")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row sub-benchmarks")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["gemm_fwd", "gemm_dx", "gemv", "quantize", "dequant"],
+    ap.add_argument("--only", choices=["gemm_fwd", "gemm_dx", "gemv", "quantize", "dequant",
+                                       "merge"],
                     help="run one kernel case a few times and exit (for profiling)")
     ap.add_argument("--M", type=int, default=1, help="tokens for --only gemv")
     args = ap.parse_args(argv)

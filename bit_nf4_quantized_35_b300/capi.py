@@ -6,7 +6,7 @@ current stream.  There is no fallback: if the library is missing, or a call
 returns an error status, the binding raises.
 
 The function names follow the C ABI:
-  qlora_nf4_sizes, qlora_quantize_nf4, qlora_dequant, qlora_workspace_size,
+  qlora_nf4_sizes, qlora_quantize_nf4, qlora_dequant, qlora_merge_lora, qlora_workspace_size,
   qlora_workspace_size_min, qlora_workspace_init, qlora_device_status, qlora_linear_fwd,
   qlora_linear_bwd, qlora_nf4_thresholds, qlora_nf4_codebook.
 """
@@ -31,7 +31,7 @@ EXPORTED = (
     "qlora_nf4_sizes", "qlora_quantize_nf4", "qlora_dequant", "qlora_workspace_size",
     "qlora_workspace_init", "qlora_device_status", "qlora_linear_fwd", "qlora_linear_bwd",
     "qlora_nf4_thresholds", "qlora_nf4_codebook", "qlora_status_string",
-    "qlora_linear_bwd_noalloc", "qlora_workspace_size_min",
+    "qlora_linear_bwd_noalloc", "qlora_workspace_size_min", "qlora_merge_lora",
 )
 
 
@@ -67,6 +67,7 @@ def load(path: str = LIB_PATH):
         "qlora_nf4_sizes": [i64, i64, i32, i32, P, P, P],
         "qlora_quantize_nf4": [P, st, P, P, P],
         "qlora_dequant": [P, P, P],
+        "qlora_merge_lora": [P, P, P, i32, f32, P, P],
         "qlora_workspace_size": [i64, i64, i64, i32, P],
         "qlora_workspace_size_min": [i64, i64, i64, i32, P],
         "qlora_workspace_init": [P, sz, P],
@@ -188,6 +189,18 @@ def dequant(w: NF4Weight, out: torch.Tensor | None = None, stream=None) -> torch
         out = torch.empty((w.rows, w.cols), dtype=torch.bfloat16, device=w.packed.device)
     s = w.struct()
     _check("qlora_dequant", load().qlora_dequant(ctypes.byref(s), _ptr(out), _stream(stream)))
+    return out
+
+
+def merge_lora(w: NF4Weight, A: torch.Tensor, B: torch.Tensor, alpha: float,
+               out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """qlora_merge_lora -> bf16 [rows, cols] = bf16(W_hat + alpha/r B A)."""
+    r = A.shape[0]
+    if out is None:
+        out = torch.empty((w.rows, w.cols), dtype=torch.bfloat16, device=w.packed.device)
+    s = w.struct()
+    _check("qlora_merge_lora", load().qlora_merge_lora(
+        ctypes.byref(s), _ptr(A), _ptr(B), r, float(alpha), _ptr(out), _stream(stream)))
     return out
 
 

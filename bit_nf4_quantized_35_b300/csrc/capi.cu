@@ -279,6 +279,33 @@ qlora_status qlora_dequant(const qlora_nf4_weight *w, uint16_t *W_out, void *str
                                     static_cast<cudaStream_t>(stream)));
 }
 
+qlora_status qlora_merge_lora(const qlora_nf4_weight *w, const uint16_t *A, const uint16_t *B,
+                              int32_t r, float alpha, uint16_t *W_out, void *stream) {
+  qlora_status st = check_weight(w, true);
+  if (st != QLORA_OK) return st;
+  if (!A || !B || !W_out) return QLORA_ERR_INVALID_ARG;
+  if (r < 8 || r > 64 || r % 8) return QLORA_ERR_SHAPE;
+  if (w->rows > (int64_t)INT32_MAX || w->cols > (int64_t)INT32_MAX) return QLORA_ERR_SHAPE;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(W_out)) return QLORA_ERR_ALIGN;
+  MergeArgs a{};
+  a.packed = w->packed;
+  a.use_code = w->group > 0;
+  a.codes = a.use_code ? w->absmax_code : reinterpret_cast<const int8_t *>(w->packed);
+  a.cvec = a.use_code ? w->scale2 : w->absmax_f32;
+  const int cdiv = w->group > 0 ? w->group : 1;
+  a.cshift = 0;
+  while ((1 << a.cshift) < cdiv) ++a.cshift;
+  a.bshift = w->block == 128 ? 1 : 0;
+  a.N = (int)w->rows;
+  a.K = (int)w->cols;
+  a.A = A;
+  a.B = B;
+  a.r = r;
+  a.s = alpha / (float)r;
+  a.out = W_out;
+  return cuda_status(launch_merge(a, static_cast<cudaStream_t>(stream)));
+}
+
 qlora_status qlora_workspace_size(int64_t M, int64_t N, int64_t K, int32_t r, size_t *bytes) {
   if (!bytes) return QLORA_ERR_INVALID_ARG;
   if (M < 0 || N < 0 || K < 0 || r < 1 || r > 64) return QLORA_ERR_SHAPE;

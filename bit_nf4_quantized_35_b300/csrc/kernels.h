@@ -106,6 +106,21 @@ cudaError_t launch_dequant(const uint8_t *packed, const int8_t *codes, const flo
                            const float *scale2, int group, int block, int64_t nblocks,
                            uint16_t *out, int num_sms, cudaStream_t s);
 
+// Adapter merge (merge.cu): out = bf16(w_hat + s . B A).
+struct MergeArgs {
+  const uint8_t *packed;
+  const int8_t *codes;  // readable memory even without DQ
+  const float *cvec;
+  int use_code, cshift, bshift;
+  int N, K;
+  const uint16_t *A;  // [r, K] bf16
+  const uint16_t *B;  // [N, r] bf16
+  int r;
+  float s;
+  uint16_t *out;  // [N, K] bf16
+};
+cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s);
+
 // Rank-r gradient contractions and layout helpers (lora_grad.cu).
 int skinny_splits(int64_t M, int C);
 int skinny_tiles(int C);

@@ -133,6 +133,22 @@ qlora_status qlora_quantize_nf4(const void *W, qlora_dtype w_dtype, const qlora_
  * Errors as for qlora_quantize_nf4. */
 qlora_status qlora_dequant(const qlora_nf4_weight *w, uint16_t *W_out, void *stream);
 
+/* Adapter merge: W_out = bf16(W_hat + (alpha / r) . B . A), [N, K] bf16.
+ * [QLoRA-26] Step 5 conclusion (adapter merge and deployment loading are
+ * what a trained adapter still has to pass) and [Select-65] (the merged
+ * model as the delivered artifact).  The Step 3 forward formula gives
+ *   x . W_hat^T + (x . A^T) . B^T . alpha / r = x . (W_hat + alpha/r . B . A)^T,
+ * so the merged weight serves the same forward without the LoRA branch (up
+ * to its one bf16 rounding).  Arithmetic: W_hat exactly as qlora_dequant
+ * produces it, B . A with bf16 operands and fp32 accumulation, one fp32
+ * multiply-add with alpha / r (fp32), one rounding to bf16.
+ *   w      quantised base weight [N, K] (const)
+ *   A      device bf16 [r, K];  B  device bf16 [N, r];  8 <= r <= 64, r % 8 == 0
+ *   W_out  device bf16 [N, K], caller-owned
+ * Errors: QLORA_ERR_INVALID_ARG, QLORA_ERR_SHAPE, QLORA_ERR_ALIGN, QLORA_ERR_CUDA. */
+qlora_status qlora_merge_lora(const qlora_nf4_weight *w, const uint16_t *A, const uint16_t *B,
+                              int32_t r, float alpha, uint16_t *W_out, void *stream);
+
 /* Workspace bytes for qlora_linear_fwd / qlora_linear_bwd at these sizes
  * (M tokens, N out features, K in features, LoRA rank r) on the current
  * device.  One workspace sized this way serves both calls.  It includes a

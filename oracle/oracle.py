@@ -72,6 +72,10 @@ def _declare(lib):
     lib.oracle_linear_bwd.argtypes = [P, P, i64, i64, i64, P, P, P, i32, f64, P, i64,
                                       P, P, P, P, P]
     lib.oracle_linear_bwd.restype = None
+    lib.oracle_bf16_rne_double.argtypes = [f64]
+    lib.oracle_bf16_rne_double.restype = ctypes.c_uint16
+    lib.oracle_merge_bf16.argtypes = [P, i64, i64, P, P, i32, f64, P, P]
+    lib.oracle_merge_bf16.restype = None
     lib.oracle_nf4_storage_bytes.argtypes = [i64, i64, i32, i32, P, P, P]
     lib.oracle_nf4_storage_bytes.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
@@ -250,6 +254,25 @@ def linear_bwd(x, dY, w, A, B, alpha: float, rows=None):
                               float(alpha), _ptr(rows), rows.size, _ptr(dX), _ptr(dA),
                               _ptr(dB), _ptr(t), _ptr(u))
     return {"dX": dX, "dA": dA, "dB": dB, "t": t, "u": u}
+
+
+def bf16_rne_double(v: float) -> int:
+    """binary64 -> bf16 bit pattern, round to nearest even (one rounding)."""
+    return int(_load().oracle_bf16_rne_double(float(v)))
+
+
+def merge_bf16(w, A, B, alpha: float):
+    """Merged weight W_hat + alpha/r B A: (bf16 bit patterns [N, K] uint16,
+    binary64 values before rounding [N, K])."""
+    w, A, B = _f32(w), _f32(A), _f32(B)
+    N, K = w.shape
+    r = A.shape[0]
+    assert A.shape == (r, K) and B.shape == (N, r)
+    exact = np.empty((N, K), dtype=np.float64)
+    bits = np.empty((N, K), dtype=np.uint16)
+    _load().oracle_merge_bf16(_ptr(w), N, K, _ptr(A), _ptr(B), r, float(alpha), _ptr(exact),
+                              _ptr(bits))
+    return bits, exact
 
 
 def storage_bytes(rows: int, cols: int, block: int = 64, group: int = 256):

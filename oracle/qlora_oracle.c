@@ -372,6 +372,52 @@ void oracle_linear_bwd(const float *x, const float *dY, int64_t M, int64_t K, in
   }
 }
 
+/* binary64 -> bf16 bits, round to nearest, ties to even: bf16 keeps 8
+ * significant bits (the binary32 exponent range), so v = m 2^e with
+ * m in [0.5, 1) is rounded as rint(m 2^8) 2^(e-8) (rint rounds half to even
+ * in the default rounding mode); below 2^-126 the spacing is fixed at
+ * 2^-133.  Finite inputs below 2^128 only. */
+uint16_t oracle_bf16_rne_double(double v) {
+  double q;
+  if (v == 0.0) {
+    q = v;
+  } else if (fabs(v) < ldexp(1.0, -126)) {
+    q = rint(ldexp(v, 133)) * ldexp(1.0, -133);
+  } else {
+    int e;
+    frexp(v, &e);
+    q = ldexp(rint(ldexp(v, 8 - e)), e - 8);
+  }
+  float f = (float)q; /* exact: q has at most 8 significant bits */
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  return (uint16_t)(u >> 16);
+}
+
+/* Adapter merge.  [QLoRA-26] Step 5 (conclusion: adapter merge and
+ * deployment loading are what a trained adapter still has to pass) and
+ * [Select-65] (a merged model as the delivered artifact).  Merging folds the
+ * LoRA branch of the forward formula into the base weight:
+ *   x W_hat^T + (x A^T) B^T alpha/r = x (W_hat + alpha/r B A)^T,
+ * so the merged weight is W_hat + (alpha/r) B A, here in bf16 (the compute
+ * dtype), rounded once from the binary64 sum (ascending j).
+ *   w_hat [N, K], A [r, K], B [N, r]; exact (nullable) gets the binary64
+ *   values before rounding, bits the bf16 patterns. */
+void oracle_merge_bf16(const float *w_hat, int64_t N, int64_t K, const float *A, const float *B,
+                       int32_t r, double alpha, double *exact, uint16_t *bits) {
+  const double s = alpha / (double)r;
+#pragma omp parallel for schedule(static)
+  for (int64_t n = 0; n < N; ++n) {
+    for (int64_t k = 0; k < K; ++k) {
+      double lora = 0.0;
+      for (int32_t j = 0; j < r; ++j) lora += (double)B[n * r + j] * (double)A[j * K + k];
+      const double v = (double)w_hat[n * K + k] + s * lora;
+      if (exact) exact[n * K + k] = v;
+      bits[n * K + k] = oracle_bf16_rne_double(v);
+    }
+  }
+}
+
 /* Storage accounting.  [QLoRA-26] Step 4 (qlora_trainable_state_ledger:
  * packed size (numel + 1) // 2 bytes) and [Finetune-4] (4.5 -> ~4.127 bits
  * per parameter): bytes of packed indices, block constants and second-level

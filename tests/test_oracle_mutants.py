@@ -16,6 +16,7 @@ import pytest
 from oracle import oracle as orc
 from tests import test_oracle_codebook as tcb
 from tests import test_oracle_linear as tli
+from tests import test_oracle_merge as tme
 from tests import test_oracle_quantize as tqu
 
 SRC = os.path.join(os.path.dirname(orc.__file__), "qlora_oracle.c")
@@ -44,6 +45,14 @@ MUTANTS = {
     "bf16_round_half_up": ("u += 0x7fffu + lsb;", "u += 0x8000u + 0 * lsb;"),
     "zero_block_index": ("#define ORACLE_ZERO_INDEX 7", "#define ORACLE_ZERO_INDEX 8"),
     "signed_absmax": ("if (m > amax) amax = m;", "if (v > amax) amax = v;"),
+    "merge_lora_sign": ("const double v = (double)w_hat[n * K + k] + s * lora;",
+                        "const double v = (double)w_hat[n * K + k] - s * lora;"),
+    "merge_drops_scaling": ("const double v = (double)w_hat[n * K + k] + s * lora;",
+                            "const double v = (double)w_hat[n * K + k] + lora;"),
+    "merge_transposed_B": ("lora += (double)B[n * r + j] * (double)A[j * K + k];",
+                           "lora += (double)B[(j * N + n) % (N * r)] * (double)A[j * K + k];"),
+    "merge_round_down": ("q = ldexp(rint(ldexp(v, 8 - e)), e - 8);",
+                         "q = ldexp(floor(ldexp(v, 8 - e)), e - 8);"),
     "storage_const_bytes": ("*const_b = nblocks * 1; /* int8 code per block */",
                             "*const_b = nblocks * 2; /* int8 code per block */"),
 }
@@ -74,6 +83,10 @@ def _pins(golden):
         lambda: tli.test_backward_matches_torch_autograd_fp64(5, 128, 64, 4),
         tli.test_zero_b_gives_base_output_and_zero_dA,
         lambda: tli.test_p1_fixture_contracts(golden),
+        tme.test_double_to_bf16_rounding_matches_brute_force,
+        tme.test_zero_factor_gives_the_dequantised_weight,
+        tme.test_merged_weight_reproduces_the_forward,
+        tme.test_hand_example,
     ]
     return pins
 
