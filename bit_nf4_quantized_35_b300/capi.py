@@ -43,7 +43,8 @@ class QloraError(RuntimeError):
 
 class _NF4WeightStruct(ctypes.Structure):
     _fields_ = [("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("block", ctypes.c_int32),
-                ("group", ctypes.c_int32), ("packed", ctypes.c_void_p),
+                ("group", ctypes.c_int32), ("codebook", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("packed", ctypes.c_void_p),
                 ("absmax_code", ctypes.c_void_p), ("absmax_f32", ctypes.c_void_p),
                 ("scale2", ctypes.c_void_p)]
 
@@ -75,8 +76,8 @@ def load(path: str = LIB_PATH):
         "qlora_linear_fwd": [P, P, i64, P, P, i32, f32, P, st, P, P, sz, u32, P],
         "qlora_linear_bwd": [P, P, P, i64, P, P, i32, f32, P, P, st, P, P, P, sz, u32, P],
         "qlora_linear_bwd_noalloc": [P, P, P, i64, P, P, i32, f32, P, P, st, P, P, u32, P],
-        "qlora_nf4_thresholds": [P],
-        "qlora_nf4_codebook": [P],
+        "qlora_nf4_thresholds": [i32, P],
+        "qlora_nf4_codebook": [i32, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -111,15 +112,18 @@ def nf4_sizes(rows: int, cols: int, block: int = 64, group: int = 256):
     return p.value, c.value, s.value
 
 
-def nf4_thresholds() -> list[float]:
+QLORA_CODEBOOK_PRINTED, QLORA_CODEBOOK_QUANTILE = 0, 1
+
+
+def nf4_thresholds(codebook: int = QLORA_CODEBOOK_PRINTED) -> list[float]:
     out = (ctypes.c_float * 15)()
-    _check("qlora_nf4_thresholds", load().qlora_nf4_thresholds(out))
+    _check("qlora_nf4_thresholds", load().qlora_nf4_thresholds(codebook, out))
     return list(out)
 
 
-def nf4_codebook() -> list[float]:
+def nf4_codebook(codebook: int = QLORA_CODEBOOK_PRINTED) -> list[float]:
     out = (ctypes.c_float * 16)()
-    _check("qlora_nf4_codebook", load().qlora_nf4_codebook(out))
+    _check("qlora_nf4_codebook", load().qlora_nf4_codebook(codebook, out))
     return list(out)
 
 
@@ -148,35 +152,38 @@ class NF4Weight:
     absmax_f32: torch.Tensor | None    # float32 [nblocks]    (group == 0)
     block: int = 64
     group: int = 256
+    codebook: int = 0  # qlora_codebook: 0 printed table, 1 quantile formula
 
     def struct(self) -> _NF4WeightStruct:
-        return _NF4WeightStruct(self.rows, self.cols, self.block, self.group,
+        return _NF4WeightStruct(self.rows, self.cols, self.block, self.group, self.codebook, 0,
                                 self.packed.data_ptr(),
                                 None if self.absmax_code is None else self.absmax_code.data_ptr(),
                                 None if self.absmax_f32 is None else self.absmax_f32.data_ptr(),
                                 None if self.scale2 is None else self.scale2.data_ptr())
 
     @staticmethod
-    def empty(rows: int, cols: int, device="cuda", block: int = 64, group: int = 256):
+    def empty(rows: int, cols: int, device="cuda", block: int = 64, group: int = 256,
+              codebook: int = 0):
         pb, cb, sb = nf4_sizes(rows, cols, block, group)
         packed = torch.empty(max(pb, 16), dtype=torch.uint8, device=device)[:pb]
         if group > 0:
             codes = torch.empty(max(cb, 16), dtype=torch.int8, device=device)[:cb]
             s2 = torch.empty(max(sb // 4, 4), dtype=torch.float32, device=device)[:sb // 4]
-            return NF4Weight(rows, cols, packed, codes, s2, None, block, group)
+            return NF4Weight(rows, cols, packed, codes, s2, None, block, group, codebook)
         absf = torch.empty(max(cb // 4, 4), dtype=torch.float32, device=device)[:cb // 4]
-        return NF4Weight(rows, cols, packed, None, None, absf, block, group)
+        return NF4Weight(rows, cols, packed, None, None, absf, block, group, codebook)
 
 
 def quantize_nf4(W: torch.Tensor, group: int = 256, out: NF4Weight | None = None,
                  nonfinite_flag: torch.Tensor | None = None, stream=None,
-                 block: int = 64) -> NF4Weight:
+                 block: int = 64, codebook: int = 0) -> NF4Weight:
     """qlora_quantize_nf4 on a contiguous fp32 or bf16 CUDA matrix [rows, cols]."""
     assert W.is_cuda and W.is_contiguous() and W.dim() == 2
     dt = {torch.float32: QLORA_F32, torch.bfloat16: QLORA_BF16}[W.dtype]
     rows, cols = W.shape
     if out is None:
-        out = NF4Weight.empty(rows, cols, W.device, block=block, group=group)
+        out = NF4Weight.empty(rows, cols, W.device, block=block, group=group,
+                              codebook=codebook)
     s = out.struct()
     _check("qlora_quantize_nf4", load().qlora_quantize_nf4(
         _ptr(W), dt, ctypes.byref(s), _ptr(nonfinite_flag), _stream(stream)))

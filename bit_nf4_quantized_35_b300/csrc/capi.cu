@@ -46,31 +46,94 @@ float funkey(uint32_t k) {
   std::memcpy(&f, &b, 4);
   return f;
 }
-float g_th[15];
-std::once_flag g_th_once;
-void compute_thresholds() {
-  static const float c[16] = {QLORA_NF4_VALUES};
-  for (int k = 0; k < 15; ++k) {
-    const float lo = c[k], hi = c[k + 1];
-    auto closer_to_hi = [&](float x) {
-      volatile float dh = std::fabs(x - hi);
-      volatile float dl = std::fabs(x - lo);
-      return dh < dl;
-    };
-    uint32_t a = fkey(lo), b = fkey(hi);  // closer_to_hi(lo) false, (hi) true
-    while (b - a > 1) {
-      const uint32_t mid = a + (b - a) / 2;
-      if (closer_to_hi(funkey(mid)))
-        b = mid;
-      else
-        a = mid;
+// Percentage points of the normal distribution: Wichura's algorithm AS 241
+// (PPND16, Applied Statistics 37(3), 1988), rational approximations with
+// about 1e-16 relative accuracy, binary64.
+double ppnd16(double p) {
+  const double q = p - 0.5;
+  if (std::fabs(q) <= 0.425) {
+    const double r = 0.180625 - q * q;
+    return q *
+           (((((((2509.0809287301226727 * r + 33430.575583588128105) * r +
+                 67265.770927008700853) * r + 45921.953931549871457) * r +
+               13731.693765509461125) * r + 1971.5909503065514427) * r +
+             133.14166789178437745) * r + 3.387132872796366608) /
+           (((((((5226.495278852854561 * r + 28729.085735721942674) * r +
+                 39307.89580009271061) * r + 21213.794301586595867) * r +
+               5394.1960214247511077) * r + 687.1870074920579083) * r +
+             42.313330701600911252) * r + 1.0);
+  }
+  double r = q < 0 ? p : 1.0 - p;
+  r = std::sqrt(-std::log(r));
+  double v;
+  if (r <= 5.0) {
+    r -= 1.6;
+    v = (((((((7.7454501427834140764e-4 * r + 0.0227238449892691845833) * r +
+              0.24178072517745061177) * r + 1.27045825245236838258) * r +
+            3.64784832476320460504) * r + 5.7694972214606914055) * r +
+          4.6303378461565452959) * r + 1.42343711074968357734) /
+        (((((((1.05075007164441684324e-9 * r + 5.475938084995344946e-4) * r +
+              0.0151986665636164571966) * r + 0.14810397642748007459) * r +
+            0.68976733498510000455) * r + 1.6763848301838038494) * r +
+          2.05319162663775882187) * r + 1.0);
+  } else {
+    r -= 5.0;
+    v = (((((((2.01033439929228813265e-7 * r + 2.71155556874348757815e-5) * r +
+              0.0012426609473880784386) * r + 0.026532189526576123093) * r +
+            0.29656057182850489123) * r + 1.7848265399172913358) * r +
+          5.4637849111641143699) * r + 6.6579046435011037772) /
+        (((((((2.04426310338993978564e-15 * r + 1.4215117583164458887e-7) * r +
+              1.8463183175100546818e-5) * r + 7.868691311456132591e-4) * r +
+            0.0148753612908506148525) * r + 0.13692988092273580531) * r +
+          0.59983220655588793769) * r + 1.0);
+  }
+  return q < 0 ? -v : v;
+}
+
+// The codebooks.  0: the printed NF4 table.  1: the quantile construction
+// q_i = Phi^-1((i - 0.5) / 16), i = 1..16 ("QLoRA and 4bit Quantization |
+// QLoRA 与 4-bit 量化", Step 2), divided by q_16 so that it runs from -1 to 1;
+// the upper half is computed and mirrored (exactly symmetric, no zero).
+struct Tables {
+  Codebook cb;
+  float th[15];
+};
+Tables g_tab[2];
+std::once_flag g_tab_once;
+
+void compute_tables() {
+  const float printed[16] = {QLORA_NF4_VALUES};
+  for (int i = 0; i < 16; ++i) g_tab[0].cb.v[i] = printed[i];
+  const double q16 = ppnd16(15.5 / 16.0);
+  for (int i = 9; i <= 16; ++i) {
+    const float c = (float)(ppnd16((i - 0.5) / 16.0) / q16);
+    g_tab[1].cb.v[i - 1] = c;
+    g_tab[1].cb.v[16 - i] = -c;
+  }
+  for (int t = 0; t < 2; ++t) {
+    const float *c = g_tab[t].cb.v;
+    for (int k = 0; k < 15; ++k) {
+      const float lo = c[k], hi = c[k + 1];
+      auto closer_to_hi = [&](float x) {
+        volatile float dh = std::fabs(x - hi);
+        volatile float dl = std::fabs(x - lo);
+        return dh < dl;
+      };
+      uint32_t a = fkey(lo), b = fkey(hi);  // closer_to_hi(lo) false, (hi) true
+      while (b - a > 1) {
+        const uint32_t mid = a + (b - a) / 2;
+        if (closer_to_hi(funkey(mid)))
+          b = mid;
+        else
+          a = mid;
+      }
+      g_tab[t].th[k] = funkey(b);
     }
-    g_th[k] = funkey(b);
   }
 }
-const float *thresholds() {
-  std::call_once(g_th_once, compute_thresholds);
-  return g_th;
+const Tables &tables(int codebook) {
+  std::call_once(g_tab_once, compute_tables);
+  return g_tab[codebook == 1 ? 1 : 0];
 }
 
 qlora_status check_weight(const qlora_nf4_weight *w, bool need_buffers) {
@@ -81,6 +144,8 @@ qlora_status check_weight(const qlora_nf4_weight *w, bool need_buffers) {
         w->group == 256))
     return QLORA_ERR_SHAPE;
   if (w->cols % w->block) return QLORA_ERR_SHAPE;
+  if (w->codebook != QLORA_CODEBOOK_PRINTED && w->codebook != QLORA_CODEBOOK_QUANTILE)
+    return QLORA_ERR_INVALID_ARG;
   if (!need_buffers) return QLORA_OK;
   if (!w->packed) return QLORA_ERR_INVALID_ARG;
   if (w->group > 0 && (!w->absmax_code || !w->scale2)) return QLORA_ERR_INVALID_ARG;
@@ -169,6 +234,7 @@ void set_block_constants(GemmArgs &g, const qlora_nf4_weight *w) {
   g.cshift = 0;
   while ((1 << g.cshift) < g.cdiv) ++g.cshift;
   g.bshift = w->block == 128 ? 1 : 0;
+  g.cb = tables(w->codebook).cb;
   if (!g.use_code) g.codes = reinterpret_cast<const int8_t *>(w->packed);
 }
 
@@ -228,17 +294,17 @@ const char *qlora_status_string(qlora_status s) {
   return "unknown status";
 }
 
-qlora_status qlora_nf4_codebook(float out[16]) {
-  if (!out) return QLORA_ERR_INVALID_ARG;
-  static const float c[16] = {QLORA_NF4_VALUES};
-  for (int i = 0; i < 16; ++i) out[i] = c[i];
+qlora_status qlora_nf4_codebook(int32_t codebook, float out[16]) {
+  if (!out || (codebook != 0 && codebook != 1)) return QLORA_ERR_INVALID_ARG;
+  const Tables &t = tables(codebook);
+  for (int i = 0; i < 16; ++i) out[i] = t.cb.v[i];
   return QLORA_OK;
 }
 
-qlora_status qlora_nf4_thresholds(float out[15]) {
-  if (!out) return QLORA_ERR_INVALID_ARG;
-  const float *t = thresholds();
-  for (int i = 0; i < 15; ++i) out[i] = t[i];
+qlora_status qlora_nf4_thresholds(int32_t codebook, float out[15]) {
+  if (!out || (codebook != 0 && codebook != 1)) return QLORA_ERR_INVALID_ARG;
+  const Tables &t = tables(codebook);
+  for (int i = 0; i < 15; ++i) out[i] = t.th[i];
   return QLORA_OK;
 }
 
@@ -264,7 +330,7 @@ qlora_status qlora_quantize_nf4(const void *W, qlora_dtype w_dtype, const qlora_
   return cuda_status(launch_quantize(W, w_dtype == QLORA_BF16, out->block, nblocks, out->group,
                                      out->packed,
                                      out->absmax_code, out->absmax_f32, out->scale2,
-                                     nonfinite_flag, thresholds(),
+                                     nonfinite_flag, tables(out->codebook).th,
                                      static_cast<cudaStream_t>(stream)));
 }
 
@@ -275,7 +341,8 @@ qlora_status qlora_dequant(const qlora_nf4_weight *w, uint16_t *W_out, void *str
   if (!aligned16(W_out)) return QLORA_ERR_ALIGN;
   const int64_t nblocks = w->rows * w->cols / w->block;
   return cuda_status(launch_dequant(w->packed, w->absmax_code, w->absmax_f32, w->scale2, w->group,
-                                    w->block, nblocks, W_out, num_sms_current(),
+                                    w->block, nblocks, W_out, tables(w->codebook).cb,
+                                    num_sms_current(),
                                     static_cast<cudaStream_t>(stream)));
 }
 
@@ -303,6 +370,7 @@ qlora_status qlora_merge_lora(const qlora_nf4_weight *w, const uint16_t *A, cons
   a.r = r;
   a.s = alpha / (float)r;
   a.out = W_out;
+  a.cb = tables(w->codebook).cb;
   return cuda_status(launch_merge(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -384,6 +452,7 @@ qlora_status qlora_linear_fwd(const qlora_nf4_weight *w, const uint16_t *x, int6
     a.y_bf16 = y_dtype == QLORA_BF16;
     a.t = reinterpret_cast<const float *>(wsb + L.t);
     a.status = reinterpret_cast<int *>(wsb + L.status);
+    a.cb = tables(w->codebook).cb;
     return cuda_status(launch_gemv(tmW, a, gplan, A, reinterpret_cast<float *>(wsb + L.part),
                                    reinterpret_cast<int *>(wsb + L.gcnt), t_save, s));
   }

@@ -68,12 +68,18 @@ struct Nf4Table {
   uint32_t hi[4];
 };
 
-__device__ __forceinline__ Nf4Table make_table(float ahat) {
-  constexpr float c[16] = {QLORA_NF4_VALUES};
+// The 16 codepoints a kernel dequantises with, passed by value in its
+// parameters (the printed table, or the quantile-formula table): the
+// products below read them from the constant bank.
+struct Codebook {
+  float v[16];
+};
+
+__device__ __forceinline__ Nf4Table make_table(float ahat, const Codebook &cb) {
   uint32_t P[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j)
-    P[j] = pack_bf16x2(__fmul_rn(c[2 * j], ahat), __fmul_rn(c[2 * j + 1], ahat));
+    P[j] = pack_bf16x2(__fmul_rn(cb.v[2 * j], ahat), __fmul_rn(cb.v[2 * j + 1], ahat));
   Nf4Table t;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {

@@ -128,7 +128,7 @@ __device__ __forceinline__ void dequant_store_row(const GemmArgs &p, const Fetch
     return;
   }
   const float ahat = p.use_code ? __fmul_rn((float)f.code, f.c) : f.c;
-  const Nf4Table t = make_table(ahat);
+  const Nf4Table t = make_table(ahat, p.cb);
   const uint32_t w[8] = {f.lo.x, f.lo.y, f.lo.z, f.lo.w, f.hi.x, f.hi.y, f.hi.z, f.hi.w};
 #pragma unroll
   for (int c = 0; c < 8; ++c) {

@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
       fence_proxy_async_smem();
       issue(u + kGemvDepth, slot);
     }
-    const Nf4Table tg = make_table(ah_g), th = make_table(ah_h);
+    const Nf4Table tg = make_table(ah_g, p.cb), th = make_table(ah_h, p.cb);
     const uint32_t wg[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
     const uint32_t wh[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
     // x slot of (token, block tq, positions 8 wi .. 8 wi + 7)

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "common.cuh"
+
 namespace qlora {
 
 // Fused dequantise + tcgen05 GEMM (gemm_tc.cu).
@@ -45,6 +47,7 @@ struct GemmArgs {
   int sk_slots_clusters;
   int sk;        // 1 when this launch splits tiles (from gemm_plan)
   int clusters;  // CTA pairs launched (from gemm_plan)
+  Codebook cb;   // the 16 codepoints of the weight's table
 };
 // Launch shape of the fused GEMM for one call: pair-tile width, split mode
 // and cluster count.  sk_slots_clusters = 0 means no split-tile area.
@@ -78,6 +81,7 @@ struct GemvArgs {
   int *status;     // device status word
   // set by the launcher from the plan:
   int S, slice_chunks, clusters, tiles_total, tiles_max;
+  Codebook cb;
 };
 // Launch shape of the decode GEMV: S CTAs per cluster (K slices of
 // slice_chunks x 256 columns), clusters owning ranges of 16-row tiles.
@@ -104,7 +108,7 @@ cudaError_t launch_quantize(const void *W, bool bf16_in, int block, int64_t nblo
                             int *nonfinite_flag, const float th[15], cudaStream_t s);
 cudaError_t launch_dequant(const uint8_t *packed, const int8_t *codes, const float *absf,
                            const float *scale2, int group, int block, int64_t nblocks,
-                           uint16_t *out, int num_sms, cudaStream_t s);
+                           uint16_t *out, const Codebook &cb, int num_sms, cudaStream_t s);
 
 // Adapter merge (merge.cu): out = bf16(w_hat + s . B A).
 struct MergeArgs {
@@ -118,6 +122,7 @@ struct MergeArgs {
   int r;
   float s;
   uint16_t *out;  // [N, K] bf16
+  Codebook cb;
 };
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s);
 

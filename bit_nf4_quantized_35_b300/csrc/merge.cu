@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_lora_kernel(const Merg
     af[ks][2] = bw(n0, j0 + 8);
     af[ks][3] = bw(n1, j0 + 8);
   }
-  const Nf4Table t0 = make_table(ah0), t1 = make_table(ah1);
+  const Nf4Table t0 = make_table(ah0, p.cb), t1 = make_table(ah1, p.cb);
   const uint32_t w0[8] = {l0.x, l0.y, l0.z, l0.w, h0.x, h0.y, h0.z, h0.w};
   const uint32_t w1[8] = {l1.x, l1.y, l1.z, l1.w, h1.x, h1.y, h1.z, h1.w};
   // this lane's column of every n-tile: block g >> 1, position 2j + (g & 1)

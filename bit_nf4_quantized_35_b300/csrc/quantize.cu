@@ -241,7 +241,8 @@ __global__ void __launch_bounds__(256) dequant_nf4_kernel(const uint8_t *__restr
                                                           const float *__restrict__ scale2,
                                                           int group, int64_t npieces,
                                                           int piece_shift,
-                                                          uint16_t *__restrict__ out) {
+                                                          uint16_t *__restrict__ out,
+                                                          const Codebook cb) {
   // piece q (16 elements) lies in block q >> piece_shift (block / 16 pieces)
   for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < npieces;
        q += (int64_t)gridDim.x * blockDim.x) {
@@ -252,7 +253,7 @@ __global__ void __launch_bounds__(256) dequant_nf4_kernel(const uint8_t *__restr
       ahat = __fmul_rn((float)codes[b], scale2[b / group]);
     else
       ahat = absf[b];
-    const Nf4Table t = make_table(ahat);
+    const Nf4Table t = make_table(ahat, cb);
     uint32_t o[8];
     lookup8(t, pk.x, o);
     lookup8(t, pk.y, o + 4);
@@ -325,7 +326,7 @@ cudaError_t launch_quantize(const void *W, bool bf16_in, int block, int64_t nblo
 
 cudaError_t launch_dequant(const uint8_t *packed, const int8_t *codes, const float *absf,
                            const float *scale2, int group, int block, int64_t nblocks,
-                           uint16_t *out, int num_sms, cudaStream_t s) {
+                           uint16_t *out, const Codebook &cb, int num_sms, cudaStream_t s) {
   if (nblocks == 0) return cudaSuccess;
   if (block != 64 && block != 128) return cudaErrorInvalidValue;
   const int64_t work = nblocks * (block / 16);
@@ -333,7 +334,7 @@ cudaError_t launch_dequant(const uint8_t *packed, const int8_t *codes, const flo
   const int64_t cap = (int64_t)num_sms * 8 * 4;
   if (grid > cap) grid = cap;
   dequant_nf4_kernel<<<(unsigned)grid, 256, 0, s>>>(packed, codes, absf, scale2, group, work,
-                                                    block == 64 ? 2 : 3, out);
+                                                    block == 64 ? 2 : 3, out, cb);
   return cudaGetLastError();
 }
 

@@ -64,6 +64,17 @@ typedef enum {
 
 typedef enum { QLORA_F32 = 0, QLORA_BF16 = 1 } qlora_dtype;
 
+/* The 16-entry table the indices point into.
+ *   QLORA_CODEBOOK_PRINTED: the NF4 table printed by create_nf4_lookup_table
+ *     ([QLoRA-26] Step 4, [QLoRA-22] Step 4): -1, -0.696, ..., 0, ..., 0.723, 1
+ *     (each the fp32 nearest to the printed decimal; index 7 is zero).
+ *   QLORA_CODEBOOK_QUANTILE: the construction of [QLoRA-26] Step 2,
+ *     q_i = Phi^-1((i - 0.5) / 16), i = 1..16, divided by q_16 so that it
+ *     runs from -1 to 1 (the page does not say how the quantiles are
+ *     normalised; this is the library's reading); symmetric, no zero.  Phi^-1
+ *     is Wichura's AS 241 in binary64, the upper half mirrored. */
+typedef enum { QLORA_CODEBOOK_PRINTED = 0, QLORA_CODEBOOK_QUANTILE = 1 } qlora_codebook;
+
 /* A quantised weight W_hat of logical shape [rows, cols] = [N out, K in].
  *
  * [Gemma-9] 9.2.1 and [QLoRA-22] "engineering notes": the weight is cut into
@@ -85,13 +96,16 @@ typedef enum { QLORA_F32 = 0, QLORA_BF16 = 1 } qlora_dtype;
  * bytes (group > 0); absmax_f32 nblocks floats (group == 0); scale2
  * ceil(nblocks/group) floats (group > 0); nblocks = rows*cols/block.
  * Supported: block in {64, 128} ([QLoRA-22] engineering notes: 64 or 128
- * weights share one scale); group in {0, 32, 64, 128, 256}.
+ * weights share one scale); group in {0, 32, 64, 128, 256}; codebook a
+ * qlora_codebook value (0, the printed table, when the struct is zeroed).
  * All pointers are device pointers owned by the caller; unused ones are NULL. */
 typedef struct {
   int64_t rows;
   int64_t cols;
   int32_t block;
   int32_t group;
+  int32_t codebook;  /* qlora_codebook */
+  int32_t reserved;  /* 0 */
   uint8_t *packed;
   int8_t *absmax_code;
   float *absmax_f32;
@@ -112,7 +126,9 @@ qlora_status qlora_nf4_sizes(int64_t rows, int64_t cols, int32_t block, int32_t 
  * Per block: a = max |w| over finite elements; each element's normalised
  * value w / a (IEEE fp32 division) is replaced by the index of the nearest
  * NF4 codepoint (fp32 distances, the lower index on an exact tie); a block
- * with a == 0 stores index 7 (the exact-zero codepoint) everywhere.  Then the
+ * with a == 0 stores index 7 everywhere (the exact-zero codepoint of the
+ * printed table; with the quantile table any index dequantises to 0 there).
+ * The table is out->codebook.  Then the
  * double quantisation above.  `out` (host struct) describes caller-allocated
  * device buffers of the sizes from qlora_nf4_sizes.
  * nonfinite_flag: NULL, or a device int32 that the kernel sets to 1 when it
@@ -255,14 +271,15 @@ qlora_status qlora_linear_bwd_noalloc(const qlora_nf4_weight *w, const uint16_t 
                                       const float *t_saved, void *dX, qlora_dtype dx_dtype,
                                       float *dA, float *dB, uint32_t flags, void *stream);
 
-/* The 15 fp32 decision thresholds the quantiser uses: element index =
- * number of thresholds <= (w / absmax).  Derived on the host from the NF4
- * table and the nearest-codepoint rule above.  Host only, no GPU needed. */
-qlora_status qlora_nf4_thresholds(float out[15]);
+/* The 15 fp32 decision thresholds the quantiser uses with table `codebook`:
+ * element index = number of thresholds <= (w / absmax).  Derived on the host
+ * from the table and the nearest-codepoint rule above.  Host only, no GPU
+ * needed.  QLORA_ERR_INVALID_ARG for an unknown codebook. */
+qlora_status qlora_nf4_thresholds(int32_t codebook, float out[15]);
 
-/* The 16 NF4 codepoints as fp32 ([QLoRA-26] Step 4 create_nf4_lookup_table).
- * Host only. */
-qlora_status qlora_nf4_codebook(float out[16]);
+/* The 16 codepoints of table `codebook` as fp32 (see qlora_codebook).  Host
+ * only.  QLORA_ERR_INVALID_ARG for an unknown codebook. */
+qlora_status qlora_nf4_codebook(int32_t codebook, float out[16]);
 
 const char *qlora_status_string(qlora_status s);
 

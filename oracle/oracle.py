@@ -63,9 +63,15 @@ def _declare(lib):
     lib.oracle_nearest_codes_scaled_bits.restype = None
     lib.oracle_bf16_rne_array.argtypes = [P, i64, P]
     lib.oracle_bf16_rne_array.restype = None
-    lib.oracle_quantize_nf4.argtypes = [P, i64, i64, i32, i32, P, P, P, P, P]
+    lib.oracle_quantize_nf4.argtypes = [P, i64, i64, i32, i32, P, P, P, P, P, i32]
     lib.oracle_quantize_nf4.restype = i64
-    lib.oracle_dequant_bf16.argtypes = [P, P, P, P, i64, i64, i32, i32, P]
+    lib.oracle_dequant_bf16.argtypes = [P, P, P, P, i64, i64, i32, i32, P, i32]
+    lib.oracle_codebook_values.argtypes = [i32, P]
+    lib.oracle_codebook_values.restype = None
+    lib.oracle_inv_normal.argtypes = [f64]
+    lib.oracle_inv_normal.restype = f64
+    lib.oracle_nearest_code_cb.argtypes = [i32, ctypes.c_float]
+    lib.oracle_nearest_code_cb.restype = ctypes.c_int
     lib.oracle_dequant_bf16.restype = ctypes.c_int
     lib.oracle_linear_fwd.argtypes = [P, i64, i64, P, i64, P, P, i32, f64, P, i64, P, P]
     lib.oracle_linear_fwd.restype = None
@@ -119,11 +125,24 @@ def set_num_threads(n: int) -> None:
     _load().oracle_set_num_threads(int(n))
 
 
-def codebook() -> np.ndarray:
-    """The 16 NF4 codepoints as binary32 (oracle_nf4_codebook)."""
+def codebook(which: int = 0) -> np.ndarray:
+    """The 16 codepoints as binary32: 0 the printed NF4 table
+    (oracle_nf4_codebook), 1 the quantile-formula table."""
     out = np.zeros(16, dtype=np.float32)
-    _load().oracle_nf4_codebook(_ptr(out))
+    if which == 0:
+        _load().oracle_nf4_codebook(_ptr(out))
+    else:
+        _load().oracle_codebook_values(which, _ptr(out))
     return out
+
+
+def inv_normal(p: float) -> float:
+    """Phi^-1(p) by bisection on the normal CDF (binary64)."""
+    return float(_load().oracle_inv_normal(float(p)))
+
+
+def nearest_code_cb(which: int, xn: float) -> int:
+    return int(_load().oracle_nearest_code_cb(which, ctypes.c_float(float(xn))))
 
 
 def nearest_code(xn: float) -> int:
@@ -164,8 +183,9 @@ class NF4Weight:
     """Quantised weight as the oracle stores it (numpy arrays)."""
 
     def __init__(self, rows, cols, block, group, packed, absmax_code, absmax_f32, scale2,
-                 idx, nonfinite):
+                 idx, nonfinite, codebook=0):
         self.rows, self.cols, self.block, self.group = rows, cols, block, group
+        self.codebook = codebook
         self.packed, self.absmax_code, self.absmax_f32, self.scale2 = (
             packed, absmax_code, absmax_f32, scale2)
         self.idx = idx
@@ -176,10 +196,12 @@ class NF4Weight:
         return self.rows * self.cols // self.block
 
 
-def quantize_nf4(w, block: int = 64, group: int = 256, want_idx: bool = True) -> NF4Weight:
+def quantize_nf4(w, block: int = 64, group: int = 256, want_idx: bool = True,
+                 codebook: int = 0) -> NF4Weight:
     """Blockwise NF4 quantisation (+ double quantisation when group > 0).
 
-    ``w`` is a 2-D array of binary32 values (bf16 inputs widened exactly)."""
+    ``w`` is a 2-D array of binary32 values (bf16 inputs widened exactly);
+    ``codebook`` 0 is the printed table, 1 the quantile-formula table."""
     w = _f32(w)
     if w.ndim != 2:
         raise ValueError("w must be 2-D [rows, cols]")
@@ -197,11 +219,12 @@ def quantize_nf4(w, block: int = 64, group: int = 256, want_idx: bool = True) ->
     nz = lambda a: _ptr(a) if a.size else ctypes.c_void_p(0)
     nonfinite = _load().oracle_quantize_nf4(
         _ptr(w), rows, cols, block, group, _ptr(packed), nz(codes), nz(absf), nz(s2),
-        _ptr(idx) if idx is not None else ctypes.c_void_p(0))
+        _ptr(idx) if idx is not None else ctypes.c_void_p(0), codebook)
     if nonfinite < 0:
         raise ValueError("oracle_quantize_nf4 rejected its arguments")
     return NF4Weight(rows, cols, block, group, packed, codes, absf, s2,
-                     idx.reshape(rows, cols) if idx is not None else None, int(nonfinite))
+                     idx.reshape(rows, cols) if idx is not None else None, int(nonfinite),
+                     codebook)
 
 
 def dequant_bf16(q: NF4Weight) -> np.ndarray:
@@ -209,7 +232,8 @@ def dequant_bf16(q: NF4Weight) -> np.ndarray:
     out = np.empty(q.rows * q.cols, dtype=np.uint16)
     nz = lambda a: _ptr(a) if a.size else ctypes.c_void_p(0)
     rc = _load().oracle_dequant_bf16(_ptr(q.packed), nz(q.absmax_code), nz(q.absmax_f32),
-                                     nz(q.scale2), q.rows, q.cols, q.block, q.group, _ptr(out))
+                                     nz(q.scale2), q.rows, q.cols, q.block, q.group, _ptr(out),
+                                     q.codebook)
     if rc != 0:
         raise ValueError("oracle_dequant_bf16 rejected its arguments")
     return out.reshape(q.rows, q.cols)

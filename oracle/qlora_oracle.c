@@ -51,6 +51,60 @@ static const float ORACLE_NF4[16] = {
 
 #define ORACLE_ZERO_INDEX 7
 
+/* Quantile-formula codebook.  [QLoRA-26] Step 2 gives the construction
+ *   q_i = Phi^-1(p_i),  p_i = (i - 0.5) / 16,  i = 1 .. 16
+ * (garbled on the page as "pi=i−0.516"), Phi the standard normal CDF.  The
+ * page does not say how the quantiles are brought to [-1, 1], where the
+ * normalised weights live; reading: divided by the largest, q_16, so that
+ * the table runs from -1 to 1 like the printed one.  The quantiles are
+ * symmetric (Phi^-1(1 - p) = -Phi^-1(p)); the upper half is computed and
+ * mirrored, so the binary32 table is exactly symmetric, with no zero.
+ * Phi^-1 here: bisection on Phi(x) = erfc(-x / sqrt 2) / 2 in binary64 until
+ * the bracket stops shrinking (erfc from the C library). */
+static double oracle_phi(double x) { return 0.5 * erfc(-x / sqrt(2.0)); }
+
+double oracle_inv_normal(double p) {
+  if (!(p > 0.0 && p < 1.0)) return NAN;
+  double lo = -40.0, hi = 40.0;
+  for (int it = 0; it < 2000; ++it) {
+    const double mid = 0.5 * (lo + hi);
+    if (mid <= lo || mid >= hi) break;
+    if (oracle_phi(mid) < p)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return 0.5 * (lo + hi);
+}
+
+static float ORACLE_NF4_QUANTILE[16];
+static int oracle_quantile_ready = 0;
+
+static void oracle_make_quantile_table(void) {
+  if (oracle_quantile_ready) return;
+  const double q16 = oracle_inv_normal(15.5 / 16.0);
+  for (int i = 9; i <= 16; ++i) {
+    const float c = (float)(oracle_inv_normal((i - 0.5) / 16.0) / q16);
+    ORACLE_NF4_QUANTILE[i - 1] = c;
+    ORACLE_NF4_QUANTILE[16 - i] = -c;
+  }
+  oracle_quantile_ready = 1;
+}
+
+/* Codebook 0: the printed table; 1: the quantile formula. */
+static const float *oracle_table(int32_t codebook) {
+  if (codebook == 1) {
+    oracle_make_quantile_table();
+    return ORACLE_NF4_QUANTILE;
+  }
+  return ORACLE_NF4;
+}
+
+void oracle_codebook_values(int32_t codebook, float out[16]) {
+  const float *t = oracle_table(codebook);
+  for (int k = 0; k < 16; ++k) out[k] = t[k];
+}
+
 void oracle_nf4_codebook(float out[16]) {
   for (int k = 0; k < 16; ++k) out[k] = ORACLE_NF4[k];
 }
@@ -59,17 +113,23 @@ void oracle_nf4_codebook(float out[16]) {
  * the closest entry of the table (0.20 -> 0.161).  Distances are binary32
  * |xn - c_k|; on an exact tie of the binary32 distances the lower index wins
  * (the pages are silent on ties). */
-int oracle_nearest_code(float xn) {
+static int oracle_nearest_in(const float *table, float xn) {
   int best = 0;
-  float bestd = fabsf(xn - ORACLE_NF4[0]);
+  float bestd = fabsf(xn - table[0]);
   for (int k = 1; k < 16; ++k) {
-    float d = fabsf(xn - ORACLE_NF4[k]);
+    float d = fabsf(xn - table[k]);
     if (d < bestd) {
       bestd = d;
       best = k;
     }
   }
   return best;
+}
+
+int oracle_nearest_code(float xn) { return oracle_nearest_in(ORACLE_NF4, xn); }
+
+int oracle_nearest_code_cb(int32_t codebook, float xn) {
+  return oracle_nearest_in(oracle_table(codebook), xn);
 }
 
 /* Indices for `count` consecutive binary32 bit patterns starting at
@@ -143,7 +203,10 @@ void oracle_bf16_rne_array(const float *in, int64_t n, uint16_t *out) {
  *    a_b = max_i |w_i|                       (exact)
  *    xn_i = w_i / a_b                        (binary32 IEEE division)
  *    idx_i = nearest codepoint of xn_i       (oracle_nearest_code)
- *    a_b == 0  ->  idx_i = 7 (the zero codepoint), no division.
+ *    a_b == 0  ->  idx_i = 7 (the zero codepoint of the printed table), no
+ *                  division; with the quantile table (no zero) any index
+ *                  dequantises to 0 there, and 7 is kept as the convention.
+ *  `codebook` selects the table: 0 printed, 1 quantile formula.
  *  Steps per group g (group > 0):
  *    gmax = max_b a_b; s2 = gmax / 127 (binary32); code_b = clamp(rint(a_b/s2))
  *    gmax == 0 -> s2 = 0 and every code 0.
@@ -153,8 +216,11 @@ void oracle_bf16_rne_array(const float *in, int64_t n, uint16_t *out) {
  */
 int64_t oracle_quantize_nf4(const float *w, int64_t rows, int64_t cols, int32_t block,
                             int32_t group, uint8_t *packed, int8_t *absmax_code,
-                            float *absmax_f32, float *scale2, uint8_t *idx_out) {
+                            float *absmax_f32, float *scale2, uint8_t *idx_out,
+                            int32_t codebook) {
   if (rows < 0 || cols < 0 || block <= 0 || (block & 1) || group < 0) return -1;
+  if (codebook != 0 && codebook != 1) return -1;
+  const float *table = oracle_table(codebook);
   if (cols % block) return -1;
   const int64_t n = rows * cols;
   const int64_t nblocks = n / block;
@@ -183,8 +249,8 @@ int64_t oracle_quantize_nf4(const float *w, int64_t rows, int64_t cols, int32_t 
       } else {
         float xn0 = wb[i] / amax;
         float xn1 = wb[i + 1] / amax;
-        q0 = oracle_nearest_code(xn0);
-        q1 = oracle_nearest_code(xn1);
+        q0 = oracle_nearest_in(table, xn0);
+        q1 = oracle_nearest_in(table, xn1);
       }
       int64_t e = b * block + i;
       if (idx_out) {
@@ -232,8 +298,11 @@ int64_t oracle_quantize_nf4(const float *w, int64_t rows, int64_t cols, int32_t 
  */
 int oracle_dequant_bf16(const uint8_t *packed, const int8_t *absmax_code,
                         const float *absmax_f32, const float *scale2, int64_t rows,
-                        int64_t cols, int32_t block, int32_t group, uint16_t *w_out) {
+                        int64_t cols, int32_t block, int32_t group, uint16_t *w_out,
+                        int32_t codebook) {
   if (rows < 0 || cols < 0 || block <= 0 || (block & 1) || group < 0) return ORACLE_EINVAL;
+  if (codebook != 0 && codebook != 1) return ORACLE_EINVAL;
+  const float *table = oracle_table(codebook);
   if (cols % block) return ORACLE_EINVAL;
   const int64_t n = rows * cols;
   const int64_t nblocks = n / block;
@@ -248,7 +317,7 @@ int oracle_dequant_bf16(const uint8_t *packed, const int8_t *absmax_code,
       int64_t e = b * block + i;
       uint8_t byte = packed[e / 2];
       int q = (e & 1) ? (byte & 0x0f) : (byte >> 4);
-      float prod = ORACLE_NF4[q] * ahat;
+      float prod = table[q] * ahat;
       w_out[e] = oracle_bf16_rne(prod);
     }
   }

@@ -110,3 +110,34 @@ def test_workspace_size_monotone(lib):
     a = capi.workspace_size(16, 4096, 4096, 16)
     b = capi.workspace_size(8192, 4096, 4096, 16)
     assert 0 < a < b
+
+
+def test_quantile_codebook_matches_oracle(lib):
+    """The library's quantile-formula table (Wichura AS 241 on the host)
+    equals the oracle's (bisection on the normal CDF) bit for bit."""
+    cb = np.array(capi.nf4_codebook(capi.QLORA_CODEBOOK_QUANTILE), dtype=np.float32)
+    assert cb.tobytes() == oracle.codebook(1).tobytes()
+
+
+def test_quantile_thresholds_reproduce_oracle_rule(lib):
+    th = np.array(capi.nf4_thresholds(capi.QLORA_CODEBOOK_QUANTILE), dtype=np.float32)
+    cb = oracle.codebook(1)
+    assert np.all(np.diff(th) > 0)
+    for k in range(15):
+        assert cb[k] < th[k] <= cb[k + 1]
+        start = _bits(float(th[k])) - 512 if th[k] > 0 else _bits(float(th[k])) - 512
+        bits = np.arange(start, start + 1025, dtype=np.int64).astype(np.uint32)
+        xs = bits.view(np.float32)
+        xs = xs[np.isfinite(xs) & (np.abs(xs) <= 1)]
+        ours = np.searchsorted(th, xs, side="right")
+        ref = np.array([oracle.nearest_code_cb(1, float(x)) for x in xs])
+        assert np.array_equal(ours, ref), k
+    rng = np.random.default_rng(8)
+    xs = rng.uniform(-1, 1, 20000).astype(np.float32)
+    ref = np.array([oracle.nearest_code_cb(1, float(x)) for x in xs])
+    assert np.array_equal(np.searchsorted(th, xs, side="right"), ref)
+
+
+def test_unknown_codebook_is_rejected(lib):
+    with pytest.raises(capi.QloraError):
+        capi.nf4_codebook(2)

@@ -21,17 +21,17 @@ from .helpers import bf16_bits
 pytestmark = pytest.mark.gpu
 
 
-def _check_merge(shape, block=64, group=256, zero_B=False):
+def _check_merge(shape, block=64, group=256, zero_B=False, codebook=0):
     d = inputs.linear_inputs(shape, with_dy=False, seed_offset=7)
     if zero_B:
         d["B"] = torch.zeros_like(d["B"])
     g = {k: v.cuda().contiguous() for k, v in d.items()}
-    q = capi.quantize_nf4(g["W"], group=group, block=block)
+    q = capi.quantize_nf4(g["W"], group=group, block=block, codebook=codebook)
     before = [t.clone() for t in (q.packed,) + tuple(x for x in (q.absmax_code, q.scale2,
                                                                     q.absmax_f32) if x is not None)]
     got = capi.merge_lora(q, g["A"], g["B"], shape.alpha)
     torch.cuda.synchronize()
-    ref_q = oracle.quantize_nf4(d["W"].float().numpy(), block, group)
+    ref_q = oracle.quantize_nf4(d["W"].float().numpy(), block, group, codebook=codebook)
     w_hat = oracle.dequant_f32(ref_q)
     ref_bits, exact = oracle.merge_bf16(w_hat, d["A"].float().numpy(), d["B"].float().numpy(),
                                         shape.alpha)
@@ -65,9 +65,10 @@ def test_merge_small(shape):
     _check_merge(shape)
 
 
-@pytest.mark.parametrize("fmt", [(64, 0), (128, 256), (128, 0)], ids=lambda f: f"b{f[0]}g{f[1]}")
+@pytest.mark.parametrize("fmt", [(64, 0, 0), (128, 256, 0), (128, 0, 0), (64, 256, 1)],
+                         ids=lambda f: f"b{f[0]}g{f[1]}cb{f[2]}")
 def test_merge_storage_formats(fmt):
-    _check_merge(SHAPES[0], block=fmt[0], group=fmt[1])
+    _check_merge(SHAPES[0], block=fmt[0], group=fmt[1], codebook=fmt[2])
 
 
 def test_merge_zero_B_is_the_dequantised_weight():

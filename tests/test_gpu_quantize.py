@@ -19,14 +19,14 @@ def _lib():
     capi.load()
 
 
-def _check_quant(W_cpu: torch.Tensor, group: int, block: int = 64):
+def _check_quant(W_cpu: torch.Tensor, group: int, block: int = 64, codebook: int = 0):
     """Quantise on the GPU and with the oracle; compare every output bit."""
     W = W_cpu.cuda().contiguous()
     flag = torch.zeros(1, dtype=torch.int32, device="cuda")
-    q = capi.quantize_nf4(W, group=group, nonfinite_flag=flag, block=block)
+    q = capi.quantize_nf4(W, group=group, nonfinite_flag=flag, block=block, codebook=codebook)
     deq = capi.dequant(q)
     torch.cuda.synchronize()
-    ref = oracle.quantize_nf4(W_cpu.float().numpy(), block, group)
+    ref = oracle.quantize_nf4(W_cpu.float().numpy(), block, group, codebook=codebook)
     assert np.array_equal(q.packed.cpu().numpy(), ref.packed), "packed bytes differ"
     if group > 0:
         assert np.array_equal(q.absmax_code.cpu().numpy(), ref.absmax_code), "codes differ"
@@ -60,6 +60,20 @@ def test_block128_groups_and_ragged_tail(group, dtype):
     W = inputs.normal((37, 384), inputs.STD_W, 12, dtype)
     W[5, 128:256] = 0.0  # an all-zero block
     _check_quant(W, group, block=128)
+
+
+@pytest.mark.parametrize("fmt", [(64, 256), (64, 0), (128, 256)], ids=lambda f: f"b{f[0]}g{f[1]}")
+def test_quantile_codebook_ragged(fmt):
+    """The quantile-formula table (symmetric, no zero): 37 x 384 weights with
+    an all-zero block and exact zeros inside blocks, every output bit."""
+    W = inputs.normal((37, 384), inputs.STD_W, 13, torch.bfloat16)
+    W[3, 128:256] = 0.0
+    W[4, 5] = 0.0
+    _check_quant(W, fmt[1], block=fmt[0], codebook=1)
+
+
+def test_quantile_codebook_bulk_matrix_full_size():
+    _check_quant(inputs.bulk_matrix(2), 256, codebook=1)
 
 
 def test_block128_bulk_matrix_full_size():

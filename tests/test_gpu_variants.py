@@ -2,8 +2,9 @@
 input ranges beyond N(0, 1), against the fp64 oracle.
 
 - Blocks of 64 and of 128 weights, block constants kept in fp32 (no double
-  quantisation, group 0) or double-quantised in groups of 64 or 256, on both
-  forward kernels (tensor-core GEMM and decode GEMV) and on the backward.
+  quantisation, group 0) or double-quantised in groups of 64 or 256, and the
+  quantile-formula codebook, on both forward kernels (tensor-core GEMM and
+  decode GEMV) and on the backward.
 - The decode GEMV at K = 14336 with heavy-tailed activations (N(0, 4) with
   +-30 outliers) and a LoRA factor A holding entries beyond the f16 range
   (|a| > 65504): the GEMV must compute with the exact bf16 W_hat and accept
@@ -23,29 +24,31 @@ pytestmark = pytest.mark.gpu
 FORCE_GEMV, FORCE_GEMM = capi.QLORA_FLAG_FORCE_GEMV, capi.QLORA_FLAG_FORCE_GEMM
 
 
-def _quantized(d, group, block=64):
+def _quantized(d, group, block=64, codebook=0):
     g = {k: v.cuda().contiguous() for k, v in d.items()}
-    q = capi.quantize_nf4(g["W"], group=group, block=block)
-    ref_q = oracle.quantize_nf4(d["W"].float().numpy(), block, group)
+    q = capi.quantize_nf4(g["W"], group=group, block=block, codebook=codebook)
+    ref_q = oracle.quantize_nf4(d["W"].float().numpy(), block, group, codebook=codebook)
     torch.cuda.synchronize()
     assert np.array_equal(q.packed.cpu().numpy(), ref_q.packed)
     return g, q, oracle.dequant_f32(ref_q)
 
 
-FMT = [(64, 0), (64, 64), (64, 256), (128, 0), (128, 64), (128, 256)]
+# (block, group, codebook): codebook 1 is the quantile-formula table
+FMT = [(64, 0, 0), (64, 64, 0), (64, 256, 0), (128, 0, 0), (128, 64, 0), (128, 256, 0),
+       (64, 256, 1), (128, 0, 1)]
 FWD_SHAPES = [
     inputs.LinearShape("N1032_K1024_M300_r16", N=1032, K=1024, M=300, r=16, alpha=32.0),
     inputs.LinearShape("N520_K4224_M5_r16", N=520, K=4224, M=5, r=16, alpha=32.0),
 ]
 
 
-@pytest.mark.parametrize("fmt", FMT, ids=lambda f: f"block{f[0]}_group{f[1]}")
+@pytest.mark.parametrize("fmt", FMT, ids=lambda f: f"block{f[0]}_group{f[1]}_cb{f[2]}")
 @pytest.mark.parametrize("path", ["gemm", "gemv"])
 def test_forward_storage_formats(fmt, path):
-    block, group = fmt
+    block, group, cb = fmt
     shape = FWD_SHAPES[0] if path == "gemm" else FWD_SHAPES[1]
     d = inputs.linear_inputs(shape, with_dy=False, seed_offset=group + block)
-    g, q, w_hat = _quantized(d, group, block)
+    g, q, w_hat = _quantized(d, group, block, cb)
     ws = capi.Workspace(shape.M, shape.N, shape.K, shape.r)
     t = torch.empty(shape.M, shape.r, dtype=torch.float32, device="cuda")
     y = capi.linear_fwd(q, g["x"], g["A"], g["B"], shape.alpha, ws, t_save=t,
@@ -58,12 +61,12 @@ def test_forward_storage_formats(fmt, path):
     assert_close(to_np_f32(t), t_ref, f"t {shape.name} {path}", max_abs=1e-3, rel_fro=1e-5)
 
 
-@pytest.mark.parametrize("fmt", FMT, ids=lambda f: f"block{f[0]}_group{f[1]}")
+@pytest.mark.parametrize("fmt", FMT, ids=lambda f: f"block{f[0]}_group{f[1]}_cb{f[2]}")
 def test_backward_storage_formats(fmt):
-    block, group = fmt
+    block, group, cb = fmt
     shape = inputs.LinearShape("N776_K1152_M260_r16", N=776, K=1152, M=260, r=16, alpha=32.0)
     d = inputs.linear_inputs(shape, seed_offset=group + block + 1)
-    g, q, w_hat = _quantized(d, group, block)
+    g, q, w_hat = _quantized(d, group, block, cb)
     ws = capi.Workspace(shape.M, shape.N, shape.K, shape.r)
     dX, dA, dB = capi.linear_bwd(q, g["x"], g["dY"], g["A"], g["B"], shape.alpha, ws)
     torch.cuda.synchronize()

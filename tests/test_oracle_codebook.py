@@ -165,3 +165,61 @@ def test_scaled_sweep_matches_block_quantisation():
     bits = 0x3E000000
     assert np.array_equal(orc.nearest_codes_scaled_bits(bits, 4096, 1.0),
                           orc.nearest_codes_bits(bits, 4096))
+
+
+# --------------------------------------------- quantile-formula codebook
+# "QLoRA and 4bit Quantization | QLoRA 与 4-bit 量化", Step 2:
+# q_i = Phi^-1((i - 0.5) / 16), i = 1..16, brought to [-1, 1] by q_16.
+
+def test_inverse_normal_textbook_points():
+    """Phi^-1 at points whose values are textbook: 0.5 -> 0, Phi(1) -> 1,
+    Phi(2) -> 2, 0.975 -> 1.959963984540054; and scipy's ndtri (an
+    independent implementation) at every p_i of the formula."""
+    from scipy.special import ndtri
+    assert abs(orc.inv_normal(0.5)) < 1e-12
+    assert abs(orc.inv_normal(0.8413447460685429) - 1.0) < 1e-12
+    assert abs(orc.inv_normal(0.9772498680518208) - 2.0) < 1e-12
+    assert abs(orc.inv_normal(0.975) - 1.959963984540054) < 1e-12
+    for i in range(1, 17):
+        p = (i - 0.5) / 16
+        assert abs(orc.inv_normal(p) - float(ndtri(p))) < 1e-12
+
+
+def test_quantile_codebook_values_and_shape():
+    """The table equals binary32(ndtri(p_i) / ndtri(p_16)) entry by entry, is
+    exactly symmetric, strictly increasing, runs from -1 to 1 and has no zero
+    (the nearest entries to zero are +-0.0421)."""
+    from scipy.special import ndtri
+    cb = orc.codebook(1)
+    q16 = float(ndtri(15.5 / 16))
+    expect = np.array([np.float32(float(ndtri((i - 0.5) / 16)) / q16) for i in range(1, 17)],
+                      dtype=np.float32)
+    assert np.array_equal(cb, expect)
+    assert np.array_equal(cb, -cb[::-1])
+    assert np.all(np.diff(cb) > 0) and cb[0] == -1.0 and cb[15] == 1.0
+    assert not np.any(cb == 0.0)
+    assert abs(cb[8] - 0.0421) < 5e-5
+
+
+def test_quantile_codebook_quantisation_is_brute_force_nearest():
+    rng = np.random.default_rng(5)
+    w = (rng.standard_normal((3, 128)) * 0.02).astype(np.float32)
+    w[2, :64] = 0.0
+    q = orc.quantize_nf4(w, 64, 0, codebook=1)
+    cb = [Fraction(float(c)) for c in orc.codebook(1)]
+    blocks, idx = w.reshape(-1, 64), q.idx.reshape(-1, 64)
+    for b in range(blocks.shape[0]):
+        a = Fraction(float(np.abs(blocks[b]).max()))
+        for i in range(64):
+            if a == 0:
+                assert idx[b, i] == 7
+                continue
+            xn = Fraction(float(blocks[b, i])) / a
+            d = [abs(xn - c) for c in cb]
+            ok = {k for k, dk in enumerate(d) if dk - min(d) <= Fraction(2) ** -22}
+            assert idx[b, i] in ok
+    # the dequantised weight is the quantile codepoint times the constant
+    deq = orc.dequant_f32(q)
+    expect = orc.bf16_bits_to_f32(orc.bf16_rne(orc.codebook(1)[q.idx.ravel()] *
+                                               np.repeat(q.absmax_f32, 64)))
+    assert np.array_equal(deq.ravel(), expect)
