@@ -73,10 +73,14 @@ def _declare(lib):
     lib.oracle_nearest_code_cb.argtypes = [i32, ctypes.c_float]
     lib.oracle_nearest_code_cb.restype = ctypes.c_int
     lib.oracle_dequant_bf16.restype = ctypes.c_int
-    lib.oracle_linear_fwd.argtypes = [P, i64, i64, P, i64, P, P, i32, f64, P, i64, P, P]
+    lib.oracle_linear_fwd.argtypes = [P, i64, i64, P, i64, P, P, i32, f64, P, i64, P, P, P, f64]
     lib.oracle_linear_fwd.restype = None
     lib.oracle_linear_bwd.argtypes = [P, P, i64, i64, i64, P, P, P, i32, f64, P, i64,
-                                      P, P, P, P, P]
+                                      P, P, P, P, P, P, f64]
+    lib.oracle_philox_stream.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
+    lib.oracle_philox_stream.restype = ctypes.c_uint64
+    lib.oracle_dropout_keep.argtypes = [ctypes.c_uint64, f64, i64, i64, P]
+    lib.oracle_dropout_keep.restype = None
     lib.oracle_linear_bwd.restype = None
     lib.oracle_bf16_rne_double.argtypes = [f64]
     lib.oracle_bf16_rne_double.restype = ctypes.c_uint16
@@ -243,8 +247,28 @@ def dequant_f32(q: NF4Weight) -> np.ndarray:
     return bf16_bits_to_f32(dequant_bf16(q)).reshape(q.rows, q.cols)
 
 
-def linear_fwd(x, w, A, B, alpha: float, rows=None):
-    """fp64 forward y = x W^T + (x A^T) B^T alpha/r on the listed rows.
+def philox_stream(seed: int, o: int) -> int:
+    """The o-th 64-bit output of the Philox4x64-10 stream keyed by seed."""
+    return int(_load().oracle_philox_stream(seed, o))
+
+
+def dropout_keep(seed: int, p: float, M: int, K: int) -> np.ndarray:
+    """LoRA dropout keep mask [M, K] (uint8 0/1) for probability p."""
+    keep = np.empty((M, K), dtype=np.uint8)
+    _load().oracle_dropout_keep(seed, float(p), M, K, _ptr(keep))
+    return keep
+
+
+def _keep_args(keep, p):
+    if keep is None:
+        return ctypes.c_void_p(0), 1.0, None
+    k = np.ascontiguousarray(keep, dtype=np.uint8)
+    return _ptr(k), 1.0 / (1.0 - float(p)), k
+
+
+def linear_fwd(x, w, A, B, alpha: float, rows=None, keep=None, p: float = 0.0):
+    """fp64 forward y = x W^T + (x A^T) B^T alpha/r on the listed rows; with
+    `keep` ([M, K] 0/1) the LoRA branch takes dropout(x) = x keep / (1 - p).
 
     Returns (y [nrows, N] float64, t [nrows, r] float64)."""
     x, w, A, B = _f32(x), _f32(w), _f32(A), _f32(B)
@@ -255,12 +279,13 @@ def linear_fwd(x, w, A, B, alpha: float, rows=None):
     rows = np.arange(M, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, np.int64)
     y = np.zeros((rows.size, N), dtype=np.float64)
     t = np.zeros((rows.size, r), dtype=np.float64)
+    kp, ks, _hold = _keep_args(keep, p)
     _load().oracle_linear_fwd(_ptr(x), M, K, _ptr(w), N, _ptr(A), _ptr(B), r, float(alpha),
-                              _ptr(rows), rows.size, _ptr(y), _ptr(t))
+                              _ptr(rows), rows.size, _ptr(y), _ptr(t), kp, ks)
     return y, t
 
 
-def linear_bwd(x, dY, w, A, B, alpha: float, rows=None):
+def linear_bwd(x, dY, w, A, B, alpha: float, rows=None, keep=None, p: float = 0.0):
     """fp64 backward.  Returns dict with dX [nrows, K], dA [r, K], dB [N, r],
     t [M, r], u [M, r] (all float64)."""
     x, dY, w, A, B = _f32(x), _f32(dY), _f32(w), _f32(A), _f32(B)
@@ -274,9 +299,10 @@ def linear_bwd(x, dY, w, A, B, alpha: float, rows=None):
     dB = np.zeros((N, r), dtype=np.float64)
     t = np.zeros((M, r), dtype=np.float64)
     u = np.zeros((M, r), dtype=np.float64)
+    kp, ks, _hold = _keep_args(keep, p)
     _load().oracle_linear_bwd(_ptr(x), _ptr(dY), M, K, N, _ptr(w), _ptr(A), _ptr(B), r,
                               float(alpha), _ptr(rows), rows.size, _ptr(dX), _ptr(dA),
-                              _ptr(dB), _ptr(t), _ptr(u))
+                              _ptr(dB), _ptr(t), _ptr(u), kp, ks)
     return {"dX": dX, "dA": dA, "dB": dB, "t": t, "u": u}
 
 

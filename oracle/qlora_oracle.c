@@ -325,6 +325,66 @@ int oracle_dequant_bf16(const uint8_t *packed, const int8_t *absmax_code,
 }
 
 /* ------------------------------------------------------------------------ */
+/* LoRA dropout on the bypass input.  [QLoRA-26] Step 5 training config and
+ * [Gemma-9] LoraConfig set lora_dropout = p: during training the LoRA
+ * branch sees dropout(x) = x . keep / (1 - p) with keep ~ Bernoulli(1 - p)
+ * per element, the base branch sees x.  The pages give no generator; the
+ * reading taken: the counter-based Philox4x64-10 generator (Salmon et al.,
+ * "Parallel random numbers: as easy as 1, 2, 3", SC 2011) keyed by the
+ * 64-bit seed (key = {seed, 0}), its 64-bit outputs in counter order
+ * starting at counter 1 (output o: counter o / 4 + 1, word o % 4), two
+ * 32-bit uniforms per output (element e of the row-major [M, K] input takes
+ * output e / 2, low half for even e, high half for odd e), and
+ * keep = (u >= round(p 2^32)). */
+static void oracle_philox4x64_10(const uint64_t ctr_in[4], const uint64_t key_in[2],
+                                 uint64_t out[4]) {
+  const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+  const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+  uint64_t c[4] = {ctr_in[0], ctr_in[1], ctr_in[2], ctr_in[3]};
+  uint64_t k[2] = {key_in[0], key_in[1]};
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) {
+      k[0] += W0;
+      k[1] += W1;
+    }
+    const unsigned __int128 p0 = (unsigned __int128)M0 * c[0];
+    const unsigned __int128 p1 = (unsigned __int128)M1 * c[2];
+    const uint64_t hi0 = (uint64_t)(p0 >> 64), lo0 = (uint64_t)p0;
+    const uint64_t hi1 = (uint64_t)(p1 >> 64), lo1 = (uint64_t)p1;
+    const uint64_t n0 = hi1 ^ c[1] ^ k[0], n2 = hi0 ^ c[3] ^ k[1];
+    c[0] = n0;
+    c[1] = lo1;
+    c[2] = n2;
+    c[3] = lo0;
+  }
+  for (int i = 0; i < 4; ++i) out[i] = c[i];
+}
+
+/* The o-th 64-bit output of the stream keyed by `seed`. */
+uint64_t oracle_philox_stream(uint64_t seed, uint64_t o) {
+  const uint64_t ctr[4] = {o / 4 + 1, 0, 0, 0};
+  const uint64_t key[2] = {seed, 0};
+  uint64_t out[4];
+  oracle_philox4x64_10(ctr, key, out);
+  return out[o % 4];
+}
+
+/* keep[m * K + k] (0 or 1) of an [M, K] input for dropout probability p. */
+void oracle_dropout_keep(uint64_t seed, double p, int64_t M, int64_t K, uint8_t *keep) {
+  double t = floor(p * 4294967296.0 + 0.5);
+  if (t > 4294967295.0) t = 4294967295.0;
+  if (t < 0.0) t = 0.0;
+  const uint64_t p32 = (uint64_t)t;
+#pragma omp parallel for schedule(static)
+  for (int64_t e2 = 0; e2 < (M * K + 1) / 2; ++e2) {
+    const uint64_t v = oracle_philox_stream(seed, (uint64_t)e2);
+    const uint64_t u0 = v & 0xffffffffull, u1 = v >> 32;
+    keep[2 * e2] = u0 >= p32;
+    if (2 * e2 + 1 < M * K) keep[2 * e2 + 1] = u1 >= p32;
+  }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Forward.  [QLoRA-26] Step 3 (garbled formula, read as
  *   y = x W_hat^T + (x A^T) B^T * alpha / r )
  * and Step 4 (TODO 2: base output through F.linear with the dequantised
@@ -334,20 +394,25 @@ int oracle_dequant_bf16(const uint8_t *packed, const int8_t *absmax_code,
  * All inputs are binary32 arrays holding bf16-exact values; every dot product
  * is accumulated in binary64 in ascending index order.
  * Only the rows listed in `rows` (nrows of them) are evaluated; outputs are
- * packed in that order: y is [nrows, N], t is [nrows, r] (t = x A^T). */
+ * packed in that order: y is [nrows, N], t is [nrows, r] (t = x A^T).
+ * With LoRA dropout (keep != NULL, [M, K] of 0/1, keep_scale = 1/(1 - p))
+ * the LoRA branch takes dropout(x): t = keep_scale * (x . keep) A^T. */
 void oracle_linear_fwd(const float *x, int64_t M, int64_t K, const float *w, int64_t N,
                        const float *A, const float *B, int32_t r, double alpha,
-                       const int64_t *rows, int64_t nrows, double *y, double *t) {
+                       const int64_t *rows, int64_t nrows, double *y, double *t,
+                       const uint8_t *keep, double keep_scale) {
   (void)M;
   const double s = alpha / (double)r;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t ri = 0; ri < nrows; ++ri) {
     const float *xm = x + rows[ri] * K;
+    const uint8_t *km = keep ? keep + rows[ri] * K : NULL;
     double *tm = t + ri * r;
     for (int32_t j = 0; j < r; ++j) {
       double acc = 0.0;
-      for (int64_t k = 0; k < K; ++k) acc += (double)xm[k] * (double)A[j * K + k];
-      tm[j] = acc;
+      for (int64_t k = 0; k < K; ++k)
+        if (!km || km[k]) acc += (double)xm[k] * (double)A[j * K + k];
+      tm[j] = km ? keep_scale * acc : acc;
     }
     for (int64_t n = 0; n < N; ++n) {
       const float *wn = w + n * K;
@@ -369,20 +434,27 @@ void oracle_linear_fwd(const float *x, int64_t M, int64_t K, const float *w, int
  *   dA = s * u^T x                  [r, K]
  *   dB = s * dY^T t                 [N, r]
  * Binary64 accumulation in ascending index order.  t_out and u_out are
- * [M, r] (all rows); dX is [nrows, K]. */
+ * [M, r] (all rows); dX is [nrows, K].
+ * With LoRA dropout (keep != NULL, keep_scale = 1/(1 - p)): t is taken from
+ * dropout(x) as in the forward, and the gradient of the LoRA branch with
+ * respect to its input passes the same mask and scale:
+ *   dX = dY W_hat + s * keep_scale * keep . (u A),   dA = s * keep_scale * u^T (x . keep). */
 void oracle_linear_bwd(const float *x, const float *dY, int64_t M, int64_t K, int64_t N,
                        const float *w, const float *A, const float *B, int32_t r,
                        double alpha, const int64_t *rows, int64_t nrows, double *dX,
-                       double *dA, double *dB, double *t_out, double *u_out) {
+                       double *dA, double *dB, double *t_out, double *u_out,
+                       const uint8_t *keep, double keep_scale) {
   const double s = alpha / (double)r;
 #pragma omp parallel for schedule(static)
   for (int64_t m = 0; m < M; ++m) {
     const float *xm = x + m * K;
     const float *gm = dY + m * N;
+    const uint8_t *km = keep ? keep + m * K : NULL;
     for (int32_t j = 0; j < r; ++j) {
       double acc = 0.0;
-      for (int64_t k = 0; k < K; ++k) acc += (double)xm[k] * (double)A[j * K + k];
-      t_out[m * r + j] = acc;
+      for (int64_t k = 0; k < K; ++k)
+        if (!km || km[k]) acc += (double)xm[k] * (double)A[j * K + k];
+      t_out[m * r + j] = km ? keep_scale * acc : acc;
       double acc2 = 0.0;
       for (int64_t n = 0; n < N; ++n) acc2 += (double)gm[n] * (double)B[n * r + j];
       u_out[m * r + j] = acc2;
@@ -403,9 +475,11 @@ void oracle_linear_bwd(const float *x, const float *dY, int64_t M, int64_t K, in
       const float *wn = w + n * K;
       for (int64_t k = 0; k < K; ++k) base[k] += g * (double)wn[k];
     }
+    const uint8_t *km = keep ? keep + m * K : NULL;
     for (int64_t k = 0; k < K; ++k) {
       double lora = 0.0;
       for (int32_t j = 0; j < r; ++j) lora += um[j] * (double)A[j * K + k];
+      if (km) lora = km[k] ? keep_scale * lora : 0.0;
       base[k] = base[k] + s * lora;
     }
   }
@@ -420,10 +494,12 @@ void oracle_linear_bwd(const float *x, const float *dY, int64_t M, int64_t K, in
     for (int64_t m = 0; m < M; ++m)
       for (int32_t j = 0; j < r; ++j) {
         const double uj = u_out[m * r + j];
-        for (int64_t k = k0; k < k1; ++k) acc[j * (k1 - k0) + (k - k0)] += uj * (double)x[m * K + k];
+        for (int64_t k = k0; k < k1; ++k)
+          if (!keep || keep[m * K + k]) acc[j * (k1 - k0) + (k - k0)] += uj * (double)x[m * K + k];
       }
+    const double sa = keep ? s * keep_scale : s;
     for (int32_t j = 0; j < r; ++j)
-      for (int64_t k = k0; k < k1; ++k) dA[j * K + k] = s * acc[j * (k1 - k0) + (k - k0)];
+      for (int64_t k = k0; k < k1; ++k) dA[j * K + k] = sa * acc[j * (k1 - k0) + (k - k0)];
     free(acc);
   }
 #pragma omp parallel for schedule(dynamic, 1)

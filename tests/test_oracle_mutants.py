@@ -16,6 +16,7 @@ import pytest
 from oracle import oracle as orc
 from tests import test_oracle_codebook as tcb
 from tests import test_oracle_linear as tli
+from tests import test_oracle_dropout as tdr
 from tests import test_oracle_merge as tme
 from tests import test_oracle_quantize as tqu
 
@@ -35,7 +36,7 @@ MUTANTS = {
                             "ahat = (float)absmax_code[b] * scale2[0];"),
     "fwd_lora_sign": ("y[ri * N + n] = base + s * lora;", "y[ri * N + n] = base - s * lora;"),
     "fwd_drops_scaling": ("y[ri * N + n] = base + s * lora;", "y[ri * N + n] = base + lora;"),
-    "bwd_dA_drops_scaling": ("dA[j * K + k] = s * acc[j * (k1 - k0) + (k - k0)];",
+    "bwd_dA_drops_scaling": ("dA[j * K + k] = sa * acc[j * (k1 - k0) + (k - k0)];",
                              "dA[j * K + k] = acc[j * (k1 - k0) + (k - k0)];"),
     "bwd_dB_uses_u": ("acc[(n - n0) * r + j] += g * t_out[m * r + j];",
                       "acc[(n - n0) * r + j] += g * u_out[m * r + j];"),
@@ -53,6 +54,12 @@ MUTANTS = {
                            "lora += (double)B[(j * N + n) % (N * r)] * (double)A[j * K + k];"),
     "merge_round_down": ("q = ldexp(rint(ldexp(v, 8 - e)), e - 8);",
                          "q = ldexp(floor(ldexp(v, 8 - e)), e - 8);"),
+    "dropout_dX_drops_scale": ("if (km) lora = km[k] ? keep_scale * lora : 0.0;",
+                               "if (km) lora = km[k] ? lora : 0.0;"),
+    "dropout_dA_ignores_mask": ("if (!keep || keep[m * K + k]) acc[j * (k1 - k0) + (k - k0)]",
+                                "if (1) acc[j * (k1 - k0) + (k - k0)]"),
+    "philox_multiplier_typo": ("M1 = 0xCA5A826395121157ull", "M1 = 0xCA5A826395121167ull"),
+    "philox_low_half_first_odd": ("keep[2 * e2 + 1] = u1 >= p32;", "keep[2 * e2 + 1] = u0 >= p32;"),
     "storage_const_bytes": ("*const_b = nblocks * 1; /* int8 code per block */",
                             "*const_b = nblocks * 2; /* int8 code per block */"),
 }
@@ -87,6 +94,9 @@ def _pins(golden):
         tme.test_zero_factor_gives_the_dequantised_weight,
         tme.test_merged_weight_reproduces_the_forward,
         tme.test_hand_example,
+        lambda: tdr.test_philox_stream_equals_numpy(1234),
+        lambda: tdr.test_keep_mask_rule_and_rate(0.1),
+        lambda: tdr.test_dropout_forward_backward_match_torch_autograd(5, 128, 64, 4, 0.1),
     ]
     return pins
 
