@@ -569,7 +569,44 @@ def sub_benchmarks(capi, layers, device, stream, args):
     del mo
     rows["llama3_7proj_fwd_bwd_M8192"] = layer_set_at(capi, layers, 8192, device, stream,
                                                       steps=3 if args.quick else 6)
+    rows["llama3_7proj_fwd_bwd_dropout0.1_M2048"] = dropout_step(capi, layers, device, stream,
+                                                                 steps=5 if args.quick else 20)
     return rows
+
+
+def dropout_step(capi, layers, device, stream, steps, p=0.1):
+    """The headline step with LoRA dropout p on every projection: per layer
+    and step, the keep mask is drawn (Philox, in the timed region), the
+    forward and backward take it (fp32 dX)."""
+    M = M_TOKENS
+    dx32 = [torch.empty((M, L["K"]), dtype=torch.float32, device=device) for L in layers]
+    masks = [torch.empty((M, capi.dropout_mask_words(L["K"])), dtype=torch.int32, device=device)
+             for L in layers]
+
+    def step(si, ev=None):
+        for li, L in enumerate(layers):
+            mk = capi.dropout_mask(1000 * si + li, p, M, L["K"], out=masks[li])
+            capi.linear_fwd(L["q"], L["x"], L["A"], L["B"], ALPHA, L["ws"], y=L["y"],
+                            t_save=L["t"], dropout=(mk, p))
+            capi.linear_bwd(L["q"], L["x"], L["dY"], L["A"], L["B"], ALPHA, L["ws"],
+                            t_saved=L["t"], dX=dx32[li], dA=L["dA"], dB=L["dB"],
+                            dropout=(mk, p))
+
+    for si in range(3):
+        step(si)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for si in range(steps):
+        step(si)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    total = sum(fwd_flops(M, L["N"], L["K"], RANK_R) + bwd_flops(M, L["N"], L["K"], RANK_R)
+                for L in layers)
+    return {"p": p, "steps": steps, "ms_per_step": round(ms, 4),
+            "tflops": round(total / (ms * 1e-3) / 1e12, 2),
+            "note": "mask drawn per layer per step inside the timed region; dX in fp32"}
 
 
 def layer_set_at(capi, layers, M, device, stream, steps):

@@ -32,6 +32,8 @@ EXPORTED = (
     "qlora_workspace_init", "qlora_device_status", "qlora_linear_fwd", "qlora_linear_bwd",
     "qlora_nf4_thresholds", "qlora_nf4_codebook", "qlora_status_string",
     "qlora_linear_bwd_noalloc", "qlora_workspace_size_min", "qlora_merge_lora",
+    "qlora_dropout_mask_words", "qlora_dropout_mask", "qlora_linear_fwd_dropout",
+    "qlora_linear_bwd_dropout",
 )
 
 
@@ -39,6 +41,10 @@ class QloraError(RuntimeError):
     def __init__(self, fn: str, status: int, msg: str):
         super().__init__(f"{fn} failed: status {status} ({msg})")
         self.status = status
+
+
+class _DropoutStruct(ctypes.Structure):
+    _fields_ = [("mask", ctypes.c_void_p), ("p", ctypes.c_float)]
 
 
 class _NF4WeightStruct(ctypes.Structure):
@@ -69,6 +75,10 @@ def load(path: str = LIB_PATH):
         "qlora_quantize_nf4": [P, st, P, P, P],
         "qlora_dequant": [P, P, P],
         "qlora_merge_lora": [P, P, P, i32, f32, P, P],
+        "qlora_dropout_mask_words": [i64, P],
+        "qlora_dropout_mask": [ctypes.c_uint64, f32, i64, i64, P, P],
+        "qlora_linear_fwd_dropout": [P, P, i64, P, P, i32, f32, P, P, st, P, P, sz, u32, P],
+        "qlora_linear_bwd_dropout": [P, P, P, i64, P, P, i32, f32, P, P, P, P, P, P, sz, u32, P],
         "qlora_workspace_size": [i64, i64, i64, i32, P],
         "qlora_workspace_size_min": [i64, i64, i64, i32, P],
         "qlora_workspace_init": [P, sz, P],
@@ -231,16 +241,40 @@ class Workspace:
         return v.value
 
 
+def dropout_mask_words(K: int) -> int:
+    v = ctypes.c_int64()
+    _check("qlora_dropout_mask_words", load().qlora_dropout_mask_words(K, ctypes.byref(v)))
+    return v.value
+
+
+def dropout_mask(seed: int, p: float, M: int, K: int, device="cuda", out=None,
+                 stream=None) -> torch.Tensor:
+    """qlora_dropout_mask -> int32 tensor [M, words_per_row] of keep bits."""
+    if out is None:
+        out = torch.empty((M, dropout_mask_words(K)), dtype=torch.int32, device=device)
+    _check("qlora_dropout_mask", load().qlora_dropout_mask(
+        ctypes.c_uint64(seed), float(p), M, K, _ptr(out), _stream(stream)))
+    return out
+
+
 def linear_fwd(w: NF4Weight, x: torch.Tensor, A: torch.Tensor, B: torch.Tensor, alpha: float,
                ws: Workspace, y: torch.Tensor | None = None, y_dtype=torch.float32,
-               t_save: torch.Tensor | None = None, flags: int = 0, stream=None) -> torch.Tensor:
-    """qlora_linear_fwd: y = x W_hat^T + (x A^T) B^T alpha/r."""
+               t_save: torch.Tensor | None = None, flags: int = 0, stream=None,
+               dropout: tuple | None = None) -> torch.Tensor:
+    """qlora_linear_fwd: y = x W_hat^T + (x A^T) B^T alpha/r; with
+    dropout=(mask, p) qlora_linear_fwd_dropout."""
     M = x.shape[0]
     r = A.shape[0]
     if y is None:
         y = torch.empty((M, w.rows), dtype=y_dtype, device=x.device)
     ydt = {torch.float32: QLORA_F32, torch.bfloat16: QLORA_BF16}[y.dtype]
     s = w.struct()
+    if dropout is not None:
+        d = _DropoutStruct(dropout[0].data_ptr(), float(dropout[1]))
+        _check("qlora_linear_fwd_dropout", load().qlora_linear_fwd_dropout(
+            ctypes.byref(s), _ptr(x), M, _ptr(A), _ptr(B), r, float(alpha), ctypes.byref(d),
+            _ptr(y), ydt, _ptr(t_save), _ptr(ws.buf), ws.nbytes, flags, _stream(stream)))
+        return y
     _check("qlora_linear_fwd", load().qlora_linear_fwd(
         ctypes.byref(s), _ptr(x), M, _ptr(A), _ptr(B), r, float(alpha), _ptr(y), ydt,
         _ptr(t_save), _ptr(ws.buf), ws.nbytes, flags, _stream(stream)))
@@ -275,8 +309,9 @@ def linear_bwd(w: NF4Weight, x: torch.Tensor, dY: torch.Tensor, A: torch.Tensor,
                B: torch.Tensor, alpha: float, ws: Workspace, t_saved: torch.Tensor | None = None,
                dX: torch.Tensor | None = None, dx_dtype=torch.float32,
                dA: torch.Tensor | None = None, dB: torch.Tensor | None = None, flags: int = 0,
-               stream=None):
-    """qlora_linear_bwd -> (dX, dA, dB)."""
+               stream=None, dropout: tuple | None = None):
+    """qlora_linear_bwd -> (dX, dA, dB); with dropout=(mask, p)
+    qlora_linear_bwd_dropout (fp32 dX)."""
     M = x.shape[0]
     r = A.shape[0]
     dev = x.device
@@ -288,6 +323,13 @@ def linear_bwd(w: NF4Weight, x: torch.Tensor, dY: torch.Tensor, A: torch.Tensor,
         dB = torch.empty((w.rows, r), dtype=torch.float32, device=dev)
     dxt = {torch.float32: QLORA_F32, torch.bfloat16: QLORA_BF16}[dX.dtype]
     s = w.struct()
+    if dropout is not None:
+        d = _DropoutStruct(dropout[0].data_ptr(), float(dropout[1]))
+        _check("qlora_linear_bwd_dropout", load().qlora_linear_bwd_dropout(
+            ctypes.byref(s), _ptr(x), _ptr(dY), M, _ptr(A), _ptr(B), r, float(alpha),
+            ctypes.byref(d), _ptr(t_saved), _ptr(dX), _ptr(dA), _ptr(dB), _ptr(ws.buf),
+            ws.nbytes, flags, _stream(stream)))
+        return dX, dA, dB
     _check("qlora_linear_bwd", load().qlora_linear_bwd(
         ctypes.byref(s), _ptr(x), _ptr(dY), M, _ptr(A), _ptr(B), r, float(alpha),
         _ptr(t_saved), _ptr(dX), dxt, _ptr(dA), _ptr(dB), _ptr(ws.buf), ws.nbytes, flags,

@@ -405,12 +405,35 @@ qlora_status qlora_device_status(void *ws, int32_t *status, void *stream) {
   return QLORA_OK;
 }
 
-qlora_status qlora_linear_fwd(const qlora_nf4_weight *w, const uint16_t *x, int64_t M,
-                              const uint16_t *A, const uint16_t *B, int32_t r, float alpha,
-                              void *y, qlora_dtype y_dtype, float *t_save, void *ws,
-                              size_t ws_bytes, uint32_t flags, void *stream) {
+}  // extern "C"
+
+namespace {
+
+int dropout_words(int64_t K) { return (int)((K + 127) / 128 * 4); }
+
+qlora_status check_dropout(const qlora_lora_dropout *dr) {
+  if (!dr) return QLORA_OK;
+  if (!dr->mask || !(dr->p >= 0.0f && dr->p < 1.0f)) return QLORA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(dr->mask) & 3u) return QLORA_ERR_ALIGN;
+  return QLORA_OK;
+}
+
+float keep_scale_of(const qlora_lora_dropout *dr) {
+  return dr ? (float)(1.0 / (1.0 - (double)dr->p)) : 1.0f;
+}
+
+qlora_status linear_fwd_impl(const qlora_nf4_weight *w, const uint16_t *x, int64_t M,
+                             const uint16_t *A, const uint16_t *B, int32_t r, float alpha,
+                             const qlora_lora_dropout *dr, void *y, qlora_dtype y_dtype,
+                             float *t_save, void *ws, size_t ws_bytes, uint32_t flags,
+                             void *stream) {
   qlora_status st = check_linear_common(w, x, M, A, B, r, ws, ws_bytes);
   if (st != QLORA_OK) return st;
+  st = check_dropout(dr);
+  if (st != QLORA_OK) return st;
+  const uint32_t *dmask = dr ? dr->mask : nullptr;
+  const int dwpr = dropout_words(w->cols);
+  const float kscale = keep_scale_of(dr);
   if (!y) return QLORA_ERR_INVALID_ARG;
   if (y_dtype != QLORA_F32 && y_dtype != QLORA_BF16) return QLORA_ERR_DTYPE;
   if (!aligned16(y) || (t_save && !aligned16(t_save))) return QLORA_ERR_ALIGN;
@@ -453,6 +476,9 @@ qlora_status qlora_linear_fwd(const qlora_nf4_weight *w, const uint16_t *x, int6
     a.t = reinterpret_cast<const float *>(wsb + L.t);
     a.status = reinterpret_cast<int *>(wsb + L.status);
     a.cb = tables(w->codebook).cb;
+    a.mask = dmask;
+    a.wpr = dwpr;
+    a.keep_scale = kscale;
     return cuda_status(launch_gemv(tmW, a, gplan, A, reinterpret_cast<float *>(wsb + L.part),
                                    reinterpret_cast<int *>(wsb + L.gcnt), t_save, s));
   }
@@ -464,7 +490,8 @@ qlora_status qlora_linear_fwd(const qlora_nf4_weight *w, const uint16_t *x, int6
   if (e != cudaSuccess) return QLORA_ERR_CUDA;
   const int bn = plan.bn;
   uint16_t *lb = reinterpret_cast<uint16_t *>(wsb + L.lb);
-  e = launch_lora_down(x, M, K, A, r, sc, t_save, lb, RP, num_sms_current(), s);
+  e = launch_lora_down(x, M, K, A, r, sc, t_save, lb, RP, num_sms_current(), s, dmask, dwpr,
+                       kscale);
   if (e != cudaSuccess) return QLORA_ERR_CUDA;
   CUtensorMap tmA, tmL1, tmL2;
   if (!make_tmap(&tmA, x, K, M, (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -495,14 +522,20 @@ qlora_status qlora_linear_fwd(const qlora_nf4_weight *w, const uint16_t *x, int6
   return cuda_status(launch_gemm(false, tmA, tmL1, tmL2, g, s));
 }
 
-qlora_status qlora_linear_bwd(const qlora_nf4_weight *w, const uint16_t *x, const uint16_t *dY,
-                              int64_t M, const uint16_t *A, const uint16_t *B, int32_t r,
-                              float alpha, const float *t_saved, void *dX, qlora_dtype dx_dtype,
-                              float *dA, float *dB, void *ws, size_t ws_bytes, uint32_t flags,
-                              void *stream) {
+qlora_status linear_bwd_impl(const qlora_nf4_weight *w, const uint16_t *x, const uint16_t *dY,
+                             int64_t M, const uint16_t *A, const uint16_t *B, int32_t r,
+                             float alpha, const qlora_lora_dropout *dr, const float *t_saved,
+                             void *dX, qlora_dtype dx_dtype, float *dA, float *dB, void *ws,
+                             size_t ws_bytes, uint32_t flags, void *stream) {
   (void)flags;
   qlora_status st = check_linear_common(w, x, M, A, B, r, ws, ws_bytes);
   if (st != QLORA_OK) return st;
+  st = check_dropout(dr);
+  if (st != QLORA_OK) return st;
+  if (dr && dx_dtype != QLORA_F32) return QLORA_ERR_DTYPE;
+  const uint32_t *dmask = dr ? dr->mask : nullptr;
+  const int dwpr = dropout_words(w->cols);
+  const float kscale = keep_scale_of(dr);
   if (!dY || !dX || !dA || !dB) return QLORA_ERR_INVALID_ARG;
   if (dx_dtype != QLORA_F32 && dx_dtype != QLORA_BF16) return QLORA_ERR_DTYPE;
   if (!aligned16(dY) || !aligned16(dX) || !aligned16(dA) || !aligned16(dB) ||
@@ -524,14 +557,15 @@ qlora_status qlora_linear_bwd(const qlora_nf4_weight *w, const uint16_t *x, cons
   cudaError_t e;
   if (!t) {
     float *tw = reinterpret_cast<float *>(wsb + L.t);
-    e = launch_lora_down(x, M, K, A, r, sc, tw, nullptr, RP, nsm, s);
+    e = launch_lora_down(x, M, K, A, r, sc, tw, nullptr, RP, nsm, s, dmask, dwpr, kscale);
     if (e != cudaSuccess) return QLORA_ERR_CUDA;
     t = tw;
   }
   e = launch_transposes(A, B, N, K, r, RP, At, Bt, nsm, s);
   if (e != cudaSuccess) return QLORA_ERR_CUDA;
-  // u = dY . B (fp32, for dA) and bf16(s . u) (operand of the dX GEMM's rank-r MMAs)
-  e = launch_lora_down(dY, M, N, Bt, r, sc, u, lb, RP, nsm, s);
+  // u = dY . B (fp32, for dA) and bf16(s . u) (operand of the dX GEMM's rank-r MMAs;
+  // with dropout bf16(s / (1 - p) . u), taken back out at the dropped positions)
+  e = launch_lora_down(dY, M, N, Bt, r, sc * kscale, u, lb, RP, nsm, s);
   if (e != cudaSuccess) return QLORA_ERR_CUDA;
   GemmPlan plan;
   e = gemm_plan(true, (int)M, K, N, RP, ws_bytes >= L.total ? L.sk_clusters : 0, &plan);
@@ -566,13 +600,77 @@ qlora_status qlora_linear_bwd(const qlora_nf4_weight *w, const uint16_t *x, cons
   set_block_constants(g, w);
   e = launch_gemm(true, tmA, tmL1, tmL2, g, s);
   if (e != cudaSuccess) return QLORA_ERR_CUDA;
+  if (dmask) {
+    e = launch_dropout_dx_fix(dmask, dwpr, M, K, lb, At, RP, static_cast<float *>(dX), nsm, s);
+    if (e != cudaSuccess) return QLORA_ERR_CUDA;
+  }
   // dB = s . dY^T . t
   int *gcnt = reinterpret_cast<int *>(wsb + L.gcnt);
   e = launch_skinny(dY, M, N, t, r, RP, part, gcnt, skinny_splits(M, N), sc, false, dB, s);
   if (e != cudaSuccess) return QLORA_ERR_CUDA;
-  // dA = s . u^T . x
-  e = launch_skinny(x, M, K, u, r, RP, part, gcnt, skinny_splits(M, K), sc, true, dA, s);
+  // dA = s . u^T . x  (with dropout s / (1 - p) . u^T . (x . keep))
+  e = launch_skinny(x, M, K, u, r, RP, part, gcnt, skinny_splits(M, K), sc * kscale, true, dA, s,
+                    dmask, dwpr);
   return cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+qlora_status qlora_linear_fwd(const qlora_nf4_weight *w, const uint16_t *x, int64_t M,
+                              const uint16_t *A, const uint16_t *B, int32_t r, float alpha,
+                              void *y, qlora_dtype y_dtype, float *t_save, void *ws,
+                              size_t ws_bytes, uint32_t flags, void *stream) {
+  return linear_fwd_impl(w, x, M, A, B, r, alpha, nullptr, y, y_dtype, t_save, ws, ws_bytes,
+                         flags, stream);
+}
+
+qlora_status qlora_linear_fwd_dropout(const qlora_nf4_weight *w, const uint16_t *x, int64_t M,
+                                      const uint16_t *A, const uint16_t *B, int32_t r,
+                                      float alpha, const qlora_lora_dropout *dropout, void *y,
+                                      qlora_dtype y_dtype, float *t_save, void *ws,
+                                      size_t ws_bytes, uint32_t flags, void *stream) {
+  if (!dropout) return QLORA_ERR_INVALID_ARG;
+  return linear_fwd_impl(w, x, M, A, B, r, alpha, dropout, y, y_dtype, t_save, ws, ws_bytes,
+                         flags, stream);
+}
+
+qlora_status qlora_linear_bwd(const qlora_nf4_weight *w, const uint16_t *x, const uint16_t *dY,
+                              int64_t M, const uint16_t *A, const uint16_t *B, int32_t r,
+                              float alpha, const float *t_saved, void *dX, qlora_dtype dx_dtype,
+                              float *dA, float *dB, void *ws, size_t ws_bytes, uint32_t flags,
+                              void *stream) {
+  return linear_bwd_impl(w, x, dY, M, A, B, r, alpha, nullptr, t_saved, dX, dx_dtype, dA, dB, ws,
+                         ws_bytes, flags, stream);
+}
+
+qlora_status qlora_linear_bwd_dropout(const qlora_nf4_weight *w, const uint16_t *x,
+                                      const uint16_t *dY, int64_t M, const uint16_t *A,
+                                      const uint16_t *B, int32_t r, float alpha,
+                                      const qlora_lora_dropout *dropout, const float *t_saved,
+                                      float *dX, float *dA, float *dB, void *ws, size_t ws_bytes,
+                                      uint32_t flags, void *stream) {
+  if (!dropout) return QLORA_ERR_INVALID_ARG;
+  return linear_bwd_impl(w, x, dY, M, A, B, r, alpha, dropout, t_saved, dX, QLORA_F32, dA, dB,
+                         ws, ws_bytes, flags, stream);
+}
+
+qlora_status qlora_dropout_mask_words(int64_t K, int64_t *words_per_row) {
+  if (!words_per_row || K < 0) return QLORA_ERR_INVALID_ARG;
+  *words_per_row = dropout_words(K);
+  return QLORA_OK;
+}
+
+qlora_status qlora_dropout_mask(uint64_t seed, float p, int64_t M, int64_t K, uint32_t *mask,
+                                void *stream) {
+  if (!mask || !(p >= 0.0f && p < 1.0f) || M < 0 || K < 0) return QLORA_ERR_INVALID_ARG;
+  if (K % 64 || K > (int64_t)INT32_MAX) return QLORA_ERR_SHAPE;
+  if (reinterpret_cast<uintptr_t>(mask) & 15u) return QLORA_ERR_ALIGN;
+  double t = std::floor((double)p * 4294967296.0 + 0.5);
+  if (t > 4294967295.0) t = 4294967295.0;
+  return cuda_status(launch_dropout_mask(seed, (uint32_t)t, M, (int)K, dropout_words(K), mask,
+                                         num_sms_current(), static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

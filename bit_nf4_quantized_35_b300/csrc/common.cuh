@@ -111,6 +111,16 @@ __device__ __forceinline__ void lookup8(const Nf4Table &t, uint32_t w, uint32_t 
   }
 }
 
+// Bit mask of 8 bf16 elements (bits of `byte`, element e = bit e) as four
+// AND masks of bf16 pairs (element 2p in the low half of word p).
+__device__ __forceinline__ void keep_masks(uint32_t byte, uint32_t (&mk)[4]) {
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const uint32_t b = byte >> (2 * p);
+    mk[p] = ((b & 1u) ? 0x0000ffffu : 0u) | ((b & 2u) ? 0xffff0000u : 0u);
+  }
+}
+
 // ------------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));

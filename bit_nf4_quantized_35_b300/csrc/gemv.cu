@@ -78,10 +78,12 @@ __device__ __forceinline__ uint4 ldg_v4_or_zero(const uint16_t *p, bool ok) {
 // ------------------------------------------------------------- t = x A^T
 // Grid: ceil(K / 256) CTAs of kTWarps warps.  tpart [gridDim.x][M][RP],
 // tfin [M][RP] (fp32, workspace), counter: one int, zero between calls.
+// With `mask` (LoRA dropout keep bits of x, wpr words per row) the dropped
+// elements of x count as zero and t is scaled by keep_scale.
 __global__ void __launch_bounds__(kTWarps * 32) lora_t_decode_kernel(
     const uint16_t *__restrict__ x, int M, int K, const uint16_t *__restrict__ A, int r, int RP,
     float *__restrict__ tpart, float *__restrict__ tfin, int *__restrict__ counter,
-    float *__restrict__ t_save) {
+    float *__restrict__ t_save, const uint32_t *__restrict__ mask, int wpr, float keep_scale) {
   __shared__ int last_s;
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -104,8 +106,15 @@ __global__ void __launch_bounds__(kTWarps * 32) lora_t_decode_kernel(
       for (int nt = 0; nt < 2; ++nt) {
         const int tok = nt * 8 + g;
         const bool okx = kin && tok < M;
-        const uint4 xv = ldg_v4_or_zero(
+        uint4 xv = ldg_v4_or_zero(
             x + (int64_t)(okx ? tok : 0) * K + (int64_t)(kin ? blk : 0) * 64 + 8 * wi, okx);
+        if (mask && okx) {  // dropout: columns blk*64 + 8wi .. +7 are byte (wi & 3) of a word
+          const uint32_t kw = __ldg(mask + (int64_t)tok * wpr + ((blk * 64 + 8 * wi) >> 5));
+          const uint32_t byte = (kw >> (8 * (wi & 3))) & 0xffu;
+          uint32_t mk[4];
+          keep_masks(byte, mk);
+          xv.x &= mk[0], xv.y &= mk[1], xv.z &= mk[2], xv.w &= mk[3];
+        }
         mma_bf16(d[nt], ag.x, ah.x, ag.y, ah.y, xv.x, xv.y);
         mma_bf16(d[nt], ag.z, ah.z, ag.w, ah.w, xv.z, xv.w);
       }
@@ -115,12 +124,12 @@ __global__ void __launch_bounds__(kTWarps * 32) lora_t_decode_kernel(
     for (int nt = 0; nt < 2; ++nt) {
       const int tok = nt * 8 + 2 * tq;
       if (tok < M) {
-        tp[tok * RP + j0] = d[nt][0];
-        tp[tok * RP + j1] = d[nt][2];
+        tp[tok * RP + j0] = keep_scale * d[nt][0];
+        tp[tok * RP + j1] = keep_scale * d[nt][2];
       }
       if (tok + 1 < M) {
-        tp[(tok + 1) * RP + j0] = d[nt][1];
-        tp[(tok + 1) * RP + j1] = d[nt][3];
+        tp[(tok + 1) * RP + j0] = keep_scale * d[nt][1];
+        tp[(tok + 1) * RP + j1] = keep_scale * d[nt][3];
       }
     }
   }
@@ -446,7 +455,8 @@ cudaError_t launch_gemv(const CUtensorMap &tmW, GemvArgs a, const GemvPlan &plan
     cfg.attrs = at;
     cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, lora_t_decode_kernel, a.x, a.M, a.K, A, a.r, a.RP,
-                                       tpart, const_cast<float *>(a.t), counter, t_save);
+                                       tpart, const_cast<float *>(a.t), counter, t_save, a.mask,
+                                       a.wpr, a.mask ? a.keep_scale : 1.0f);
     if (e != cudaSuccess) return e;
   }
   const int nt = a.M > 8 ? 2 : 1;

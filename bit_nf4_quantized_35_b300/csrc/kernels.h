@@ -79,6 +79,9 @@ struct GemvArgs {
   int y_bf16;
   const float *t;  // [M, RP] fp32 in the workspace, written by the t kernel
   int *status;     // device status word
+  const uint32_t *mask;  // LoRA dropout keep bits of x ([M][wpr]) or null
+  int wpr;
+  float keep_scale;
   // set by the launcher from the plan:
   int S, slice_chunks, clusters, tiles_total, tiles_max;
   Codebook cb;
@@ -98,9 +101,12 @@ cudaError_t launch_gemv(const CUtensorMap &tmW, GemvArgs a, const GemvPlan &plan
                         cudaStream_t s);
 // out[m, j] = sum_c G[m, c] H[j, c] (fp32, j < r) and outb[m, j] = bf16(s . out[m, j])
 // (j < r_pad, zero beyond r); either output may be null.  H has r rows of C.
+// With `mask` (LoRA dropout keep bits of G, wpr words per row) the dropped
+// elements of G are zeroed and out = keep_scale . G H^T, outb = bf16(s . out).
 cudaError_t launch_lora_down(const uint16_t *G, int64_t M, int C, const uint16_t *H, int r,
                              float s, float *out, uint16_t *outb, int r_pad, int num_sms,
-                             cudaStream_t st);
+                             cudaStream_t st, const uint32_t *mask = nullptr, int wpr = 0,
+                             float keep_scale = 1.0f);
 
 // Quantise / dequantise (quantize.cu).
 cudaError_t launch_quantize(const void *W, bool bf16_in, int block, int64_t nblocks, int group,
@@ -132,9 +138,20 @@ int skinny_tiles(int C);
 // dst = sc . G^T V for G [M, C] bf16, V [M, r] fp32: dst[c * r + j], or
 // dst[j * C + c] with transpose.  part: splits * C * RP floats of scratch;
 // tile_count: skinny_tiles(C) ints, zero before the call and after it.
+// With `mask` (dropout keep bits of G, wpr words per row) the dropped
+// elements of G count as zero.
 cudaError_t launch_skinny(const uint16_t *G, int64_t M, int C, const float *V, int r, int RP,
                           float *part, int *tile_count, int splits, float sc, bool transpose,
-                          float *dst, cudaStream_t s);
+                          float *dst, cudaStream_t s, const uint32_t *mask = nullptr,
+                          int wpr = 0);
+
+// LoRA dropout (dropout.cu).  Keep bits [M][wpr] uint32 of an [M, K] input.
+cudaError_t launch_dropout_mask(uint64_t seed, uint32_t p32, int64_t M, int K, int wpr,
+                                uint32_t *mask, int num_sms, cudaStream_t s);
+// dX[m, k] -= sum_j lb[m, j] At[k, j] (bf16 operands, fp32) at every dropped (m, k).
+cudaError_t launch_dropout_dx_fix(const uint32_t *mask, int wpr, int64_t M, int K,
+                                  const uint16_t *lb, const uint16_t *At, int RP, float *dX,
+                                  int num_sms, cudaStream_t s);
 cudaError_t launch_transposes(const uint16_t *A, const uint16_t *B, int N, int K, int r, int RP,
                               uint16_t *At, uint16_t *Bt, int num_sms, cudaStream_t s);
 

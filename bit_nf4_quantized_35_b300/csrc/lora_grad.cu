@@ -69,7 +69,7 @@ template <int RPT>  // r_pad / 8
 __global__ void __launch_bounds__(kGradThreads) lora_grad_tc_kernel(
     const uint16_t *__restrict__ G, int64_t M, int C, const float *__restrict__ V, int r,
     int64_t rows_per_split, float *__restrict__ part, int *__restrict__ tile_count, float sc,
-    int transpose, float *__restrict__ dst) {
+    int transpose, float *__restrict__ dst, const uint32_t *__restrict__ mask, int wpr) {
   pdl_wait_release();
   constexpr int RPAD = RPT * 8;
   constexpr int NJ = 2 * RPAD;  // hi rows then lo rows
@@ -127,6 +127,26 @@ __global__ void __launch_bounds__(kGradThreads) lora_grad_tc_kernel(
     cp_async_wait<kGradStages - 2>();  // this thread's copies of chunk ch have landed
     __syncthreads();                   // everyone's; chunk ch - 1 is fully consumed
     issue(ch + kGradStages - 1);       // into the buffer chunk ch - 1 used
+    if (mask) {
+      // dropout: zero the dropped elements of G in chunk ch (keep bits of the
+      // mask; a piece of 8 columns is one byte of a keep word)
+      const int64_t mb = m_lo + (int64_t)ch * kGradRows;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = threadIdx.x + u * kGradThreads;
+        const int row = i >> 4, cc = (i & 15) * 8;
+        const int64_t m = mb + row;
+        const int c = c0 + cc;
+        if (m < m_hi && c < C) {
+          const uint32_t kw = __ldg(mask + m * wpr + (c >> 5));
+          uint32_t mk[4];
+          keep_masks((kw >> (c & 31)) & 0xffu, mk);
+          const uint32_t a = smem_u32(gs + (cur * kGradRows + row) * kGsPitch + cc);
+          const uint4 v = lds_v4(a);
+          sts_v4(a, v.x & mk[0], v.y & mk[1], v.z & mk[2], v.w & mk[3]);
+        }
+      }
+    }
     // V rows of chunk ch -> bf16 hi / lo, transposed
     for (int i = threadIdx.x; i < kGradRows * RPAD; i += kGradThreads) {
       const int row = i / RPAD, j = i % RPAD;
@@ -279,7 +299,8 @@ constexpr int kDownWarps = 16;
 template <int NT>  // n8 tiles: r_pad / 8
 __global__ void __launch_bounds__(kDownWarps * 32) lora_down_kernel(
     const uint16_t *__restrict__ G, int64_t M, int C, const uint16_t *__restrict__ H, int r,
-    float s, float *__restrict__ out, uint16_t *__restrict__ outb, int r_pad) {
+    float s, float *__restrict__ out, uint16_t *__restrict__ outb, int r_pad,
+    const uint32_t *__restrict__ mask, int wpr, float keep_scale) {
   pdl_wait_release();
   constexpr int U = NT <= 2 ? 4 : (NT <= 4 ? 2 : 1);  // chunks in flight per lane
   __shared__ float red[kDownWarps / 2][16][NT * 8];
@@ -304,12 +325,19 @@ __global__ void __launch_bounds__(kDownWarps * 32) lora_down_kernel(
   const uint16_t *g8p = G + (vg8 ? rg8 : 0) * C;
   for (int c0 = c_lo; c0 < c_hi; c0 += 32 * U) {
     uint4 a[U], b[U], h[U][NT];
+    uint32_t ma[U], mb[U];  // dropout keep words of rows rg, rg8 (all ones without dropout)
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int cc = c0 + u * 32 + q * 8;
       const bool cv = cc < c_hi;  // C % 8 == 0
       a[u] = ldg_nc_v4(g0p + (cv ? cc : 0));
       b[u] = ldg_nc_v4(g8p + (cv ? cc : 0));
+      ma[u] = mb[u] = 0xffffffffu;
+      if (mask) {
+        const int wd = (cv ? cc : 0) >> 5;
+        ma[u] = __ldg(mask + (vg ? rg : 0) * wpr + wd);
+        mb[u] = __ldg(mask + (vg8 ? rg8 : 0) * wpr + wd);
+      }
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int j = nt * 8 + g;
@@ -320,10 +348,20 @@ __global__ void __launch_bounds__(kDownWarps * 32) lora_down_kernel(
     for (int u = 0; u < U; ++u) {
       const bool cv = c0 + u * 32 + q * 8 < c_hi;
       const bool k0 = vg && cv, k8 = vg8 && cv;
-      const uint32_t A0[4] = {k0 ? a[u].x : 0u, k0 ? a[u].y : 0u, k0 ? a[u].z : 0u,
-                              k0 ? a[u].w : 0u};
-      const uint32_t A8[4] = {k8 ? b[u].x : 0u, k8 ? b[u].y : 0u, k8 ? b[u].z : 0u,
-                              k8 ? b[u].w : 0u};
+      uint32_t A0[4] = {k0 ? a[u].x : 0u, k0 ? a[u].y : 0u, k0 ? a[u].z : 0u,
+                        k0 ? a[u].w : 0u};
+      uint32_t A8[4] = {k8 ? b[u].x : 0u, k8 ? b[u].y : 0u, k8 ? b[u].z : 0u,
+                        k8 ? b[u].w : 0u};
+      if (mask) {  // dropout: zero the dropped elements (byte q of the keep word)
+        uint32_t m0[4], m8[4];
+        keep_masks((ma[u] >> (8 * q)) & 0xffu, m0);
+        keep_masks((mb[u] >> (8 * q)) & 0xffu, m8);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          A0[e] &= m0[e];
+          A8[e] &= m8[e];
+        }
+      }
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const bool hv = nt * 8 + g < r && cv;
@@ -376,7 +414,7 @@ __global__ void __launch_bounds__(kDownWarps * 32) lora_down_kernel(
                      : "=f"(peer)
                      : "r"(mapa_shared(smem_u32(&fin[row][j]), 1))
                      : "memory");
-      const float v = fin[row][j] + peer;
+      const float v = (fin[row][j] + peer) * keep_scale;
       if (out && j < r) out[m * r + j] = v;
       if (outb && j < r_pad)
         outb[m * r_pad + j] = j < r ? __bfloat16_as_ushort(__float2bfloat16_rn(s * v)) : (uint16_t)0;
@@ -389,7 +427,8 @@ __global__ void __launch_bounds__(kDownWarps * 32) lora_down_kernel(
 template <int NT>
 static cudaError_t launch_down(unsigned gx, const uint16_t *G, int64_t M, int C,
                                const uint16_t *H, int r, float s, float *out, uint16_t *outb,
-                               int r_pad, cudaStream_t st) {
+                               int r_pad, const uint32_t *mask, int wpr, float keep_scale,
+                               cudaStream_t st) {
   // Wide inputs: two CTAs per row block (a cluster), so that more SMs stream.
   const bool split = C >= 8192;
   cudaLaunchConfig_t cfg = {};
@@ -404,26 +443,28 @@ static cudaError_t launch_down(unsigned gx, const uint16_t *G, int64_t M, int C,
   attrs[1].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = split ? 2 : 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, lora_down_kernel<NT>, G, M, C, H, r, s, out, outb, r_pad);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, lora_down_kernel<NT>, G, M, C, H, r, s, out, outb,
+                                     r_pad, mask, wpr, keep_scale);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 cudaError_t launch_lora_down(const uint16_t *G, int64_t M, int C, const uint16_t *H, int r,
                              float s, float *out, uint16_t *outb, int r_pad, int num_sms,
-                             cudaStream_t st) {
+                             cudaStream_t st, const uint32_t *mask, int wpr, float keep_scale) {
   (void)num_sms;
   if (M == 0) return cudaSuccess;
   const unsigned gx = (unsigned)((M + 15) / 16);
+  const float ks = mask ? keep_scale : 1.0f;
   switch ((r + 7) / 8) {
     case 1:
-    case 2: return launch_down<2>(gx, G, M, C, H, r, s, out, outb, r_pad, st);
+    case 2: return launch_down<2>(gx, G, M, C, H, r, s, out, outb, r_pad, mask, wpr, ks, st);
     case 3:
-    case 4: return launch_down<4>(gx, G, M, C, H, r, s, out, outb, r_pad, st);
+    case 4: return launch_down<4>(gx, G, M, C, H, r, s, out, outb, r_pad, mask, wpr, ks, st);
     case 5:
-    case 6: return launch_down<6>(gx, G, M, C, H, r, s, out, outb, r_pad, st);
+    case 6: return launch_down<6>(gx, G, M, C, H, r, s, out, outb, r_pad, mask, wpr, ks, st);
     case 7:
-    case 8: return launch_down<8>(gx, G, M, C, H, r, s, out, outb, r_pad, st);
+    case 8: return launch_down<8>(gx, G, M, C, H, r, s, out, outb, r_pad, mask, wpr, ks, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -444,7 +485,8 @@ int skinny_tiles(int C) { return (C + kGradCols - 1) / kGradCols; }
 template <int RPT>
 static cudaError_t launch_grad(dim3 grid, const uint16_t *G, int64_t M, int C, const float *V,
                                int r, int64_t rps, float *part, int *tile_count, float sc,
-                               bool transpose, float *dst, cudaStream_t s) {
+                               bool transpose, float *dst, const uint32_t *mask, int wpr,
+                               cudaStream_t s) {
   const int smem = grad_smem_bytes(RPT * 8);
   static bool set = false;
   if (!set) {
@@ -462,22 +504,30 @@ static cudaError_t launch_grad(dim3 grid, const uint16_t *G, int64_t M, int C, c
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, lora_grad_tc_kernel<RPT>, G, M, C, V, r, rps, part,
-                                     tile_count, sc, transpose ? 1 : 0, dst);
+                                     tile_count, sc, transpose ? 1 : 0, dst, mask, wpr);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 cudaError_t launch_skinny(const uint16_t *G, int64_t M, int C, const float *V, int r, int RP,
                           float *part, int *tile_count, int splits, float sc, bool transpose,
-                          float *dst, cudaStream_t s) {
+                          float *dst, cudaStream_t s, const uint32_t *mask, int wpr) {
   if (C == 0) return cudaSuccess;
   const int64_t rps = ((M + splits - 1) / splits + kGradRows - 1) / kGradRows * kGradRows;
   dim3 grid((C + kGradCols - 1) / kGradCols, splits);
   switch (RP) {
-    case 16: return launch_grad<2>(grid, G, M, C, V, r, rps, part, tile_count, sc, transpose, dst, s);
-    case 32: return launch_grad<4>(grid, G, M, C, V, r, rps, part, tile_count, sc, transpose, dst, s);
-    case 48: return launch_grad<6>(grid, G, M, C, V, r, rps, part, tile_count, sc, transpose, dst, s);
-    case 64: return launch_grad<8>(grid, G, M, C, V, r, rps, part, tile_count, sc, transpose, dst, s);
+    case 16:
+      return launch_grad<2>(grid, G, M, C, V, r, rps, part, tile_count, sc, transpose, dst, mask,
+                            wpr, s);
+    case 32:
+      return launch_grad<4>(grid, G, M, C, V, r, rps, part, tile_count, sc, transpose, dst, mask,
+                            wpr, s);
+    case 48:
+      return launch_grad<6>(grid, G, M, C, V, r, rps, part, tile_count, sc, transpose, dst, mask,
+                            wpr, s);
+    case 64:
+      return launch_grad<8>(grid, G, M, C, V, r, rps, part, tile_count, sc, transpose, dst, mask,
+                            wpr, s);
     default: return cudaErrorInvalidValue;
   }
 }

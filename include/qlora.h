@@ -38,7 +38,8 @@
  *   - The NF4 buffers are const in the forward and backward calls: that is
  *     the frozen-base contract ([QLoRA-26] Step 4 "frozen base gradient
  *     contract"); nothing is ever written to them after quantisation.
- *   - No bias and no dropout on either branch ([QLoRA-26] Step 3 formula).
+ *   - No bias on either branch ([QLoRA-26] Step 3 formula); LoRA dropout on
+ *     the bypass input through the *_dropout calls below.
  */
 #ifndef QLORA_B300_H
 #define QLORA_B300_H
@@ -237,6 +238,58 @@ qlora_status qlora_linear_bwd(const qlora_nf4_weight *w, const uint16_t *x, cons
                               float alpha, const float *t_saved, void *dX, qlora_dtype dx_dtype,
                               float *dA, float *dB, void *ws, size_t ws_bytes, uint32_t flags,
                               void *stream);
+
+/* LoRA dropout on the bypass input.  [QLoRA-26] Step 5 training config and
+ * [Gemma-9] LoraConfig (lora_dropout): in training the LoRA branch takes
+ * dropout(x) = x . keep / (1 - p), keep ~ Bernoulli(1 - p) per element of
+ * x, while the base branch takes x:
+ *   y  = x . W_hat^T + s . (dropout(x) . A^T) . B^T          (s = alpha / r)
+ *   t  = dropout(x) . A^T,  u = dY . B
+ *   dX = dY . W_hat + s / (1 - p) . keep . (u . A)
+ *   dA = s / (1 - p) . u^T . (x . keep),   dB = s . dY^T . t
+ * `mask` holds the keep bits of the [M, K] input x as produced by
+ * qlora_dropout_mask (device, caller-owned, const in the calls); p is the
+ * probability it was drawn with (0 <= p < 1; 1/(1 - p) in fp32). */
+typedef struct {
+  const uint32_t *mask;
+  float p;
+} qlora_lora_dropout;
+
+/* Words (uint32) per row of the keep mask of an [M, K] input:
+ * ceil(K / 128) * 4 (a row is a whole number of 16-byte pieces).  Host only. */
+qlora_status qlora_dropout_mask_words(int64_t K, int64_t *words_per_row);
+
+/* Draw the keep mask of an [M, K] input (device, [M][words_per_row] uint32;
+ * bit b of word w of row m is element k = 32 w + b; bits past K are 0).
+ * The pages name no generator; this library uses the counter-based
+ * Philox4x64-10 (Salmon et al., SC 2011) keyed by {seed, 0}: element
+ * e = m K + k takes the 32-bit half (e mod 2, low half first) of 64-bit
+ * output e / 2 of the stream, output o being word o mod 4 of the block at
+ * counter {o / 4 + 1, 0, 0, 0}; it is kept when that uniform is at least
+ * round(p 2^32).  Requires K % 64 == 0, 0 <= p < 1, mask 16-byte aligned.
+ * Errors: QLORA_ERR_INVALID_ARG, QLORA_ERR_SHAPE, QLORA_ERR_ALIGN, QLORA_ERR_CUDA. */
+qlora_status qlora_dropout_mask(uint64_t seed, float p, int64_t M, int64_t K, uint32_t *mask,
+                                void *stream);
+
+/* qlora_linear_fwd with LoRA dropout (dropout != NULL): the same arguments
+ * and results, t_save receiving t = dropout(x) . A^T.  Both forward kernels
+ * (GEMM and decode GEMV) take it. */
+qlora_status qlora_linear_fwd_dropout(const qlora_nf4_weight *w, const uint16_t *x, int64_t M,
+                                      const uint16_t *A, const uint16_t *B, int32_t r,
+                                      float alpha, const qlora_lora_dropout *dropout, void *y,
+                                      qlora_dtype y_dtype, float *t_save, void *ws,
+                                      size_t ws_bytes, uint32_t flags, void *stream);
+
+/* qlora_linear_bwd with LoRA dropout (dropout != NULL; the mask of the
+ * forward).  dX is fp32: the dX GEMM seeds its accumulator with
+ * s / (1 - p) . u . A at every position and a second kernel takes that term
+ * back out where x was dropped. */
+qlora_status qlora_linear_bwd_dropout(const qlora_nf4_weight *w, const uint16_t *x,
+                                      const uint16_t *dY, int64_t M, const uint16_t *A,
+                                      const uint16_t *B, int32_t r, float alpha,
+                                      const qlora_lora_dropout *dropout, const float *t_saved,
+                                      float *dX, float *dA, float *dB, void *ws, size_t ws_bytes,
+                                      uint32_t flags, void *stream);
 
 /* Backward without a caller workspace, for callers that cannot allocate
  * device memory (code that runs during CUDA graph capture, hosts whose
