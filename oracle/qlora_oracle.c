@@ -53,7 +53,7 @@ static const float ORACLE_NF4[16] = {
 
 /* Quantile-formula codebook.  [QLoRA-26] Step 2 gives the construction
  *   q_i = Phi^-1(p_i),  p_i = (i - 0.5) / 16,  i = 1 .. 16
- * (garbled on the page as "pi=i−0.516"), Phi the standard normal CDF.  The
+ * (garbled in the page's extraction), Phi the standard normal CDF.  The
  * page does not say how the quantiles are brought to [-1, 1], where the
  * normalised weights live; reading: divided by the largest, q_16, so that
  * the table runs from -1 to 1 like the printed one.  The quantiles are
