@@ -98,25 +98,43 @@ __global__ void __launch_bounds__(kTWarps * 32) lora_t_decode_kernel(
     const uint16_t *a1p = A + (int64_t)(j1 < r ? j1 : 0) * K + (int64_t)(kin ? blk : 0) * 64;
     const bool ok0 = kin && j0 < r, ok1 = kin && j1 < r;
     float d[2][4] = {};
+    // every load of the lane first (plain read-only loads the compiler may
+    // schedule freely), then the MMAs
+    const uint4 z4 = make_uint4(0, 0, 0, 0);
+    uint4 ag[8], ah[8], xv[2][8];
+    uint32_t kw[2][2];
 #pragma unroll
     for (int wi = 0; wi < 8; ++wi) {
-      const uint4 ag = ldg_v4_or_zero(a0p + 8 * wi, ok0);
-      const uint4 ah = ldg_v4_or_zero(a1p + 8 * wi, ok1);
+      ag[wi] = ok0 ? __ldg(reinterpret_cast<const uint4 *>(a0p + 8 * wi)) : z4;
+      ah[wi] = ok1 ? __ldg(reinterpret_cast<const uint4 *>(a1p + 8 * wi)) : z4;
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int tok = nt * 8 + g;
+      const bool okx = kin && tok < M;
+      const uint16_t *xr = x + (int64_t)(okx ? tok : 0) * K + (int64_t)(kin ? blk : 0) * 64;
+#pragma unroll
+      for (int wi = 0; wi < 8; ++wi)
+        xv[nt][wi] = okx ? __ldg(reinterpret_cast<const uint4 *>(xr + 8 * wi)) : z4;
+      // dropout: the block's 64 columns are two keep words
+      kw[nt][0] = kw[nt][1] = 0xffffffffu;
+      if (mask && okx) {
+        kw[nt][0] = __ldg(mask + (int64_t)tok * wpr + blk * 2);
+        kw[nt][1] = __ldg(mask + (int64_t)tok * wpr + blk * 2 + 1);
+      }
+    }
+#pragma unroll
+    for (int wi = 0; wi < 8; ++wi) {
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        const int tok = nt * 8 + g;
-        const bool okx = kin && tok < M;
-        uint4 xv = ldg_v4_or_zero(
-            x + (int64_t)(okx ? tok : 0) * K + (int64_t)(kin ? blk : 0) * 64 + 8 * wi, okx);
-        if (mask && okx) {  // dropout: columns blk*64 + 8wi .. +7 are byte (wi & 3) of a word
-          const uint32_t kw = __ldg(mask + (int64_t)tok * wpr + ((blk * 64 + 8 * wi) >> 5));
-          const uint32_t byte = (kw >> (8 * (wi & 3))) & 0xffu;
+        uint4 v = xv[nt][wi];
+        if (mask) {  // columns blk*64 + 8wi .. +7: byte (wi & 3) of word wi / 4
           uint32_t mk[4];
-          keep_masks(byte, mk);
-          xv.x &= mk[0], xv.y &= mk[1], xv.z &= mk[2], xv.w &= mk[3];
+          keep_masks((kw[nt][wi >> 2] >> (8 * (wi & 3))) & 0xffu, mk);
+          v.x &= mk[0], v.y &= mk[1], v.z &= mk[2], v.w &= mk[3];
         }
-        mma_bf16(d[nt], ag.x, ah.x, ag.y, ah.y, xv.x, xv.y);
-        mma_bf16(d[nt], ag.z, ah.z, ag.w, ah.w, xv.z, xv.w);
+        mma_bf16(d[nt], ag[wi].x, ah[wi].x, ag[wi].y, ah[wi].y, v.x, v.y);
+        mma_bf16(d[nt], ag[wi].z, ah[wi].z, ag[wi].w, ah[wi].w, v.z, v.w);
       }
     }
     float *tp = tpart + (int64_t)kt * M * RP;
@@ -186,6 +204,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
   const GemvSmem SL = gemv_smem(p.M, MT, p.slice_chunks, p.tiles_max, p.RP);
   const uint32_t ring_u = base + SL.ring;
   const uint32_t xs_u = base + SL.xs;
+  const uint4 *xsm = reinterpret_cast<const uint4 *>(smem + SL.xs);  // x tile, 16-byte slots
   float *part = reinterpret_cast<float *>(smem + SL.part);
   float *tsum = reinterpret_cast<float *>(smem + SL.tsum);
   float *tfin = reinterpret_cast<float *>(smem + SL.tfin);
@@ -320,7 +339,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
       for (int nt = 0; nt < NT; ++nt) {
         const int tok = nt == 0 ? tok_lo : tok_hi;
         uint4 xv = make_uint4(0, 0, 0, 0);
-        if (tok < p.M) xv = lds_v4(xs_u + (tok * spr + xswz(tok, s_base + wi)) * 16);
+        if (tok < p.M) xv = xsm[tok * spr + xswz(tok, s_base + wi)];
         mma_bf16(acc[nt], og[0], oh[0], og[1], oh[1], xv.x, xv.y);
         mma_bf16(acc[nt], og[2], oh[2], og[3], oh[3], xv.z, xv.w);
       }

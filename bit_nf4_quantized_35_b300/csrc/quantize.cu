@@ -178,9 +178,14 @@ __global__ void __launch_bounds__(256 * kR) quantize_nf4_kernel(const void *__re
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const float xn = __fmul_rn(elem(p, e), y);
-      // nearest integer of 16 xn + 15.5, i.e. the bucket floor(16 xn + 16),
-      // in the low mantissa bits (1.5 * 2^23 puts the unit at bit 0)
-      const float u = __fmaf_rn(xn, 16.0f, 12582927.5f);
+      // bucket floor(16 xn + 16): v = 16 xn + 15.5 (one rounding, off by at
+      // most 2^-20), then v + 1.5 * 2^23 rounds to the nearest integer of v,
+      // which lands in the low mantissa bits (the unit is bit 0 there).  An
+      // element within 2^-20 of a bucket edge may take the neighbouring
+      // bucket, which gives the same index (no threshold within 2^-10 of an
+      // edge).
+      const float v = __fmaf_rn(xn, 16.0f, 15.5f);
+      const float u = __fadd_rn(v, 12582912.0f);
       const int j = __float_as_int(u) & 63;
       const float d = __fsub_rn(xn, bth_s[j]);
       risky |= fabsf(d) < kQuantBand;
