@@ -161,7 +161,7 @@ qlora_status check_weight(const qlora_nf4_weight *w, bool need_buffers) {
 // area of the fused GEMM (fp32 partial tiles and their counters, sized for
 // every cluster the device can run), which calls use when it is there.
 struct WsLayout {
-  size_t status, t, u, lb, bt, at, part, gcnt, total_min, skcnt, skpart, total;
+  size_t status, t, u, lb, bt, at, part, part_a, gcnt, gcnt_a, total_min, skcnt, skpart, total;
   int sk_clusters;
 };
 WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int r) {
@@ -180,12 +180,18 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int r) {
   off += round_up_sz((size_t)RP * N * 2, 256);
   L.at = off;
   off += round_up_sz((size_t)K * RP * 2, 256);
+  // dB and dA run in one launch: their partial sums and their column-tile
+  // counters (zero between calls) are separate, dB's first
   L.part = off;
-  const size_t pn = (size_t)skinny_splits(M, (int)N) * N, pk = (size_t)skinny_splits(M, (int)K) * K;
-  off += round_up_sz((pn > pk ? pn : pk) * RP * 4, 256);
-  L.gcnt = off;  // column-tile counters of the dA / dB kernel (zero between calls)
+  int sn = 1, sk = 1;
+  skinny_splits_pair(M, (int)N, (int)K, &sn, &sk);
+  const size_t pn = (size_t)sn * N, pk = (size_t)sk * K;
+  L.part_a = off + round_up_sz(pn * RP * 4, 256);
+  off = L.part_a + round_up_sz(pk * RP * 4, 256);
+  L.gcnt = off;
   const int tn = skinny_tiles((int)N), tk = skinny_tiles((int)K);
-  off += round_up_sz((size_t)(tn > tk ? tn : tk) * sizeof(int), 256);
+  L.gcnt_a = off + round_up_sz((size_t)tn * sizeof(int), 256);
+  off = L.gcnt_a + round_up_sz((size_t)tk * sizeof(int), 256);
   L.total_min = off;
   L.sk_clusters = gemm_cluster_bound();
   L.skcnt = off;
@@ -604,13 +610,17 @@ qlora_status linear_bwd_impl(const qlora_nf4_weight *w, const uint16_t *x, const
     e = launch_dropout_dx_fix(dmask, dwpr, M, K, lb, At, RP, static_cast<float *>(dX), nsm, s);
     if (e != cudaSuccess) return QLORA_ERR_CUDA;
   }
-  // dB = s . dY^T . t
+  // dB = s . dY^T . t and dA = s . u^T . x (with dropout s / (1 - p) . u^T . (x . keep)),
+  // one launch
   int *gcnt = reinterpret_cast<int *>(wsb + L.gcnt);
-  e = launch_skinny(dY, M, N, t, r, RP, part, gcnt, skinny_splits(M, N), sc, false, dB, s);
-  if (e != cudaSuccess) return QLORA_ERR_CUDA;
-  // dA = s . u^T . x  (with dropout s / (1 - p) . u^T . (x . keep))
-  e = launch_skinny(x, M, K, u, r, RP, part, gcnt, skinny_splits(M, K), sc * kscale, true, dA, s,
-                    dmask, dwpr);
+  int *gcnt_a = reinterpret_cast<int *>(wsb + L.gcnt_a);
+  float *part_a = reinterpret_cast<float *>(wsb + L.part_a);
+  int sn = 1, sk = 1;
+  skinny_splits_pair(M, N, K, &sn, &sk);
+  const SkinnyJob jb = skinny_job(dY, M, N, t, part, gcnt, sn, sc, false, dB, nullptr, 0);
+  const SkinnyJob ja = skinny_job(x, M, K, u, part_a, gcnt_a, sk, sc * kscale, true, dA, dmask,
+                                  dwpr);
+  e = launch_skinny2(jb, ja, M, r, RP, s);
   return cuda_status(e);
 }
 

@@ -133,11 +133,34 @@ struct MergeArgs {
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s);
 
 // Rank-r gradient contractions and layout helpers (lora_grad.cu).
-int skinny_splits(int64_t M, int C);
+int skinny_splits(int64_t M, int C, int budget = 296);
+void skinny_splits_pair(int64_t M, int N, int K, int *sn, int *sk);
 int skinny_tiles(int C);
 // dst = sc . G^T V for G [M, C] bf16, V [M, r] fp32: dst[c * r + j], or
 // dst[j * C + c] with transpose.  part: splits * C * RP floats of scratch;
 // tile_count: skinny_tiles(C) ints, zero before the call and after it.
+// One contraction dst = sc . G^T V of the dA / dB kernel (see launch_skinny).
+struct SkinnyJob {
+  const uint16_t *G;
+  int C;
+  const float *V;
+  int64_t rows_per_split;
+  int splits, tiles;
+  float *part;      // splits * C * RP floats of scratch
+  int *tile_count;  // tiles ints, zero before and after
+  float sc;
+  int transpose;
+  float *dst;
+  const uint32_t *mask;  // dropout keep bits of G or null
+  int wpr;
+};
+SkinnyJob skinny_job(const uint16_t *G, int64_t M, int C, const float *V, float *part,
+                     int *tile_count, int splits, float sc, bool transpose, float *dst,
+                     const uint32_t *mask, int wpr);
+// Two independent contractions over the same M rows in one launch (their
+// part and tile_count areas must not overlap).
+cudaError_t launch_skinny2(const SkinnyJob &j0, const SkinnyJob &j1, int64_t M, int r, int RP,
+                           cudaStream_t s);
 // With `mask` (dropout keep bits of G, wpr words per row) the dropped
 // elements of G count as zero.
 cudaError_t launch_skinny(const uint16_t *G, int64_t M, int C, const float *V, int r, int RP,

@@ -65,12 +65,30 @@ __host__ __device__ inline int grad_smem_bytes(int RPAD) {
          (2 * RPAD) * kVtPitch * 2 + 16;
 }
 
+// One launch may run two independent contractions (dB and dA of one
+// backward): CTAs [0, tiles0 * splits0) take job 0, the rest job 1; a CTA's
+// column tile and M split come from its index within its job.
 template <int RPT>  // r_pad / 8
-__global__ void __launch_bounds__(kGradThreads) lora_grad_tc_kernel(
-    const uint16_t *__restrict__ G, int64_t M, int C, const float *__restrict__ V, int r,
-    int64_t rows_per_split, float *__restrict__ part, int *__restrict__ tile_count, float sc,
-    int transpose, float *__restrict__ dst, const uint32_t *__restrict__ mask, int wpr) {
+__global__ void __launch_bounds__(kGradThreads) lora_grad_tc_kernel(const SkinnyJob j0,
+                                                                    const SkinnyJob j1,
+                                                                    int64_t M, int r) {
   pdl_wait_release();
+  const int n0 = j0.tiles * j0.splits;
+  const bool second = (int)blockIdx.x >= n0;
+  const SkinnyJob &jb = second ? j1 : j0;
+  const int local = second ? (int)blockIdx.x - n0 : (int)blockIdx.x;
+  const int tile = local % jb.tiles, split = local / jb.tiles, nsplits = jb.splits;
+  const uint16_t *__restrict__ G = jb.G;
+  const int C = jb.C;
+  const float *__restrict__ V = jb.V;
+  const int64_t rows_per_split = jb.rows_per_split;
+  float *__restrict__ part = jb.part;
+  int *__restrict__ tile_count = jb.tile_count;
+  const float sc = jb.sc;
+  const int transpose = jb.transpose;
+  float *__restrict__ dst = jb.dst;
+  const uint32_t *__restrict__ mask = jb.mask;
+  const int wpr = jb.wpr;
   constexpr int RPAD = RPT * 8;
   constexpr int NJ = 2 * RPAD;  // hi rows then lo rows
   constexpr int NTT = NJ / 8;   // n8 tiles
@@ -81,8 +99,8 @@ __global__ void __launch_bounds__(kGradThreads) lora_grad_tc_kernel(
   int *last_flag = reinterpret_cast<int *>(vt + NJ * kVtPitch);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
-  const int c0 = blockIdx.x * kGradCols;
-  const int64_t m_lo = (int64_t)blockIdx.y * rows_per_split;
+  const int c0 = tile * kGradCols;
+  const int64_t m_lo = (int64_t)split * rows_per_split;
   const int64_t m_hi = min(M, m_lo + rows_per_split);
   const int nchunks = m_hi > m_lo ? (int)((m_hi - m_lo + kGradRows - 1) / kGradRows) : 0;
 
@@ -189,7 +207,7 @@ __global__ void __launch_bounds__(kGradThreads) lora_grad_tc_kernel(
     for (int h = 0; h < 2; ++h) {
       const int c = c0 + cw + g + 8 * h;
       if (c < C) {
-        float *p = part + ((int64_t)blockIdx.y * C + c) * RPAD + j;
+        float *p = part + ((int64_t)split * C + c) * RPAD + j;
         __stcg(p, d[nt][2 * h] + d[RPT + nt][2 * h]);
         __stcg(p + 1, d[nt][2 * h + 1] + d[RPT + nt][2 * h + 1]);
       }
@@ -202,9 +220,9 @@ __global__ void __launch_bounds__(kGradThreads) lora_grad_tc_kernel(
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    const int prev = atomicAdd(tile_count + blockIdx.x, 1);
-    const bool last = prev == (int)gridDim.y - 1;
-    if (last) atomicExch(tile_count + blockIdx.x, 0);
+    const int prev = atomicAdd(tile_count + tile, 1);
+    const bool last = prev == nsplits - 1;
+    if (last) atomicExch(tile_count + tile, 0);
     __threadfence();
     *last_flag = last ? 1 : 0;
   }
@@ -223,7 +241,7 @@ __global__ void __launch_bounds__(kGradThreads) lora_grad_tc_kernel(
     const float4 *src = pbase + (int64_t)c * (RPAD / 4) + j4 / 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     int sp = 0;
-    for (; sp + 8 <= (int)gridDim.y; sp += 8) {
+    for (; sp + 8 <= nsplits; sp += 8) {
       float4 w[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) w[k] = __ldcg(src + (int64_t)(sp + k) * sp_stride);
@@ -235,7 +253,7 @@ __global__ void __launch_bounds__(kGradThreads) lora_grad_tc_kernel(
         acc.w += w[k].w;
       }
     }
-    for (; sp < (int)gridDim.y; ++sp) {
+    for (; sp < nsplits; ++sp) {
       const float4 w = __ldcg(src + (int64_t)sp * sp_stride);
       acc.x += w.x;
       acc.y += w.y;
@@ -471,21 +489,29 @@ cudaError_t launch_lora_down(const uint16_t *G, int64_t M, int C, const uint16_t
 
 // M splits per column tile: as many as keep all CTAs in one wave of two
 // CTAs per SM (148 SMs), with at least 2 chunks of 64 rows per split.
-int skinny_splits(int64_t M, int C) {
+int skinny_splits(int64_t M, int C, int budget) {
   const int coltiles = (C + kGradCols - 1) / kGradCols;
-  int64_t sp = 296 / coltiles;
+  int64_t sp = budget / (coltiles > 0 ? coltiles : 1);
   int64_t maxsp = (M + 2 * kGradRows - 1) / (2 * kGradRows);
   if (sp > maxsp) sp = maxsp;
   if (sp < 1) sp = 1;
   return (int)sp;
 }
 
+// dB (C = N) and dA (C = K) share one launch: the 296 CTAs of one wave (two
+// per SM) are shared in proportion to their column tiles, so that every CTA
+// gets about the same rows x columns.
+void skinny_splits_pair(int64_t M, int N, int K, int *sn, int *sk) {
+  const int tn = (N + kGradCols - 1) / kGradCols, tk = (K + kGradCols - 1) / kGradCols;
+  const int tot = tn + tk > 0 ? tn + tk : 1;
+  *sn = skinny_splits(M, N, 296 * tn / tot);
+  *sk = skinny_splits(M, K, 296 * tk / tot);
+}
+
 int skinny_tiles(int C) { return (C + kGradCols - 1) / kGradCols; }
 
 template <int RPT>
-static cudaError_t launch_grad(dim3 grid, const uint16_t *G, int64_t M, int C, const float *V,
-                               int r, int64_t rps, float *part, int *tile_count, float sc,
-                               bool transpose, float *dst, const uint32_t *mask, int wpr,
+static cudaError_t launch_grad(const SkinnyJob &j0, const SkinnyJob &j1, int64_t M, int r,
                                cudaStream_t s) {
   const int smem = grad_smem_bytes(RPT * 8);
   static bool set = false;
@@ -496,40 +522,59 @@ static cudaError_t launch_grad(dim3 grid, const uint16_t *G, int64_t M, int C, c
     set = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
+  cfg.gridDim = dim3((unsigned)(j0.tiles * j0.splits + j1.tiles * j1.splits), 1, 1);
   cfg.blockDim = dim3(kGradThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attrs[1] = {pdl_attr()};
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, lora_grad_tc_kernel<RPT>, G, M, C, V, r, rps, part,
-                                     tile_count, sc, transpose ? 1 : 0, dst, mask, wpr);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, lora_grad_tc_kernel<RPT>, j0, j1, M, r);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+SkinnyJob skinny_job(const uint16_t *G, int64_t M, int C, const float *V, float *part,
+                     int *tile_count, int splits, float sc, bool transpose, float *dst,
+                     const uint32_t *mask, int wpr) {
+  SkinnyJob j{};
+  j.G = G;
+  j.C = C;
+  j.V = V;
+  j.splits = C > 0 ? splits : 0;
+  j.tiles = (C + kGradCols - 1) / kGradCols;
+  j.rows_per_split = ((M + splits - 1) / splits + kGradRows - 1) / kGradRows * kGradRows;
+  j.part = part;
+  j.tile_count = tile_count;
+  j.sc = sc;
+  j.transpose = transpose ? 1 : 0;
+  j.dst = dst;
+  j.mask = mask;
+  j.wpr = wpr;
+  return j;
+}
+
+cudaError_t launch_skinny2(const SkinnyJob &j0, const SkinnyJob &j1, int64_t M, int r, int RP,
+                           cudaStream_t s) {
+  if (j0.tiles * j0.splits + j1.tiles * j1.splits == 0) return cudaSuccess;
+  switch (RP) {
+    case 16: return launch_grad<2>(j0, j1, M, r, s);
+    case 32: return launch_grad<4>(j0, j1, M, r, s);
+    case 48: return launch_grad<6>(j0, j1, M, r, s);
+    case 64: return launch_grad<8>(j0, j1, M, r, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_skinny(const uint16_t *G, int64_t M, int C, const float *V, int r, int RP,
                           float *part, int *tile_count, int splits, float sc, bool transpose,
                           float *dst, cudaStream_t s, const uint32_t *mask, int wpr) {
   if (C == 0) return cudaSuccess;
-  const int64_t rps = ((M + splits - 1) / splits + kGradRows - 1) / kGradRows * kGradRows;
-  dim3 grid((C + kGradCols - 1) / kGradCols, splits);
-  switch (RP) {
-    case 16:
-      return launch_grad<2>(grid, G, M, C, V, r, rps, part, tile_count, sc, transpose, dst, mask,
-                            wpr, s);
-    case 32:
-      return launch_grad<4>(grid, G, M, C, V, r, rps, part, tile_count, sc, transpose, dst, mask,
-                            wpr, s);
-    case 48:
-      return launch_grad<6>(grid, G, M, C, V, r, rps, part, tile_count, sc, transpose, dst, mask,
-                            wpr, s);
-    case 64:
-      return launch_grad<8>(grid, G, M, C, V, r, rps, part, tile_count, sc, transpose, dst, mask,
-                            wpr, s);
-    default: return cudaErrorInvalidValue;
-  }
+  const SkinnyJob j0 = skinny_job(G, M, C, V, part, tile_count, splits, sc, transpose, dst, mask,
+                                  wpr);
+  SkinnyJob none{};
+  none.tiles = 1;
+  return launch_skinny2(j0, none, M, r, RP, s);
 }
 
 cudaError_t launch_transposes(const uint16_t *A, const uint16_t *B, int N, int K, int r, int RP,
