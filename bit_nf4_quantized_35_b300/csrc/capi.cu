@@ -336,7 +336,7 @@ qlora_status qlora_quantize_nf4(const void *W, qlora_dtype w_dtype, const qlora_
   return cuda_status(launch_quantize(W, w_dtype == QLORA_BF16, out->block, nblocks, out->group,
                                      out->packed,
                                      out->absmax_code, out->absmax_f32, out->scale2,
-                                     nonfinite_flag, tables(out->codebook).th,
+                                     nonfinite_flag, tables(out->codebook).th, num_sms_current(),
                                      static_cast<cudaStream_t>(stream)));
 }
 

@@ -111,7 +111,8 @@ cudaError_t launch_lora_down(const uint16_t *G, int64_t M, int C, const uint16_t
 // Quantise / dequantise (quantize.cu).
 cudaError_t launch_quantize(const void *W, bool bf16_in, int block, int64_t nblocks, int group,
                             uint8_t *packed, int8_t *codes, float *absf, float *scale2,
-                            int *nonfinite_flag, const float th[15], cudaStream_t s);
+                            int *nonfinite_flag, const float th[15], int num_sms,
+                            cudaStream_t s);
 cudaError_t launch_dequant(const uint8_t *packed, const int8_t *codes, const float *absf,
                            const float *scale2, int group, int block, int64_t nblocks,
                            uint16_t *out, const Codebook &cb, int num_sms, cudaStream_t s);

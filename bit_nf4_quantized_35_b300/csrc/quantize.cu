@@ -64,9 +64,22 @@ __device__ __forceinline__ constexpr int nib_shift(int e) { return 8 * (e >> 1) 
 // 2^-20 both lie on the same side of the threshold.
 constexpr float kQuantBand = 9.5367431640625e-07f;  // 2^-20
 
-// kR = block / 64: a CTA of 256 kR threads quantises 256 consecutive blocks
-// (one double-quantisation group of 256, or several smaller groups); the
-// 8 kR lanes of a block reduce its maximum with shuffles.
+// kR = block / 64.  A CTA of 256 kR threads takes groups of 256 consecutive
+// blocks (one double-quantisation group of 256, or several smaller groups):
+// group g, g + gridDim.x, ... (persistent grid).  The 8 kR lanes of a block
+// reduce its maximum with shuffles.  Each thread streams its own 16-byte
+// pieces of the next groups through a kQStages-deep cp.async ring in shared
+// memory (it reads back only what it copied, so the ring needs no block
+// barrier), so the loads of later groups are in flight while a group is
+// computed.
+constexpr int kQStages = 3;
+template <bool kBf16In>
+__host__ __device__ constexpr int quant_pieces() { return kBf16In ? 8 : 16; }  // 16 B per thread per group
+template <bool kBf16In, int kR>
+__host__ __device__ constexpr int quant_smem_bytes() {
+  return kQStages * quant_pieces<kBf16In>() * 256 * kR * 16;
+}
+
 template <bool kBf16In, int kR>
 __global__ void __launch_bounds__(256 * kR) quantize_nf4_kernel(const void *__restrict__ W,
                                                            int64_t nblocks, int group,
@@ -76,6 +89,7 @@ __global__ void __launch_bounds__(256 * kR) quantize_nf4_kernel(const void *__re
                                                            float *__restrict__ scale2,
                                                            int *__restrict__ nonfinite_flag,
                                                            const QuantTables tab) {
+  extern __shared__ __align__(16) uint4 qring[];  // [stage][piece][thread]
   __shared__ float th_s[16];
   __shared__ float bth_s[64];
   __shared__ int bbase_s[64];
@@ -83,159 +97,184 @@ __global__ void __launch_bounds__(256 * kR) quantize_nf4_kernel(const void *__re
   __shared__ float wmax_s[8];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sub = lane >> 3, li = lane & 7;
+  const int nthr = 256 * kR;
   const int64_t nchunks = nblocks * kR;  // 64-element chunks
+  const int64_t ngroups = (nblocks + 255) / 256;
+  constexpr int kP = quant_pieces<kBf16In>();
   if (tid < 16) th_s[tid] = tab.th[tid];
   if (tid < 64) {
     bth_s[tid] = tab.bth[tid];
     bbase_s[tid] = tab.bbase[tid];
   }
-
-  const int64_t blk0 = (int64_t)blockIdx.x * 256;  // first block of the CTA
-  const int64_t ch0 = blk0 * kR;                   // its first 64-element chunk
-
-  // Issue every load of this thread first (8 passes x 8 elements), kept raw.
-  // Pass p, warp w, lane group `sub` covers chunk p * 32 kR + 4 w + sub.
-  constexpr int kWords = kBf16In ? 4 : 8;  // 32-bit words per pass
-  uint32_t raw[8][kWords];
-  bool inb[8];
+  // Pass p, warp w, lane group `sub` covers chunk p * 32 kR + 4 w + sub of a
+  // group; lane li the 8 elements li * 8 .. li * 8 + 7 of that chunk.
+  auto issue = [&](int64_t grp, int stage) {
+    if (grp < ngroups) {
+      const int64_t ch0 = grp * 256 * kR;
 #pragma unroll
-  for (int p = 0; p < 8; ++p) {
-    const int c = p * 32 * kR + warp * 4 + sub;
-    const int64_t gb = ch0 + c;  // global chunk
-    inb[p] = gb < nchunks;
-    if (kBf16In) {
-      uint4 u = make_uint4(0, 0, 0, 0);
-      if (inb[p])
-        u = ldg_nc_v4(reinterpret_cast<const uint16_t *>(W) + gb * kBlock + li * 8);
-      raw[p][0] = u.x, raw[p][1] = u.y, raw[p][2] = u.z, raw[p][3] = u.w;
-    } else {
-      uint4 u0 = make_uint4(0, 0, 0, 0), u1 = u0;
-      if (inb[p]) {
-        const float *src = reinterpret_cast<const float *>(W) + gb * kBlock + li * 8;
-        u0 = ldg_nc_v4(src);
-        u1 = ldg_nc_v4(src + 4);
+      for (int p = 0; p < 8; ++p) {
+        const int64_t gb = ch0 + p * 32 * kR + warp * 4 + sub;
+        const bool ok = gb < nchunks;
+        if (kBf16In) {
+          const uint16_t *src = reinterpret_cast<const uint16_t *>(W) + (ok ? gb * kBlock + li * 8 : 0);
+          cp_async16(smem_u32(&qring[(stage * kP + p) * nthr + tid]), src, ok ? 16u : 0u);
+        } else {
+          const float *src = reinterpret_cast<const float *>(W) + (ok ? gb * kBlock + li * 8 : 0);
+          cp_async16(smem_u32(&qring[(stage * kP + 2 * p) * nthr + tid]), src, ok ? 16u : 0u);
+          cp_async16(smem_u32(&qring[(stage * kP + 2 * p + 1) * nthr + tid]), src + 4,
+                     ok ? 16u : 0u);
+        }
       }
-      raw[p][0] = u0.x, raw[p][1] = u0.y, raw[p][2] = u0.z, raw[p][3] = u0.w;
-      raw[p][4] = u1.x, raw[p][5] = u1.y, raw[p][6] = u1.z, raw[p][7] = u1.w;
     }
-  }
+    cp_async_commit();
+  };
+  const int64_t G = gridDim.x;
+  for (int s0 = 0; s0 < kQStages - 1; ++s0) issue(blockIdx.x + s0 * G, s0);
   __syncthreads();  // tables visible
 
-  auto elem = [&](int p, int e) -> float {
-    if (kBf16In) return (e & 1) ? bf16_hi(raw[p][e >> 1]) : bf16_lo(raw[p][e >> 1]);
-    return __uint_as_float(raw[p][e]);
-  };
-
   int nonfinite = 0;
+  int it = 0;
+  for (int64_t grp = blockIdx.x; grp < ngroups; grp += G, ++it) {
+    const int64_t blk0 = grp * 256;   // first block of the group
+    const int64_t ch0 = blk0 * kR;    // its first 64-element chunk
+    cp_async_wait<kQStages - 2>();    // this thread's pieces of group grp have landed
+    issue(grp + (kQStages - 1) * G, (it + kQStages - 1) % kQStages);  // the stage read last time
+    const int stage = it % kQStages;
+    constexpr int kWords = kBf16In ? 4 : 8;  // 32-bit words per pass
+    uint32_t raw[8][kWords];
+    bool inb[8];
 #pragma unroll
-  for (int p = 0; p < 8; ++p) {
-    const int c = p * 32 * kR + warp * 4 + sub;
-    // Block absmax as the largest magnitude bit pattern (the order of
-    // non-negative floats); a pattern >= 0x7f800000 means an infinite or NaN
-    // element, and the maximum is then taken over the finite ones only.
-    uint32_t mb;
-    if (kBf16In) {
-      uint32_t m2 = 0;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) m2 = __vmaxu2(m2, raw[p][q] & 0x7fff7fffu);
-      mb = max(m2 << 16, m2 & 0xffff0000u);
-    } else {
-      mb = 0;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) mb = max(mb, raw[p][q] & 0x7fffffffu);
+    for (int p = 0; p < 8; ++p) {
+      inb[p] = ch0 + p * 32 * kR + warp * 4 + sub < nchunks;
+      if (kBf16In) {
+        const uint4 u = qring[(stage * kP + p) * nthr + tid];
+        raw[p][0] = u.x, raw[p][1] = u.y, raw[p][2] = u.z, raw[p][3] = u.w;
+      } else {
+        const uint4 u0 = qring[(stage * kP + 2 * p) * nthr + tid];
+        const uint4 u1 = qring[(stage * kP + 2 * p + 1) * nthr + tid];
+        raw[p][0] = u0.x, raw[p][1] = u0.y, raw[p][2] = u0.z, raw[p][3] = u0.w;
+        raw[p][4] = u1.x, raw[p][5] = u1.y, raw[p][6] = u1.z, raw[p][7] = u1.w;
+      }
     }
-    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
-    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
-    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
-    if (kR == 2) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
-    const bool nf = mb >= 0x7f800000u;
-    if (__any_sync(0xffffffffu, nf)) {  // rare: some block of the warp is not finite
-      uint32_t mf = 0;
+
+    auto elem = [&](int p, int e) -> float {
+      if (kBf16In) return (e & 1) ? bf16_hi(raw[p][e >> 1]) : bf16_lo(raw[p][e >> 1]);
+      return __uint_as_float(raw[p][e]);
+    };
+
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      const int c = p * 32 * kR + warp * 4 + sub;
+      // Block absmax as the largest magnitude bit pattern (the order of
+      // non-negative floats); a pattern >= 0x7f800000 means an infinite or NaN
+      // element, and the maximum is then taken over the finite ones only.
+      uint32_t mb;
+      if (kBf16In) {
+        uint32_t m2 = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) m2 = __vmaxu2(m2, raw[p][q] & 0x7fff7fffu);
+        mb = max(m2 << 16, m2 & 0xffff0000u);
+      } else {
+        mb = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) mb = max(mb, raw[p][q] & 0x7fffffffu);
+      }
+      mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+      mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+      mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
+      if (kR == 2) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
+      const bool nf = mb >= 0x7f800000u;
+      if (__any_sync(0xffffffffu, nf)) {  // rare: some block of the warp is not finite
+        uint32_t mf = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint32_t bits = __float_as_uint(elem(p, e)) & 0x7fffffffu;
+          if (bits < 0x7f800000u) mf = max(mf, bits);
+        }
+        mf = max(mf, __shfl_xor_sync(0xffffffffu, mf, 1));
+        mf = max(mf, __shfl_xor_sync(0xffffffffu, mf, 2));
+        mf = max(mf, __shfl_xor_sync(0xffffffffu, mf, 4));
+        if (kR == 2) mf = max(mf, __shfl_xor_sync(0xffffffffu, mf, 8));
+        if (nf) {
+          mb = mf;
+          ++nonfinite;
+        }
+      }
+      const float amax = __uint_as_float(mb);
+      if (li == 0 && (sub % kR) == 0) amax_s[c / kR] = amax;  // 0 for blocks past the end
+      // Fast path: xn' = w . RN(1/a) and the bucket tables; an element whose
+      // xn' lies within the band of a threshold is decided again with the
+      // IEEE quotient.  Block constants outside [2^-126, 2^126] (reciprocal
+      // out of the normal range) take the IEEE path for every element.
+      const bool fast = !tab.exact_only && amax >= 1.17549435e-38f && amax <= 8.50705917e+37f;
+      const float y = __frcp_rn(amax);
+      uint32_t word = 0;
+      bool risky = false;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const uint32_t bits = __float_as_uint(elem(p, e)) & 0x7fffffffu;
-        if (bits < 0x7f800000u) mf = max(mf, bits);
+        const float xn = __fmul_rn(elem(p, e), y);
+        // bucket floor(16 xn + 16): v = 16 xn + 15.5 (one rounding, off by at
+        // most 2^-20), then v + 1.5 * 2^23 rounds to the nearest integer of v,
+        // which lands in the low mantissa bits (the unit is bit 0 there).  An
+        // element within 2^-20 of a bucket edge may take the neighbouring
+        // bucket, which gives the same index (no threshold within 2^-10 of an
+        // edge).
+        const float v = __fmaf_rn(xn, 16.0f, 15.5f);
+        const float u = __fadd_rn(v, 12582912.0f);
+        const int j = __float_as_int(u) & 63;
+        const float d = __fsub_rn(xn, bth_s[j]);
+        risky |= fabsf(d) < kQuantBand;
+        const uint32_t q = (uint32_t)(bbase_s[j] + (d >= 0.0f ? 1 : 0));
+        word |= q << nib_shift(e);
       }
-      mf = max(mf, __shfl_xor_sync(0xffffffffu, mf, 1));
-      mf = max(mf, __shfl_xor_sync(0xffffffffu, mf, 2));
-      mf = max(mf, __shfl_xor_sync(0xffffffffu, mf, 4));
-      if (kR == 2) mf = max(mf, __shfl_xor_sync(0xffffffffu, mf, 8));
-      if (nf) {
-        mb = mf;
-        ++nonfinite;
-      }
-    }
-    const float amax = __uint_as_float(mb);
-    if (li == 0 && (sub % kR) == 0) amax_s[c / kR] = amax;  // 0 for blocks past the end
-    // Fast path: xn' = w . RN(1/a) and the bucket tables; an element whose
-    // xn' lies within the band of a threshold is decided again with the
-    // IEEE quotient.  Block constants outside [2^-126, 2^126] (reciprocal
-    // out of the normal range) take the IEEE path for every element.
-    const bool fast = !tab.exact_only && amax >= 1.17549435e-38f && amax <= 8.50705917e+37f;
-    const float y = __frcp_rn(amax);
-    uint32_t word = 0;
-    bool risky = false;
+      if (amax == 0.0f) {
+        word = 0x77777777u;  // every index is the exact-zero codepoint
+      } else if (__any_sync(0xffffffffu, risky || !fast)) {
+        if (risky || !fast) {
+          word = 0;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float xn = __fmul_rn(elem(p, e), y);
-      // bucket floor(16 xn + 16): v = 16 xn + 15.5 (one rounding, off by at
-      // most 2^-20), then v + 1.5 * 2^23 rounds to the nearest integer of v,
-      // which lands in the low mantissa bits (the unit is bit 0 there).  An
-      // element within 2^-20 of a bucket edge may take the neighbouring
-      // bucket, which gives the same index (no threshold within 2^-10 of an
-      // edge).
-      const float v = __fmaf_rn(xn, 16.0f, 15.5f);
-      const float u = __fadd_rn(v, 12582912.0f);
-      const int j = __float_as_int(u) & 63;
-      const float d = __fsub_rn(xn, bth_s[j]);
-      risky |= fabsf(d) < kQuantBand;
-      const uint32_t q = (uint32_t)(bbase_s[j] + (d >= 0.0f ? 1 : 0));
-      word |= q << nib_shift(e);
+          for (int e = 0; e < 8; ++e)
+            word |= (uint32_t)nf4_index(__fdiv_rn(elem(p, e), amax), th_s) << nib_shift(e);
+        }
+      }
+      if (inb[p]) *reinterpret_cast<uint32_t *>(packed + (ch0 + c) * 32 + li * 4) = word;
     }
-    if (amax == 0.0f) {
-      word = 0x77777777u;  // every index is the exact-zero codepoint
-    } else if (__any_sync(0xffffffffu, risky || !fast)) {
-      if (risky || !fast) {
-        word = 0;
+    __syncthreads();  // amax_s complete
+
+    // Second level: one scale per `group` consecutive block constants, by
+    // threads 0..255 (warps 0..7); the others only take the block barriers.
+    const bool dq = tid < 256;
+    const float a = dq ? amax_s[tid] : 0.0f;
+    const int64_t gb = blk0 + tid;
+    if (group == 0) {
+      if (dq && gb < nblocks) absf[gb] = a;
+    } else {
+      float m = a;
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          word |= (uint32_t)nf4_index(__fdiv_rn(elem(p, e), amax), th_s) << nib_shift(e);
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0 && dq) wmax_s[warp] = m;
+      __syncthreads();
+      if (dq) {
+        const int wpg = group >> 5;  // warps per group (group >= 32)
+        const int w0 = (warp / wpg) * wpg;
+        float gmax = 0.0f;
+        for (int w = w0; w < w0 + wpg; ++w) gmax = fmaxf(gmax, wmax_s[w]);
+        const float s2 = __fdiv_rn(gmax, 127.0f);
+        float c = 0.0f;
+        if (s2 != 0.0f) c = rintf(__fdiv_rn(a, s2));
+        c = fminf(fmaxf(c, -127.0f), 127.0f);
+        if (gb < nblocks) {
+          codes[gb] = (int8_t)(int)c;
+          if ((tid % group) == 0) scale2[gb / group] = s2;
+        }
       }
     }
-    if (inb[p]) *reinterpret_cast<uint32_t *>(packed + (ch0 + c) * 32 + li * 4) = word;
+    __syncthreads();  // amax_s and wmax_s are free for the next group
   }
+  cp_async_wait<0>();
   if (nonfinite_flag) {
     nonfinite = __any_sync(0xffffffffu, nonfinite != 0);
     if (nonfinite && lane == 0) atomicExch(nonfinite_flag, 1);
-  }
-  __syncthreads();
-
-  // Second level: one scale per `group` consecutive block constants, by
-  // threads 0..255 (warps 0..7); the others only take the block barrier.
-  const bool dq = tid < 256;
-  const float a = dq ? amax_s[tid] : 0.0f;
-  const int64_t gb = blk0 + tid;
-  if (group == 0) {
-    if (dq && gb < nblocks) absf[gb] = a;
-    return;
-  }
-  float m = a;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if (lane == 0 && dq) wmax_s[warp] = m;
-  __syncthreads();
-  if (!dq) return;
-  const int wpg = group >> 5;  // warps per group (group >= 32)
-  const int w0 = (warp / wpg) * wpg;
-  float gmax = 0.0f;
-  for (int w = w0; w < w0 + wpg; ++w) gmax = fmaxf(gmax, wmax_s[w]);
-  const float s2 = __fdiv_rn(gmax, 127.0f);
-  float c = 0.0f;
-  if (s2 != 0.0f) c = rintf(__fdiv_rn(a, s2));
-  c = fminf(fmaxf(c, -127.0f), 127.0f);
-  if (gb < nblocks) {
-    codes[gb] = (int8_t)(int)c;
-    if ((tid % group) == 0) scale2[gb / group] = s2;
   }
 }
 
@@ -301,32 +340,49 @@ static void build_quant_tables(const float th[15], QuantTables &t) {
   }
 }
 
+template <bool kBf16In, int kR>
+static cudaError_t launch_q(const void *W, int64_t nblocks, int group, uint8_t *packed,
+                            int8_t *codes, float *absf, float *scale2, int *nonfinite_flag,
+                            const QuantTables &tab, int num_sms, cudaStream_t s) {
+  constexpr int smem = quant_smem_bytes<kBf16In, kR>();
+  static bool set = false;
+  if (!set) {
+    cudaError_t e = cudaFuncSetAttribute(quantize_nf4_kernel<kBf16In, kR>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    set = true;
+  }
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &per_sm, quantize_nf4_kernel<kBf16In, kR>, 256 * kR, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  const int64_t ngroups = (nblocks + 255) / 256;
+  int64_t grid = (int64_t)num_sms * per_sm;
+  if (grid > ngroups) grid = ngroups;
+  quantize_nf4_kernel<kBf16In, kR><<<(unsigned)grid, 256 * kR, smem, s>>>(
+      W, nblocks, group, packed, codes, absf, scale2, nonfinite_flag, tab);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_quantize(const void *W, bool bf16_in, int block, int64_t nblocks, int group,
                             uint8_t *packed, int8_t *codes, float *absf, float *scale2,
-                            int *nonfinite_flag, const float th[15], cudaStream_t s) {
+                            int *nonfinite_flag, const float th[15], int num_sms,
+                            cudaStream_t s) {
   if (nblocks == 0) return cudaSuccess;
   QuantTables tab;
   build_quant_tables(th, tab);
-  const int64_t grid = (nblocks + 255) / 256;
-  const unsigned g = (unsigned)grid;
-  if (block == 64) {
-    if (bf16_in)
-      quantize_nf4_kernel<true, 1><<<g, 256, 0, s>>>(W, nblocks, group, packed, codes, absf,
-                                                      scale2, nonfinite_flag, tab);
-    else
-      quantize_nf4_kernel<false, 1><<<g, 256, 0, s>>>(W, nblocks, group, packed, codes, absf,
-                                                       scale2, nonfinite_flag, tab);
-  } else if (block == 128) {
-    if (bf16_in)
-      quantize_nf4_kernel<true, 2><<<g, 512, 0, s>>>(W, nblocks, group, packed, codes, absf,
-                                                      scale2, nonfinite_flag, tab);
-    else
-      quantize_nf4_kernel<false, 2><<<g, 512, 0, s>>>(W, nblocks, group, packed, codes, absf,
-                                                       scale2, nonfinite_flag, tab);
-  } else {
-    return cudaErrorInvalidValue;
-  }
-  return cudaGetLastError();
+  if (block == 64)
+    return bf16_in ? launch_q<true, 1>(W, nblocks, group, packed, codes, absf, scale2,
+                                       nonfinite_flag, tab, num_sms, s)
+                   : launch_q<false, 1>(W, nblocks, group, packed, codes, absf, scale2,
+                                        nonfinite_flag, tab, num_sms, s);
+  if (block == 128)
+    return bf16_in ? launch_q<true, 2>(W, nblocks, group, packed, codes, absf, scale2,
+                                       nonfinite_flag, tab, num_sms, s)
+                   : launch_q<false, 2>(W, nblocks, group, packed, codes, absf, scale2,
+                                        nonfinite_flag, tab, num_sms, s);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_dequant(const uint8_t *packed, const int8_t *codes, const float *absf,
