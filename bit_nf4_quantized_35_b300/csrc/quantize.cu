@@ -30,15 +30,17 @@ namespace qlora {
 // Decision tables of the nearest-codepoint rule (built on the host from the
 // 15 thresholds; see launch_quantize):
 //   th[k]     the thresholds: index = #{k : x >= th[k]} (th[15] = 2)
-//   bth[j]    for the 1/16-wide bucket j of [-1, 1] (x in [-1 + j/16,
-//             -1 + (j+1)/16)), the one threshold inside it, or 2 when none
-//   bbase[j]  #{k : th[k] < -1 + j/16}
-// Entries 32 and 63 repeat buckets 31 and 0: the bucket arithmetic below
-// yields them for x just above 1 and just below -1.
+//   bth[j]    for the 1/16-wide bucket j of [-1, 1] (x in [e_j, e_j + 1/16),
+//             e_j = -1 + j/16, or -1 + (j - 1/2)/16 with the shifted grid),
+//             the one threshold inside it, or 2 when none
+//   bbase[j]  #{k : th[k] < e_j}
+// Entries past the last bucket repeat it and entry 63 repeats bucket 0: the
+// bucket arithmetic below yields them for x just above 1 and just below -1.
 struct QuantTables {
   float th[16];
   float bth[64];
   int bbase[64];
+  float bias;      // 15.5: buckets start at -1 + j/16; 16: at -1 + (j - 1/2)/16
   int exact_only;  // 1: the tables do not fit the bucket rule; divide every element
 };
 
@@ -219,7 +221,7 @@ __global__ void __launch_bounds__(256 * kR) quantize_nf4_kernel(const void *__re
         // element within 2^-20 of a bucket edge may take the neighbouring
         // bucket, which gives the same index (no threshold within 2^-10 of an
         // edge).
-        const float v = __fmaf_rn(xn, 16.0f, 15.5f);
+        const float v = __fmaf_rn(xn, 16.0f, tab.bias);
         const float u = __fadd_rn(v, 12582912.0f);
         const int j = __float_as_int(u) & 63;
         const float d = __fsub_rn(xn, bth_s[j]);
@@ -313,12 +315,15 @@ __global__ void __launch_bounds__(256) dequant_nf4_kernel(const uint8_t *__restr
 // and no threshold lies within 2^-10 of a bucket edge (an element whose
 // bucket is computed from the reciprocal-based value, up to 2^-22 off, then
 // still gets the bucket's answer); otherwise every element is divided.
-static void build_quant_tables(const float th[15], QuantTables &t) {
+static bool fill_quant_tables(const float th[15], double shift, QuantTables &t) {
   for (int i = 0; i < 15; ++i) t.th[i] = th[i];
   t.th[15] = 2.0f;
-  t.exact_only = 0;
-  for (int j = 0; j < 32; ++j) {
-    const double lo = -1.0 + j / 16.0, hi = -1.0 + (j + 1) / 16.0;
+  t.bias = (float)(15.5 + shift);  // bucket j = floor(16 x + 16 + shift)
+  bool ok = true;
+  const int nb = shift > 0 ? 33 : 32;  // buckets covering [-1, 1]
+  for (int j = 0; j < 64; ++j) {
+    const int jj = j < nb ? j : (j == 63 ? 0 : nb - 1);
+    const double lo = -1.0 + (jj - shift) / 16.0, hi = lo + 1.0 / 16.0;
     int base = 0, inside = 0;
     float th_in = 2.0f;
     for (int k = 0; k < 15; ++k) {
@@ -328,16 +333,28 @@ static void build_quant_tables(const float th[15], QuantTables &t) {
         ++inside;
         th_in = th[k];
       }
-      if (std::fabs(v - lo) < 1.0 / 1024 || std::fabs(v - hi) < 1.0 / 1024) t.exact_only = 1;
+      if (std::fabs(v - lo) < 1.0 / 1024 || std::fabs(v - hi) < 1.0 / 1024) ok = false;
     }
-    if (inside > 1) t.exact_only = 1;
+    if (inside > 1) ok = false;
     t.bth[j] = th_in;
     t.bbase[j] = base;
   }
-  for (int j = 32; j < 64; ++j) {  // never produced, except 32 (x just above 1) and 63 (just below -1)
-    t.bth[j] = j == 63 ? t.bth[0] : t.bth[31];
-    t.bbase[j] = j == 63 ? t.bbase[0] : t.bbase[31];
-  }
+  return ok;
+}
+
+// Bucket tables for the fast decision path, from the 15 sorted thresholds.
+// Valid when every 1/16-wide bucket holds at most one threshold and no
+// threshold lies within 2^-10 of a bucket edge (an element whose bucket is
+// computed from the reciprocal-based value, up to 2^-22 off, then still gets
+// the bucket's answer).  The grid starting at -1 is tried first, then the one
+// shifted by half a bucket (the quantile table has a threshold at 0); when
+// neither fits, every element is divided.
+static void build_quant_tables(const float th[15], QuantTables &t) {
+  t.exact_only = 0;
+  if (fill_quant_tables(th, 0.0, t)) return;
+  if (fill_quant_tables(th, 0.5, t)) return;
+  fill_quant_tables(th, 0.0, t);
+  t.exact_only = 1;
 }
 
 template <bool kBf16In, int kR>
