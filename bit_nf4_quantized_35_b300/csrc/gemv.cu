@@ -233,17 +233,28 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
   __syncthreads();
 
   // ---- 1. the first units of every warp's ring (the weights were written
-  // before the t kernel, which has passed its own dependency wait)
-  auto issue = [&](int u, int slot) {
-    const int tile = t0 + u / Cc, chunk = c0 + u % Cc;
+  // before the t kernel, which has passed its own dependency wait).  Units
+  // are walked with (tile, chunk) cursors, chunk fastest.
+  auto issue = [&](int tile, int chunk, int slot) {
     const uint32_t bar = bars_u + (warp * kGemvDepth + slot) * 8;
     mbar_arrive_expect_tx(bar, kUnitBytes);
-    tma_load_2d(ring_u + (warp * kGemvDepth + slot) * kUnitBytes, &tmW, bar, chunk * 128,
-                tile * 16);
+    tma_load_2d(ring_u + (warp * kGemvDepth + slot) * kUnitBytes, &tmW, bar,
+                (c0 + chunk) * 128, (t0 + tile) * 16);
+  };
+  const int ut0 = Cc > 0 ? u0 / Cc : 0, uc0 = Cc > 0 ? u0 - ut0 * Cc : 0;  // first unit
+  int it_t = ut0, it_c = uc0;  // issue cursor
+  auto step = [&](int &t, int &c) {
+    if (++c == Cc) {
+      c = 0;
+      ++t;
+    }
   };
   if (lane == 0) {
     tma_prefetch_desc(&tmW);
-    for (int i = 0; i < kGemvDepth && u0 + i < u1; ++i) issue(u0 + i, i);
+    for (int i = 0; i < kGemvDepth && u0 + i < u1; ++i) {
+      issue(it_t, it_c, i);
+      step(it_t, it_c);
+    }
   }
 
   // ---- 2. x slice -> shared memory (tokens < M; zero past K), swizzled
@@ -287,27 +298,36 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
     ++seg;
   };
   // a_hat of the lane's two rows, loaded one unit ahead
-  auto ahat_unit = [&](int u, float &a, float &b) {
-    const int tile = t0 + u / Cc, chunk = c0 + u % Cc;
-    const int kc = chunk * 4 + tq;
-    a = ahat_of(tile * 16 + g, kc);
-    b = ahat_of(tile * 16 + g + 8, kc);
+  auto ahat_unit = [&](int tile, int chunk, float &a, float &b) {
+    const int kc = (c0 + chunk) * 4 + tq;
+    a = ahat_of((t0 + tile) * 16 + g, kc);
+    b = ahat_of((t0 + tile) * 16 + g + 8, kc);
   };
+  // x slot of (token, block tq, positions 8 wi .. 8 wi + 7) of chunk c:
+  // row tok, slot c * 32 + tq * 8 + (wi ^ x3) with x3 = tq | (tok & 1) << 2
+  // (the swizzle of xswz with (s >> 3) & 3 = tq); per-lane offsets of wi.
+  int xoff[8];
+#pragma unroll
+  for (int wi = 0; wi < 8; ++wi) xoff[wi] = wi ^ (tq | ((g & 1) << 2));
+  const bool xv_lo = tok_lo < p.M, xv_hi = tok_hi < p.M;
+  const uint4 *xr_lo = xsm + (xv_lo ? tok_lo : 0) * spr + tq * 8;
+  const uint4 *xr_hi = xsm + (xv_hi ? tok_hi : 0) * spr + tq * 8;
   float ah_g = 0.f, ah_h = 0.f;
-  if (u0 < u1) ahat_unit(u0, ah_g, ah_h);
+  int tile = ut0, chunk = uc0;  // consume cursor
+  if (u0 < u1) ahat_unit(tile, chunk, ah_g, ah_h);
   int done = 0;  // units consumed
-  for (int u = u0; u < u1; ++u) {
-    const int i = u - u0;
+  for (int i = 0; i < u1 - u0; ++i) {
     const int slot = i % kGemvDepth;
-    const int tile = u / Cc, chunk = u % Cc;
     if (tile != cur) {
       if (cur >= 0) flush(cur);
       cur = tile;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
     }
+    int ntile = tile, nchunk = chunk;
+    step(ntile, nchunk);
     float nah_g = 0.f, nah_h = 0.f;
-    if (u + 1 < u1) ahat_unit(u + 1, nah_g, nah_h);
+    if (i + 1 < u1 - u0) ahat_unit(ntile, nchunk, nah_g, nah_h);
     const uint32_t bar = bars_u + (warp * kGemvDepth + slot) * 8;
     if (!mbar_wait_bounded(bar, (uint32_t)(i / kGemvDepth) & 1u, err_u, p.status)) {
       ok = false;
@@ -321,15 +341,15 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
     const uint4 v1 = lds_v4(sb + (g + 8) * 128 + (((2 * tq + 1) ^ g) << 4));
     ++done;
     __syncwarp();
-    if (lane == 0 && u + kGemvDepth < u1) {
+    if (lane == 0 && i + kGemvDepth < u1 - u0) {
       fence_proxy_async_smem();
-      issue(u + kGemvDepth, slot);
+      issue(it_t, it_c, slot);
+      step(it_t, it_c);
     }
     const Nf4Table tg = make_table(ah_g, p.cb), th = make_table(ah_h, p.cb);
     const uint32_t wg[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
     const uint32_t wh[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    // x slot of (token, block tq, positions 8 wi .. 8 wi + 7)
-    const int s_base = chunk * 32 + tq * 8;
+    const uint4 *xlo = xr_lo + chunk * 32, *xhi = xr_hi + chunk * 32;
 #pragma unroll
     for (int wi = 0; wi < 8; ++wi) {
       uint32_t og[4], oh[4];
@@ -337,15 +357,16 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
       lookup8(th, wh[wi], oh);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const int tok = nt == 0 ? tok_lo : tok_hi;
-        uint4 xv = make_uint4(0, 0, 0, 0);
-        if (tok < p.M) xv = xsm[tok * spr + xswz(tok, s_base + wi)];
+        const bool v = nt == 0 ? xv_lo : xv_hi;
+        const uint4 xv = v ? (nt == 0 ? xlo : xhi)[xoff[wi]] : make_uint4(0, 0, 0, 0);
         mma_bf16(acc[nt], og[0], oh[0], og[1], oh[1], xv.x, xv.y);
         mma_bf16(acc[nt], og[2], oh[2], og[3], oh[3], xv.z, xv.w);
       }
     }
     ah_g = nah_g;
     ah_h = nah_h;
+    tile = ntile;
+    chunk = nchunk;
   }
   if (ok && cur >= 0) flush(cur);
   if (!ok && lane == 0) {
@@ -420,13 +441,59 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
 }
 
 // ------------------------------------------------------------ launchers
-// Cluster size S (K slices) and the split: S minimises the 2 KB units per SM,
-// ceil(tiles / clusters) x ceil(chunks / S), among the S whose shared memory
-// fits; ties go to the smaller S.
+// Largest dynamic shared memory of a GEMV CTA; set once on both instances so
+// that the occupancy query and the launch see the same limit.
+static constexpr int kGemvSmemMax = 232448;
+
+static cudaError_t gemv_smem_attr() {
+  static bool set = false;
+  if (set) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(qlora_gemv_kernel<1>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvSmemMax);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(qlora_gemv_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kGemvSmemMax);
+  if (e != cudaSuccess) return e;
+  set = true;
+  return cudaSuccess;
+}
+
+// Clusters of S CTAs (smem bytes each) that the device runs at once: a
+// cluster never spans two GPCs, so S * this can be below the SM count.
+static int gemv_resident_clusters(int nt, int S, int smem, int want) {
+  if (gemv_smem_attr() != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(want * S, 1, 1);
+  cfg.blockDim = dim3(kGemvWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = S;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  const cudaError_t e =
+      nt == 2 ? cudaOccupancyMaxActiveClusters(&n, qlora_gemv_kernel<2>, &cfg)
+              : cudaOccupancyMaxActiveClusters(&n, qlora_gemv_kernel<1>, &cfg);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+// Cluster size S (CTAs per cluster, each taking a slice of K) and the cluster
+// count: S minimises the 2 KB units on the busiest CTA, ceil(tiles / clusters)
+// x ceil(chunks / S), among the S whose shared memory fits, with the cluster
+// count cut to what the device holds at once (one wave); ties go to the
+// smaller S.
 int gemv_plan(int N, int K, int M, int r, int num_sms, GemvPlan *out) {
   if (M < 1 || M > 16 || N < 1 || K < 64 || r < 1 || r > 64) return -1;
   const int RP = (r + 15) & ~15;
   const int MT = M > 8 ? 16 : 8;
+  const int nt = M > 8 ? 2 : 1;
   const int T = (N + 15) / 16;
   const int C = (K + kChunk - 1) / kChunk;
   GemvPlan best{};
@@ -437,10 +504,21 @@ int gemv_plan(int N, int K, int M, int r, int num_sms, GemvPlan *out) {
     int clusters = num_sms / S;
     if (clusters > T) clusters = T;
     if (clusters < 1) continue;
-    const int tiles_max = (T + clusters - 1) / clusters;
+    int tiles_max = 0, smem = 0;
+    bool fits = false;
+    for (int pass = 0; pass < 4 && clusters >= 1; ++pass) {
+      tiles_max = (T + clusters - 1) / clusters;
+      smem = gemv_smem(M, MT, sc, tiles_max, RP).total;
+      if (smem > kGemvSmemMax) break;
+      const int res = gemv_resident_clusters(nt, S, smem, clusters);
+      if (res >= clusters) {
+        fits = true;
+        break;
+      }
+      clusters = res;
+    }
+    if (!fits) continue;
     const int64_t load = (int64_t)tiles_max * sc;
-    const GemvSmem L = gemv_smem(M, MT, sc, tiles_max, RP);
-    if (L.total > 232448) continue;
     if (best_load < 0 || load < best_load) {
       best_load = load;
       best.S = S;
@@ -448,7 +526,7 @@ int gemv_plan(int N, int K, int M, int r, int num_sms, GemvPlan *out) {
       best.clusters = clusters;
       best.tiles_total = T;
       best.tiles_max = tiles_max;
-      best.smem = L.total;
+      best.smem = smem;
     }
   }
   if (best_load < 0) return -1;
@@ -479,18 +557,8 @@ cudaError_t launch_gemv(const CUtensorMap &tmW, GemvArgs a, const GemvPlan &plan
     if (e != cudaSuccess) return e;
   }
   const int nt = a.M > 8 ? 2 : 1;
-  static size_t smem_set[2] = {0, 0};
-  cudaError_t e;
-  if ((size_t)plan.smem > smem_set[nt - 1]) {
-    if (nt == 2)
-      e = cudaFuncSetAttribute(qlora_gemv_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               plan.smem);
-    else
-      e = cudaFuncSetAttribute(qlora_gemv_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               plan.smem);
-    if (e != cudaSuccess) return e;
-    smem_set[nt - 1] = plan.smem;
-  }
+  cudaError_t e = gemv_smem_attr();
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(plan.clusters * plan.S, 1, 1);
   cfg.blockDim = dim3(kGemvWarps * 32, 1, 1);

@@ -229,16 +229,16 @@ __global__ void __launch_bounds__(256 * kR) quantize_nf4_kernel(const void *__re
         const uint32_t q = (uint32_t)(bbase_s[j] + (d >= 0.0f ? 1 : 0));
         word |= q << nib_shift(e);
       }
-      if (amax == 0.0f) {
-        word = 0x77777777u;  // every index is the exact-zero codepoint
-      } else if (__any_sync(0xffffffffu, risky || !fast)) {
-        if (risky || !fast) {
-          word = 0;
+      // The vote is taken by every lane of the warp (lanes of all-zero
+      // blocks and of blocks past the end included), outside any branch.
+      const bool redo = amax != 0.0f && (risky || !fast);
+      if (__any_sync(0xffffffffu, redo) && redo) {
+        word = 0;
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            word |= (uint32_t)nf4_index(__fdiv_rn(elem(p, e), amax), th_s) << nib_shift(e);
-        }
+        for (int e = 0; e < 8; ++e)
+          word |= (uint32_t)nf4_index(__fdiv_rn(elem(p, e), amax), th_s) << nib_shift(e);
       }
+      if (amax == 0.0f) word = 0x77777777u;  // every index is the exact-zero codepoint
       if (inb[p]) *reinterpret_cast<uint32_t *>(packed + (ch0 + c) * 32 + li * 4) = word;
     }
     __syncthreads();  // amax_s complete
