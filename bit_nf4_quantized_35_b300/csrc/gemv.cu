@@ -408,33 +408,34 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
     const int share = (nrows + S - 1) / S;
     const int r_lo = min((int)rank * share, nrows), r_hi = min(r_lo + share, nrows);
     const uint32_t tsum_u = base + SL.tsum;
-    for (int rl = r_lo + (int)threadIdx.x; rl < r_hi; rl += blockDim.x) {
+    const int nr = r_hi - r_lo;
+    // one (row, token) output per thread and pass, rows fastest
+    for (int i = threadIdx.x; i < nr * p.M; i += blockDim.x) {
+      const int m = i / nr, rl = r_lo + (i - m * nr);
       const int n = row0 + rl;
       const uint16_t *brow = p.B + (int64_t)n * p.r;
-      const uint32_t off = tsum_u + ((rl >> 4) * 16 * MT + (rl & 15) * MT) * 4;
-      for (int m = 0; m < p.M; ++m) {
-        float v = 0.f;
-        for (int q = 0; q < S; ++q) v += ld_dsmem_f32(off + m * 4, (uint32_t)q);
-        float l = 0.f;
-        for (int c = 0; c < p.r; c += 8) {
-          const uint4 bw = ldg_nc_v4(brow + c);
-          const float *tc = tfin + m * p.RP + c;
-          l = fmaf(tc[0], bf16_lo(bw.x), l);
-          l = fmaf(tc[1], bf16_hi(bw.x), l);
-          l = fmaf(tc[2], bf16_lo(bw.y), l);
-          l = fmaf(tc[3], bf16_hi(bw.y), l);
-          l = fmaf(tc[4], bf16_lo(bw.z), l);
-          l = fmaf(tc[5], bf16_hi(bw.z), l);
-          l = fmaf(tc[6], bf16_lo(bw.w), l);
-          l = fmaf(tc[7], bf16_hi(bw.w), l);
-        }
-        const float y = fmaf(p.s, l, v);
-        const int64_t o = (int64_t)m * p.N + n;
-        if (p.y_bf16)
-          reinterpret_cast<__nv_bfloat16 *>(p.y)[o] = __float2bfloat16_rn(y);
-        else
-          reinterpret_cast<float *>(p.y)[o] = y;
+      const uint32_t off = tsum_u + ((rl >> 4) * 16 * MT + (rl & 15) * MT + m) * 4;
+      float v = 0.f;
+      for (int q = 0; q < S; ++q) v += ld_dsmem_f32(off, (uint32_t)q);
+      float l = 0.f;
+      const float *tc = tfin + m * p.RP;
+      for (int c = 0; c < p.r; c += 8) {
+        const uint4 bw = ldg_nc_v4(brow + c);
+        l = fmaf(tc[c + 0], bf16_lo(bw.x), l);
+        l = fmaf(tc[c + 1], bf16_hi(bw.x), l);
+        l = fmaf(tc[c + 2], bf16_lo(bw.y), l);
+        l = fmaf(tc[c + 3], bf16_hi(bw.y), l);
+        l = fmaf(tc[c + 4], bf16_lo(bw.z), l);
+        l = fmaf(tc[c + 5], bf16_hi(bw.z), l);
+        l = fmaf(tc[c + 6], bf16_lo(bw.w), l);
+        l = fmaf(tc[c + 7], bf16_hi(bw.w), l);
       }
+      const float y = fmaf(p.s, l, v);
+      const int64_t o = (int64_t)m * p.N + n;
+      if (p.y_bf16)
+        reinterpret_cast<__nv_bfloat16 *>(p.y)[o] = __float2bfloat16_rn(y);
+      else
+        reinterpret_cast<float *>(p.y)[o] = y;
     }
   }
   cluster_sync();  // keep this CTA's tile sums alive until the peers have read them
