@@ -827,8 +827,8 @@ def run_reference(args, ws_n, rank):
 def run_case(args):
     """One kernel case, args.steps launches after args.warmup, for profilers:
     gemm_fwd / gemm_dx on the 4096x14336 gate projection at 2048 tokens,
-    gemv on the same weight at --M tokens, quantise / dequantise of one
-    4096x14336 matrix."""
+    gemv on the same weight at --M tokens, quantise (bf16 or fp32 weight) /
+    dequantise / adapter merge of one 14336x4096 matrix."""
     from bit_nf4_quantized_35_b300 import build as libbuild
     libbuild.build()
     from bit_nf4_quantized_35_b300 import capi
@@ -845,6 +845,7 @@ def run_case(args):
     ws = capi.Workspace(M, N, K, RANK_R, device=dev)
     out_q = capi.NF4Weight.empty(N, K, dev)
     out_w = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+    W32 = W.float() if args.only == "quantize_f32" else None
     fns = {
         "gemm_fwd": lambda: capi.linear_fwd(q, x, A, B, ALPHA, ws, y_dtype=torch.bfloat16,
                                             t_save=t),
@@ -852,6 +853,7 @@ def run_case(args):
                                            dx_dtype=torch.bfloat16),
         "gemv": lambda: capi.linear_fwd(q, x, A, B, ALPHA, ws, y_dtype=torch.bfloat16, t_save=t),
         "quantize": lambda: capi.quantize_nf4(W, out=out_q),
+        "quantize_f32": lambda: capi.quantize_nf4(W32, out=out_q),
         "dequant": lambda: capi.dequant(q, out=out_w),
         "merge": lambda: capi.merge_lora(q, A, B, ALPHA, out=out_w),
     }
@@ -879,8 +881,8 @@ def main(argv=None):
     ap.add_argument("--quick", action="store_true", help="smaller sub-benchmarks")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row sub-benchmarks")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["gemm_fwd", "gemm_dx", "gemv", "quantize", "dequant",
-                                       "merge"],
+    ap.add_argument("--only", choices=["gemm_fwd", "gemm_dx", "gemv", "quantize",
+                                       "quantize_f32", "dequant", "merge"],
                     help="run one kernel case a few times and exit (for profiling)")
     ap.add_argument("--M", type=int, default=1, help="tokens for --only gemv")
     args = ap.parse_args(argv)

@@ -74,12 +74,16 @@ constexpr float kQuantBand = 9.5367431640625e-07f;  // 2^-20
 // memory (it reads back only what it copied, so the ring needs no block
 // barrier), so the loads of later groups are in flight while a group is
 // computed.
+// The ring of fp32 weights in 128-weight blocks (3 x 128 KB) does not fit in
+// shared memory: that case loads each group straight into registers.
 constexpr int kQStages = 3;
 template <bool kBf16In>
 __host__ __device__ constexpr int quant_pieces() { return kBf16In ? 8 : 16; }  // 16 B per thread per group
 template <bool kBf16In, int kR>
+__host__ __device__ constexpr bool quant_ring() { return kBf16In || kR == 1; }
+template <bool kBf16In, int kR>
 __host__ __device__ constexpr int quant_smem_bytes() {
-  return kQStages * quant_pieces<kBf16In>() * 256 * kR * 16;
+  return quant_ring<kBf16In, kR>() ? kQStages * quant_pieces<kBf16In>() * 256 * kR * 16 : 0;
 }
 
 template <bool kBf16In, int kR>
@@ -110,8 +114,9 @@ __global__ void __launch_bounds__(256 * kR) quantize_nf4_kernel(const void *__re
   }
   // Pass p, warp w, lane group `sub` covers chunk p * 32 kR + 4 w + sub of a
   // group; lane li the 8 elements li * 8 .. li * 8 + 7 of that chunk.
+  constexpr bool kRing = quant_ring<kBf16In, kR>();
   auto issue = [&](int64_t grp, int stage) {
-    if (grp < ngroups) {
+    if (kRing && grp < ngroups) {
       const int64_t ch0 = grp * 256 * kR;
 #pragma unroll
       for (int p = 0; p < 8; ++p) {
@@ -148,7 +153,14 @@ __global__ void __launch_bounds__(256 * kR) quantize_nf4_kernel(const void *__re
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
       inb[p] = ch0 + p * 32 * kR + warp * 4 + sub < nchunks;
-      if (kBf16In) {
+      if constexpr (!kRing) {
+        const float *src = reinterpret_cast<const float *>(W) +
+                           (ch0 + p * 32 * kR + warp * 4 + sub) * kBlock + li * 8;
+        const uint4 u0 = inb[p] ? ldg_nc_v4(src) : make_uint4(0, 0, 0, 0);
+        const uint4 u1 = inb[p] ? ldg_nc_v4(src + 4) : make_uint4(0, 0, 0, 0);
+        raw[p][0] = u0.x, raw[p][1] = u0.y, raw[p][2] = u0.z, raw[p][3] = u0.w;
+        raw[p][4] = u1.x, raw[p][5] = u1.y, raw[p][6] = u1.z, raw[p][7] = u1.w;
+      } else if constexpr (kBf16In) {
         const uint4 u = qring[(stage * kP + p) * nthr + tid];
         raw[p][0] = u.x, raw[p][1] = u.y, raw[p][2] = u.z, raw[p][3] = u.w;
       } else {
