@@ -3,7 +3,13 @@
 //
 // y[m, n] = sum_k x[m, k] w_hat[n, k] + s . sum_j t[m, j] B[n, j],  t = x A^T
 // ("QLoRA and 4bit Quantization | QLoRA 与 4-bit 量化", Step 3 formula), with
-// w_hat = bf16(c_idx . a_hat) exactly as the dequantiser produces it.
+// the block constant applied after each block's dot product:
+//   sum_k x[m, k] w_hat[n, k]  ~  sum_b a_hat[n, b] . sum_{k in b} c'[idx[n, k]] x[m, k]
+// where c' is the codepoint rounded to bf16.  This skips the bf16 rounding of
+// every w_hat = bf16(c . a_hat): each term differs from x . w_hat by at most
+// 2^-8 |x . w_hat| (two bf16 roundings of the same product), so an output
+// differs from the exact-w_hat product by at most 2^-8 sum_k |x w_hat| plus
+// the fp32 accumulation error.
 //
 // Two kernels, launched back to back with programmatic dependent launch:
 //   lora_t_decode_kernel  t = x A^T.  CTA kt covers 256 columns of K; its
@@ -24,18 +30,20 @@
 // (tile major, chunk minor) are shared out as 16 contiguous ranges, one per
 // warp; each warp brings its units into its own ring of 2 KB slots with
 // tiled TMA loads (128-byte swizzle, one mbarrier per slot), so up to
-// 16 x kGemvDepth units are in flight per SM with no register cost.
+// 16 x (2 or 3) units are in flight per SM with no register cost.
 //
 // The arithmetic of a unit (one warp): mma.sync m16n8k16 bf16, A = 16 weight
-// rows, B = up to 8 tokens per n-tile, fp32 accumulation.  The contraction
-// order inside a unit is free, so lane (g, tq) takes whole 64-blocks: lane
-// group tq owns block tq of the unit, and MMA j covers positions 4j .. 4j+3
-// of every lane group's block.  A lane therefore dequantises rows g and g+8
-// of one block (64 + 64 weights) with two per-block tables
-// T[i] = bf16(c_i . a_hat) indexed by byte permutes (the dequantiser's
-// routine, so the MMA operands are the exact bf16 W_hat), and reads the
-// matching x values from shared memory, where x is stored with a 16-byte
-// XOR swizzle that keeps every fragment load free of bank conflicts.
+// rows, B = up to 8 tokens per n-tile, fp32 accumulation.  Each 64-block of
+// the unit gets four MMAs of its own (lane group tq holds block positions
+// 16tq .. 16tq+15; the contraction order inside a block is free, x is read in
+// the same order), so the block's partial sums can be scaled by its a_hat
+// (an fp32 multiply-add per accumulator) before they join the running sums.
+// The A operands come from a 256-entry table in shared memory that maps a
+// packed byte to its two codepoints (bf16x2): one 4-byte load per weight
+// pair, from the lane's own copy of the table (32 copies, so a warp's loads
+// never share a bank).  This keeps the ALU work per weight at a byte extract
+// and an address multiply-add, against a byte-permute table of the block's
+// scaled codepoints that would have to be rebuilt for every block.
 //
 // Reduction (fixed order, deterministic, no atomics): a warp's sum over one
 // tile's chunks goes to the CTA's tile sums when the warp covered the whole
@@ -49,7 +57,7 @@
 namespace qlora {
 
 constexpr int kGemvWarps = 16;
-constexpr int kGemvDepth = 3;        // TMA ring slots per warp
+constexpr int kGemvDepthMax = 3;     // TMA ring slots per warp (3, or 2 when shared memory is short)
 constexpr int kUnitBytes = 2048;     // 16 rows x 128 packed bytes
 constexpr int kChunk = 256;          // columns of K per unit
 constexpr int kTWarps = 4;           // t kernel: one warp per 16 rows of A (r <= 64)
@@ -171,27 +179,45 @@ __global__ void __launch_bounds__(kTWarps * 32) lora_t_decode_kernel(
 }
 
 // ------------------------------------------------------------ main kernel
+// Codepoint-pair table: entry v (a packed byte: element 2j in the high
+// nibble, 2j+1 in the low) is bf16x2 {bf16(c[v >> 4]), bf16(c[v & 15])},
+// held in kTblCopies copies, entry-major, so that lane L reads copy L and a
+// warp's 32 lookups touch 32 different banks whatever the bytes are.
+constexpr int kTblCopies = 32;
+constexpr int kTblBytes = 256 * kTblCopies * 4;
+
 struct GemvSmem {
-  int ring, xs, part, tsum, tfin, bars, err, total;
+  int ring, tbl, xs, xstride, part, tsum, tfin, bars, err, total;
 };
 __host__ __device__ inline GemvSmem gemv_smem(int M, int MT, int slice_chunks, int tiles_max,
-                                              int RP) {
+                                              int RP, int depth) {
   GemvSmem L;
-  L.ring = 0;  // 16 warps x kGemvDepth slots x 2 KB, 1024-byte aligned
-  L.xs = L.ring + kGemvWarps * kGemvDepth * kUnitBytes;
-  L.part = L.xs + M * slice_chunks * kChunk * 2;       // [16 warps][2][16 rows][MT] f32
-  L.tsum = L.part + kGemvWarps * 2 * 16 * MT * 4;      // [tiles_max][16 rows][MT] f32
-  L.tfin = L.tsum + tiles_max * 16 * MT * 4;           // [M][RP] f32
-  L.bars = L.tfin + M * RP * 4;                        // [16][kGemvDepth] mbarriers
+  L.ring = 0;  // 16 warps x depth slots x 2 KB, 1024-byte aligned
+  L.tbl = L.ring + kGemvWarps * depth * kUnitBytes;
+  L.xs = L.tbl + kTblBytes;
+  L.xstride = slice_chunks * kChunk * 2 + 16;            // bytes per token row (+16: banks)
+  L.part = L.xs + M * L.xstride;                         // [16 warps][2][16 rows][MT] f32
+  L.tsum = L.part + kGemvWarps * 2 * 16 * MT * 4;        // [tiles_max][16 rows][MT] f32
+  L.tfin = L.tsum + tiles_max * 16 * MT * 4;             // [M][RP] f32
+  L.bars = L.tfin + M * RP * 4;                          // [16][depth] mbarriers
   L.bars = (L.bars + 7) & ~7;
-  L.err = L.bars + kGemvWarps * kGemvDepth * 8;
-  L.total = L.err + 16 + 1024;                         // + alignment slack of the base
+  L.err = L.bars + kGemvWarps * depth * 8;
+  L.total = L.err + 16 + 1024;                           // + alignment slack of the base
   return L;
 }
 
-// Physical 16-byte slot of logical slot s of token row tok in the x tile.
-__device__ __forceinline__ int xswz(int tok, int s) {
-  return s ^ (((s >> 3) & 3) | ((tok & 1) << 2));
+__device__ __forceinline__ uint2 lds_v2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void sts_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v));
+}
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
 }
 
 template <int NT>
@@ -201,10 +227,11 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
   constexpr int MT = NT * 8;
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t *smem = smem_raw + (base - smem_u32(smem_raw));
-  const GemvSmem SL = gemv_smem(p.M, MT, p.slice_chunks, p.tiles_max, p.RP);
+  const int depth = p.depth;
+  const GemvSmem SL = gemv_smem(p.M, MT, p.slice_chunks, p.tiles_max, p.RP, depth);
   const uint32_t ring_u = base + SL.ring;
+  const uint32_t tbl_u = base + SL.tbl;
   const uint32_t xs_u = base + SL.xs;
-  const uint4 *xsm = reinterpret_cast<const uint4 *>(smem + SL.xs);  // x tile, 16-byte slots
   float *part = reinterpret_cast<float *>(smem + SL.part);
   float *tsum = reinterpret_cast<float *>(smem + SL.tsum);
   float *tfin = reinterpret_cast<float *>(smem + SL.tfin);
@@ -227,7 +254,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
   const int u0 = U * warp / kGemvWarps, u1 = U * (warp + 1) / kGemvWarps;
   const int kbr = p.K >> 6;  // 64-chunks per weight row
 
-  if (threadIdx.x < kGemvWarps * kGemvDepth) mbar_init(bars_u + threadIdx.x * 8, 1);
+  if (threadIdx.x < kGemvWarps * depth) mbar_init(bars_u + threadIdx.x * 8, 1);
   if (threadIdx.x == 0) st_shared_volatile(err_u, 0u);
   fence_barrier_init();
   __syncthreads();
@@ -236,9 +263,9 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
   // before the t kernel, which has passed its own dependency wait).  Units
   // are walked with (tile, chunk) cursors, chunk fastest.
   auto issue = [&](int tile, int chunk, int slot) {
-    const uint32_t bar = bars_u + (warp * kGemvDepth + slot) * 8;
+    const uint32_t bar = bars_u + (warp * depth + slot) * 8;
     mbar_arrive_expect_tx(bar, kUnitBytes);
-    tma_load_2d(ring_u + (warp * kGemvDepth + slot) * kUnitBytes, &tmW, bar,
+    tma_load_2d(ring_u + (warp * depth + slot) * kUnitBytes, &tmW, bar,
                 (c0 + chunk) * 128, (t0 + tile) * 16);
   };
   const int ut0 = Cc > 0 ? u0 / Cc : 0, uc0 = Cc > 0 ? u0 - ut0 * Cc : 0;  // first unit
@@ -251,13 +278,18 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
   };
   if (lane == 0) {
     tma_prefetch_desc(&tmW);
-    for (int i = 0; i < kGemvDepth && u0 + i < u1; ++i) {
+    for (int i = 0; i < depth && u0 + i < u1; ++i) {
       issue(it_t, it_c, i);
       step(it_t, it_c);
     }
   }
 
-  // ---- 2. x slice -> shared memory (tokens < M; zero past K), swizzled
+  // ---- 2. the codepoint-pair table and the x slice (tokens < M; zero past
+  // K) -> shared memory
+  for (int i = threadIdx.x; i < 256 * kTblCopies; i += blockDim.x) {
+    const int v = i / kTblCopies;
+    sts_u32(tbl_u + i * 4, pack_bf16x2(p.cb.v[v >> 4], p.cb.v[v & 15]));
+  }
   const int spr = p.slice_chunks * (kChunk / 8);  // 16-byte slots per token row
   {
     const int kc0 = c0 * kChunk;
@@ -266,7 +298,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
       const int col = kc0 + s * 8;
       const uint4 v =
           col < p.K ? ldg_nc_v4(p.x + (int64_t)tok * p.K + col) : make_uint4(0, 0, 0, 0);
-      sts_v4(xs_u + (tok * spr + xswz(tok, s)) * 16, v.x, v.y, v.z, v.w);
+      sts_v4(xs_u + tok * SL.xstride + s * 16, v.x, v.y, v.z, v.w);
     }
   }
 
@@ -277,9 +309,14 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
     const float cv = ldg_nc_f32(p.cvec + (b >> p.cshift));
     return p.use_code ? __fmul_rn((float)ldg_nc_s8(p.codes + b), cv) : cv;
   };
-  __syncthreads();  // x staged
+  __syncthreads();  // table and x staged
 
-  // ---- 3. main loop
+  // ---- 3. main loop.  In a unit, block b (columns 64b .. 64b+63 of the
+  // chunk) is contracted by four MMAs of its own: lane group tq holds the
+  // block's positions 16tq .. 16tq+15 (packed bytes 8tq .. 8tq+7), MMA s
+  // taking positions 16tq + 4s .. +3 (bytes 2s, 2s+1).  The four MMAs give
+  // the block's partial dot products, which are then scaled by the block's
+  // a_hat (rows g and g+8) into the running sums.
   const int tok_lo = g, tok_hi = 8 + g;  // this lane's tokens in n-tiles 0 and 1
   float acc[NT][4];
   int cur = -1, seg = 0;
@@ -297,27 +334,29 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
     }
     ++seg;
   };
-  // a_hat of the lane's two rows, loaded one unit ahead
+  // a_hat of the lane's two rows in block tq, loaded one unit ahead; the
+  // lane group's four blocks are exchanged with shuffles
   auto ahat_unit = [&](int tile, int chunk, float &a, float &b) {
     const int kc = (c0 + chunk) * 4 + tq;
     a = ahat_of((t0 + tile) * 16 + g, kc);
     b = ahat_of((t0 + tile) * 16 + g + 8, kc);
   };
-  // x slot of (token, block tq, positions 8 wi .. 8 wi + 7) of chunk c:
-  // row tok, slot c * 32 + tq * 8 + (wi ^ x3) with x3 = tq | (tok & 1) << 2
-  // (the swizzle of xswz with (s >> 3) & 3 = tq); per-lane offsets of wi.
-  int xoff[8];
+  // byte offset of this lane's 8 bytes of block b in a swizzled 128-byte row
+  // (rows g and g + 8 share the pattern: 16-byte granule j sits at j ^ g)
+  uint32_t woff[4];
 #pragma unroll
-  for (int wi = 0; wi < 8; ++wi) xoff[wi] = wi ^ (tq | ((g & 1) << 2));
+  for (int b = 0; b < 4; ++b) woff[b] = ((uint32_t)((2 * b + (tq >> 1)) ^ g) << 4) | ((tq & 1) << 3);
+  const uint32_t tlane = tbl_u + lane * 4;  // this lane's copy of the table
   const bool xv_lo = tok_lo < p.M, xv_hi = tok_hi < p.M;
-  const uint4 *xr_lo = xsm + (xv_lo ? tok_lo : 0) * spr + tq * 8;
-  const uint4 *xr_hi = xsm + (xv_hi ? tok_hi : 0) * spr + tq * 8;
+  const uint32_t xr_lo = xs_u + (xv_lo ? tok_lo : 0) * SL.xstride + tq * 32;
+  const uint32_t xr_hi = xs_u + (xv_hi ? tok_hi : 0) * SL.xstride + tq * 32;
   float ah_g = 0.f, ah_h = 0.f;
   int tile = ut0, chunk = uc0;  // consume cursor
   if (u0 < u1) ahat_unit(tile, chunk, ah_g, ah_h);
   int done = 0;  // units consumed
+  int slot = 0;
+  uint32_t phase = 0;
   for (int i = 0; i < u1 - u0; ++i) {
-    const int slot = i % kGemvDepth;
     if (tile != cur) {
       if (cur >= 0) flush(cur);
       cur = tile;
@@ -328,39 +367,67 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
     step(ntile, nchunk);
     float nah_g = 0.f, nah_h = 0.f;
     if (i + 1 < u1 - u0) ahat_unit(ntile, nchunk, nah_g, nah_h);
-    const uint32_t bar = bars_u + (warp * kGemvDepth + slot) * 8;
-    if (!mbar_wait_bounded(bar, (uint32_t)(i / kGemvDepth) & 1u, err_u, p.status)) {
+    const uint32_t bar = bars_u + (warp * depth + slot) * 8;
+    // the verdict is made warp-uniform: the loop below shuffles across the warp
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar, phase, err_u, p.status))) {
       ok = false;
       break;
     }
-    // this lane's 32 packed bytes of rows g and g + 8, block tq (128-byte swizzle)
-    const uint32_t sb = ring_u + (warp * kGemvDepth + slot) * kUnitBytes;
-    const uint4 w0 = lds_v4(sb + g * 128 + (((2 * tq) ^ g) << 4));
-    const uint4 w1 = lds_v4(sb + g * 128 + (((2 * tq + 1) ^ g) << 4));
-    const uint4 v0 = lds_v4(sb + (g + 8) * 128 + (((2 * tq) ^ g) << 4));
-    const uint4 v1 = lds_v4(sb + (g + 8) * 128 + (((2 * tq + 1) ^ g) << 4));
+    const uint32_t sb = ring_u + (warp * depth + slot) * kUnitBytes;
+    uint2 wg[4], wh[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      wg[b] = lds_v2(sb + g * 128 + woff[b]);
+      wh[b] = lds_v2(sb + (g + 8) * 128 + woff[b]);
+    }
     ++done;
     __syncwarp();
-    if (lane == 0 && i + kGemvDepth < u1 - u0) {
+    if (lane == 0 && i + depth < u1 - u0) {
       fence_proxy_async_smem();
       issue(it_t, it_c, slot);
       step(it_t, it_c);
     }
-    const Nf4Table tg = make_table(ah_g, p.cb), th = make_table(ah_h, p.cb);
-    const uint32_t wg[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-    const uint32_t wh[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    const uint4 *xlo = xr_lo + chunk * 32, *xhi = xr_hi + chunk * 32;
+    if (++slot == depth) {
+      slot = 0;
+      phase ^= 1u;
+    }
+    const uint32_t xc = (uint32_t)chunk * (kChunk * 2);
 #pragma unroll
-    for (int wi = 0; wi < 8; ++wi) {
-      uint32_t og[4], oh[4];
-      lookup8(tg, wg[wi], og);
-      lookup8(th, wh[wi], oh);
+    for (int b = 0; b < 4; ++b) {
+      const float sg = __shfl_sync(0xffffffffu, ah_g, (g << 2) | b);
+      const float sh = __shfl_sync(0xffffffffu, ah_h, (g << 2) | b);
+      uint4 x0[NT], x1[NT];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const bool v = nt == 0 ? xv_lo : xv_hi;
-        const uint4 xv = v ? (nt == 0 ? xlo : xhi)[xoff[wi]] : make_uint4(0, 0, 0, 0);
-        mma_bf16(acc[nt], og[0], oh[0], og[1], oh[1], xv.x, xv.y);
-        mma_bf16(acc[nt], og[2], oh[2], og[3], oh[3], xv.z, xv.w);
+        const uint32_t xa = (nt == 0 ? xr_lo : xr_hi) + xc + b * 128;
+        x0[nt] = v ? lds_v4(xa) : make_uint4(0, 0, 0, 0);
+        x1[nt] = v ? lds_v4(xa + 16) : make_uint4(0, 0, 0, 0);
+      }
+      float d[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const uint32_t wgw = s < 2 ? wg[b].x : wg[b].y, whw = s < 2 ? wh[b].x : wh[b].y;
+        const uint32_t j0 = (s & 1) * 2;  // bytes j0, j0 + 1 of the word
+        const uint32_t a0 = lds_u32(tlane + prmt(wgw, 0u, 0x4440u | j0) * 128u);
+        const uint32_t a2 = lds_u32(tlane + prmt(wgw, 0u, 0x4441u | j0) * 128u);
+        const uint32_t a1 = lds_u32(tlane + prmt(whw, 0u, 0x4440u | j0) * 128u);
+        const uint32_t a3 = lds_u32(tlane + prmt(whw, 0u, 0x4441u | j0) * 128u);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint32_t b0 = s == 0 ? x0[nt].x : s == 1 ? x0[nt].z : s == 2 ? x1[nt].x : x1[nt].z;
+          const uint32_t b1 = s == 0 ? x0[nt].y : s == 1 ? x0[nt].w : s == 2 ? x1[nt].y : x1[nt].w;
+          mma_bf16(d[nt], a0, a1, a2, a3, b0, b1);
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        acc[nt][0] = fmaf(sg, d[nt][0], acc[nt][0]);
+        acc[nt][1] = fmaf(sg, d[nt][1], acc[nt][1]);
+        acc[nt][2] = fmaf(sh, d[nt][2], acc[nt][2]);
+        acc[nt][3] = fmaf(sh, d[nt][3], acc[nt][3]);
       }
     }
     ah_g = nah_g;
@@ -371,11 +438,10 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
   if (ok && cur >= 0) flush(cur);
   if (!ok && lane == 0) {
     // error path: wait (bounded) for this warp's copies still in flight,
-    // units done .. min(done + kGemvDepth, count) - 1
+    // units done .. min(done + depth, count) - 1
     const int cnt = u1 - u0;
-    for (int i = done; i < cnt && i < done + kGemvDepth; ++i)
-      mbar_drain(bars_u + (warp * kGemvDepth + i % kGemvDepth) * 8,
-                 (uint32_t)(i / kGemvDepth) & 1u);
+    for (int i = done; i < cnt && i < done + depth; ++i)
+      mbar_drain(bars_u + (warp * depth + i % depth) * 8, (uint32_t)(i / depth) & 1u);
   }
   __syncthreads();
 
@@ -502,32 +568,37 @@ int gemv_plan(int N, int K, int M, int r, int num_sms, GemvPlan *out) {
   for (int S = 1; S <= 8; ++S) {
     const int sc = (C + S - 1) / S;
     if ((S - 1) * sc >= C) continue;  // every rank gets chunks
-    int clusters = num_sms / S;
-    if (clusters > T) clusters = T;
-    if (clusters < 1) continue;
-    int tiles_max = 0, smem = 0;
-    bool fits = false;
-    for (int pass = 0; pass < 4 && clusters >= 1; ++pass) {
-      tiles_max = (T + clusters - 1) / clusters;
-      smem = gemv_smem(M, MT, sc, tiles_max, RP).total;
-      if (smem > kGemvSmemMax) break;
-      const int res = gemv_resident_clusters(nt, S, smem, clusters);
-      if (res >= clusters) {
-        fits = true;
-        break;
+    for (int depth = kGemvDepthMax; depth >= 2; --depth) {
+      int clusters = num_sms / S;
+      if (clusters > T) clusters = T;
+      if (clusters < 1) break;
+      int tiles_max = 0, smem = 0;
+      bool fits = false;
+      for (int pass = 0; pass < 4 && clusters >= 1; ++pass) {
+        tiles_max = (T + clusters - 1) / clusters;
+        smem = gemv_smem(M, MT, sc, tiles_max, RP, depth).total;
+        if (smem > kGemvSmemMax) break;
+        const int res = gemv_resident_clusters(nt, S, smem, clusters);
+        if (res >= clusters) {
+          fits = true;
+          break;
+        }
+        clusters = res;
       }
-      clusters = res;
-    }
-    if (!fits) continue;
-    const int64_t load = (int64_t)tiles_max * sc;
-    if (best_load < 0 || load < best_load) {
-      best_load = load;
-      best.S = S;
-      best.slice_chunks = sc;
-      best.clusters = clusters;
-      best.tiles_total = T;
-      best.tiles_max = tiles_max;
-      best.smem = smem;
+      if (!fits) continue;
+      // a shallower ring only when the deeper one does not fit
+      const int64_t load = (int64_t)tiles_max * sc;
+      if (best_load < 0 || load < best_load) {
+        best_load = load;
+        best.S = S;
+        best.slice_chunks = sc;
+        best.clusters = clusters;
+        best.tiles_total = T;
+        best.tiles_max = tiles_max;
+        best.smem = smem;
+        best.depth = depth;
+      }
+      break;
     }
   }
   if (best_load < 0) return -1;
@@ -543,6 +614,7 @@ cudaError_t launch_gemv(const CUtensorMap &tmW, GemvArgs a, const GemvPlan &plan
   a.clusters = plan.clusters;
   a.tiles_total = plan.tiles_total;
   a.tiles_max = plan.tiles_max;
+  a.depth = plan.depth;
   // t = x A^T into the workspace (a.t), partials in tpart
   {
     cudaLaunchConfig_t cfg = {};

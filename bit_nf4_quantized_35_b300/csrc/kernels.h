@@ -83,13 +83,13 @@ struct GemvArgs {
   int wpr;
   float keep_scale;
   // set by the launcher from the plan:
-  int S, slice_chunks, clusters, tiles_total, tiles_max;
+  int S, slice_chunks, clusters, tiles_total, tiles_max, depth;
   Codebook cb;
 };
 // Launch shape of the decode GEMV: S CTAs per cluster (K slices of
 // slice_chunks x 256 columns), clusters owning ranges of 16-row tiles.
 struct GemvPlan {
-  int S, slice_chunks, clusters, tiles_total, tiles_max, smem;
+  int S, slice_chunks, clusters, tiles_total, tiles_max, smem, depth;
 };
 // 0 when the decode kernel takes this shape on num_sms SMs (plan filled), else -1.
 int gemv_plan(int N, int K, int M, int r, int num_sms, GemvPlan *plan);

@@ -3,7 +3,10 @@
 Inputs follow the seeded recipe of bit_nf4_quantized_35_b300.inputs.  The
 weight seen by the oracle is the oracle's own dequantisation of the oracle's
 own quantisation (bit-identical to the GPU's, as test_gpu_quantize checks).
-Tolerance: max |err| <= 2e-2 and relative Frobenius error <= 1e-2."""
+Tolerance: max |err| <= 2e-2 and relative Frobenius error <= 1e-2; for the
+decode GEMV, whose block constant scales each block's dot product of bf16
+codepoints, each output within its derived bound (helpers.gemv_bound) and the
+same relative Frobenius error."""
 import numpy as np
 import pytest
 import torch
@@ -11,7 +14,7 @@ import torch
 from bit_nf4_quantized_35_b300 import capi, inputs
 from oracle import oracle
 
-from .helpers import MAX_ABS, REL_FRO, assert_close, to_np_f32
+from .helpers import MAX_ABS, REL_FRO, assert_close, assert_close_bound, gemv_bound, to_np_f32
 
 pytestmark = pytest.mark.gpu
 
@@ -63,7 +66,11 @@ def test_forward_small(shape, path):
     y, t = _fwd(shape, g, q, ws, FORCE_GEMV if path == "gemv" else FORCE_GEMM)
     y_ref, t_ref = oracle.linear_fwd(d["x"].float().numpy(), w_hat, d["A"].float().numpy(),
                                      d["B"].float().numpy(), shape.alpha)
-    assert_close(to_np_f32(y), y_ref, f"y {shape.name} {path}")
+    if path == "gemv":
+        assert_close_bound(to_np_f32(y), y_ref, gemv_bound(d["x"].float().numpy(), w_hat),
+                           f"y {shape.name} {path}")
+    else:
+        assert_close(to_np_f32(y), y_ref, f"y {shape.name} {path}")
     assert_close(to_np_f32(t), t_ref, f"t {shape.name} {path}", max_abs=1e-3, rel_fro=1e-5)
 
 
@@ -172,7 +179,8 @@ def test_gate_decode_gemv_full_size(M):
     y, t = _fwd(shape, g, q, ws)
     y_ref, _ = oracle.linear_fwd(d["x"].float().numpy(), w_hat, d["A"].float().numpy(),
                                  d["B"].float().numpy(), shape.alpha)
-    assert_close(to_np_f32(y), y_ref, f"y gate decode M={M}")
+    assert_close_bound(to_np_f32(y), y_ref, gemv_bound(d["x"].float().numpy(), w_hat),
+                       f"y gate decode M={M}")
 
 
 GEMV_WIDE_K = [
@@ -182,8 +190,7 @@ GEMV_WIDE_K = [
     # r = 40 (three 16-wide tiles of t, the last one ragged), N = 1032 (a
     # ragged last row pair), 9 tokens (two 8-token tiles)
     inputs.LinearShape("ragged_N1032_K4160_M9_r40", N=1032, K=4160, M=9, r=40, alpha=80.0),
-    # 448 rows per cluster: the shared ring slots do not fit next to the
-    # per-row arrays, so the register-only main loop runs
+    # 2000 16-row tiles: 14 or 13 tiles per CTA
     inputs.LinearShape("tall_N32000_K4096_M1_r16", N=32000, K=4096, M=1, r=16, alpha=32.0),
 ]
 
@@ -195,7 +202,8 @@ def test_decode_gemv_wide_k(shape):
     y, t = _fwd(shape, g, q, ws, FORCE_GEMV)
     y_ref, t_ref = oracle.linear_fwd(d["x"].float().numpy(), w_hat, d["A"].float().numpy(),
                                      d["B"].float().numpy(), shape.alpha)
-    assert_close(to_np_f32(y), y_ref, f"y {shape.name}")
+    assert_close_bound(to_np_f32(y), y_ref, gemv_bound(d["x"].float().numpy(), w_hat),
+                       f"y {shape.name}")
     assert_close(to_np_f32(t), t_ref, f"t {shape.name}", max_abs=1e-3, rel_fro=1e-5)
     y16, _ = _fwd(shape, g, q, ws, FORCE_GEMV, y_dtype=torch.bfloat16)
     assert torch.equal(y16, y.to(torch.bfloat16)), "bf16 output is not the rounded fp32 result"
