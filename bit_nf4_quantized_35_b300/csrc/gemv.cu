@@ -71,6 +71,17 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D = A B (no accumulator input)
+__device__ __forceinline__ void mma_bf16_zc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                            uint32_t a3, uint32_t b0, uint32_t b1) {
+  const float z = 0.f;
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
+}
+
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank) {
   uint32_t ra;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_addr), "r"(rank));
@@ -196,7 +207,8 @@ __host__ __device__ inline GemvSmem gemv_smem(int M, int MT, int slice_chunks, i
   L.tbl = L.ring + kGemvWarps * depth * kUnitBytes;
   L.xs = L.tbl + kTblBytes;
   L.xstride = slice_chunks * kChunk * 2 + 16;            // bytes per token row (+16: banks)
-  L.part = L.xs + M * L.xstride;                         // [16 warps][2][16 rows][MT] f32
+  L.part = L.xs + (M + 1) * L.xstride;                   // x rows, then a zero row
+  // [16 warps][2][16 rows][MT] f32 partial sums follow
   L.tsum = L.part + kGemvWarps * 2 * 16 * MT * 4;        // [tiles_max][16 rows][MT] f32
   L.tfin = L.tsum + tiles_max * 16 * MT * 4;             // [M][RP] f32
   L.bars = L.tfin + M * RP * 4;                          // [16][depth] mbarriers
@@ -293,21 +305,23 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
   const int spr = p.slice_chunks * (kChunk / 8);  // 16-byte slots per token row
   {
     const int kc0 = c0 * kChunk;
-    for (int i = threadIdx.x; i < p.M * spr; i += blockDim.x) {
-      const int tok = i / spr, s = i - tok * spr;
+    for (int i = threadIdx.x; i < (p.M + 1) * spr; i += blockDim.x) {
+      const int tok = i / spr, s = i - tok * spr;  // row M: zeros, read by lanes past M
       const int col = kc0 + s * 8;
-      const uint4 v =
-          col < p.K ? ldg_nc_v4(p.x + (int64_t)tok * p.K + col) : make_uint4(0, 0, 0, 0);
+      const uint4 v = tok < p.M && col < p.K ? ldg_nc_v4(p.x + (int64_t)tok * p.K + col)
+                                             : make_uint4(0, 0, 0, 0);
       sts_v4(xs_u + tok * SL.xstride + s * 16, v.x, v.y, v.z, v.w);
     }
   }
 
   // block constant a_hat of weight row n, 64-chunk kc of that row (0 outside W)
+  // (loads clamped into the arrays, the value then zeroed: no branches)
   auto ahat_of = [&](int n, int kc) -> float {
-    if (n >= p.N || kc >= kbr) return 0.f;
-    const int64_t b = ((int64_t)n * kbr + kc) >> p.bshift;
+    const bool in = n < p.N && kc < kbr;
+    const int64_t b = in ? ((int64_t)n * kbr + kc) >> p.bshift : 0;
     const float cv = ldg_nc_f32(p.cvec + (b >> p.cshift));
-    return p.use_code ? __fmul_rn((float)ldg_nc_s8(p.codes + b), cv) : cv;
+    const float a = p.use_code ? __fmul_rn((float)ldg_nc_s8(p.codes + b), cv) : cv;
+    return in ? a : 0.f;
   };
   __syncthreads();  // table and x staged
 
@@ -348,8 +362,9 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
   for (int b = 0; b < 4; ++b) woff[b] = ((uint32_t)((2 * b + (tq >> 1)) ^ g) << 4) | ((tq & 1) << 3);
   const uint32_t tlane = tbl_u + lane * 4;  // this lane's copy of the table
   const bool xv_lo = tok_lo < p.M, xv_hi = tok_hi < p.M;
-  const uint32_t xr_lo = xs_u + (xv_lo ? tok_lo : 0) * SL.xstride + tq * 32;
-  const uint32_t xr_hi = xs_u + (xv_hi ? tok_hi : 0) * SL.xstride + tq * 32;
+  // lanes whose token is past M read the zero row
+  const uint32_t xr_lo = xs_u + (xv_lo ? tok_lo : p.M) * SL.xstride + tq * 32;
+  const uint32_t xr_hi = xs_u + (xv_hi ? tok_hi : p.M) * SL.xstride + tq * 32;
   float ah_g = 0.f, ah_h = 0.f;
   int tile = ut0, chunk = uc0;  // consume cursor
   if (u0 < u1) ahat_unit(tile, chunk, ah_g, ah_h);
@@ -381,16 +396,6 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
       wh[b] = lds_v2(sb + (g + 8) * 128 + woff[b]);
     }
     ++done;
-    __syncwarp();
-    if (lane == 0 && i + depth < u1 - u0) {
-      fence_proxy_async_smem();
-      issue(it_t, it_c, slot);
-      step(it_t, it_c);
-    }
-    if (++slot == depth) {
-      slot = 0;
-      phase ^= 1u;
-    }
     const uint32_t xc = (uint32_t)chunk * (kChunk * 2);
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
@@ -399,14 +404,11 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
       uint4 x0[NT], x1[NT];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const bool v = nt == 0 ? xv_lo : xv_hi;
         const uint32_t xa = (nt == 0 ? xr_lo : xr_hi) + xc + b * 128;
-        x0[nt] = v ? lds_v4(xa) : make_uint4(0, 0, 0, 0);
-        x1[nt] = v ? lds_v4(xa + 16) : make_uint4(0, 0, 0, 0);
+        x0[nt] = lds_v4(xa);
+        x1[nt] = lds_v4(xa + 16);
       }
       float d[NT][4];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
         const uint32_t wgw = s < 2 ? wg[b].x : wg[b].y, whw = s < 2 ? wh[b].x : wh[b].y;
@@ -419,7 +421,10 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
         for (int nt = 0; nt < NT; ++nt) {
           const uint32_t b0 = s == 0 ? x0[nt].x : s == 1 ? x0[nt].z : s == 2 ? x1[nt].x : x1[nt].z;
           const uint32_t b1 = s == 0 ? x0[nt].y : s == 1 ? x0[nt].w : s == 2 ? x1[nt].y : x1[nt].w;
-          mma_bf16(d[nt], a0, a1, a2, a3, b0, b1);
+          if (s == 0)
+            mma_bf16_zc(d[nt], a0, a1, a2, a3, b0, b1);
+          else
+            mma_bf16(d[nt], a0, a1, a2, a3, b0, b1);
         }
       }
 #pragma unroll
@@ -429,6 +434,18 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
         acc[nt][2] = fmaf(sh, d[nt][2], acc[nt][2]);
         acc[nt][3] = fmaf(sh, d[nt][3], acc[nt][3]);
       }
+    }
+    // the slot's bytes are in registers and used: refill it with the unit
+    // depth places ahead
+    __syncwarp();
+    if (lane == 0 && i + depth < u1 - u0) {
+      fence_proxy_async_smem();
+      issue(it_t, it_c, slot);
+      step(it_t, it_c);
+    }
+    if (++slot == depth) {
+      slot = 0;
+      phase ^= 1u;
     }
     ah_g = nah_g;
     ah_h = nah_h;
