@@ -62,9 +62,11 @@ constexpr int kUnitBytes = 2048;     // 16 rows x 128 packed bytes
 constexpr int kChunk = 256;          // columns of K per unit
 constexpr int kTWarps = 4;           // t kernel: one warp per 16 rows of A (r <= 64)
 
+// The MMAs are plain register functions (no volatile): the compiler may
+// interleave them with the shared-memory loads that feed them.
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -75,7 +77,7 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
 __device__ __forceinline__ void mma_bf16_zc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                             uint32_t a3, uint32_t b0, uint32_t b1) {
   const float z = 0.f;
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%10,%10,%10,%10};"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
@@ -218,18 +220,8 @@ __host__ __device__ inline GemvSmem gemv_smem(int M, int MT, int slice_chunks, i
   return L;
 }
 
-__device__ __forceinline__ uint2 lds_v2(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
-}
 __device__ __forceinline__ void sts_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v));
-}
-__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
 }
 
 template <int NT>
@@ -360,11 +352,13 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
   uint32_t woff[4];
 #pragma unroll
   for (int b = 0; b < 4; ++b) woff[b] = ((uint32_t)((2 * b + (tq >> 1)) ^ g) << 4) | ((tq & 1) << 3);
-  const uint32_t tlane = tbl_u + lane * 4;  // this lane's copy of the table
+  // Shared-memory reads below are ordinary C++ loads (the compiler schedules
+  // them; the mbarrier waits and the proxy fence are compiler barriers).
+  const uint32_t *tlane = reinterpret_cast<const uint32_t *>(smem + SL.tbl) + lane;  // own copy
   const bool xv_lo = tok_lo < p.M, xv_hi = tok_hi < p.M;
   // lanes whose token is past M read the zero row
-  const uint32_t xr_lo = xs_u + (xv_lo ? tok_lo : p.M) * SL.xstride + tq * 32;
-  const uint32_t xr_hi = xs_u + (xv_hi ? tok_hi : p.M) * SL.xstride + tq * 32;
+  const uint8_t *xr_lo = smem + SL.xs + (xv_lo ? tok_lo : p.M) * SL.xstride + tq * 32;
+  const uint8_t *xr_hi = smem + SL.xs + (xv_hi ? tok_hi : p.M) * SL.xstride + tq * 32;
   float ah_g = 0.f, ah_h = 0.f;
   int tile = ut0, chunk = uc0;  // consume cursor
   if (u0 < u1) ahat_unit(tile, chunk, ah_g, ah_h);
@@ -388,15 +382,15 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
       ok = false;
       break;
     }
-    const uint32_t sb = ring_u + (warp * depth + slot) * kUnitBytes;
+    const uint8_t *sb = smem + SL.ring + (warp * depth + slot) * kUnitBytes;
     uint2 wg[4], wh[4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      wg[b] = lds_v2(sb + g * 128 + woff[b]);
-      wh[b] = lds_v2(sb + (g + 8) * 128 + woff[b]);
+      wg[b] = *reinterpret_cast<const uint2 *>(sb + g * 128 + woff[b]);
+      wh[b] = *reinterpret_cast<const uint2 *>(sb + (g + 8) * 128 + woff[b]);
     }
     ++done;
-    const uint32_t xc = (uint32_t)chunk * (kChunk * 2);
+    const int xc = chunk * (kChunk * 2);
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       const float sg = __shfl_sync(0xffffffffu, ah_g, (g << 2) | b);
@@ -404,19 +398,19 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
       uint4 x0[NT], x1[NT];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const uint32_t xa = (nt == 0 ? xr_lo : xr_hi) + xc + b * 128;
-        x0[nt] = lds_v4(xa);
-        x1[nt] = lds_v4(xa + 16);
+        const uint4 *xa = reinterpret_cast<const uint4 *>((nt == 0 ? xr_lo : xr_hi) + xc + b * 128);
+        x0[nt] = xa[0];
+        x1[nt] = xa[1];
       }
       float d[NT][4];
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
         const uint32_t wgw = s < 2 ? wg[b].x : wg[b].y, whw = s < 2 ? wh[b].x : wh[b].y;
         const uint32_t j0 = (s & 1) * 2;  // bytes j0, j0 + 1 of the word
-        const uint32_t a0 = lds_u32(tlane + prmt(wgw, 0u, 0x4440u | j0) * 128u);
-        const uint32_t a2 = lds_u32(tlane + prmt(wgw, 0u, 0x4441u | j0) * 128u);
-        const uint32_t a1 = lds_u32(tlane + prmt(whw, 0u, 0x4440u | j0) * 128u);
-        const uint32_t a3 = lds_u32(tlane + prmt(whw, 0u, 0x4441u | j0) * 128u);
+        const uint32_t a0 = tlane[prmt(wgw, 0u, 0x4440u | j0) * kTblCopies];
+        const uint32_t a2 = tlane[prmt(wgw, 0u, 0x4441u | j0) * kTblCopies];
+        const uint32_t a1 = tlane[prmt(whw, 0u, 0x4440u | j0) * kTblCopies];
+        const uint32_t a3 = tlane[prmt(whw, 0u, 0x4441u | j0) * kTblCopies];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const uint32_t b0 = s == 0 ? x0[nt].x : s == 1 ? x0[nt].z : s == 2 ? x1[nt].x : x1[nt].z;

@@ -38,10 +38,12 @@ constexpr int kGradStages = 4;  // cp.async ring depth
 constexpr int kGsPitch = 136;   // halves per G-tile row (128 + 8)
 constexpr int kVtPitch = 72;    // halves per V^T row (64 + 8)
 
+// A plain register function (no volatile): the compiler may interleave the
+// MMAs with the fragment loads.
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
                                                uint32_t a2, uint32_t a3, uint32_t b0,
                                                uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])

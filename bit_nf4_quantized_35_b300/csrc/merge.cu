@@ -25,9 +25,11 @@ namespace qlora {
 
 constexpr int kMergeWarps = 8;
 
+// A plain register function (no volatile), so that the compiler can
+// interleave the MMAs with the loads and the table lookups.
 __device__ __forceinline__ void mma_bf16_m(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                            uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -101,7 +103,6 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_lora_kernel(const Merg
   const uint32_t w0[8] = {l0.x, l0.y, l0.z, l0.w, h0.x, h0.y, h0.z, h0.w};
   const uint32_t w1[8] = {l1.x, l1.y, l1.z, l1.w, h1.x, h1.y, h1.z, h1.w};
   // this lane's column of every n-tile: block g >> 1, position 2j + (g & 1)
-  const uint32_t as_u = smem_u32(as);
   const int bcol = (g >> 1) * 64 + (g & 1);
   uint16_t *out0 = p.out + (int64_t)n0 * p.K + (int64_t)blk * 64;
   uint16_t *out1 = p.out + (int64_t)n1 * p.K + (int64_t)blk * 64;
@@ -115,12 +116,11 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_lora_kernel(const Merg
     for (int q = 0; q < 4; ++q) {
       const int j = wi * 4 + q;  // n-tile: positions 2j, 2j + 1
       float d[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint32_t arow = as_u + ((bcol + 2 * j) * RP) * 2 + tq * 4 * 2;
+      const uint2 *arow = reinterpret_cast<const uint2 *>(as + (bcol + 2 * j) * RP + tq * 4);
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
-        uint32_t b0, b1;
-        asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(b0), "=r"(b1) : "r"(arow + ks * 32));
-        mma_bf16_m(d, af[ks][0], af[ks][1], af[ks][2], af[ks][3], b0, b1);
+        const uint2 bv = arow[ks * 4];  // 16 ranks = 32 bytes = 4 uint2 per step
+        mma_bf16_m(d, af[ks][0], af[ks][1], af[ks][2], af[ks][3], bv.x, bv.y);
       }
       r0[q] = pack_bf16x2(fmaf(p.s, d[0], bf16_lo(o0[q])), fmaf(p.s, d[1], bf16_hi(o0[q])));
       r1[q] = pack_bf16x2(fmaf(p.s, d[2], bf16_lo(o1[q])), fmaf(p.s, d[3], bf16_hi(o1[q])));
