@@ -30,7 +30,7 @@
 // (tile major, chunk minor) are shared out as 16 contiguous ranges, one per
 // warp; each warp brings its units into its own ring of 2 KB slots with
 // tiled TMA loads (128-byte swizzle, one mbarrier per slot), so up to
-// 16 x (2 or 3) units are in flight per SM with no register cost.
+// 16 x (2 to 4) units are in flight per SM with no register cost.
 //
 // The arithmetic of a unit (one warp): mma.sync m16n8k16 bf16, A = 16 weight
 // rows, B = up to 8 tokens per n-tile, fp32 accumulation.  Each 64-block of
@@ -51,13 +51,15 @@
 // are added in warp order.  The S CTAs of a cluster then add their tile sums
 // in rank order through distributed shared memory, each finishing its share
 // of the cluster's rows with the LoRA term s . t . B^T.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
 namespace qlora {
 
 constexpr int kGemvWarps = 16;
-constexpr int kGemvDepthMax = 3;     // TMA ring slots per warp (3, or 2 when shared memory is short)
+constexpr int kGemvDepthMax = 4;     // TMA ring slots per warp (4 down to 2, as shared memory allows)
 constexpr int kUnitBytes = 2048;     // 16 rows x 128 packed bytes
 constexpr int kChunk = 256;          // columns of K per unit
 constexpr int kTWarps = 4;           // t kernel: one warp per 16 rows of A (r <= 64)
@@ -200,10 +202,10 @@ constexpr int kTblCopies = 32;
 constexpr int kTblBytes = 256 * kTblCopies * 4;
 
 struct GemvSmem {
-  int ring, tbl, xs, xstride, part, tsum, tfin, bars, err, total;
+  int ring, tbl, xs, xstride, part, tsum, tfin, bs, wr, bars, err, cbs, total;
 };
 __host__ __device__ inline GemvSmem gemv_smem(int M, int MT, int slice_chunks, int tiles_max,
-                                              int RP, int depth) {
+                                              int RP, int depth, int S) {
   GemvSmem L;
   L.ring = 0;  // 16 warps x depth slots x 2 KB, 1024-byte aligned
   L.tbl = L.ring + kGemvWarps * depth * kUnitBytes;
@@ -213,16 +215,16 @@ __host__ __device__ inline GemvSmem gemv_smem(int M, int MT, int slice_chunks, i
   // [16 warps][2][16 rows][MT] f32 partial sums follow
   L.tsum = L.part + kGemvWarps * 2 * 16 * MT * 4;        // [tiles_max][16 rows][MT] f32
   L.tfin = L.tsum + tiles_max * 16 * MT * 4;             // [M][RP] f32
-  L.bars = L.tfin + M * RP * 4;                          // [16][depth] mbarriers
+  L.bs = L.tfin + M * RP * 4;                            // B rows of the epilogue share
+  L.wr = L.bs + ((tiles_max * 16 + S - 1) / S) * RP * 2;  // warp ranges of the tiles
+  L.bars = L.wr + (2 * tiles_max + kGemvWarps) * 4;      // [16][depth] mbarriers
   L.bars = (L.bars + 7) & ~7;
   L.err = L.bars + kGemvWarps * depth * 8;
-  L.total = L.err + 16 + 1024;                           // + alignment slack of the base
+  L.cbs = L.err + 16;                                    // the 16 codepoints (fp32)
+  L.total = L.cbs + 64 + 1024;                           // + alignment slack of the base
   return L;
 }
 
-__device__ __forceinline__ void sts_u32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v));
-}
 
 template <int NT>
 __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
@@ -232,7 +234,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t *smem = smem_raw + (base - smem_u32(smem_raw));
   const int depth = p.depth;
-  const GemvSmem SL = gemv_smem(p.M, MT, p.slice_chunks, p.tiles_max, p.RP, depth);
+  const GemvSmem SL = gemv_smem(p.M, MT, p.slice_chunks, p.tiles_max, p.RP, depth, p.S);
   const uint32_t ring_u = base + SL.ring;
   const uint32_t tbl_u = base + SL.tbl;
   const uint32_t xs_u = base + SL.xs;
@@ -263,9 +265,39 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
   fence_barrier_init();
   __syncthreads();
 
-  // ---- 1. the first units of every warp's ring (the weights were written
-  // before the t kernel, which has passed its own dependency wait).  Units
-  // are walked with (tile, chunk) cursors, chunk fastest.
+  // ---- 1. copies that the weight stream would queue behind go out first:
+  // the x slice (tokens < M, zero past K, and a zero row M read by lanes
+  // whose token is past M) and the B rows of this CTA's epilogue share
+  // (plain async copies; everything before the t kernel on the stream has
+  // completed: the t kernel releases its dependents only after its own
+  // grid-dependency wait)
+  const int spr = p.slice_chunks * (kChunk / 8);  // 16-byte slots per token row
+  {
+    const int kc0 = c0 * kChunk;
+    for (int i = threadIdx.x; i < (p.M + 1) * spr; i += blockDim.x) {
+      const int tok = i / spr, s = i - tok * spr;
+      const int col = kc0 + s * 8;
+      const bool in = tok < p.M && col < p.K;
+      cp_async16(xs_u + tok * SL.xstride + s * 16,
+                 p.x + (in ? (int64_t)tok * p.K + col : 0), in ? 16u : 0u);
+    }
+    cp_async_commit();
+  }
+  const int row0 = t0 * 16;
+  const int nrows = min(t1 * 16, p.N) - row0;
+  const int share = (nrows + S - 1) / S;
+  const int r_lo = min((int)rank * share, nrows), r_hi = min(r_lo + share, nrows);
+  const int nr = r_hi - r_lo;
+  {
+    const int pieces = nr * p.r / 8;  // rows are contiguous: r * 2 bytes each, r % 8 == 0
+    const uint16_t *src = p.B + (int64_t)(row0 + r_lo) * p.r;
+    for (int i = threadIdx.x; i < pieces; i += blockDim.x)
+      cp_async16(base + SL.bs + i * 16, src + (int64_t)i * 8, 16u);
+    cp_async_commit();
+  }
+
+  // ---- 2. the first units of every warp's ring.  Units are walked with
+  // (tile, chunk) cursors, chunk fastest.
   auto issue = [&](int tile, int chunk, int slot) {
     const uint32_t bar = bars_u + (warp * depth + slot) * 8;
     mbar_arrive_expect_tx(bar, kUnitBytes);
@@ -288,23 +320,25 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
     }
   }
 
-  // ---- 2. the codepoint-pair table and the x slice (tokens < M; zero past
-  // K) -> shared memory
-  for (int i = threadIdx.x; i < 256 * kTblCopies; i += blockDim.x) {
-    const int v = i / kTblCopies;
-    sts_u32(tbl_u + i * 4, pack_bf16x2(p.cb.v[v >> 4], p.cb.v[v & 15]));
+  // ---- 3. the codepoint-pair table; the warp ranges of the tiles for the
+  // combine step (first and last warp of tile t; first tile of warp w)
+  float *cbs = reinterpret_cast<float *>(smem + SL.cbs);
+  int *wr = reinterpret_cast<int *>(smem + SL.wr);
+  if (threadIdx.x < 16) cbs[threadIdx.x] = p.cb.v[threadIdx.x];
+  if (threadIdx.x < Tc) {
+    auto warp_of = [&](int uu) { return (kGemvWarps * (uu + 1) - 1) / U; };
+    wr[2 * threadIdx.x] = warp_of(threadIdx.x * Cc);
+    wr[2 * threadIdx.x + 1] = warp_of((threadIdx.x + 1) * Cc - 1);
   }
-  const int spr = p.slice_chunks * (kChunk / 8);  // 16-byte slots per token row
-  {
-    const int kc0 = c0 * kChunk;
-    for (int i = threadIdx.x; i < (p.M + 1) * spr; i += blockDim.x) {
-      const int tok = i / spr, s = i - tok * spr;  // row M: zeros, read by lanes past M
-      const int col = kc0 + s * 8;
-      const uint4 v = tok < p.M && col < p.K ? ldg_nc_v4(p.x + (int64_t)tok * p.K + col)
-                                             : make_uint4(0, 0, 0, 0);
-      sts_v4(xs_u + tok * SL.xstride + s * 16, v.x, v.y, v.z, v.w);
-    }
+  if (threadIdx.x < kGemvWarps)
+    wr[2 * p.tiles_max + threadIdx.x] = Cc > 0 ? (U * (int)threadIdx.x / kGemvWarps) / Cc : 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < 256 * (kTblCopies / 4); i += blockDim.x) {
+    const int v = i / (kTblCopies / 4);
+    const uint32_t e = pack_bf16x2(cbs[v >> 4], cbs[v & 15]);
+    sts_v4(tbl_u + i * 16, e, e, e, e);
   }
+  cp_async_wait<1>();  // this thread's x pieces have landed (the B rows may not have)
 
   // block constant a_hat of weight row n, 64-chunk kc of that row (0 outside W)
   // (loads clamped into the arrays, the value then zeroed: no branches)
@@ -317,7 +351,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
   };
   __syncthreads();  // table and x staged
 
-  // ---- 3. main loop.  In a unit, block b (columns 64b .. 64b+63 of the
+  // ---- 4. main loop.  In a unit, block b (columns 64b .. 64b+63 of the
   // chunk) is contracted by four MMAs of its own: lane group tq holds the
   // block's positions 16tq .. 16tq+15 (packed bytes 8tq .. 8tq+7), MMA s
   // taking positions 16tq + 4s .. +3 (bytes 2s, 2s+1).  The four MMAs give
@@ -456,48 +490,44 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
   }
   __syncthreads();
 
-  // ---- 4. partial segments of each tile, added in warp order
-  auto warp_of = [&](int uu) { return (kGemvWarps * (uu + 1) - 1) / U; };
+  // ---- 5. partial segments of each tile, added in warp order
   for (int i = threadIdx.x; i < Tc * 16 * MT; i += blockDim.x) {
     const int tile = i / (16 * MT), e = i - tile * 16 * MT;
-    const int wa = warp_of(tile * Cc), wb = warp_of((tile + 1) * Cc - 1);
+    const int wa = wr[2 * tile], wb = wr[2 * tile + 1];
     if (wa == wb) continue;  // one warp covered the whole tile
     float v = 0.f;
     for (int w = wa; w <= wb; ++w) {
-      const int sw = (U * w / kGemvWarps) / Cc;  // first tile of warp w
+      const int sw = wr[2 * p.tiles_max + w];  // first tile of warp w
       v += part[(w * 2 + (sw == tile ? 0 : 1)) * 16 * MT + e];
     }
     tsum[tile * 16 * MT + e] = v;
   }
+  cp_async_wait<0>();  // the B rows of the epilogue
   __syncthreads();
   cluster_sync();  // every CTA's tile sums are complete
 
-  // ---- 5. t from the t kernel (the only input written by the kernel before)
+  // ---- 6. t from the t kernel (the only input written by the kernel before)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   for (int i = threadIdx.x; i < p.M * p.RP; i += blockDim.x) tfin[i] = __ldcg(p.t + i);
   __syncthreads();
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  // ---- 6. this CTA's share of the cluster's rows: y = sum over ranks + s t B^T
+  // ---- 7. this CTA's share of the cluster's rows: y = sum over ranks + s t B^T
   {
-    const int row0 = t0 * 16;
-    const int nrows = min(t1 * 16, p.N) - row0;
-    const int share = (nrows + S - 1) / S;
-    const int r_lo = min((int)rank * share, nrows), r_hi = min(r_lo + share, nrows);
     const uint32_t tsum_u = base + SL.tsum;
-    const int nr = r_hi - r_lo;
+    const uint16_t *bsm = reinterpret_cast<const uint16_t *>(smem + SL.bs);
     // one (row, token) output per thread and pass, rows fastest
     for (int i = threadIdx.x; i < nr * p.M; i += blockDim.x) {
       const int m = i / nr, rl = r_lo + (i - m * nr);
       const int n = row0 + rl;
-      const uint16_t *brow = p.B + (int64_t)n * p.r;
+      const uint16_t *brow = bsm + (rl - r_lo) * p.r;
       const uint32_t off = tsum_u + ((rl >> 4) * 16 * MT + (rl & 15) * MT + m) * 4;
       float v = 0.f;
       for (int q = 0; q < S; ++q) v += ld_dsmem_f32(off, (uint32_t)q);
       float l = 0.f;
       const float *tc = tfin + m * p.RP;
       for (int c = 0; c < p.r; c += 8) {
-        const uint4 bw = ldg_nc_v4(brow + c);
+        const uint4 bw = *reinterpret_cast<const uint4 *>(brow + c);
         l = fmaf(tc[c + 0], bf16_lo(bw.x), l);
         l = fmaf(tc[c + 1], bf16_hi(bw.x), l);
         l = fmaf(tc[c + 2], bf16_lo(bw.y), l);
@@ -567,7 +597,44 @@ static int gemv_resident_clusters(int nt, int S, int smem, int want) {
 // x ceil(chunks / S), among the S whose shared memory fits, with the cluster
 // count cut to what the device holds at once (one wave); ties go to the
 // smaller S.
+static int gemv_plan_uncached(int N, int K, int M, int r, int num_sms, GemvPlan *out);
+
+// The plan depends on the shape and the device only; the occupancy queries
+// behind it cost host time, so recent plans are kept (a small ring, under a
+// lock: the library may be called from several host threads).
 int gemv_plan(int N, int K, int M, int r, int num_sms, GemvPlan *out) {
+  struct Entry {
+    int N, K, M, r, num_sms, dev, rc;
+    GemvPlan plan;
+  };
+  static std::mutex mu;
+  static Entry cache[16];
+  static int filled = 0, next = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < filled; ++i) {
+      const Entry &e = cache[i];
+      if (e.N == N && e.K == K && e.M == M && e.r == r && e.num_sms == num_sms && e.dev == dev) {
+        if (out && e.rc == 0) *out = e.plan;
+        return e.rc;
+      }
+    }
+  }
+  GemvPlan plan{};
+  const int rc = gemv_plan_uncached(N, K, M, r, num_sms, &plan);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    cache[next] = Entry{N, K, M, r, num_sms, dev, rc, plan};
+    next = (next + 1) % 16;
+    if (filled < 16) ++filled;
+  }
+  if (out && rc == 0) *out = plan;
+  return rc;
+}
+
+static int gemv_plan_uncached(int N, int K, int M, int r, int num_sms, GemvPlan *out) {
   if (M < 1 || M > 16 || N < 1 || K < 64 || r < 1 || r > 64) return -1;
   const int RP = (r + 15) & ~15;
   const int MT = M > 8 ? 16 : 8;
@@ -587,7 +654,7 @@ int gemv_plan(int N, int K, int M, int r, int num_sms, GemvPlan *out) {
       bool fits = false;
       for (int pass = 0; pass < 4 && clusters >= 1; ++pass) {
         tiles_max = (T + clusters - 1) / clusters;
-        smem = gemv_smem(M, MT, sc, tiles_max, RP, depth).total;
+        smem = gemv_smem(M, MT, sc, tiles_max, RP, depth, S).total;
         if (smem > kGemvSmemMax) break;
         const int res = gemv_resident_clusters(nt, S, smem, clusters);
         if (res >= clusters) {
