@@ -9,13 +9,14 @@
 // again to int8 with one fp32 scale per group of block constants.
 //
 // Both kernels are HBM-bound.  Layout of the work:
-//   quantise: one CTA of 256 threads per 256 consecutive blocks (one double
-//     quantisation group of 256, or several smaller groups).  Eight lanes
-//     share a block: each lane reads 16 bytes of bf16 (or 32 of fp32), the
-//     block maximum is an 8-lane shuffle reduction, and the lane writes its
-//     8 indices as one 32-bit word, so each warp instruction moves 512
-//     contiguous bytes in and 128 contiguous bytes out.  All eight passes of
-//     a thread are loaded before the first is used.
+//   quantise: persistent CTAs of 512 threads, each taking groups of 256
+//     consecutive blocks (one double quantisation group of 256, or several
+//     smaller groups), the input of each group brought into shared memory
+//     by one bulk copy a few groups ahead.  Eight lanes share a block
+//     (sixteen for 128-weight blocks): each lane reads 16 bytes of bf16 (or
+//     32 of fp32), the block maximum is a shuffle reduction, and the lane
+//     writes its 8 indices as one 32-bit word, so each warp instruction
+//     moves 512 contiguous bytes in and 128 contiguous bytes out.
 //   dequantise: four lanes per block, 16 elements per lane; the per-block
 //     scaled table T[i] = bf16(c_i * a_hat) is built once per lane and
 //     indexed with byte permutes (the same routine the fused GEMM producer
@@ -66,110 +67,142 @@ __device__ __forceinline__ constexpr int nib_shift(int e) { return 8 * (e >> 1) 
 // 2^-20 both lie on the same side of the threshold.
 constexpr float kQuantBand = 9.5367431640625e-07f;  // 2^-20
 
-// kR = block / 64.  A CTA of 256 kR threads takes groups of 256 consecutive
-// blocks (one double-quantisation group of 256, or several smaller groups):
-// group g, g + gridDim.x, ... (persistent grid).  The 8 kR lanes of a block
-// reduce its maximum with shuffles.  Each thread streams its own 16-byte
-// pieces of the next groups through a kQStages-deep cp.async ring in shared
-// memory (it reads back only what it copied, so the ring needs no block
-// barrier), so the loads of later groups are in flight while a group is
-// computed.
-// The ring of fp32 weights in 128-weight blocks (3 x 128 KB) does not fit in
-// shared memory: that case loads each group straight into registers.
+// kR = block / 64.  A CTA of kQThreads threads takes groups of 256
+// consecutive blocks (one double-quantisation group of 256, or several
+// smaller groups): group g, g + gridDim.x, ... (persistent grid).  Pass p,
+// warp w, lane group `sub` (8 lanes) covers 64-element chunk p * 64 + 4 w + sub
+// of the group, lane li its elements 8 li .. 8 li + 7; the 8 kR lanes of a
+// block reduce its maximum with shuffles.
+//
+// kBulk: the group's input (contiguous, 32 kR KB of bf16 or 64 kR KB of fp32)
+// comes into one of kQStages shared-memory stages with a single bulk copy
+// (cp.async.bulk, completion on the stage's mbarrier); one thread refills a
+// stage as soon as every thread has read it, so the next stages' copies are
+// in flight while a group is computed.  Without kBulk (fp32 weights in
+// 128-weight blocks: three 128 KB stages would not fit) every thread loads
+// its pieces straight into registers.
+constexpr int kQThreads = 512;
 constexpr int kQStages = 3;
-template <bool kBf16In>
-__host__ __device__ constexpr int quant_pieces() { return kBf16In ? 8 : 16; }  // 16 B per thread per group
 template <bool kBf16In, int kR>
-__host__ __device__ constexpr bool quant_ring() { return kBf16In || kR == 1; }
+__host__ __device__ constexpr bool quant_bulk() { return kBf16In || kR == 1; }
+template <bool kBf16In, int kR>
+__host__ __device__ constexpr int quant_stage_bytes() { return 256 * kR * 64 * (kBf16In ? 2 : 4); }
 template <bool kBf16In, int kR>
 __host__ __device__ constexpr int quant_smem_bytes() {
-  return quant_ring<kBf16In, kR>() ? kQStages * quant_pieces<kBf16In>() * 256 * kR * 16 : 0;
+  return quant_bulk<kBf16In, kR>() ? kQStages * quant_stage_bytes<kBf16In, kR>() + 128 : 0;
 }
 
 template <bool kBf16In, int kR>
-__global__ void __launch_bounds__(256 * kR) quantize_nf4_kernel(const void *__restrict__ W,
-                                                           int64_t nblocks, int group,
-                                                           uint8_t *__restrict__ packed,
-                                                           int8_t *__restrict__ codes,
-                                                           float *__restrict__ absf,
-                                                           float *__restrict__ scale2,
-                                                           int *__restrict__ nonfinite_flag,
-                                                           const QuantTables tab) {
-  extern __shared__ __align__(16) uint4 qring[];  // [stage][piece][thread]
+__global__ void __launch_bounds__(kQThreads) quantize_nf4_kernel(const void *__restrict__ W,
+                                                             int64_t nblocks, int group,
+                                                             uint8_t *__restrict__ packed,
+                                                             int8_t *__restrict__ codes,
+                                                             float *__restrict__ absf,
+                                                             float *__restrict__ scale2,
+                                                             int *__restrict__ nonfinite_flag,
+                                                             const QuantTables tab) {
+  extern __shared__ __align__(128) uint8_t qsm[];  // [stage][group input]; mbarriers at the end
   __shared__ float th_s[16];
   __shared__ float bth_s[64];
   __shared__ int bbase_s[64];
   __shared__ float amax_s[256];
   __shared__ float wmax_s[8];
+  __shared__ uint32_t qerr_s;
+  constexpr bool kBulk = quant_bulk<kBf16In, kR>();
+  constexpr int kStage = quant_stage_bytes<kBf16In, kR>();
+  constexpr int kPasses = 4 * kR;
+  constexpr int kEsz = kBf16In ? 2 : 4;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sub = lane >> 3, li = lane & 7;
-  const int nthr = 256 * kR;
   const int64_t nchunks = nblocks * kR;  // 64-element chunks
   const int64_t ngroups = (nblocks + 255) / 256;
-  constexpr int kP = quant_pieces<kBf16In>();
+  const int64_t G = gridDim.x;
+  const uint32_t sm_u = smem_u32(qsm);
+  const uint32_t bars_u = sm_u + kQStages * kStage;  // kQStages mbarriers (kBulk)
   if (tid < 16) th_s[tid] = tab.th[tid];
   if (tid < 64) {
     bth_s[tid] = tab.bth[tid];
     bbase_s[tid] = tab.bbase[tid];
   }
-  // Pass p, warp w, lane group `sub` covers chunk p * 32 kR + 4 w + sub of a
-  // group; lane li the 8 elements li * 8 .. li * 8 + 7 of that chunk.
-  constexpr bool kRing = quant_ring<kBf16In, kR>();
-  auto issue = [&](int64_t grp, int stage) {
-    if (kRing && grp < ngroups) {
-      const int64_t ch0 = grp * 256 * kR;
-#pragma unroll
-      for (int p = 0; p < 8; ++p) {
-        const int64_t gb = ch0 + p * 32 * kR + warp * 4 + sub;
-        const bool ok = gb < nchunks;
-        if (kBf16In) {
-          const uint16_t *src = reinterpret_cast<const uint16_t *>(W) + (ok ? gb * kBlock + li * 8 : 0);
-          cp_async16(smem_u32(&qring[(stage * kP + p) * nthr + tid]), src, ok ? 16u : 0u);
-        } else {
-          const float *src = reinterpret_cast<const float *>(W) + (ok ? gb * kBlock + li * 8 : 0);
-          cp_async16(smem_u32(&qring[(stage * kP + 2 * p) * nthr + tid]), src, ok ? 16u : 0u);
-          cp_async16(smem_u32(&qring[(stage * kP + 2 * p + 1) * nthr + tid]), src + 4,
-                     ok ? 16u : 0u);
-        }
-      }
-    }
-    cp_async_commit();
+  if (kBulk && tid < kQStages) mbar_init(bars_u + tid * 8, 1);
+  if (tid == 0) qerr_s = 0u;
+  if (kBulk) fence_barrier_init();
+  __syncthreads();  // tables and barriers ready
+
+  // one bulk copy of group grp's input into stage st (thread 0)
+  auto issue = [&](int64_t grp, int st) {
+    const int64_t e0 = grp * 256 * kR * 64;
+    const int64_t el = min((int64_t)256 * kR * 64, nchunks * 64 - e0);
+    const uint32_t bytes = (uint32_t)(el * kEsz);  // a multiple of 128
+    const uint32_t bar = bars_u + st * 8;
+    mbar_arrive_expect_tx(bar, bytes);
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(sm_u + st * kStage),
+        "l"(reinterpret_cast<const uint8_t *>(W) + e0 * kEsz), "r"(bytes), "r"(bar)
+        : "memory");
   };
-  const int64_t G = gridDim.x;
-  for (int s0 = 0; s0 < kQStages - 1; ++s0) issue(blockIdx.x + s0 * G, s0);
-  __syncthreads();  // tables visible
+  if (kBulk && tid == 0)
+    for (int st = 0; st < kQStages; ++st)
+      if (blockIdx.x + st * G < ngroups) issue(blockIdx.x + st * G, st);
 
   int nonfinite = 0;
   int it = 0;
   for (int64_t grp = blockIdx.x; grp < ngroups; grp += G, ++it) {
     const int64_t blk0 = grp * 256;   // first block of the group
     const int64_t ch0 = blk0 * kR;    // its first 64-element chunk
-    cp_async_wait<kQStages - 2>();    // this thread's pieces of group grp have landed
-    issue(grp + (kQStages - 1) * G, (it + kQStages - 1) % kQStages);  // the stage read last time
-    const int stage = it % kQStages;
+    const int st = it % kQStages;
     constexpr int kWords = kBf16In ? 4 : 8;  // 32-bit words per pass
-    uint32_t raw[8][kWords];
-    bool inb[8];
+    uint32_t raw[kPasses][kWords];
+    bool inb[kPasses];
+    if constexpr (kBulk) {
+      // bounded wait on the stage (~2 s); past the limit the group is
+      // computed from whatever the stage holds and the error is reported
+      const uint32_t bar = bars_u + st * 8;
+      const uint32_t ph = (uint32_t)(it / kQStages) & 1u;
+      if (!mbar_try_wait(bar, ph)) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(bar, ph))
+          if (clock64() - t0 > (1ll << 32)) {
+            qerr_s = 1u;
+            break;
+          }
+      }
+      const uint8_t *stg = qsm + st * kStage;
 #pragma unroll
-    for (int p = 0; p < 8; ++p) {
-      inb[p] = ch0 + p * 32 * kR + warp * 4 + sub < nchunks;
-      if constexpr (!kRing) {
-        const float *src = reinterpret_cast<const float *>(W) +
-                           (ch0 + p * 32 * kR + warp * 4 + sub) * kBlock + li * 8;
+      for (int p = 0; p < kPasses; ++p) {
+        const int c = p * 64 + warp * 4 + sub;
+        inb[p] = ch0 + c < nchunks;
+        const uint4 *src = reinterpret_cast<const uint4 *>(stg + (c * 64 + li * 8) * kEsz);
+        const uint4 u0 = src[0];
+        raw[p][0] = u0.x, raw[p][1] = u0.y, raw[p][2] = u0.z, raw[p][3] = u0.w;
+        if constexpr (!kBf16In) {
+          const uint4 u1 = src[1];
+          raw[p][4] = u1.x, raw[p][5] = u1.y, raw[p][6] = u1.z, raw[p][7] = u1.w;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int p = 0; p < kPasses; ++p) {
+        const int c = p * 64 + warp * 4 + sub;
+        inb[p] = ch0 + c < nchunks;
+        const uint8_t *src = reinterpret_cast<const uint8_t *>(W) +
+                             ((inb[p] ? ch0 + c : 0) * 64 + li * 8) * kEsz;
         const uint4 u0 = inb[p] ? ldg_nc_v4(src) : make_uint4(0, 0, 0, 0);
-        const uint4 u1 = inb[p] ? ldg_nc_v4(src + 4) : make_uint4(0, 0, 0, 0);
         raw[p][0] = u0.x, raw[p][1] = u0.y, raw[p][2] = u0.z, raw[p][3] = u0.w;
-        raw[p][4] = u1.x, raw[p][5] = u1.y, raw[p][6] = u1.z, raw[p][7] = u1.w;
-      } else if constexpr (kBf16In) {
-        const uint4 u = qring[(stage * kP + p) * nthr + tid];
-        raw[p][0] = u.x, raw[p][1] = u.y, raw[p][2] = u.z, raw[p][3] = u.w;
-      } else {
-        const uint4 u0 = qring[(stage * kP + 2 * p) * nthr + tid];
-        const uint4 u1 = qring[(stage * kP + 2 * p + 1) * nthr + tid];
-        raw[p][0] = u0.x, raw[p][1] = u0.y, raw[p][2] = u0.z, raw[p][3] = u0.w;
-        raw[p][4] = u1.x, raw[p][5] = u1.y, raw[p][6] = u1.z, raw[p][7] = u1.w;
+        if constexpr (!kBf16In) {
+          const uint4 u1 = inb[p] ? ldg_nc_v4(src + 16) : make_uint4(0, 0, 0, 0);
+          raw[p][4] = u1.x, raw[p][5] = u1.y, raw[p][6] = u1.z, raw[p][7] = u1.w;
+        }
       }
     }
+    // chunks past the end of the weight (the stage holds stale bytes there)
+    // count as zeros
+#pragma unroll
+    for (int p = 0; p < kPasses; ++p)
+      if (!inb[p])
+#pragma unroll
+        for (int q = 0; q < kWords; ++q) raw[p][q] = 0u;
 
     auto elem = [&](int p, int e) -> float {
       if (kBf16In) return (e & 1) ? bf16_hi(raw[p][e >> 1]) : bf16_lo(raw[p][e >> 1]);
@@ -177,8 +210,8 @@ __global__ void __launch_bounds__(256 * kR) quantize_nf4_kernel(const void *__re
     };
 
 #pragma unroll
-    for (int p = 0; p < 8; ++p) {
-      const int c = p * 32 * kR + warp * 4 + sub;
+    for (int p = 0; p < kPasses; ++p) {
+      const int c = p * 64 + warp * 4 + sub;
       // Block absmax as the largest magnitude bit pattern (the order of
       // non-negative floats); a pattern >= 0x7f800000 means an infinite or NaN
       // element, and the maximum is then taken over the finite ones only.
@@ -253,7 +286,11 @@ __global__ void __launch_bounds__(256 * kR) quantize_nf4_kernel(const void *__re
       if (amax == 0.0f) word = 0x77777777u;  // every index is the exact-zero codepoint
       if (inb[p]) *reinterpret_cast<uint32_t *>(packed + (ch0 + c) * 32 + li * 4) = word;
     }
-    __syncthreads();  // amax_s complete
+    __syncthreads();  // amax_s complete; every thread is done with the stage
+    if (kBulk && tid == 0 && grp + kQStages * G < ngroups) {
+      fence_proxy_async_smem();
+      issue(grp + kQStages * G, st);
+    }
 
     // Second level: one scale per `group` consecutive block constants, by
     // threads 0..255 (warps 0..7); the others only take the block barriers.
@@ -285,10 +322,10 @@ __global__ void __launch_bounds__(256 * kR) quantize_nf4_kernel(const void *__re
     }
     __syncthreads();  // amax_s and wmax_s are free for the next group
   }
-  cp_async_wait<0>();
   if (nonfinite_flag) {
     nonfinite = __any_sync(0xffffffffu, nonfinite != 0);
     if (nonfinite && lane == 0) atomicExch(nonfinite_flag, 1);
+    if (tid == 0 && qerr_s) atomicExch(nonfinite_flag, kStatusTimeout);
   }
 }
 
@@ -383,13 +420,13 @@ static cudaError_t launch_q(const void *W, int64_t nblocks, int group, uint8_t *
   }
   int per_sm = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &per_sm, quantize_nf4_kernel<kBf16In, kR>, 256 * kR, smem);
+      &per_sm, quantize_nf4_kernel<kBf16In, kR>, kQThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
   const int64_t ngroups = (nblocks + 255) / 256;
   int64_t grid = (int64_t)num_sms * per_sm;
   if (grid > ngroups) grid = ngroups;
-  quantize_nf4_kernel<kBf16In, kR><<<(unsigned)grid, 256 * kR, smem, s>>>(
+  quantize_nf4_kernel<kBf16In, kR><<<(unsigned)grid, kQThreads, smem, s>>>(
       W, nblocks, group, packed, codes, absf, scale2, nonfinite_flag, tab);
   return cudaGetLastError();
 }

@@ -134,7 +134,9 @@ qlora_status qlora_nf4_sizes(int64_t rows, int64_t cols, int32_t block, int32_t 
  * device buffers of the sizes from qlora_nf4_sizes.
  * nonfinite_flag: NULL, or a device int32 that the kernel sets to 1 when it
  * meets a NaN or infinite weight (the caller zeroes it first); indices of
- * such blocks are unspecified.
+ * such blocks are unspecified.  It is set to QLORA_ERR_TIMEOUT instead when
+ * a copy of the weight into shared memory did not complete within the
+ * kernel's time limit (about 2 s); all outputs are then unspecified.
  * Errors: QLORA_ERR_INVALID_ARG (null buffers), QLORA_ERR_SHAPE (block not 64
  * or 128, unsupported group, cols % block), QLORA_ERR_DTYPE, QLORA_ERR_ALIGN,
  * QLORA_ERR_CUDA. */
