@@ -9,7 +9,7 @@
 // again to int8 with one fp32 scale per group of block constants.
 //
 // Both kernels are HBM-bound.  Layout of the work:
-//   quantise: persistent CTAs of 512 threads, each taking groups of 256
+//   quantise: persistent CTAs of 1024 threads, each taking groups of 256
 //     consecutive blocks (one double quantisation group of 256, or several
 //     smaller groups), the input of each group brought into shared memory
 //     by one bulk copy a few groups ahead.  Eight lanes share a block
@@ -60,19 +60,21 @@ __device__ __forceinline__ constexpr int nib_shift(int e) { return 8 * (e >> 1) 
 
 // Band (absolute, in normalised units) around each threshold inside which
 // the reciprocal-based value may fall on the other side of the threshold
-// than the IEEE quotient.  With y = RN(1/a) and xn' = RN(w . y):
-//   xn' = (w/a)(1 + d1)(1 + d2),  RN(w/a) = (w/a)(1 + d3),  |di| <= 2^-24,
-// so |xn' - RN(w/a)| < 2^-22 |w/a| <= 2^-22 (normal range; a subnormal xn'
+// than the IEEE quotient.  With y the hardware reciprocal (rcp.approx: at
+// most 1 ulp from 1/a, so y = (1/a)(1 + d1) with |d1| <= 2^-23 for a normal
+// a and y) and xn' = RN(w . y):
+//   xn' = (w/a)(1 + d1)(1 + d2),  RN(w/a) = (w/a)(1 + d3),  |d2|, |d3| <= 2^-24,
+// so |xn' - RN(w/a)| < 2^-21.4 |w/a| <= 2^-21.4 (normal range; a subnormal xn'
 // is at most 2^-126 from it, far from every threshold).  Outside a band of
 // 2^-20 both lie on the same side of the threshold.
 constexpr float kQuantBand = 9.5367431640625e-07f;  // 2^-20
 
-// kR = block / 64.  A CTA of kQThreads threads takes groups of 256
-// consecutive blocks (one double-quantisation group of 256, or several
-// smaller groups): group g, g + gridDim.x, ... (persistent grid).  Pass p,
-// warp w, lane group `sub` (8 lanes) covers 64-element chunk p * 64 + 4 w + sub
-// of the group, lane li its elements 8 li .. 8 li + 7; the 8 kR lanes of a
-// block reduce its maximum with shuffles.
+// kR = block / 64.  A CTA of T threads takes groups of 256 consecutive
+// blocks (one double-quantisation group of 256, or several smaller groups):
+// group g, g + gridDim.x, ... (persistent grid).  Pass p, warp w, lane group
+// `sub` (8 lanes) covers 64-element chunk p * T / 8 + 4 w + sub of the group,
+// lane li its elements 8 li .. 8 li + 7; the 8 kR lanes of a block reduce its
+// maximum with shuffles.
 //
 // kBulk: the group's input (contiguous, 32 kR KB of bf16 or 64 kR KB of fp32)
 // comes into one of kQStages shared-memory stages with a single bulk copy
@@ -81,10 +83,12 @@ constexpr float kQuantBand = 9.5367431640625e-07f;  // 2^-20
 // in flight while a group is computed.  Without kBulk (fp32 weights in
 // 128-weight blocks: three 128 KB stages would not fit) every thread loads
 // its pieces straight into registers.
-constexpr int kQThreads = 512;
 constexpr int kQStages = 3;
 template <bool kBf16In, int kR>
 __host__ __device__ constexpr bool quant_bulk() { return kBf16In || kR == 1; }
+// 32 warps with the staged input; 16 when every thread holds all its pieces
+template <bool kBf16In, int kR>
+__host__ __device__ constexpr int quant_threads() { return quant_bulk<kBf16In, kR>() ? 1024 : 512; }
 template <bool kBf16In, int kR>
 __host__ __device__ constexpr int quant_stage_bytes() { return 256 * kR * 64 * (kBf16In ? 2 : 4); }
 template <bool kBf16In, int kR>
@@ -93,7 +97,7 @@ __host__ __device__ constexpr int quant_smem_bytes() {
 }
 
 template <bool kBf16In, int kR>
-__global__ void __launch_bounds__(kQThreads) quantize_nf4_kernel(const void *__restrict__ W,
+__global__ void __launch_bounds__(quant_threads<kBf16In, kR>()) quantize_nf4_kernel(const void *__restrict__ W,
                                                              int64_t nblocks, int group,
                                                              uint8_t *__restrict__ packed,
                                                              int8_t *__restrict__ codes,
@@ -104,13 +108,15 @@ __global__ void __launch_bounds__(kQThreads) quantize_nf4_kernel(const void *__r
   extern __shared__ __align__(128) uint8_t qsm[];  // [stage][group input]; mbarriers at the end
   __shared__ float th_s[16];
   __shared__ float bth_s[64];
-  __shared__ int bbase_s[64];
+  __shared__ int bbase1_s[64];
   __shared__ float amax_s[256];
   __shared__ float wmax_s[8];
   __shared__ uint32_t qerr_s;
   constexpr bool kBulk = quant_bulk<kBf16In, kR>();
   constexpr int kStage = quant_stage_bytes<kBf16In, kR>();
-  constexpr int kPasses = 4 * kR;
+  constexpr int kT = quant_threads<kBf16In, kR>();
+  constexpr int kCpp = kT / 8;                 // chunks per pass
+  constexpr int kPasses = 256 * kR / kCpp;
   constexpr int kEsz = kBf16In ? 2 : 4;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sub = lane >> 3, li = lane & 7;
@@ -122,7 +128,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_nf4_kernel(const void *__r
   if (tid < 16) th_s[tid] = tab.th[tid];
   if (tid < 64) {
     bth_s[tid] = tab.bth[tid];
-    bbase_s[tid] = tab.bbase[tid];
+    bbase1_s[tid] = tab.bbase[tid] + 1;
   }
   if (kBulk && tid < kQStages) mbar_init(bars_u + tid * 8, 1);
   if (tid == 0) qerr_s = 0u;
@@ -171,7 +177,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_nf4_kernel(const void *__r
       const uint8_t *stg = qsm + st * kStage;
 #pragma unroll
       for (int p = 0; p < kPasses; ++p) {
-        const int c = p * 64 + warp * 4 + sub;
+        const int c = p * kCpp + warp * 4 + sub;
         inb[p] = ch0 + c < nchunks;
         const uint4 *src = reinterpret_cast<const uint4 *>(stg + (c * 64 + li * 8) * kEsz);
         const uint4 u0 = src[0];
@@ -184,7 +190,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_nf4_kernel(const void *__r
     } else {
 #pragma unroll
       for (int p = 0; p < kPasses; ++p) {
-        const int c = p * 64 + warp * 4 + sub;
+        const int c = p * kCpp + warp * 4 + sub;
         inb[p] = ch0 + c < nchunks;
         const uint8_t *src = reinterpret_cast<const uint8_t *>(W) +
                              ((inb[p] ? ch0 + c : 0) * 64 + li * 8) * kEsz;
@@ -197,12 +203,14 @@ __global__ void __launch_bounds__(kQThreads) quantize_nf4_kernel(const void *__r
       }
     }
     // chunks past the end of the weight (the stage holds stale bytes there)
-    // count as zeros
+    // count as zeros; only the last group has any
+    if (grp == ngroups - 1) {
 #pragma unroll
-    for (int p = 0; p < kPasses; ++p)
-      if (!inb[p])
+      for (int p = 0; p < kPasses; ++p)
+        if (!inb[p])
 #pragma unroll
-        for (int q = 0; q < kWords; ++q) raw[p][q] = 0u;
+          for (int q = 0; q < kWords; ++q) raw[p][q] = 0u;
+    }
 
     auto elem = [&](int p, int e) -> float {
       if (kBf16In) return (e & 1) ? bf16_hi(raw[p][e >> 1]) : bf16_lo(raw[p][e >> 1]);
@@ -211,7 +219,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_nf4_kernel(const void *__r
 
 #pragma unroll
     for (int p = 0; p < kPasses; ++p) {
-      const int c = p * 64 + warp * 4 + sub;
+      const int c = p * kCpp + warp * 4 + sub;
       // Block absmax as the largest magnitude bit pattern (the order of
       // non-negative floats); a pattern >= 0x7f800000 means an infinite or NaN
       // element, and the maximum is then taken over the finite ones only.
@@ -249,14 +257,16 @@ __global__ void __launch_bounds__(kQThreads) quantize_nf4_kernel(const void *__r
       }
       const float amax = __uint_as_float(mb);
       if (li == 0 && (sub % kR) == 0) amax_s[c / kR] = amax;  // 0 for blocks past the end
-      // Fast path: xn' = w . RN(1/a) and the bucket tables; an element whose
-      // xn' lies within the band of a threshold is decided again with the
-      // IEEE quotient.  Block constants outside [2^-126, 2^126] (reciprocal
-      // out of the normal range) take the IEEE path for every element.
+      // Fast path: xn' = w . y with y the hardware reciprocal of a (within 1
+      // ulp of 1/a) and the bucket tables; an element whose xn' lies within
+      // the band of a threshold is decided again with the IEEE quotient.
+      // Block constants outside [2^-126, 2^126] (reciprocal out of the normal
+      // range) take the IEEE path for every element.
       const bool fast = !tab.exact_only && amax >= 1.17549435e-38f && amax <= 8.50705917e+37f;
-      const float y = __frcp_rn(amax);
+      float y;
+      asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(amax));
       uint32_t word = 0;
-      bool risky = false;
+      float dmin = 1.0f;  // smallest |xn' - threshold| of the lane's elements
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float xn = __fmul_rn(elem(p, e), y);
@@ -270,13 +280,16 @@ __global__ void __launch_bounds__(kQThreads) quantize_nf4_kernel(const void *__r
         const float u = __fadd_rn(v, 12582912.0f);
         const int j = __float_as_int(u) & 63;
         const float d = __fsub_rn(xn, bth_s[j]);
-        risky |= fabsf(d) < kQuantBand;
-        const uint32_t q = (uint32_t)(bbase_s[j] + (d >= 0.0f ? 1 : 0));
+        dmin = fminf(dmin, fabsf(d));
+        // index = #{thresholds below the bucket} + (d >= 0): bbase1 holds the
+        // count plus one, and the sign bit of d takes the one away (d is +0,
+        // never -0, when xn' equals the threshold)
+        const uint32_t q = (uint32_t)bbase1_s[j] - (__float_as_uint(d) >> 31);
         word |= q << nib_shift(e);
       }
       // The vote is taken by every lane of the warp (lanes of all-zero
       // blocks and of blocks past the end included), outside any branch.
-      const bool redo = amax != 0.0f && (risky || !fast);
+      const bool redo = amax != 0.0f && (dmin < kQuantBand || !fast);
       if (__any_sync(0xffffffffu, redo) && redo) {
         word = 0;
 #pragma unroll
@@ -420,13 +433,13 @@ static cudaError_t launch_q(const void *W, int64_t nblocks, int group, uint8_t *
   }
   int per_sm = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &per_sm, quantize_nf4_kernel<kBf16In, kR>, kQThreads, smem);
+      &per_sm, quantize_nf4_kernel<kBf16In, kR>, quant_threads<kBf16In, kR>(), smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
   const int64_t ngroups = (nblocks + 255) / 256;
   int64_t grid = (int64_t)num_sms * per_sm;
   if (grid > ngroups) grid = ngroups;
-  quantize_nf4_kernel<kBf16In, kR><<<(unsigned)grid, kQThreads, smem, s>>>(
+  quantize_nf4_kernel<kBf16In, kR><<<(unsigned)grid, quant_threads<kBf16In, kR>(), smem, s>>>(
       W, nblocks, group, packed, codes, absf, scale2, nonfinite_flag, tab);
   return cudaGetLastError();
 }
