@@ -826,15 +826,16 @@ def run_reference(args, ws_n, rank):
 
 def run_case(args):
     """One kernel case, args.steps launches after args.warmup, for profilers:
-    gemm_fwd / gemm_dx on the 4096x14336 gate projection at 2048 tokens,
+    gemm_fwd / gemm_dx on the 14336x4096 gate projection at 2048 tokens,
     gemv on the same weight at --M tokens, quantise (bf16 or fp32 weight) /
-    dequantise / adapter merge of one 14336x4096 matrix."""
+    dequantise / adapter merge of one 14336x4096 matrix, the backward with
+    LoRA dropout (p = 0.1, mask drawn each call) at 2048 tokens."""
     from bit_nf4_quantized_35_b300 import build as libbuild
     libbuild.build()
     from bit_nf4_quantized_35_b300 import capi
     dev = 0
     N, K = 14336, 4096
-    M = M_TOKENS if args.only.startswith("gemm") else args.M
+    M = M_TOKENS if args.only.startswith(("gemm", "dropout")) else args.M
     W = gen_bf16((N, K), 0.02, 100, dev)
     q = capi.quantize_nf4(W)
     A = gen_bf16((RANK_R, K), 0.01, 200, dev)
@@ -846,6 +847,7 @@ def run_case(args):
     out_q = capi.NF4Weight.empty(N, K, dev)
     out_w = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
     W32 = W.float() if args.only == "quantize_f32" else None
+    mask = torch.empty((M, capi.dropout_mask_words(K)), dtype=torch.int32, device=dev)
     fns = {
         "gemm_fwd": lambda: capi.linear_fwd(q, x, A, B, ALPHA, ws, y_dtype=torch.bfloat16,
                                             t_save=t),
@@ -856,6 +858,9 @@ def run_case(args):
         "quantize_f32": lambda: capi.quantize_nf4(W32, out=out_q),
         "dequant": lambda: capi.dequant(q, out=out_w),
         "merge": lambda: capi.merge_lora(q, A, B, ALPHA, out=out_w),
+        "dropout_bwd": lambda: capi.linear_bwd(
+            q, x, dY, A, B, ALPHA, ws, t_saved=t, dropout=(
+                capi.dropout_mask(7, 0.1, M, K, out=mask), 0.1)),
     }
     capi.linear_fwd(q, x, A, B, ALPHA, ws, t_save=t)
     fn = fns[args.only]
@@ -882,7 +887,7 @@ def main(argv=None):
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row sub-benchmarks")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["gemm_fwd", "gemm_dx", "gemv", "quantize",
-                                       "quantize_f32", "dequant", "merge"],
+                                       "quantize_f32", "dequant", "merge", "dropout_bwd"],
                     help="run one kernel case a few times and exit (for profiling)")
     ap.add_argument("--M", type=int, default=1, help="tokens for --only gemv")
     args = ap.parse_args(argv)
