@@ -534,7 +534,7 @@ def sub_benchmarks(capi, layers, device, stream, args):
     rows["quantize_bulk"] = {"matrices": nmat, "weights": nw, "ms": round(qms, 3),
                              "GBps_total": round(bytes_total / (qms * 1e-3) / 1e9, 1),
                              "frac_of_hbm": round(bytes_total / (qms * 1e-3) / 1e9 / hbm, 4),
-                             "note": "8 distinct 235 MB matrices cycled (> L2)"}
+                             "note": "8 distinct 117 MB matrices cycled (> L2)"}
     # dequantisation to bf16 of the same matrices
     outw = torch.empty((Rq, Cq), dtype=torch.bfloat16, device=device)
     e0.record()
