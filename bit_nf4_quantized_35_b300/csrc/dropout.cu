@@ -94,30 +94,51 @@ cudaError_t launch_dropout_mask(uint64_t seed, uint32_t p32, int64_t M, int K, i
 
 // dX[m, k] -= sum_j lb[m, j] At[k, j] at every dropped (m, k): the dX GEMM
 // seeded its accumulator with exactly these bf16 operands for every (m, k).
-// One thread per mask word (32 columns of one row).
+// One thread per 8 columns of one row (one byte of a keep word): the row of lb
+// and each dropped column's row of At are read with 16-byte loads.
+template <int KS>  // KS = RP / 8 16-byte pieces per row
 __global__ void __launch_bounds__(256) dropout_dx_fix_kernel(
     const uint32_t *__restrict__ mask, int wpr, int64_t M, int K,
-    const uint16_t *__restrict__ lb, const uint16_t *__restrict__ At, int RP,
-    float *__restrict__ dX) {
+    const uint16_t *__restrict__ lb, const uint16_t *__restrict__ At, float *__restrict__ dX) {
   pdl_wait_release();
-  const int64_t total = M * wpr;
+  constexpr int RP = KS * 8;
+  const int k8s = K >> 3;  // pieces of 8 columns per row (K % 64 == 0)
+  const int64_t total = M * k8s;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t m = i / wpr;
-    const int w = (int)(i - m * wpr);
-    if (w * 32 >= K) continue;
-    uint32_t drop = ~mask[i];
+    const int64_t m = i / k8s;
+    const int p8 = (int)(i - m * k8s);
+    const uint32_t w = __ldg(mask + m * wpr + (p8 >> 2));
+    uint32_t drop = ~(w >> ((p8 & 3) * 8)) & 0xffu;
     if (drop == 0u) continue;
-    float um[64];
-    const uint16_t *lr = lb + m * RP;
-    for (int j = 0; j < RP; ++j) um[j] = __uint_as_float((uint32_t)lr[j] << 16);
+    float um[RP];
+    const uint4 *lr = reinterpret_cast<const uint4 *>(lb + m * RP);
+#pragma unroll
+    for (int q = 0; q < KS; ++q) {
+      const uint4 v = __ldg(lr + q);
+      um[8 * q + 0] = bf16_lo(v.x), um[8 * q + 1] = bf16_hi(v.x);
+      um[8 * q + 2] = bf16_lo(v.y), um[8 * q + 3] = bf16_hi(v.y);
+      um[8 * q + 4] = bf16_lo(v.z), um[8 * q + 5] = bf16_hi(v.z);
+      um[8 * q + 6] = bf16_lo(v.w), um[8 * q + 7] = bf16_hi(v.w);
+    }
     while (drop) {
       const int b = __ffs(drop) - 1;
       drop &= drop - 1;
-      const int k = w * 32 + b;
-      const uint16_t *ak = At + (int64_t)k * RP;
+      const int k = p8 * 8 + b;
+      const uint4 *ak = reinterpret_cast<const uint4 *>(At + (int64_t)k * RP);
       float v = 0.f;
-      for (int j = 0; j < RP; ++j) v = fmaf(um[j], __uint_as_float((uint32_t)ak[j] << 16), v);
+#pragma unroll
+      for (int q = 0; q < KS; ++q) {
+        const uint4 a = __ldg(ak + q);
+        v = fmaf(um[8 * q + 0], bf16_lo(a.x), v);
+        v = fmaf(um[8 * q + 1], bf16_hi(a.x), v);
+        v = fmaf(um[8 * q + 2], bf16_lo(a.y), v);
+        v = fmaf(um[8 * q + 3], bf16_hi(a.y), v);
+        v = fmaf(um[8 * q + 4], bf16_lo(a.z), v);
+        v = fmaf(um[8 * q + 5], bf16_hi(a.z), v);
+        v = fmaf(um[8 * q + 6], bf16_lo(a.w), v);
+        v = fmaf(um[8 * q + 7], bf16_hi(a.w), v);
+      }
       dX[m * K + k] -= v;
     }
   }
@@ -127,7 +148,7 @@ cudaError_t launch_dropout_dx_fix(const uint32_t *mask, int wpr, int64_t M, int 
                                   const uint16_t *lb, const uint16_t *At, int RP, float *dX,
                                   int num_sms, cudaStream_t s) {
   if (M == 0) return cudaSuccess;
-  const int64_t total = M * wpr;
+  const int64_t total = M * (K / 8);
   int64_t grid = (total + 255) / 256;
   if (grid > (int64_t)num_sms * 16) grid = (int64_t)num_sms * 16;
   cudaLaunchConfig_t cfg = {};
@@ -137,10 +158,13 @@ cudaError_t launch_dropout_dx_fix(const uint32_t *mask, int wpr, int64_t M, int 
   cudaLaunchAttribute at[1] = {pdl_attr()};
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  cudaError_t e =
-      cudaLaunchKernelEx(&cfg, dropout_dx_fix_kernel, mask, wpr, M, K, lb, At, RP, dX);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  switch (RP / 8) {
+    case 2: return cudaLaunchKernelEx(&cfg, dropout_dx_fix_kernel<2>, mask, wpr, M, K, lb, At, dX);
+    case 4: return cudaLaunchKernelEx(&cfg, dropout_dx_fix_kernel<4>, mask, wpr, M, K, lb, At, dX);
+    case 6: return cudaLaunchKernelEx(&cfg, dropout_dx_fix_kernel<6>, mask, wpr, M, K, lb, At, dX);
+    case 8: return cudaLaunchKernelEx(&cfg, dropout_dx_fix_kernel<8>, mask, wpr, M, K, lb, At, dX);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace qlora

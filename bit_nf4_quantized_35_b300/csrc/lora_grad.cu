@@ -142,30 +142,44 @@ __global__ void __launch_bounds__(kGradThreads) lora_grad_tc_kernel(const Skinny
   const int cw = warp * 16;  // this warp's 16 columns inside the tile
   // ldmatrix lane roles: matrix mi = lane >> 3, row within it lane & 7
   const int mi = lane >> 3, lr = lane & 7;
+  // dropout: the keep words of a chunk's pieces (a piece of 8 columns is one
+  // byte of a keep word), loaded one chunk ahead so that their latency is
+  // hidden behind the previous chunk's MMAs
+  uint32_t kwc[4], kwn[4];
+  auto load_kw = [&](int chx, uint32_t (&kw)[4]) {
+    const int64_t mb = m_lo + (int64_t)chx * kGradRows;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = threadIdx.x + u * kGradThreads;
+      const int row = i >> 4, cc = (i & 15) * 8;
+      const int64_t m = mb + row;
+      const int c = c0 + cc;
+      kw[u] = (m < m_hi && c < C) ? __ldg(mask + m * wpr + (c >> 5)) : 0xffffffffu;
+    }
+  };
+  if (mask) load_kw(0, kwc);
   for (int ch = 0; ch < nchunks; ++ch) {
     const int cur = ch % kGradStages;
     cp_async_wait<kGradStages - 2>();  // this thread's copies of chunk ch have landed
     __syncthreads();                   // everyone's; chunk ch - 1 is fully consumed
     issue(ch + kGradStages - 1);       // into the buffer chunk ch - 1 used
     if (mask) {
-      // dropout: zero the dropped elements of G in chunk ch (keep bits of the
-      // mask; a piece of 8 columns is one byte of a keep word)
-      const int64_t mb = m_lo + (int64_t)ch * kGradRows;
+      if (ch + 1 < nchunks) load_kw(ch + 1, kwn);
+      // zero the dropped elements of G in chunk ch
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int i = threadIdx.x + u * kGradThreads;
         const int row = i >> 4, cc = (i & 15) * 8;
-        const int64_t m = mb + row;
         const int c = c0 + cc;
-        if (m < m_hi && c < C) {
-          const uint32_t kw = __ldg(mask + m * wpr + (c >> 5));
-          uint32_t mk[4];
-          keep_masks((kw >> (c & 31)) & 0xffu, mk);
-          const uint32_t a = smem_u32(gs + (cur * kGradRows + row) * kGsPitch + cc);
-          const uint4 v = lds_v4(a);
-          sts_v4(a, v.x & mk[0], v.y & mk[1], v.z & mk[2], v.w & mk[3]);
-        }
+        uint32_t mk[4];
+        keep_masks((kwc[u] >> (c & 31)) & 0xffu, mk);
+        const uint32_t a = smem_u32(gs + (cur * kGradRows + row) * kGsPitch + cc);
+        const uint4 v = lds_v4(a);
+        sts_v4(a, v.x & mk[0], v.y & mk[1], v.z & mk[2], v.w & mk[3]);
       }
+      if (ch + 1 < nchunks)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) kwc[u] = kwn[u];
     }
     // V rows of chunk ch -> bf16 hi / lo, transposed
     for (int i = threadIdx.x; i < kGradRows * RPAD; i += kGradThreads) {
