@@ -342,9 +342,10 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
 
   // block constant a_hat of weight row n, 64-chunk kc of that row (0 outside W)
   // (loads clamped into the arrays, the value then zeroed: no branches)
+  // (32-bit indices: the plan admits only weights with N * K / 64 < 2^31)
   auto ahat_of = [&](int n, int kc) -> float {
     const bool in = n < p.N && kc < kbr;
-    const int64_t b = in ? ((int64_t)n * kbr + kc) >> p.bshift : 0;
+    const int b = in ? (n * kbr + kc) >> p.bshift : 0;
     const float cv = ldg_nc_f32(p.cvec + (b >> p.cshift));
     const float a = p.use_code ? __fmul_rn((float)ldg_nc_s8(p.codes + b), cv) : cv;
     return in ? a : 0.f;
@@ -636,6 +637,7 @@ int gemv_plan(int N, int K, int M, int r, int num_sms, GemvPlan *out) {
 
 static int gemv_plan_uncached(int N, int K, int M, int r, int num_sms, GemvPlan *out) {
   if (M < 1 || M > 16 || N < 1 || K < 64 || r < 1 || r > 64) return -1;
+  if ((int64_t)N * (K / 64) >= ((int64_t)1 << 31)) return -1;  // 32-bit block indices
   const int RP = (r + 15) & ~15;
   const int MT = M > 8 ? 16 : 8;
   const int nt = M > 8 ? 2 : 1;
