@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(quant_threads<kBf16In, kR>()) quantize_nf4_ker
   __shared__ float th_s[16];
   __shared__ float bth_s[64];
   __shared__ int bbase1_s[64];
-  __shared__ float amax_s[256];
+  __shared__ float amax_s[2][256];  // block maxima of the last two groups
   __shared__ float wmax_s[8];
   __shared__ uint32_t qerr_s;
   constexpr bool kBulk = quant_bulk<kBf16In, kR>();
@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(quant_threads<kBf16In, kR>()) quantize_nf4_ker
         }
       }
       const float amax = __uint_as_float(mb);
-      if (li == 0 && (sub % kR) == 0) amax_s[c / kR] = amax;  // 0 for blocks past the end
+      if (li == 0 && (sub % kR) == 0) amax_s[it & 1][c / kR] = amax;  // 0 past the end
       // Fast path: xn' = w . y with y the hardware reciprocal of a (within 1
       // ulp of 1/a) and the bucket tables; an element whose xn' lies within
       // the band of a threshold is decided again with the IEEE quotient.
@@ -299,26 +299,28 @@ __global__ void __launch_bounds__(quant_threads<kBf16In, kR>()) quantize_nf4_ker
       if (amax == 0.0f) word = 0x77777777u;  // every index is the exact-zero codepoint
       if (inb[p]) *reinterpret_cast<uint32_t *>(packed + (ch0 + c) * 32 + li * 4) = word;
     }
-    __syncthreads();  // amax_s complete; every thread is done with the stage
+    __syncthreads();  // amax_s[it & 1] complete; every thread is done with the stage
     if (kBulk && tid == 0 && grp + kQStages * G < ngroups) {
       fence_proxy_async_smem();
       issue(grp + kQStages * G, st);
     }
 
     // Second level: one scale per `group` consecutive block constants, by
-    // threads 0..255 (warps 0..7); the others only take the block barriers.
-    const bool dq = tid < 256;
-    const float a = dq ? amax_s[tid] : 0.0f;
-    const int64_t gb = blk0 + tid;
-    if (group == 0) {
-      if (dq && gb < nblocks) absf[gb] = a;
-    } else {
-      float m = a;
+    // threads 0..255 (warps 0..7), while the other warps go on to the next
+    // group: the block maxima are double-buffered, and the 8 warps meet at a
+    // barrier of their own (the next CTA-wide barrier, after the next group's
+    // elements, orders this step before the buffers are reused).
+    if (tid < 256) {
+      const float a = amax_s[it & 1][tid];
+      const int64_t gb = blk0 + tid;
+      if (group == 0) {
+        if (gb < nblocks) absf[gb] = a;
+      } else {
+        float m = a;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (lane == 0 && dq) wmax_s[warp] = m;
-      __syncthreads();
-      if (dq) {
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) wmax_s[warp] = m;
+        asm volatile("bar.sync 1, 256;" ::: "memory");
         const int wpg = group >> 5;  // warps per group (group >= 32)
         const int w0 = (warp / wpg) * wpg;
         float gmax = 0.0f;
@@ -333,7 +335,6 @@ __global__ void __launch_bounds__(quant_threads<kBf16In, kR>()) quantize_nf4_ker
         }
       }
     }
-    __syncthreads();  // amax_s and wmax_s are free for the next group
   }
   if (nonfinite_flag) {
     nonfinite = __any_sync(0xffffffffu, nonfinite != 0);
