@@ -17,10 +17,10 @@
 //     32 of fp32), the block maximum is a shuffle reduction, and the lane
 //     writes its 8 indices as one 32-bit word, so each warp instruction
 //     moves 512 contiguous bytes in and 128 contiguous bytes out.
-//   dequantise: two lanes per block (four for 128-weight blocks), 32
-//     elements per lane; the per-block scaled table T[i] = bf16(c_i * a_hat)
-//     is built once per lane and indexed with byte permutes (the same
-//     routine the fused GEMM producer uses), 64-byte stores.
+//   dequantise: four lanes per block, 16 elements per lane; the per-block
+//     scaled table T[i] = bf16(c_i * a_hat) is built once per lane and
+//     indexed with byte permutes (the same routine the fused GEMM producer
+//     uses), 32-byte stores.
 #include <cmath>
 
 #include "common.cuh"
@@ -358,28 +358,23 @@ __global__ void __launch_bounds__(256) dequant_nf4_kernel(const uint8_t *__restr
                                                           int piece_shift,
                                                           uint16_t *__restrict__ out,
                                                           const Codebook cb) {
-  // piece q (32 elements, 16 packed bytes) lies in block q >> piece_shift
-  // (block / 32 pieces); the lane builds the block's table once for its 32
+  // piece q (16 elements) lies in block q >> piece_shift (block / 16 pieces)
   for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < npieces;
        q += (int64_t)gridDim.x * blockDim.x) {
     const int64_t b = q >> piece_shift;
-    const uint4 pk = ldg_nc_v4(packed + q * 16);
+    const uint2 pk = ldg_nc_v2(packed + q * 8);
     float ahat;
     if (group > 0)
       ahat = __fmul_rn((float)codes[b], scale2[b / group]);
     else
       ahat = absf[b];
     const Nf4Table t = make_table(ahat, cb);
-    uint32_t o[16];
+    uint32_t o[8];
     lookup8(t, pk.x, o);
     lookup8(t, pk.y, o + 4);
-    lookup8(t, pk.z, o + 8);
-    lookup8(t, pk.w, o + 12);
-    uint4 *dst = reinterpret_cast<uint4 *>(out + q * 32);
+    uint4 *dst = reinterpret_cast<uint4 *>(out + q * 16);
     dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
     dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-    dst[2] = make_uint4(o[8], o[9], o[10], o[11]);
-    dst[3] = make_uint4(o[12], o[13], o[14], o[15]);
   }
 }
 
@@ -481,12 +476,12 @@ cudaError_t launch_dequant(const uint8_t *packed, const int8_t *codes, const flo
                            uint16_t *out, const Codebook &cb, int num_sms, cudaStream_t s) {
   if (nblocks == 0) return cudaSuccess;
   if (block != 64 && block != 128) return cudaErrorInvalidValue;
-  const int64_t work = nblocks * (block / 32);
+  const int64_t work = nblocks * (block / 16);
   int64_t grid = (work + 255) / 256;
   const int64_t cap = (int64_t)num_sms * 8 * 4;
   if (grid > cap) grid = cap;
   dequant_nf4_kernel<<<(unsigned)grid, 256, 0, s>>>(packed, codes, absf, scale2, group, work,
-                                                    block == 64 ? 1 : 2, out, cb);
+                                                    block == 64 ? 2 : 3, out, cb);
   return cudaGetLastError();
 }
 
