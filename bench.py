@@ -425,7 +425,9 @@ def run_ours(args, ws_n, rank, device):
         },
         "roofline": {
             "kernel": "qlora_gemm_kernel<false> (fused NF4 dequant + tcgen05 GEMM + LoRA) on "
-                      "gate_proj 14336x4096 at M=2048: its forward launches in the timed steps",
+                      "gate_proj 14336x4096 at M=2048: CUDA events around each gate forward "
+                      "call of the timed steps, which is the t = x.A^T pre-pass (about 4% of "
+                      "it) and this GEMM launch; flops are the whole call's",
             "flops_per_launch": gate_flops,
             "avg_launch_ms": round(layer_ms[gi], 4),
             "bound": "tensor",
