@@ -520,7 +520,7 @@ qlora_status linear_fwd_impl(const qlora_nf4_weight *w, const uint16_t *x, int64
   g.s = sc;
   g.out = y;
   g.out_bf16 = y_dtype == QLORA_BF16;
-  g.stages = gemm_pick_stages(RP, bn);
+  g.stages = gemm_pick_stages(RP);
   g.status = reinterpret_cast<int *>(wsb + L.status);
   g.bn = bn;
   set_gemm_plan(g, plan, L, wsb);
@@ -599,7 +599,7 @@ qlora_status linear_bwd_impl(const qlora_nf4_weight *w, const uint16_t *x, const
   g.s = sc;
   g.out = dX;
   g.out_bf16 = dx_dtype == QLORA_BF16;
-  g.stages = gemm_pick_stages(RP, bn);
+  g.stages = gemm_pick_stages(RP);
   g.status = reinterpret_cast<int *>(wsb + L.status);
   g.bn = bn;
   set_gemm_plan(g, plan, L, wsb);

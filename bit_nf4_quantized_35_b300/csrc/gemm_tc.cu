@@ -77,12 +77,9 @@ __device__ __forceinline__ int prod_index(int w) {
 static_assert(kEpiWarp3 % 4 == 3 && kMmaWarp % 4 == 3 && kTmaWarp % 4 == 3,
               "roles sharing the MMA issuer's scheduler");
 constexpr int kABytes = GBM * GBK * 2;     // 16 KB
-// A stage: this CTA's 128 activation rows (16 KB), then its half of the B
-// tile, bn/2 rows of 128 bytes rounded up to the 1 KB swizzle atom (16 KB at
-// bn = 256, 8 KB at bn = 128: narrower tiles get more stages in flight).
-__host__ __device__ inline int gemm_stage_bytes(int, int bn) {
-  return kABytes + (((bn / 2) * GBK * 2 + 1023) & ~1023);
-}
+constexpr int kBBytes = kHalfN * GBK * 2;  // 16 KB (this CTA's half of B)
+
+__host__ __device__ inline int gemm_stage_bytes(int) { return kABytes + kBBytes; }
 __host__ __device__ inline int gemm_upa_bytes(int r_pad) { return (r_pad / 16) * GBM * 32; }
 __host__ __device__ inline int gemm_upb_bytes(int r_pad) { return (r_pad / 16) * kHalfN * 32; }
 // Epilogue staging: per epilogue warp 32 rows x 16 fp32 columns, row pitch
@@ -90,8 +87,8 @@ __host__ __device__ inline int gemm_upb_bytes(int r_pad) { return (r_pad / 16) *
 constexpr int kStagePitch = 80;
 constexpr int kStageWarpBytes = 32 * kStagePitch;  // 2560
 constexpr int kStageBytes = 4 * kStageWarpBytes;   // 10 KB
-__host__ inline int gemm_smem_bytes(int stages, int r_pad, int bn) {
-  return 1024 + stages * gemm_stage_bytes(r_pad, bn) +
+__host__ inline int gemm_smem_bytes(int stages, int r_pad) {
+  return 1024 + stages * gemm_stage_bytes(r_pad) +
          2 * (gemm_upa_bytes(r_pad) + gemm_upb_bytes(r_pad)) + kStageBytes + 256;
 }
 
@@ -217,7 +214,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int S = p.stages, RP = p.r_pad;
-  const int SB = gemm_stage_bytes(RP, p.bn);
+  const int SB = gemm_stage_bytes(RP);
   const int UPA = gemm_upa_bytes(RP), UPB = gemm_upb_bytes(RP);
   uint8_t *upa = smem + S * SB;           // 2 buffers
   uint8_t *upb = upa + 2 * UPA;           // 2 buffers
@@ -789,10 +786,7 @@ int gemm_cluster_bound() {
 cudaError_t gemm_plan(bool dx, int M, int out_cols, int kdim, int r_pad, int sk_slots_clusters,
                       GemmPlan *plan) {
   int maxc = 0;
-  // (one CTA per SM at any stage count and tile width: the query at the
-  // widest tile stands for all)
-  cudaError_t e =
-      max_active_clusters(dx, gemm_smem_bytes(gemm_pick_stages(r_pad, GBN), r_pad, GBN), &maxc);
+  cudaError_t e = max_active_clusters(dx, gemm_smem_bytes(gemm_pick_stages(r_pad), r_pad), &maxc);
   if (e != cudaSuccess) return e;
   const int64_t mp = (M + 2 * GBM - 1) / (2 * GBM);
   const int64_t num_k = (kdim + GBK - 1) / GBK;
@@ -821,7 +815,7 @@ cudaError_t launch_gemm(bool dx, const CUtensorMap &tmA, const CUtensorMap &tmL1
   if (args.clusters < 1) return cudaSuccess;  // nothing to compute
   if (args.sk && (!args.sk_part || !args.sk_count || args.clusters > args.sk_slots_clusters))
     return cudaErrorInvalidValue;
-  const int smem = gemm_smem_bytes(args.stages, args.r_pad, args.bn);
+  const int smem = gemm_smem_bytes(args.stages, args.r_pad);
   int maxc = 0;
   cudaError_t e = max_active_clusters(dx, smem, &maxc);
   if (e != cudaSuccess) return e;
@@ -847,9 +841,9 @@ cudaError_t launch_gemm(bool dx, const CUtensorMap &tmA, const CUtensorMap &tmL1
   return cudaGetLastError();
 }
 
-int gemm_pick_stages(int r_pad, int bn) {
-  for (int st = 8; st >= 2; --st)
-    if (gemm_smem_bytes(st, r_pad, bn) <= 232448) return st;
+int gemm_pick_stages(int r_pad) {
+  for (int st = 7; st >= 2; --st)
+    if (gemm_smem_bytes(st, r_pad) <= 232448) return st;
   return 0;
 }
 

@@ -61,7 +61,7 @@ cudaError_t gemm_plan(bool dx, int M, int out_cols, int kdim, int r_pad, int sk_
 int gemm_cluster_bound();
 cudaError_t launch_gemm(bool dx, const CUtensorMap &tmA, const CUtensorMap &tmL1,
                         const CUtensorMap &tmL2, const GemmArgs &args, cudaStream_t s);
-int gemm_pick_stages(int r_pad, int bn);
+int gemm_pick_stages(int r_pad);
 
 // Decode GEMV (gemv.cu): t kernel + weight-streaming kernel.
 struct GemvArgs {
