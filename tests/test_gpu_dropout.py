@@ -63,6 +63,9 @@ def _run(shape, p, seed, flags=0, t_saved=True):
 SHAPES = [
     inputs.LinearShape("drop_N520_K384_M200_r16", N=520, K=384, M=200, r=16, alpha=32.0),
     inputs.LinearShape("drop_N264_K1024_M129_r8", N=264, K=1024, M=129, r=8, alpha=16.0),
+    # r = 40 and 64: three and four 16-wide rank steps in the dX correction
+    inputs.LinearShape("drop_N136_K512_M77_r40", N=136, K=512, M=77, r=40, alpha=80.0),
+    inputs.LinearShape("drop_N256_K320_M64_r64", N=256, K=320, M=64, r=64, alpha=128.0),
 ]
 
 
