@@ -3,13 +3,7 @@
 //
 // y[m, n] = sum_k x[m, k] w_hat[n, k] + s . sum_j t[m, j] B[n, j],  t = x A^T
 // ("QLoRA and 4bit Quantization | QLoRA 与 4-bit 量化", Step 3 formula), with
-// the block constant applied after each block's dot product:
-//   sum_k x[m, k] w_hat[n, k]  ~  sum_b a_hat[n, b] . sum_{k in b} c'[idx[n, k]] x[m, k]
-// where c' is the codepoint rounded to bf16.  This skips the bf16 rounding of
-// every w_hat = bf16(c . a_hat): each term differs from x . w_hat by at most
-// 2^-8 |x . w_hat| (two bf16 roundings of the same product), so an output
-// differs from the exact-w_hat product by at most 2^-8 sum_k |x w_hat| plus
-// the fp32 accumulation error.
+// w_hat = bf16(c_idx . a_hat) exactly as the dequantiser produces it.
 //
 // Two kernels, launched back to back with programmatic dependent launch:
 //   lora_t_decode_kernel  t = x A^T.  CTA kt covers 256 columns of K; its
@@ -33,17 +27,15 @@
 // 16 x (2 to 4) units are in flight per SM with no register cost.
 //
 // The arithmetic of a unit (one warp): mma.sync m16n8k16 bf16, A = 16 weight
-// rows, B = up to 8 tokens per n-tile, fp32 accumulation.  Each 64-block of
-// the unit gets four MMAs of its own (lane group tq holds block positions
-// 16tq .. 16tq+15; the contraction order inside a block is free, x is read in
-// the same order), so the block's partial sums can be scaled by its a_hat
-// (an fp32 multiply-add per accumulator) before they join the running sums.
-// The A operands come from a 256-entry table in shared memory that maps a
-// packed byte to its two codepoints (bf16x2): one 4-byte load per weight
-// pair, from the lane's own copy of the table (32 copies, so a warp's loads
-// never share a bank).  This keeps the ALU work per weight at a byte extract
-// and an address multiply-add, against a byte-permute table of the block's
-// scaled codepoints that would have to be rebuilt for every block.
+// rows, B = up to 8 tokens per n-tile, fp32 accumulation.  The contraction
+// order inside a unit is free, so lane group tq owns 64-block tq of the unit
+// and MMA j covers positions 4j .. 4j+3 of every lane group's block.  A lane
+// therefore dequantises rows g and g+8 of one block (64 + 64 weights) with
+// two per-block tables T[i] = bf16(c_i . a_hat) indexed by byte permutes (the
+// dequantiser's routine, so the MMA operands are the exact bf16 W_hat), and
+// reads the matching x values from shared memory, where x is stored with a
+// 16-byte XOR swizzle that keeps every fragment load free of bank conflicts.
+// Lanes whose token is past M read a zero row of x.
 //
 // Reduction (fixed order, deterministic, no atomics): a warp's sum over one
 // tile's chunks goes to the CTA's tile sums when the warp covered the whole
@@ -73,17 +65,6 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// D = A B (no accumulator input)
-__device__ __forceinline__ void mma_bf16_zc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                            uint32_t a3, uint32_t b0, uint32_t b1) {
-  const float z = 0.f;
-  asm(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%10,%10,%10,%10};"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
 }
 
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank) {
@@ -194,23 +175,15 @@ __global__ void __launch_bounds__(kTWarps * 32) lora_t_decode_kernel(
 }
 
 // ------------------------------------------------------------ main kernel
-// Codepoint-pair table: entry v (a packed byte: element 2j in the high
-// nibble, 2j+1 in the low) is bf16x2 {bf16(c[v >> 4]), bf16(c[v & 15])},
-// held in kTblCopies copies, entry-major, so that lane L reads copy L and a
-// warp's 32 lookups touch 32 different banks whatever the bytes are.
-constexpr int kTblCopies = 32;
-constexpr int kTblBytes = 256 * kTblCopies * 4;
-
 struct GemvSmem {
-  int ring, tbl, xs, xstride, part, tsum, tfin, bs, wr, bars, err, cbs, total;
+  int ring, xs, xstride, part, tsum, tfin, bs, wr, bars, err, total;
 };
 __host__ __device__ inline GemvSmem gemv_smem(int M, int MT, int slice_chunks, int tiles_max,
                                               int RP, int depth, int S) {
   GemvSmem L;
   L.ring = 0;  // 16 warps x depth slots x 2 KB, 1024-byte aligned
-  L.tbl = L.ring + kGemvWarps * depth * kUnitBytes;
-  L.xs = L.tbl + kTblBytes;
-  L.xstride = slice_chunks * kChunk * 2 + 16;            // bytes per token row (+16: banks)
+  L.xs = L.ring + kGemvWarps * depth * kUnitBytes;
+  L.xstride = slice_chunks * kChunk * 2;                 // bytes per token row
   L.part = L.xs + (M + 1) * L.xstride;                   // x rows, then a zero row
   // [16 warps][2][16 rows][MT] f32 partial sums follow
   L.tsum = L.part + kGemvWarps * 2 * 16 * MT * 4;        // [tiles_max][16 rows][MT] f32
@@ -220,11 +193,17 @@ __host__ __device__ inline GemvSmem gemv_smem(int M, int MT, int slice_chunks, i
   L.bars = L.wr + (2 * tiles_max + kGemvWarps) * 4;      // [16][depth] mbarriers
   L.bars = (L.bars + 7) & ~7;
   L.err = L.bars + kGemvWarps * depth * 8;
-  L.cbs = L.err + 16;                                    // the 16 codepoints (fp32)
-  L.total = L.cbs + 64 + 1024;                           // + alignment slack of the base
+  L.total = L.err + 16 + 1024;                           // + alignment slack of the base
   return L;
 }
 
+
+// Physical 16-byte slot of logical slot s of token row tok in the x tile: a
+// lane's eight fragment loads of one unit, and the loads of the 8 lanes of a
+// quarter warp, fall on distinct bank groups.
+__device__ __forceinline__ int xswz(int tok, int s) {
+  return s ^ (((s >> 3) & 3) | ((tok & 1) << 2));
+}
 
 template <int NT>
 __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
@@ -236,7 +215,6 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
   const int depth = p.depth;
   const GemvSmem SL = gemv_smem(p.M, MT, p.slice_chunks, p.tiles_max, p.RP, depth, p.S);
   const uint32_t ring_u = base + SL.ring;
-  const uint32_t tbl_u = base + SL.tbl;
   const uint32_t xs_u = base + SL.xs;
   float *part = reinterpret_cast<float *>(smem + SL.part);
   float *tsum = reinterpret_cast<float *>(smem + SL.tsum);
@@ -278,7 +256,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
       const int tok = i / spr, s = i - tok * spr;
       const int col = kc0 + s * 8;
       const bool in = tok < p.M && col < p.K;
-      cp_async16(xs_u + tok * SL.xstride + s * 16,
+      cp_async16(xs_u + tok * SL.xstride + xswz(tok, s) * 16,
                  p.x + (in ? (int64_t)tok * p.K + col : 0), in ? 16u : 0u);
     }
     cp_async_commit();
@@ -320,11 +298,9 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
     }
   }
 
-  // ---- 3. the codepoint-pair table; the warp ranges of the tiles for the
-  // combine step (first and last warp of tile t; first tile of warp w)
-  float *cbs = reinterpret_cast<float *>(smem + SL.cbs);
+  // ---- 3. the warp ranges of the tiles for the combine step (first and
+  // last warp of tile t; first tile of warp w)
   int *wr = reinterpret_cast<int *>(smem + SL.wr);
-  if (threadIdx.x < 16) cbs[threadIdx.x] = p.cb.v[threadIdx.x];
   if (threadIdx.x < Tc) {
     auto warp_of = [&](int uu) { return (kGemvWarps * (uu + 1) - 1) / U; };
     wr[2 * threadIdx.x] = warp_of(threadIdx.x * Cc);
@@ -332,12 +308,6 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
   }
   if (threadIdx.x < kGemvWarps)
     wr[2 * p.tiles_max + threadIdx.x] = Cc > 0 ? (U * (int)threadIdx.x / kGemvWarps) / Cc : 0;
-  __syncthreads();
-  for (int i = threadIdx.x; i < 256 * (kTblCopies / 4); i += blockDim.x) {
-    const int v = i / (kTblCopies / 4);
-    const uint32_t e = pack_bf16x2(cbs[v >> 4], cbs[v & 15]);
-    sts_v4(tbl_u + i * 16, e, e, e, e);
-  }
   cp_async_wait<1>();  // this thread's x pieces have landed (the B rows may not have)
 
   // block constant a_hat of weight row n, 64-chunk kc of that row (0 outside W)
@@ -350,14 +320,13 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
     const float a = p.use_code ? __fmul_rn((float)ldg_nc_s8(p.codes + b), cv) : cv;
     return in ? a : 0.f;
   };
-  __syncthreads();  // table and x staged
+  __syncthreads();  // x and the warp ranges staged
 
-  // ---- 4. main loop.  In a unit, block b (columns 64b .. 64b+63 of the
-  // chunk) is contracted by four MMAs of its own: lane group tq holds the
-  // block's positions 16tq .. 16tq+15 (packed bytes 8tq .. 8tq+7), MMA s
-  // taking positions 16tq + 4s .. +3 (bytes 2s, 2s+1).  The four MMAs give
-  // the block's partial dot products, which are then scaled by the block's
-  // a_hat (rows g and g+8) into the running sums.
+  // ---- 4. main loop.  The contraction order inside a unit is free, so lane
+  // group tq owns 64-block tq of the unit and MMA j covers positions
+  // 4j .. 4j+3 of every lane group's block: a lane dequantises rows g and g+8
+  // of one whole block with the block's scaled table (the dequantiser's
+  // routine), so the MMA operands are the exact bf16 w_hat.
   const int tok_lo = g, tok_hi = 8 + g;  // this lane's tokens in n-tiles 0 and 1
   float acc[NT][4];
   int cur = -1, seg = 0;
@@ -375,25 +344,25 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
     }
     ++seg;
   };
-  // a_hat of the lane's two rows in block tq, loaded one unit ahead; the
-  // lane group's four blocks are exchanged with shuffles
+  // a_hat of the lane's two rows in block tq, loaded one unit ahead
   auto ahat_unit = [&](int tile, int chunk, float &a, float &b) {
     const int kc = (c0 + chunk) * 4 + tq;
     a = ahat_of((t0 + tile) * 16 + g, kc);
     b = ahat_of((t0 + tile) * 16 + g + 8, kc);
   };
-  // byte offset of this lane's 8 bytes of block b in a swizzled 128-byte row
-  // (rows g and g + 8 share the pattern: 16-byte granule j sits at j ^ g)
-  uint32_t woff[4];
-#pragma unroll
-  for (int b = 0; b < 4; ++b) woff[b] = ((uint32_t)((2 * b + (tq >> 1)) ^ g) << 4) | ((tq & 1) << 3);
   // Shared-memory reads below are ordinary C++ loads (the compiler schedules
   // them; the mbarrier waits and the proxy fence are compiler barriers).
-  const uint32_t *tlane = reinterpret_cast<const uint32_t *>(smem + SL.tbl) + lane;  // own copy
+  // x slot of (token, block tq, positions 8 wi .. 8 wi + 7) of chunk c: row
+  // tok, slot c * 32 + tq * 8 + (wi ^ x3), x3 = tq | (tok & 1) << 2 (xswz with
+  // (s >> 3) & 3 = tq); lanes whose token is past M read the zero row.
+  int xoff[8];
+#pragma unroll
+  for (int wi = 0; wi < 8; ++wi) xoff[wi] = wi ^ (tq | ((g & 1) << 2));
   const bool xv_lo = tok_lo < p.M, xv_hi = tok_hi < p.M;
-  // lanes whose token is past M read the zero row
-  const uint8_t *xr_lo = smem + SL.xs + (xv_lo ? tok_lo : p.M) * SL.xstride + tq * 32;
-  const uint8_t *xr_hi = smem + SL.xs + (xv_hi ? tok_hi : p.M) * SL.xstride + tq * 32;
+  const uint4 *xr_lo =
+      reinterpret_cast<const uint4 *>(smem + SL.xs + (xv_lo ? tok_lo : p.M) * SL.xstride) + tq * 8;
+  const uint4 *xr_hi =
+      reinterpret_cast<const uint4 *>(smem + SL.xs + (xv_hi ? tok_hi : p.M) * SL.xstride) + tq * 8;
   float ah_g = 0.f, ah_h = 0.f;
   int tile = ut0, chunk = uc0;  // consume cursor
   if (u0 < u1) ahat_unit(tile, chunk, ah_g, ah_h);
@@ -412,56 +381,32 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) qlora_gemv_kernel(
     float nah_g = 0.f, nah_h = 0.f;
     if (i + 1 < u1 - u0) ahat_unit(ntile, nchunk, nah_g, nah_h);
     const uint32_t bar = bars_u + (warp * depth + slot) * 8;
-    // the verdict is made warp-uniform: the loop below shuffles across the warp
     if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar, phase, err_u, p.status))) {
       ok = false;
       break;
     }
+    // this lane's 32 packed bytes of rows g and g + 8, block tq (128-byte swizzle)
     const uint8_t *sb = smem + SL.ring + (warp * depth + slot) * kUnitBytes;
-    uint2 wg[4], wh[4];
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      wg[b] = *reinterpret_cast<const uint2 *>(sb + g * 128 + woff[b]);
-      wh[b] = *reinterpret_cast<const uint2 *>(sb + (g + 8) * 128 + woff[b]);
-    }
+    const uint4 w0 = *reinterpret_cast<const uint4 *>(sb + g * 128 + (((2 * tq) ^ g) << 4));
+    const uint4 w1 = *reinterpret_cast<const uint4 *>(sb + g * 128 + (((2 * tq + 1) ^ g) << 4));
+    const uint4 v0 = *reinterpret_cast<const uint4 *>(sb + (g + 8) * 128 + (((2 * tq) ^ g) << 4));
+    const uint4 v1 =
+        *reinterpret_cast<const uint4 *>(sb + (g + 8) * 128 + (((2 * tq + 1) ^ g) << 4));
     ++done;
-    const int xc = chunk * (kChunk * 2);
+    const Nf4Table tg = make_table(ah_g, p.cb), th = make_table(ah_h, p.cb);
+    const uint32_t wg[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    const uint32_t wh[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    const uint4 *xlo = xr_lo + chunk * 32, *xhi = xr_hi + chunk * 32;
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const float sg = __shfl_sync(0xffffffffu, ah_g, (g << 2) | b);
-      const float sh = __shfl_sync(0xffffffffu, ah_h, (g << 2) | b);
-      uint4 x0[NT], x1[NT];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const uint4 *xa = reinterpret_cast<const uint4 *>((nt == 0 ? xr_lo : xr_hi) + xc + b * 128);
-        x0[nt] = xa[0];
-        x1[nt] = xa[1];
-      }
-      float d[NT][4];
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const uint32_t wgw = s < 2 ? wg[b].x : wg[b].y, whw = s < 2 ? wh[b].x : wh[b].y;
-        const uint32_t j0 = (s & 1) * 2;  // bytes j0, j0 + 1 of the word
-        const uint32_t a0 = tlane[prmt(wgw, 0u, 0x4440u | j0) * kTblCopies];
-        const uint32_t a2 = tlane[prmt(wgw, 0u, 0x4441u | j0) * kTblCopies];
-        const uint32_t a1 = tlane[prmt(whw, 0u, 0x4440u | j0) * kTblCopies];
-        const uint32_t a3 = tlane[prmt(whw, 0u, 0x4441u | j0) * kTblCopies];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const uint32_t b0 = s == 0 ? x0[nt].x : s == 1 ? x0[nt].z : s == 2 ? x1[nt].x : x1[nt].z;
-          const uint32_t b1 = s == 0 ? x0[nt].y : s == 1 ? x0[nt].w : s == 2 ? x1[nt].y : x1[nt].w;
-          if (s == 0)
-            mma_bf16_zc(d[nt], a0, a1, a2, a3, b0, b1);
-          else
-            mma_bf16(d[nt], a0, a1, a2, a3, b0, b1);
-        }
-      }
+    for (int wi = 0; wi < 8; ++wi) {
+      uint32_t og[4], oh[4];
+      lookup8(tg, wg[wi], og);
+      lookup8(th, wh[wi], oh);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        acc[nt][0] = fmaf(sg, d[nt][0], acc[nt][0]);
-        acc[nt][1] = fmaf(sg, d[nt][1], acc[nt][1]);
-        acc[nt][2] = fmaf(sh, d[nt][2], acc[nt][2]);
-        acc[nt][3] = fmaf(sh, d[nt][3], acc[nt][3]);
+        const uint4 xv = (nt == 0 ? xlo : xhi)[xoff[wi]];
+        mma_bf16(acc[nt], og[0], oh[0], og[1], oh[1], xv.x, xv.y);
+        mma_bf16(acc[nt], og[2], oh[2], og[3], oh[3], xv.z, xv.w);
       }
     }
     // the slot's bytes are in registers and used: refill it with the unit

@@ -6,12 +6,9 @@
  *     quantisation of the block constants,
  *   - dequantisation of that weight to bf16,
  *   - the forward pass  y = x . W_hat^T + (x . A^T) . B^T . alpha / r
- *     (a fused dequantise + tensor-core GEMM for M > 16 tokens, which
- *     computes with the exact bf16 W_hat the dequantiser produces, and a
- *     memory-bound decode GEMV streaming the packed weights for M <= 16,
- *     which scales each 64-block's dot product of bf16 codepoints by the
- *     block constant in fp32: within 2^-8 sum|x . W_hat| of the exact-W_hat
- *     product per output, plus the fp32 accumulation error),
+ *     (a fused dequantise + tensor-core GEMM for M > 16 tokens, a
+ *     memory-bound decode GEMV streaming the packed weights for M <= 16;
+ *     both compute with the exact bf16 W_hat the dequantiser produces),
  *   - the backward pass dX, dA and dB with the NF4 buffers frozen.
  *
  * Sources of each operation (page title -- section):

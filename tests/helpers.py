@@ -49,31 +49,3 @@ def assert_close(got, ref, what: str, max_abs: float = MAX_ABS, rel_fro: float =
         f"{what}: max|err|={ma:.3e} (tol {max_abs:.0e}), rel-Frobenius={rf:.3e} (tol {rel_fro:.0e})")
     return ma, rf
 
-
-def gemv_bound(x, w_hat) -> np.ndarray:
-    """Per-output error bound of the decode GEMV against the exact-w_hat
-    product: the GEMV scales each block's dot product of bf16 codepoints by
-    the block constant instead of rounding every w_hat = bf16(c a_hat), so a
-    term c' a_hat x differs from w_hat x by at most 2^-8 (1 + 2^-8) |w_hat x|
-    (c' = bf16(c) and w_hat each within 2^-9 of c and c a_hat); the fp32
-    accumulation (64 terms per block, then K/64 block sums) adds at most
-    (K/64 + 66) 2^-23 of the same magnitude sum."""
-    x = np.abs(np.asarray(x, dtype=np.float64))
-    w = np.abs(np.asarray(w_hat, dtype=np.float64))
-    K = w.shape[1]
-    return (2.0 ** -8 * (1 + 2.0 ** -8) + (K / 64 + 66) * 2.0 ** -23) * (x @ w.T)
-
-
-def assert_close_bound(got, ref, bound, what: str, rel_fro: float = REL_FRO):
-    """Every |got - ref| within its bound (plus 1e-5 |ref| + 1e-6 for the
-    fp32 LoRA term), and the relative Frobenius error within rel_fro."""
-    got = np.asarray(got, dtype=np.float64)
-    ref = np.asarray(ref, dtype=np.float64)
-    lim = np.asarray(bound, dtype=np.float64) + 1e-5 * np.abs(ref) + 1e-6
-    diff = np.abs(got - ref)
-    bad = diff > lim
-    ma, rf = errors(got, ref)
-    assert not bad.any() and rf <= rel_fro, (
-        f"{what}: {int(bad.sum())} outputs beyond their bound (worst |err|/bound "
-        f"{float(np.max(diff / lim)):.3g}), rel-Frobenius={rf:.3e} (tol {rel_fro:.0e})")
-    return ma, rf

@@ -7,8 +7,7 @@
     dA, dB; saved and recomputed t) against the fp64 oracle with that mask;
   * p = 0 gives exactly the results of the calls without dropout;
   * the full gate projection at 2048 tokens.
-Tolerance: max |err| <= 2e-2 and relative Frobenius error <= 1e-2 (the decode
-GEMV: each output within its derived bound, helpers.gemv_bound)."""
+Tolerance: max |err| <= 2e-2 and relative Frobenius error <= 1e-2."""
 import numpy as np
 import pytest
 import torch
@@ -16,7 +15,7 @@ import torch
 from bit_nf4_quantized_35_b300 import capi, inputs
 from oracle import oracle
 
-from .helpers import assert_close, assert_close_bound, gemv_bound, to_np_f32
+from .helpers import assert_close, to_np_f32
 
 pytestmark = pytest.mark.gpu
 
@@ -101,8 +100,7 @@ def test_dropout_decode_gemv():
     y_ref, t_ref = oracle.linear_fwd(d["x"].float().numpy(), w_hat, d["A"].float().numpy(),
                                      d["B"].float().numpy(), shape.alpha, keep=keep,
                                      p=np.float32(0.2))
-    assert_close_bound(to_np_f32(y), y_ref, gemv_bound(d["x"].float().numpy(), w_hat),
-                       "y gemv dropout")
+    assert_close(to_np_f32(y), y_ref, "y gemv dropout")
     assert_close(to_np_f32(t), t_ref, "t gemv dropout", max_abs=1e-3, rel_fro=1e-5)
 
 

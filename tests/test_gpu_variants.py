@@ -7,11 +7,9 @@ input ranges beyond N(0, 1), against the fp64 oracle.
   decode GEMV) and on the backward.
 - The decode GEMV at K = 14336 with heavy-tailed activations (N(0, 4) with
   +-30 outliers) and a LoRA factor A holding entries beyond the f16 range
-  (|a| > 65504): the GEMV must accept every bf16 A, as the tensor-core path
-  does.
-Tolerance: max |err| <= 2e-2 and relative Frobenius error <= 1e-2; decode GEMV
-outputs each within their derived bound (helpers.gemv_bound) and the same
-relative Frobenius error."""
+  (|a| > 65504): the GEMV must compute with the exact bf16 W_hat and accept
+  every bf16 A, as the tensor-core path does.
+Tolerance: max |err| <= 2e-2 and relative Frobenius error <= 1e-2."""
 import numpy as np
 import pytest
 import torch
@@ -19,7 +17,7 @@ import torch
 from bit_nf4_quantized_35_b300 import capi, inputs
 from oracle import oracle
 
-from .helpers import assert_close, assert_close_bound, gemv_bound, to_np_f32
+from .helpers import assert_close, to_np_f32
 
 pytestmark = pytest.mark.gpu
 
@@ -59,11 +57,7 @@ def test_forward_storage_formats(fmt, path):
     assert ws.device_status() == 0
     y_ref, t_ref = oracle.linear_fwd(d["x"].float().numpy(), w_hat, d["A"].float().numpy(),
                                      d["B"].float().numpy(), shape.alpha)
-    what = f"y {shape.name} {path} block {block} group {group}"
-    if path == "gemv":
-        assert_close_bound(to_np_f32(y), y_ref, gemv_bound(d["x"].float().numpy(), w_hat), what)
-    else:
-        assert_close(to_np_f32(y), y_ref, what)
+    assert_close(to_np_f32(y), y_ref, f"y {shape.name} {path} block {block} group {group}")
     assert_close(to_np_f32(t), t_ref, f"t {shape.name} {path}", max_abs=1e-3, rel_fro=1e-5)
 
 
@@ -119,10 +113,7 @@ def test_gemv_heavy_tailed_inputs_wide_k(M):
         assert ws.device_status() == 0
         yv = to_np_f32(y)
         assert np.all(np.isfinite(yv)), f"{path}: non-finite outputs"
-        if path == "gemv":
-            assert_close_bound(yv, y_ref, gemv_bound(np_["x"], w_hat), f"y {shape.name} {path}")
-        else:
-            assert_close(yv, y_ref, f"y {shape.name} {path}")
+        assert_close(yv, y_ref, f"y {shape.name} {path}")
         # t ~ 1e5 here: fp32 accumulation, checked relative to its size
         tv = to_np_f32(t)
         assert_close(tv, t_ref, f"t {shape.name} {path}",
