@@ -377,6 +377,8 @@ qlora_status qlora_merge_lora(const qlora_nf4_weight *w, const uint16_t *A, cons
   a.s = alpha / (float)r;
   a.out = W_out;
   a.cb = tables(w->codebook).cb;
+  a.k31 = 0x80000000u;
+  a.k16 = 0x10000u;
   return cuda_status(launch_merge(a, static_cast<cudaStream_t>(stream)));
 }
 

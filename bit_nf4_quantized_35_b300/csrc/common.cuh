@@ -91,14 +91,15 @@ __device__ __forceinline__ Nf4Table make_table(float ahat, const Codebook &cb) {
 
 // Dequantise the 8 indices of one packed 32-bit word (byte j holds elements
 // 2j [high nibble] and 2j+1 [low nibble]) to 8 bf16 values, element e in
-// half (e & 1) of out[e >> 1].
-__device__ __forceinline__ void lookup8(const Nf4Table &t, uint32_t w, uint32_t out[4]) {
-  const uint32_t m = w & 0x77777777u;                          // low 3 bits of each index
-  const uint32_t s = ((w >> 1) & 0x44444444u) | 0x32103210u;   // bit 3 -> byte chooser
+// half (e & 1) of out[e >> 1].  m = w & 0x77777777 holds the low 3 bits of
+// each index, s = ((w >> 1) & 0x44444444) | 0x32103210 chooses the byte by
+// bit 3; m_hi and s_hi are m >> 16 and s >> 16.
+__device__ __forceinline__ void lookup8_parts(const Nf4Table &t, uint32_t m, uint32_t s,
+                                              uint32_t m_hi, uint32_t s_hi, uint32_t out[4]) {
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const uint32_t mh = h ? (m >> 16) : m;
-    const uint32_t sh = h ? (s >> 16) : s;
+    const uint32_t mh = h ? m_hi : m;
+    const uint32_t sh = h ? s_hi : s;
     const uint32_t la = prmt(t.lo[0], t.lo[1], mh);
     const uint32_t lb = prmt(t.lo[2], t.lo[3], mh);
     const uint32_t ha = prmt(t.hi[0], t.hi[1], mh);
@@ -109,6 +110,26 @@ __device__ __forceinline__ void lookup8(const Nf4Table &t, uint32_t w, uint32_t 
     out[2 * h + 0] = prmt(lo, hi, 0x4051u);
     out[2 * h + 1] = prmt(lo, hi, 0x6273u);
   }
+}
+__device__ __forceinline__ void lookup8(const Nf4Table &t, uint32_t w, uint32_t out[4]) {
+  const uint32_t m = w & 0x77777777u;
+  const uint32_t s = ((w >> 1) & 0x44444444u) | 0x32103210u;
+  lookup8_parts(t, m, s, m >> 16, s >> 16, out);
+}
+// The same with the three right shifts done as high-word multiplies by
+// k31 = 2^31 and k16 = 2^16 (kernel parameters, so that the compiler cannot
+// turn them back into shifts): they then run on the multiply pipe instead of
+// the integer pipe that carries the byte permutes.
+__device__ __forceinline__ uint32_t mul_hi_u32(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.hi.u32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ void lookup8_mulhi(const Nf4Table &t, uint32_t w, uint32_t out[4],
+                                              uint32_t k31, uint32_t k16) {
+  const uint32_t m = w & 0x77777777u;
+  const uint32_t s = (mul_hi_u32(w, k31) & 0x44444444u) | 0x32103210u;
+  lookup8_parts(t, m, s, mul_hi_u32(m, k16), mul_hi_u32(s, k16), out);
 }
 
 // Bit mask of 8 bf16 elements (bits of `byte`, element e = bit e) as four

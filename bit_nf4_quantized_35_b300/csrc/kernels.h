@@ -130,6 +130,7 @@ struct MergeArgs {
   float s;
   uint16_t *out;  // [N, K] bf16
   Codebook cb;
+  uint32_t k31, k16;  // 2^31 and 2^16 (multipliers of lookup8_mulhi)
 };
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s);
 

@@ -10,7 +10,8 @@
 // B rows while it computes the current one; a CTA of 8 warps shares the chunk
 // of A, staged once in shared memory.
 //   - w_hat: lane (g, tq) dequantises rows g and g+8 of block tq with the
-//     per-block byte-permute table (the dequantiser's routine: exact bf16).
+//     per-block byte-permute table (the dequantiser's routine: exact bf16),
+//     its shifts on the multiply pipe (the integer pipe is the busier one).
 //   - B A: bf16 mma.sync m16n8k16 (fp32 accumulation), A-operand = 16 rows
 //     of B, B-operand = A.  The columns of n-tile j are mapped to positions
 //     2j, 2j+1 of each lane group's block (column c -> block c / 2, position
@@ -133,8 +134,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_lora_kernel(const Merg
 #pragma unroll
     for (int wi = 0; wi < 8; ++wi) {
       uint32_t o0[4], o1[4];
-      lookup8(t0, w0[wi], o0);
-      lookup8(t1, w1[wi], o1);
+      lookup8_mulhi(t0, w0[wi], o0, p.k31, p.k16);
+      lookup8_mulhi(t1, w1[wi], o1, p.k31, p.k16);
       uint32_t r0[4], r1[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
