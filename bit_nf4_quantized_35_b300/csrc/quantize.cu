@@ -31,18 +31,18 @@ namespace qlora {
 // Decision tables of the nearest-codepoint rule (built on the host from the
 // 15 thresholds; see launch_quantize):
 //   th[k]     the thresholds: index = #{k : x >= th[k]} (th[15] = 2)
-//   bth[j]    for the 1/16-wide bucket j of [-1, 1] (x in [e_j, e_j + 1/16),
-//             e_j = -1 + j/16, or -1 + (j - 1/2)/16 with the shifted grid),
-//             the one threshold inside it, or 2 when none
-//   bbase[j]  #{k : th[k] < e_j}
-// Entries past the last bucket repeat it and entry 63 repeats bucket 0: the
-// bucket arithmetic below yields them for x just above 1 and just below -1.
+//   for the 1/16-wide bucket i of [-1, 1] (x in [-1 + i/16, -1 + (i + 1)/16),
+//   i = -1 .. 32), at slot i + 1:
+//   thp[]     the largest float below the one threshold inside the bucket
+//             (2 when there is none)
+//   base[]    the number of thresholds below the bucket
+// (two 34-word arrays: a warp's lookups then meet no bank conflict unless two
+// lanes hold elements near -1 and near +1 at once)
 struct QuantTables {
   float th[16];
-  float bth[64];
-  int bbase[64];
-  float bias;      // 15.5: buckets start at -1 + j/16; 16: at -1 + (j - 1/2)/16
-  int exact_only;  // 1: the tables do not fit the bucket rule; divide every element
+  float thp[34];
+  int base[34];
+  int exact_only;  // 1: some bucket holds two thresholds; divide every element
 };
 
 // Number of thresholds <= x, by bisection over the sorted thresholds.
@@ -59,14 +59,15 @@ __device__ __forceinline__ int nf4_index(float x, const float *th) {
 __device__ __forceinline__ constexpr int nib_shift(int e) { return 8 * (e >> 1) + ((e & 1) ? 0 : 4); }
 
 // Band (absolute, in normalised units) around each threshold inside which
-// the reciprocal-based value may fall on the other side of the threshold
-// than the IEEE quotient.  With y the hardware reciprocal (rcp.approx: at
-// most 1 ulp from 1/a, so y = (1/a)(1 + d1) with |d1| <= 2^-23 for a normal
-// a and y) and xn' = RN(w . y):
-//   xn' = (w/a)(1 + d1)(1 + d2),  RN(w/a) = (w/a)(1 + d3),  |d2|, |d3| <= 2^-24,
-// so |xn' - RN(w/a)| < 2^-21.4 |w/a| <= 2^-21.4 (normal range; a subnormal xn'
-// is at most 2^-126 from it, far from every threshold).  Outside a band of
-// 2^-20 both lie on the same side of the threshold.
+// the reciprocal-based decision may differ from the one on the IEEE quotient.
+// With y the hardware reciprocal (rcp.approx: at most 1 ulp from 1/a, so
+// y = (1/a)(1 + d1) with |d1| <= 2^-23 for a normal a and y), the fast path
+// compares the exact product z = w y (inside an FMA) with thp = pred(th):
+//   z = (w/a)(1 + d1),  RN(w/a) = (w/a)(1 + d3),  |d3| <= 2^-24,
+// so |z - RN(w/a)| < 2^-22.4 |w/a| <= 2^-22.4.  If [z > thp] and
+// [RN(w/a) >= th] differ, then |thp - z| <= 2^-22.4 (RN(w/a) >= th means
+// RN(w/a) > thp, and RN(w/a) < th means RN(w/a) <= thp), so every element
+// whose |RN(thp - z)| is at least 2^-20 is decided the same way by both.
 constexpr float kQuantBand = 9.5367431640625e-07f;  // 2^-20
 
 // kR = block / 64.  A CTA of T threads takes groups of 256 consecutive
@@ -113,8 +114,7 @@ __global__ void __launch_bounds__(quant_threads<kBf16In, kR>()) quantize_nf4_ker
                                                              const QuantTables tab) {
   extern __shared__ __align__(128) uint8_t qsm[];  // [stage][group input]; mbarriers at the end
   __shared__ float th_s[16];
-  __shared__ float bth_s[64];
-  __shared__ int bbase1_s[64];
+  __shared__ uint32_t bt_s[68];  // thp[34] then base[34]
   __shared__ float amax_s[2][256];  // block maxima of the last two groups
   __shared__ float wmax_s[8];
   __shared__ uint32_t qerr_s;
@@ -132,9 +132,9 @@ __global__ void __launch_bounds__(quant_threads<kBf16In, kR>()) quantize_nf4_ker
   const uint32_t sm_u = smem_u32(qsm);
   const uint32_t bars_u = sm_u + kQStages * kStage;  // kQStages mbarriers (kBulk)
   if (tid < 16) th_s[tid] = tab.th[tid];
-  if (tid < 64) {
-    bth_s[tid] = tab.bth[tid];
-    bbase1_s[tid] = tab.bbase[tid] + 1;
+  if (tid < 34) {
+    bt_s[tid] = __float_as_uint(tab.thp[tid]);
+    bt_s[34 + tid] = (uint32_t)tab.base[tid];
   }
   if (kBulk && tid < kQStages) mbar_init(bars_u + tid * 8, 1);
   if (tid == 0) qerr_s = 0u;
@@ -259,38 +259,54 @@ __global__ void __launch_bounds__(quant_threads<kBf16In, kR>()) quantize_nf4_ker
         if (nf) {
           mb = mf;
           ++nonfinite;
+          // the block's non-finite elements become zeros (their indices are
+          // unspecified), so that every element below is a finite |w| <= amax
+#pragma unroll
+          for (int q = 0; q < kWords; ++q) {
+            uint32_t v = raw[p][q];
+            if (kBf16In) {
+              if ((v & 0x7f800000u) == 0x7f800000u) v &= 0x0000ffffu;
+              if ((v & 0x00007f80u) == 0x00007f80u) v &= 0xffff0000u;
+            } else if ((v & 0x7f800000u) == 0x7f800000u) {
+              v = 0u;
+            }
+            raw[p][q] = v;
+          }
         }
       }
       const float amax = __uint_as_float(mb);
       if (li == 0 && (sub % kR) == 0) amax_s[it & 1][c / kR] = amax;  // 0 past the end
-      // Fast path: xn' = w . y with y the hardware reciprocal of a (within 1
-      // ulp of 1/a) and the bucket tables; an element whose xn' lies within
-      // the band of a threshold is decided again with the IEEE quotient.
-      // Block constants outside [2^-126, 2^126] (reciprocal out of the normal
-      // range) take the IEEE path for every element.
-      const bool fast = !tab.exact_only && amax >= 1.17549435e-38f && amax <= 8.50705917e+37f;
+      // Fast path: y the hardware reciprocal of a (within 1 ulp of 1/a);
+      // the bucket of z = w y and its threshold test are one FMA each, and
+      // an element whose test lies within the band is decided again with
+      // the IEEE quotient.  Block constants outside [2^-120, 2^120] take the
+      // IEEE path for every element (y = 0 keeps their buckets in range).
+      const bool fast = !tab.exact_only && amax >= 0x1p-120f && amax <= 0x1p120f;
       float y;
       asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(amax));
+      y = fast ? y : 0.0f;
+      const float y16 = y * 16.0f;
+      // u = RD(16 w y + 16 + 1.5 . 2^23) = 1.5 . 2^23 + i, i = floor(16 z + 16)
+      // in [-1, 32] (|w| <= a), exactly (one rounding, toward -inf, to the
+      // integers); the bit pattern of u is 0x4b400000 + i, so thp[i + 1]
+      // lies at bits(u) . 4 + (bt_s + 4 - 0x4b400000 . 4), modulo 2^32, and
+      // base[i + 1] 136 bytes further.
+      const uint32_t tb = smem_u32(bt_s) + 4u - 0x2d000000u;
       uint32_t word = 0;
-      float dmin = 1.0f;  // smallest |xn' - threshold| of the lane's elements
+      float dmin = 1.0f;  // smallest |thp - z| of the lane's elements
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float xn = __fmul_rn(elem(p, e), y);
-        // bucket floor(16 xn + 16): v = 16 xn + 15.5 (one rounding, off by at
-        // most 2^-20), then v + 1.5 * 2^23 rounds to the nearest integer of v,
-        // which lands in the low mantissa bits (the unit is bit 0 there).  An
-        // element within 2^-20 of a bucket edge may take the neighbouring
-        // bucket, which gives the same index (no threshold within 2^-10 of an
-        // edge).
-        const float v = __fmaf_rn(xn, 16.0f, tab.bias);
-        const float u = __fadd_rn(v, 12582912.0f);
-        const int j = __float_as_int(u) & 63;
-        const float d = __fsub_rn(xn, bth_s[j]);
+        const float w = elem(p, e);
+        const float u = __fmaf_rd(w, y16, 12582928.0f);
+        const uint32_t ad = __float_as_uint(u) * 4u + tb;
+        uint32_t thp, base;
+        asm("ld.shared.u32 %0, [%2];\n\tld.shared.u32 %1, [%2+136];"
+            : "=r"(thp), "=r"(base)
+            : "r"(ad));
+        // d = RN(thp - z): negative exactly when z > thp (a zero is +0)
+        const float d = fmaf(-w, y, __uint_as_float(thp));
         dmin = fminf(dmin, fabsf(d));
-        // index = #{thresholds below the bucket} + (d >= 0): bbase1 holds the
-        // count plus one, and the sign bit of d takes the one away (d is +0,
-        // never -0, when xn' equals the threshold)
-        const uint32_t q = (uint32_t)bbase1_s[j] - (__float_as_uint(d) >> 31);
+        const uint32_t q = base + (__float_as_uint(d) >> 31);
         word |= q << nib_shift(e);
       }
       // The vote is taken by every lane of the warp (lanes of all-zero
@@ -380,50 +396,31 @@ __global__ void __launch_bounds__(256) dequant_nf4_kernel(const uint8_t *__restr
 
 // ----------------------------------------------------------- host launchers
 // Bucket tables for the fast decision path, from the 15 sorted thresholds.
-// Valid when every 1/16-wide bucket of [-1, 1] holds at most one threshold
-// and no threshold lies within 2^-10 of a bucket edge (an element whose
-// bucket is computed from the reciprocal-based value, up to 2^-22 off, then
-// still gets the bucket's answer); otherwise every element is divided.
-static bool fill_quant_tables(const float th[15], double shift, QuantTables &t) {
+// The bucket of an element is found exactly, so the tables are valid when no
+// 1/16-wide bucket holds two thresholds (true of both codebooks, whose
+// thresholds lie more than 1/16 apart); otherwise every element is divided.
+static void build_quant_tables(const float th[15], QuantTables &t) {
   for (int i = 0; i < 15; ++i) t.th[i] = th[i];
   t.th[15] = 2.0f;
-  t.bias = (float)(15.5 + shift);  // bucket j = floor(16 x + 16 + shift)
   bool ok = true;
-  const int nb = shift > 0 ? 33 : 32;  // buckets covering [-1, 1]
-  for (int j = 0; j < 64; ++j) {
-    const int jj = j < nb ? j : (j == 63 ? 0 : nb - 1);
-    const double lo = -1.0 + (jj - shift) / 16.0, hi = lo + 1.0 / 16.0;
+  for (int s = 0; s < 34; ++s) {
+    const double lo = -1.0 + (s - 1) / 16.0, hi = lo + 1.0 / 16.0;
     int base = 0, inside = 0;
     float th_in = 2.0f;
     for (int k = 0; k < 15; ++k) {
       const double v = th[k];
-      if (v < lo) ++base;
-      if (v >= lo && v < hi) {
+      if (v < lo) {
+        ++base;
+      } else if (v < hi) {
         ++inside;
         th_in = th[k];
       }
-      if (std::fabs(v - lo) < 1.0 / 1024 || std::fabs(v - hi) < 1.0 / 1024) ok = false;
     }
     if (inside > 1) ok = false;
-    t.bth[j] = th_in;
-    t.bbase[j] = base;
+    t.thp[s] = inside ? std::nextafterf(th_in, -INFINITY) : 2.0f;
+    t.base[s] = base;
   }
-  return ok;
-}
-
-// Bucket tables for the fast decision path, from the 15 sorted thresholds.
-// Valid when every 1/16-wide bucket holds at most one threshold and no
-// threshold lies within 2^-10 of a bucket edge (an element whose bucket is
-// computed from the reciprocal-based value, up to 2^-22 off, then still gets
-// the bucket's answer).  The grid starting at -1 is tried first, then the one
-// shifted by half a bucket (the quantile table has a threshold at 0); when
-// neither fits, every element is divided.
-static void build_quant_tables(const float th[15], QuantTables &t) {
-  t.exact_only = 0;
-  if (fill_quant_tables(th, 0.0, t)) return;
-  if (fill_quant_tables(th, 0.5, t)) return;
-  fill_quant_tables(th, 0.0, t);
-  t.exact_only = 1;
+  t.exact_only = ok ? 0 : 1;
 }
 
 template <bool kBf16In, int kR>
