@@ -379,7 +379,18 @@ qlora_status qlora_merge_lora(const qlora_nf4_weight *w, const uint16_t *A, cons
   a.cb = tables(w->codebook).cb;
   a.k31 = 0x80000000u;
   a.k16 = 0x10000u;
-  return cuda_status(launch_merge(a, static_cast<cudaStream_t>(stream)));
+  // W_out as [N][K / 64][64] bf16: one box is a 16-row x 256-column tile
+  auto fn = encode_fn();
+  if (!fn) return QLORA_ERR_CUDA;
+  CUtensorMap tmO;
+  const cuuint64_t dims[3] = {64, (cuuint64_t)w->cols / 64, (cuuint64_t)w->rows};
+  const cuuint64_t strides[2] = {128, (cuuint64_t)w->cols * 2};
+  const cuuint32_t box[3] = {64, 4, 16}, estr[3] = {1, 1, 1};
+  if (fn(&tmO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, W_out, dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return QLORA_ERR_CUDA;
+  return cuda_status(launch_merge(tmO, a, static_cast<cudaStream_t>(stream)));
 }
 
 qlora_status qlora_workspace_size(int64_t M, int64_t N, int64_t K, int32_t r, size_t *bytes) {

@@ -20,7 +20,14 @@
 //   - A chunk in shared memory as [256 columns][RP ranks] bf16 with the
 //     ranks of a row interleaved (0 1 8 9 2 3 10 11 ...) so that a lane's two
 //     B-operand words are one 8-byte load.
-//   - epilogue: fp32 w_hat + s . (B A), one rounding to bf16, 16-byte stores.
+//   - epilogue: fp32 w_hat + s . (B A), one rounding to bf16, into the warp's
+//     8 KB staging tile in shared memory (the 128-byte swizzle of a tensor
+//     map: 16-byte chunk q of 128-byte line L at L . 128 + (q ^ (L & 7)) . 16,
+//     which keeps the eight lanes of each store phase on distinct banks), then
+//     one TMA tensor store of the 16 x 256 tile (rows past N and blocks past
+//     K / 64 are clipped by the copy).  Storing each lane's 16 bytes straight
+//     to global memory instead touches 32 rows' lines per instruction and
+//     took twice as long.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -28,6 +35,11 @@ namespace qlora {
 
 constexpr int kMergeWarps = 8;
 constexpr int kMergeTilesPerWarp = 4;
+constexpr int kMergeTileBytes = 16 * 256 * 2;  // one warp's staged output tile
+
+// Dynamic shared memory of the kernel: the warps' output tiles (1024-byte
+// aligned for the swizzle; 1024 bytes of slack), then the A chunk.
+static int merge_smem_bytes(int ks) { return 1024 + kMergeWarps * kMergeTileBytes + 256 * ks * 16 * 2; }
 
 // A plain register function (no volatile), so that the compiler can
 // interleave the MMAs with the loads and the table lookups.
@@ -47,9 +59,15 @@ __device__ __forceinline__ int rank_slot(int j) {
 }
 
 template <int KS>  // KS = RP / 16 rank steps
-__global__ void __launch_bounds__(kMergeWarps * 32) merge_lora_kernel(const MergeArgs p) {
-  __shared__ __align__(16) uint16_t as[256 * KS * 16];
+__global__ void __launch_bounds__(kMergeWarps * 32)
+    merge_lora_kernel(const __grid_constant__ CUtensorMap tmO, const MergeArgs p) {
+  extern __shared__ uint8_t msm_raw[];
+  const uint32_t raw_u = smem_u32(msm_raw);
+  const uint32_t tiles_u = (raw_u + 1023u) & ~1023u;
+  uint16_t *as = reinterpret_cast<uint16_t *>(msm_raw + (tiles_u - raw_u) +
+                                              kMergeWarps * kMergeTileBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t obuf = tiles_u + warp * kMergeTileBytes;
   const int g = lane >> 2, tq = lane & 3;
   const int chunk = blockIdx.y;
   const int kc0 = chunk * 256;
@@ -122,15 +140,17 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_lora_kernel(const Merg
     TileIn nxt;
     const bool more = tile + tstride < ntiles;
     if (more) fetch(tile + tstride, nxt);
-    const int n0 = tile * 16 + g, n1 = n0 + 8;
-    const bool ok0 = kin && n0 < p.N, ok1 = kin && n1 < p.N;
     const Nf4Table t0 = make_table(cur.ah0, p.cb), t1 = make_table(cur.ah1, p.cb);
+    // the previous tile's store has read the staging tile
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    __syncwarp();
     const uint32_t w0[8] = {cur.l0.x, cur.l0.y, cur.l0.z, cur.l0.w,
                             cur.h0.x, cur.h0.y, cur.h0.z, cur.h0.w};
     const uint32_t w1[8] = {cur.l1.x, cur.l1.y, cur.l1.z, cur.l1.w,
                             cur.h1.x, cur.h1.y, cur.h1.z, cur.h1.w};
-    uint16_t *out0 = p.out + (int64_t)n0 * p.K + (int64_t)blk * 64;
-    uint16_t *out1 = p.out + (int64_t)n1 * p.K + (int64_t)blk * 64;
+    // 128-byte lines of rows g and g + 8 in block tq (same swizzle: 32 lines apart)
+    const uint32_t line0 = g * 4 + tq;
+    const uint32_t row0_u = obuf + line0 * 128, row1_u = row0_u + 32 * 128;
 #pragma unroll
     for (int wi = 0; wi < 8; ++wi) {
       uint32_t o0[4], o1[4];
@@ -150,15 +170,31 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_lora_kernel(const Merg
         r0[q] = pack_bf16x2(fmaf(p.s, d[0], bf16_lo(o0[q])), fmaf(p.s, d[1], bf16_hi(o0[q])));
         r1[q] = pack_bf16x2(fmaf(p.s, d[2], bf16_lo(o1[q])), fmaf(p.s, d[3], bf16_hi(o1[q])));
       }
-      if (ok0) *reinterpret_cast<uint4 *>(out0 + wi * 8) = make_uint4(r0[0], r0[1], r0[2], r0[3]);
-      if (ok1) *reinterpret_cast<uint4 *>(out1 + wi * 8) = make_uint4(r1[0], r1[1], r1[2], r1[3]);
+      const uint32_t q16 = (wi ^ (line0 & 7)) << 4;
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row0_u + q16), "r"(r0[0]),
+                   "r"(r0[1]), "r"(r0[2]), "r"(r0[3]) : "memory");
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row1_u + q16), "r"(r1[0]),
+                   "r"(r1[1]), "r"(r1[2]), "r"(r1[3]) : "memory");
+    }
+    fence_proxy_async_smem();  // the tile's generic-proxy writes, before the async store
+    __syncwarp();
+    if (lane == 0) {
+      asm volatile(
+          "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];"
+          ::"l"(reinterpret_cast<uint64_t>(&tmO)), "r"(0), "r"(chunk * 4), "r"(tile * 16),
+          "r"(obuf)
+          : "memory");
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
     }
     if (more) cur = nxt;
   }
+  // every store of the warp complete before the CTA ends
+  if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s) {
+cudaError_t launch_merge(const CUtensorMap &tmO, const MergeArgs &a, cudaStream_t s) {
   if (a.N == 0 || a.K == 0) return cudaSuccess;
+  static bool attr_set[5] = {false, false, false, false, false};
   const int tiles = (a.N + 15) / 16;
   // each warp takes up to kMergeTilesPerWarp row tiles of its chunk
   const int per_cta = kMergeWarps * kMergeTilesPerWarp;
@@ -170,11 +206,22 @@ cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s) {
   cfg.attrs = at;
   cfg.numAttrs = 1;
   const int ks = (a.r + 15) / 16;
+  if (ks < 1 || ks > 4) return cudaErrorInvalidValue;
+  cfg.dynamicSmemBytes = merge_smem_bytes(ks);
+  auto go = [&](auto kern) -> cudaError_t {
+    if (!attr_set[ks]) {
+      const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)cfg.dynamicSmemBytes);
+      if (e != cudaSuccess) return e;
+      attr_set[ks] = true;
+    }
+    return cudaLaunchKernelEx(&cfg, kern, tmO, a);
+  };
   switch (ks) {
-    case 1: return cudaLaunchKernelEx(&cfg, merge_lora_kernel<1>, a);
-    case 2: return cudaLaunchKernelEx(&cfg, merge_lora_kernel<2>, a);
-    case 3: return cudaLaunchKernelEx(&cfg, merge_lora_kernel<3>, a);
-    case 4: return cudaLaunchKernelEx(&cfg, merge_lora_kernel<4>, a);
+    case 1: return go(merge_lora_kernel<1>);
+    case 2: return go(merge_lora_kernel<2>);
+    case 3: return go(merge_lora_kernel<3>);
+    case 4: return go(merge_lora_kernel<4>);
   }
   return cudaErrorInvalidValue;
 }
