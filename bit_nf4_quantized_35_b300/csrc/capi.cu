@@ -390,7 +390,8 @@ qlora_status qlora_merge_lora(const qlora_nf4_weight *w, const uint16_t *A, cons
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return QLORA_ERR_CUDA;
-  return cuda_status(launch_merge(tmO, a, static_cast<cudaStream_t>(stream)));
+  return cuda_status(
+      launch_merge(tmO, a, num_sms_current(), static_cast<cudaStream_t>(stream)));
 }
 
 qlora_status qlora_workspace_size(int64_t M, int64_t N, int64_t K, int32_t r, size_t *bytes) {

@@ -134,7 +134,8 @@ struct MergeArgs {
 };
 // tmO: 3-D bf16 tensor map of `out` viewed as [N][K / 64][64], box 64 x 4 x 16,
 // 128-byte swizzle (see qlora_merge_lora).
-cudaError_t launch_merge(const CUtensorMap &tmO, const MergeArgs &a, cudaStream_t s);
+cudaError_t launch_merge(const CUtensorMap &tmO, const MergeArgs &a, int num_sms,
+                         cudaStream_t s);
 
 // Rank-r gradient contractions and layout helpers (lora_grad.cu).
 int skinny_splits(int64_t M, int C, int budget = 296);

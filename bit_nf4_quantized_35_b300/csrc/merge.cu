@@ -4,11 +4,14 @@
 // the merged adapter is what deployment loads; the forward formula of Step 3
 // gives x W_hat^T + s (x A^T) B^T = x (W_hat + s B A)^T).
 //
-// HBM-bound (0.5 packed + 2 output bytes per weight).  A warp takes units of
-// 16 rows x 256 columns (4 blocks of 64), up to four row tiles of one
-// 256-column chunk, loading the next tile's packed bytes, block constants and
-// B rows while it computes the current one; a CTA of 8 warps shares the chunk
-// of A, staged once in shared memory.
+// HBM-bound (0.5 packed + 2 output bytes per weight).  Units of 16 rows x 256
+// columns (4 blocks of 64); one wave of CTAs (as many as are resident), each
+// taking an equal contiguous share of the units in chunk-major order.  The 8
+// warps of a CTA take the row tiles of one 256-column chunk in turn, loading
+// the next tile's packed bytes, block constants and B rows while they compute
+// the current one; the chunk of A is staged once per chunk in shared memory
+// (a CTA meets one or two chunks), while each warp's first loads are in
+// flight.
 //   - w_hat: lane (g, tq) dequantises rows g and g+8 of block tq with the
 //     per-block byte-permute table (the dequantiser's routine: exact bf16),
 //     its shifts on the multiply pipe (the integer pipe is the busier one).
@@ -34,12 +37,13 @@
 namespace qlora {
 
 constexpr int kMergeWarps = 8;
-constexpr int kMergeTilesPerWarp = 4;
 constexpr int kMergeTileBytes = 16 * 256 * 2;  // one warp's staged output tile
 
 // Dynamic shared memory of the kernel: the warps' output tiles (1024-byte
 // aligned for the swizzle; 1024 bytes of slack), then the A chunk.
-static int merge_smem_bytes(int ks) { return 1024 + kMergeWarps * kMergeTileBytes + 256 * ks * 16 * 2; }
+static int merge_smem_bytes(int ks) {
+  return 1024 + kMergeWarps * kMergeTileBytes + 256 * ks * 16 * 2;
+}
 
 // A plain register function (no volatile), so that the compiler can
 // interleave the MMAs with the loads and the table lookups.
@@ -69,39 +73,20 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t obuf = tiles_u + warp * kMergeTileBytes;
   const int g = lane >> 2, tq = lane & 3;
-  const int chunk = blockIdx.y;
-  const int kc0 = chunk * 256;
   constexpr int RP = KS * 16;
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  // A chunk -> shared memory, transposed and rank-interleaved (0 past r or
-  // K): 16-byte loads of 8 columns of one rank, scattered to the 8 columns
-  for (int i = threadIdx.x; i < 32 * RP; i += blockDim.x) {
-    const int j = i / 32, c8 = (i - j * 32) * 8;
-    const int k = kc0 + c8;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (j < p.r && k < p.K) v = ldg_nc_v4(p.A + (int64_t)j * p.K + k);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    const int sl = rank_slot(j);
-#pragma unroll
-    for (int e = 0; e < 8; ++e)
-      as[(c8 + e) * RP + sl] = (uint16_t)(w[e >> 1] >> ((e & 1) * 16));
-  }
-  __syncthreads();
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
-  const int blk = chunk * 4 + tq;  // 64-chunk of the row
   const int kbr = p.K >> 6;
-  const bool kin = blk < kbr;
-  // The warp's row tiles: tile0, tile0 + kMergeWarps, ... (gridDim.x * kMergeWarps apart)
-  const int tstride = gridDim.x * kMergeWarps;
   const int ntiles = (p.N + 15) / 16;
+  // this CTA's units: [u0, u1) of the chunk-major (chunk, row tile) order
+  const int64_t units = (int64_t)((p.K + 255) / 256) * ntiles;
+  const int64_t u0 = units * blockIdx.x / gridDim.x, u1 = units * (blockIdx.x + 1) / gridDim.x;
   // packed bytes, block constant and B fragments of one tile's rows n0, n1
   struct TileIn {
     uint4 l0, h0, l1, h1;
     float ah0, ah1;
     uint32_t af[KS][4];
   };
-  auto fetch = [&](int tile, TileIn &d) {
+  auto fetch = [&](int blk, int tile, TileIn &d) {
+    const bool kin = blk < kbr;
     const int n0 = tile * 16 + g, n1 = n0 + 8;
     auto one = [&](int n, uint4 &lo, uint4 &hi, float &ahat) {
       const bool ok = kin && n < p.N;
@@ -131,75 +116,97 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   };
   // this lane's column of every n-tile: block g >> 1, position 2j + (g & 1)
   const int bcol = (g >> 1) * 64 + (g & 1);
-  int tile = blockIdx.x * kMergeWarps + warp;
-  if (tile >= ntiles) return;
-  TileIn cur;
-  fetch(tile, cur);
-  for (; tile < ntiles; tile += tstride) {
-    // the next tile's loads are in flight while this one is computed
-    TileIn nxt;
-    const bool more = tile + tstride < ntiles;
-    if (more) fetch(tile + tstride, nxt);
-    const Nf4Table t0 = make_table(cur.ah0, p.cb), t1 = make_table(cur.ah1, p.cb);
-    // the previous tile's store has read the staging tile
-    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-    __syncwarp();
-    const uint32_t w0[8] = {cur.l0.x, cur.l0.y, cur.l0.z, cur.l0.w,
-                            cur.h0.x, cur.h0.y, cur.h0.z, cur.h0.w};
-    const uint32_t w1[8] = {cur.l1.x, cur.l1.y, cur.l1.z, cur.l1.w,
-                            cur.h1.x, cur.h1.y, cur.h1.z, cur.h1.w};
-    // 128-byte lines of rows g and g + 8 in block tq (same swizzle: 32 lines apart)
-    const uint32_t line0 = g * 4 + tq;
-    const uint32_t row0_u = obuf + line0 * 128, row1_u = row0_u + 32 * 128;
+  // 128-byte lines of rows g and g + 8 in block tq (same swizzle: 32 lines apart)
+  const uint32_t line0 = g * 4 + tq;
+  const uint32_t row0_u = obuf + line0 * 128, row1_u = row0_u + 32 * 128;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  for (int chunk = (int)(u0 / ntiles); (int64_t)chunk * ntiles < u1; ++chunk) {
+    const int64_t cbase = (int64_t)chunk * ntiles;
+    const int lo = (int)((u0 > cbase ? u0 : cbase) - cbase);
+    const int hi = (int)((u1 < cbase + ntiles ? u1 : cbase + ntiles) - cbase);
+    const int kc0 = chunk * 256;
+    const int blk = chunk * 4 + tq;  // 64-chunk of the row
+    int tile = lo + warp;
+    TileIn cur;
+    if (tile < hi) fetch(blk, tile, cur);  // in flight while A is staged
+    __syncthreads();  // the previous chunk's A is no longer read
+    // A chunk -> shared memory, transposed and rank-interleaved (0 past r or
+    // K): 16-byte loads of 8 columns of one rank, scattered to the 8 columns
+    for (int i = threadIdx.x; i < 32 * RP; i += blockDim.x) {
+      const int j = i / 32, c8 = (i - j * 32) * 8;
+      const int k = kc0 + c8;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (j < p.r && k < p.K) v = ldg_nc_v4(p.A + (int64_t)j * p.K + k);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      const int sl = rank_slot(j);
 #pragma unroll
-    for (int wi = 0; wi < 8; ++wi) {
-      uint32_t o0[4], o1[4];
-      lookup8_mulhi(t0, w0[wi], o0, p.k31, p.k16);
-      lookup8_mulhi(t1, w1[wi], o1, p.k31, p.k16);
-      uint32_t r0[4], r1[4];
+      for (int e = 0; e < 8; ++e)
+        as[(c8 + e) * RP + sl] = (uint16_t)(w[e >> 1] >> ((e & 1) * 16));
+    }
+    __syncthreads();
+    for (; tile < hi; tile += kMergeWarps) {
+      // the next tile's loads are in flight while this one is computed
+      TileIn nxt;
+      const bool more = tile + kMergeWarps < hi;
+      if (more) fetch(blk, tile + kMergeWarps, nxt);
+      const Nf4Table t0 = make_table(cur.ah0, p.cb), t1 = make_table(cur.ah1, p.cb);
+      // the previous tile's store has read the staging tile
+      if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      __syncwarp();
+      const uint32_t w0[8] = {cur.l0.x, cur.l0.y, cur.l0.z, cur.l0.w,
+                              cur.h0.x, cur.h0.y, cur.h0.z, cur.h0.w};
+      const uint32_t w1[8] = {cur.l1.x, cur.l1.y, cur.l1.z, cur.l1.w,
+                              cur.h1.x, cur.h1.y, cur.h1.z, cur.h1.w};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int j = wi * 4 + q;  // n-tile: positions 2j, 2j + 1
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint2 *arow = reinterpret_cast<const uint2 *>(as + (bcol + 2 * j) * RP + tq * 4);
+      for (int wi = 0; wi < 8; ++wi) {
+        uint32_t o0[4], o1[4];
+        lookup8_mulhi(t0, w0[wi], o0, p.k31, p.k16);
+        lookup8_mulhi(t1, w1[wi], o1, p.k31, p.k16);
+        uint32_t r0[4], r1[4];
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          const uint2 bv = arow[ks * 4];  // 16 ranks = 32 bytes = 4 uint2 per step
-          mma_bf16_m(d, cur.af[ks][0], cur.af[ks][1], cur.af[ks][2], cur.af[ks][3], bv.x, bv.y);
+        for (int q = 0; q < 4; ++q) {
+          const int j = wi * 4 + q;  // n-tile: positions 2j, 2j + 1
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
+          const uint2 *arow = reinterpret_cast<const uint2 *>(as + (bcol + 2 * j) * RP + tq * 4);
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) {
+            const uint2 bv = arow[ks * 4];  // 16 ranks = 32 bytes = 4 uint2 per step
+            mma_bf16_m(d, cur.af[ks][0], cur.af[ks][1], cur.af[ks][2], cur.af[ks][3], bv.x, bv.y);
+          }
+          r0[q] = pack_bf16x2(fmaf(p.s, d[0], bf16_lo(o0[q])), fmaf(p.s, d[1], bf16_hi(o0[q])));
+          r1[q] = pack_bf16x2(fmaf(p.s, d[2], bf16_lo(o1[q])), fmaf(p.s, d[3], bf16_hi(o1[q])));
         }
-        r0[q] = pack_bf16x2(fmaf(p.s, d[0], bf16_lo(o0[q])), fmaf(p.s, d[1], bf16_hi(o0[q])));
-        r1[q] = pack_bf16x2(fmaf(p.s, d[2], bf16_lo(o1[q])), fmaf(p.s, d[3], bf16_hi(o1[q])));
+        const uint32_t q16 = (wi ^ (line0 & 7)) << 4;
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row0_u + q16), "r"(r0[0]),
+                     "r"(r0[1]), "r"(r0[2]), "r"(r0[3]) : "memory");
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row1_u + q16), "r"(r1[0]),
+                     "r"(r1[1]), "r"(r1[2]), "r"(r1[3]) : "memory");
       }
-      const uint32_t q16 = (wi ^ (line0 & 7)) << 4;
-      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row0_u + q16), "r"(r0[0]),
-                   "r"(r0[1]), "r"(r0[2]), "r"(r0[3]) : "memory");
-      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row1_u + q16), "r"(r1[0]),
-                   "r"(r1[1]), "r"(r1[2]), "r"(r1[3]) : "memory");
+      fence_proxy_async_smem();  // the tile's generic-proxy writes, before the async store
+      __syncwarp();
+      if (lane == 0) {
+        asm volatile(
+            "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];"
+            ::"l"(reinterpret_cast<uint64_t>(&tmO)), "r"(0), "r"(chunk * 4), "r"(tile * 16),
+            "r"(obuf)
+            : "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      }
+      if (more) cur = nxt;
     }
-    fence_proxy_async_smem();  // the tile's generic-proxy writes, before the async store
-    __syncwarp();
-    if (lane == 0) {
-      asm volatile(
-          "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];"
-          ::"l"(reinterpret_cast<uint64_t>(&tmO)), "r"(0), "r"(chunk * 4), "r"(tile * 16),
-          "r"(obuf)
-          : "memory");
-      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-    }
-    if (more) cur = nxt;
   }
   // every store of the warp complete before the CTA ends
   if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-cudaError_t launch_merge(const CUtensorMap &tmO, const MergeArgs &a, cudaStream_t s) {
+cudaError_t launch_merge(const CUtensorMap &tmO, const MergeArgs &a, int num_sms,
+                         cudaStream_t s) {
   if (a.N == 0 || a.K == 0) return cudaSuccess;
   static bool attr_set[5] = {false, false, false, false, false};
-  const int tiles = (a.N + 15) / 16;
-  // each warp takes up to kMergeTilesPerWarp row tiles of its chunk
-  const int per_cta = kMergeWarps * kMergeTilesPerWarp;
+  const int64_t units = (int64_t)((a.N + 15) / 16) * ((a.K + 255) / 256);
+  static int occ[5] = {0, 0, 0, 0, 0};  // resident CTAs per SM of each instance
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((tiles + per_cta - 1) / per_cta, (a.K + 255) / 256, 1);
   cfg.blockDim = dim3(kMergeWarps * 32, 1, 1);
   cfg.stream = s;
   cudaLaunchAttribute at[1] = {pdl_attr()};
@@ -214,7 +221,14 @@ cudaError_t launch_merge(const CUtensorMap &tmO, const MergeArgs &a, cudaStream_
                                                  (int)cfg.dynamicSmemBytes);
       if (e != cudaSuccess) return e;
       attr_set[ks] = true;
+      int n = 0;
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kMergeWarps * 32, cfg.dynamicSmemBytes);
+      occ[ks] = n > 0 ? n : 1;
     }
+    // one wave, and no more CTAs than one per 8 units
+    const int64_t want = (units + kMergeWarps - 1) / kMergeWarps;
+    const int64_t cap = (int64_t)num_sms * occ[ks];
+    cfg.gridDim = dim3((unsigned)(want < cap ? want : cap), 1, 1);
     return cudaLaunchKernelEx(&cfg, kern, tmO, a);
   };
   switch (ks) {
