@@ -89,6 +89,28 @@ def test_merge_storage_formats(fmt):
     _check_merge(SHAPES[0], block=fmt[0], group=fmt[1], codebook=fmt[2])
 
 
+@pytest.mark.parametrize("shape", [
+    inputs.LinearShape("merge_N8_K64_r8", N=8, K=64, M=1, r=8, alpha=16.0),
+    inputs.LinearShape("merge_N24_K192_r16", N=24, K=192, M=1, r=16, alpha=32.0),
+    inputs.LinearShape("merge_N1_K128_r8", N=1, K=128, M=1, r=8, alpha=8.0),
+], ids=lambda s: s.name)
+def test_merge_smaller_than_one_store_tile(shape):
+    """Weights smaller than one 16-row x 256-column output tile (fewer rows
+    than 16, fewer than four 64-column blocks): the parts of the tile past
+    the weight must not be written."""
+    d = inputs.linear_inputs(shape, with_dy=False, seed_offset=7)
+    g = {k: v.cuda().contiguous() for k, v in d.items()}
+    q = capi.quantize_nf4(g["W"])
+    guard = torch.full((shape.N * shape.K + 4096,), 0x7fc1, dtype=torch.int16, device="cuda")
+    out = guard[:shape.N * shape.K].view(torch.bfloat16).view(shape.N, shape.K)
+    capi.merge_lora(q, g["A"], g["B"], shape.alpha, out=out)
+    torch.cuda.synchronize()
+    assert torch.all(guard[shape.N * shape.K:] == 0x7fc1)  # nothing past the weight
+    ref = capi.merge_lora(q, g["A"], g["B"], shape.alpha)
+    assert torch.equal(out, ref)
+    _check_merge(shape)
+
+
 def test_merge_zero_B_is_the_dequantised_weight():
     _check_merge(SHAPES[0], zero_B=True)
 
