@@ -233,6 +233,27 @@ bool make_tmap(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
   return r == CUDA_SUCCESS;
 }
 
+// The down-projection out = G . H^T (G [M, C], H [r, C], bf16 row-major):
+// inputs of 8192 columns or more stream through the TMA ring kernel (its two
+// tensor maps made here), narrower ones through the register kernel.
+cudaError_t run_lora_down(const uint16_t *G, int64_t M, int C, const uint16_t *H, int r, float s,
+                          float *out, uint16_t *outb, int r_pad, int *status, cudaStream_t st,
+                          const uint32_t *mask = nullptr, int wpr = 0, float keep_scale = 1.0f) {
+  if (M == 0) return cudaSuccess;
+  if (C < 8192)
+    return launch_lora_down(G, M, C, H, r, s, out, outb, r_pad, num_sms_current(), st, mask, wpr,
+                            keep_scale);
+  const int nt = (r + 7) / 8 + ((r + 7) / 8) % 2;  // an even number of 8-row tiles
+  CUtensorMap tmG, tmH;
+  if (!make_tmap(&tmG, G, (uint64_t)C, (uint64_t)M, (uint64_t)C * 2, 64, 16,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap(&tmH, H, (uint64_t)C, (uint64_t)r, (uint64_t)C * 2, 64, (uint32_t)(nt * 8),
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  return launch_lora_down_tma(tmG, tmH, M, C, r, s, out, outb, r_pad, num_sms_current(), status,
+                              st, mask, wpr, keep_scale);
+}
+
 void set_block_constants(GemmArgs &g, const qlora_nf4_weight *w) {
   g.use_code = w->group > 0;
   g.cvec = w->group > 0 ? w->scale2 : w->absmax_f32;
@@ -510,8 +531,8 @@ qlora_status linear_fwd_impl(const qlora_nf4_weight *w, const uint16_t *x, int64
   if (e != cudaSuccess) return QLORA_ERR_CUDA;
   const int bn = plan.bn;
   uint16_t *lb = reinterpret_cast<uint16_t *>(wsb + L.lb);
-  e = launch_lora_down(x, M, K, A, r, sc, t_save, lb, RP, num_sms_current(), s, dmask, dwpr,
-                       kscale);
+  e = run_lora_down(x, M, K, A, r, sc, t_save, lb, RP, reinterpret_cast<int *>(wsb + L.status), s,
+                    dmask, dwpr, kscale);
   if (e != cudaSuccess) return QLORA_ERR_CUDA;
   CUtensorMap tmA, tmL1, tmL2;
   if (!make_tmap(&tmA, x, K, M, (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -577,7 +598,8 @@ qlora_status linear_bwd_impl(const qlora_nf4_weight *w, const uint16_t *x, const
   cudaError_t e;
   if (!t) {
     float *tw = reinterpret_cast<float *>(wsb + L.t);
-    e = launch_lora_down(x, M, K, A, r, sc, tw, nullptr, RP, nsm, s, dmask, dwpr, kscale);
+    e = run_lora_down(x, M, K, A, r, sc, tw, nullptr, RP, reinterpret_cast<int *>(wsb + L.status),
+                      s, dmask, dwpr, kscale);
     if (e != cudaSuccess) return QLORA_ERR_CUDA;
     t = tw;
   }
@@ -585,7 +607,8 @@ qlora_status linear_bwd_impl(const qlora_nf4_weight *w, const uint16_t *x, const
   if (e != cudaSuccess) return QLORA_ERR_CUDA;
   // u = dY . B (fp32, for dA) and bf16(s . u) (operand of the dX GEMM's rank-r MMAs;
   // with dropout bf16(s / (1 - p) . u), taken back out at the dropped positions)
-  e = launch_lora_down(dY, M, N, Bt, r, sc * kscale, u, lb, RP, nsm, s);
+  e = run_lora_down(dY, M, N, Bt, r, sc * kscale, u, lb, RP, reinterpret_cast<int *>(wsb + L.status),
+                    s);
   if (e != cudaSuccess) return QLORA_ERR_CUDA;
   GemmPlan plan;
   e = gemm_plan(true, (int)M, K, N, RP, ws_bytes >= L.total ? L.sk_clusters : 0, &plan);

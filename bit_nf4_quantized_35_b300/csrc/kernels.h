@@ -107,6 +107,15 @@ cudaError_t launch_lora_down(const uint16_t *G, int64_t M, int C, const uint16_t
                              float s, float *out, uint16_t *outb, int r_pad, int num_sms,
                              cudaStream_t st, const uint32_t *mask = nullptr, int wpr = 0,
                              float keep_scale = 1.0f);
+// The same for wide inputs (C >= 8192), from TMA tensor maps: tmG of G [M, C]
+// (box 64 x 16), tmH of H [r, C] (box 64 x r_pad8, r_pad8 = 8 . an even number
+// of 8-row tiles >= r), both in the 128-byte swizzle.  status: the device
+// status word (its waits are bounded).
+cudaError_t launch_lora_down_tma(const CUtensorMap &tmG, const CUtensorMap &tmH, int64_t M,
+                                 int C, int r, float s, float *out, uint16_t *outb, int r_pad,
+                                 int num_sms, int *status, cudaStream_t st,
+                                 const uint32_t *mask = nullptr, int wpr = 0,
+                                 float keep_scale = 1.0f);
 
 // Quantise / dequantise (quantize.cu).
 cudaError_t launch_quantize(const void *W, bool bf16_in, int block, int64_t nblocks, int group,

@@ -65,6 +65,8 @@ SHAPES = [
     # r = 40 and 64: three and four 16-wide rank steps in the dX correction
     inputs.LinearShape("drop_N136_K512_M77_r40", N=136, K=512, M=77, r=40, alpha=80.0),
     inputs.LinearShape("drop_N256_K320_M64_r64", N=256, K=320, M=64, r=64, alpha=128.0),
+    # K >= 8192: t = x A^T with the keep mask through the TMA ring kernel
+    inputs.LinearShape("drop_N136_K8256_M40_r24", N=136, K=8256, M=40, r=24, alpha=48.0),
 ]
 
 

@@ -49,6 +49,11 @@ SMALL = [
     inputs.LinearShape("tiles_N768_K512_M384_r32", N=768, K=512, M=384, r=32, alpha=64.0),
     inputs.LinearShape("r64_N256_K256_M130_r64", N=256, K=256, M=130, r=64, alpha=128.0),
     inputs.LinearShape("r24_N136_K192_M17_r24", N=136, K=192, M=17, r=24, alpha=48.0),
+    # 8192 columns or more: the down-projections stream through the TMA ring
+    # kernel (u = dY B over N = 8200, t = x A^T over K = 8256; both end in a
+    # partial 256-column stage)
+    inputs.LinearShape("wideN_N8200_K256_M50_r40", N=8200, K=256, M=50, r=40, alpha=80.0),
+    inputs.LinearShape("wideK_N136_K8256_M33_r16", N=136, K=8256, M=33, r=16, alpha=32.0),
 ]
 
 
