@@ -607,8 +607,8 @@ qlora_status linear_bwd_impl(const qlora_nf4_weight *w, const uint16_t *x, const
   if (e != cudaSuccess) return QLORA_ERR_CUDA;
   // u = dY . B (fp32, for dA) and bf16(s . u) (operand of the dX GEMM's rank-r MMAs;
   // with dropout bf16(s / (1 - p) . u), taken back out at the dropped positions)
-  e = run_lora_down(dY, M, N, Bt, r, sc * kscale, u, lb, RP, reinterpret_cast<int *>(wsb + L.status),
-                    s);
+  e = run_lora_down(dY, M, N, Bt, r, sc * kscale, u, lb, RP,
+                    reinterpret_cast<int *>(wsb + L.status), s);
   if (e != cudaSuccess) return QLORA_ERR_CUDA;
   GemmPlan plan;
   e = gemm_plan(true, (int)M, K, N, RP, ws_bytes >= L.total ? L.sk_clusters : 0, &plan);

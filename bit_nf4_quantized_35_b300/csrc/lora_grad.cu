@@ -591,7 +591,8 @@ __global__ void __launch_bounds__(kDownThreads) lora_down_tma_kernel(
         const int col = (k0 + i) * kDownCols;
         mbar_arrive_expect_tx(full, SB);
 #pragma unroll
-        for (int bx = 0; bx < 4; ++bx) tma_load_2d(st + bx * GB, &tmG, full, col + 64 * bx, (int)m0);
+        for (int bx = 0; bx < 4; ++bx)
+          tma_load_2d(st + bx * GB, &tmG, full, col + 64 * bx, (int)m0);
 #pragma unroll
         for (int bx = 0; bx < 4; ++bx)
           tma_load_2d(st + 4 * GB + bx * HB, &tmH, full, col + 64 * bx, 0);
@@ -695,7 +696,8 @@ __global__ void __launch_bounds__(kDownThreads) lora_down_tma_kernel(
       v *= keep_scale;
       if (out && j < r) out[m * r + j] = v;
       if (outb && j < r_pad)
-        outb[m * r_pad + j] = j < r ? __bfloat16_as_ushort(__float2bfloat16_rn(s * v)) : (uint16_t)0;
+        outb[m * r_pad + j] =
+            j < r ? __bfloat16_as_ushort(__float2bfloat16_rn(s * v)) : (uint16_t)0;
     }
   }
   if (S > 1) cluster_sync();  // the peers' sums are read before they exit

@@ -222,7 +222,8 @@ cudaError_t launch_merge(const CUtensorMap &tmO, const MergeArgs &a, int num_sms
       if (e != cudaSuccess) return e;
       attr_set[ks] = true;
       int n = 0;
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kMergeWarps * 32, cfg.dynamicSmemBytes);
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kMergeWarps * 32,
+                                                    cfg.dynamicSmemBytes);
       occ[ks] = n > 0 ? n : 1;
     }
     // one wave, and no more CTAs than one per 8 units
