@@ -102,6 +102,24 @@ def test_edge_values():
     assert np.all(idx[0] == 7)
 
 
+@pytest.mark.parametrize("a_bits", [0x3F80, 0x3C99, 0x0080, 0x44D5, 0x0003, 0x7F7F],
+                         ids=["1", "0.0187", "min-normal", "1704", "subnormal", "max"])
+@pytest.mark.parametrize("group", [256, 0])
+def test_bf16_every_value_under_absmax(a_bits, group):
+    """Every finite bf16 value w with |w| <= a, as the non-maximal elements of
+    blocks of 64 whose absmax is a (the bf16 input path), bit-exact against
+    the oracle on the same values."""
+    pats = np.arange(0x10000, dtype=np.uint32)
+    vals = (pats << 16).view(np.float32)
+    a = np.array([a_bits << 16], dtype=np.uint32).view(np.float32)[0]
+    vals = vals[np.isfinite(vals) & (np.abs(vals) <= a)]
+    n = -(-vals.size // 63) * 63
+    vals = np.concatenate([vals, np.zeros(n - vals.size, np.float32)]).reshape(-1, 63)
+    blocks = np.concatenate([np.full((vals.shape[0], 1), a, np.float32), vals], axis=1)
+    W = torch.from_numpy(blocks.reshape(-1, 1024) if blocks.size % 1024 == 0 else blocks)
+    _check_quant(W.to(torch.bfloat16), group)
+
+
 def test_nonfinite_flag():
     W = inputs.normal((4, 128), inputs.STD_W, 5, torch.float32)
     W[1, 7] = float("nan")
