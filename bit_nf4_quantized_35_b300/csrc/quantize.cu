@@ -96,6 +96,14 @@ template <bool kBf16In, int kR>
 __host__ __device__ constexpr int quant_threads() {
   return (kBf16In && kR == 1) ? 512 : (quant_bulk<kBf16In, kR>() ? 1024 : 512);
 }
+// bf16 weights in 64-weight blocks: one more warp per CTA runs the double
+// quantisation of each group while the 16 others start the next group.
+template <bool kBf16In, int kR>
+__host__ __device__ constexpr bool quant_dq_warp() { return kBf16In && kR == 1; }
+template <bool kBf16In, int kR>
+__host__ __device__ constexpr int quant_launch_threads() {
+  return quant_threads<kBf16In, kR>() + (quant_dq_warp<kBf16In, kR>() ? 32 : 0);
+}
 template <bool kBf16In, int kR>
 __host__ __device__ constexpr int quant_stage_bytes() { return 256 * kR * 64 * (kBf16In ? 2 : 4); }
 template <bool kBf16In, int kR>
@@ -103,8 +111,12 @@ __host__ __device__ constexpr int quant_smem_bytes() {
   return quant_bulk<kBf16In, kR>() ? kQStages * quant_stage_bytes<kBf16In, kR>() + 128 : 0;
 }
 
+// (a minimum of 0 resident CTAs leaves the register budget of the other
+// instances to the compiler, as without the bound)
 template <bool kBf16In, int kR>
-__global__ void __launch_bounds__(quant_threads<kBf16In, kR>()) quantize_nf4_kernel(const void *__restrict__ W,
+__global__ void __launch_bounds__(quant_launch_threads<kBf16In, kR>(),
+                                  quant_dq_warp<kBf16In, kR>() ? 2 : 0)
+    quantize_nf4_kernel(const void *__restrict__ W,
                                                              int64_t nblocks, int group,
                                                              uint8_t *__restrict__ packed,
                                                              int8_t *__restrict__ codes,
@@ -120,7 +132,8 @@ __global__ void __launch_bounds__(quant_threads<kBf16In, kR>()) quantize_nf4_ker
   __shared__ uint32_t qerr_s;
   constexpr bool kBulk = quant_bulk<kBf16In, kR>();
   constexpr int kStage = quant_stage_bytes<kBf16In, kR>();
-  constexpr int kT = quant_threads<kBf16In, kR>();
+  constexpr int kT = quant_threads<kBf16In, kR>();  // threads of the element passes
+  constexpr bool kDqWarp = quant_dq_warp<kBf16In, kR>();
   constexpr int kCpp = kT / 8;                 // chunks per pass
   constexpr int kPasses = 256 * kR / kCpp;
   constexpr int kEsz = kBf16In ? 2 : 4;
@@ -164,6 +177,7 @@ __global__ void __launch_bounds__(quant_threads<kBf16In, kR>()) quantize_nf4_ker
     const int64_t blk0 = grp * 256;   // first block of the group
     const int64_t ch0 = blk0 * kR;    // its first 64-element chunk
     const int st = it % kQStages;
+    if (!kDqWarp || warp < kT / 32) {  // the element passes
     constexpr int kWords = kBf16In ? 4 : 8;  // 32-bit words per pass
     uint32_t raw[kPasses][kWords];
     bool inb[kPasses];
@@ -321,6 +335,7 @@ __global__ void __launch_bounds__(quant_threads<kBf16In, kR>()) quantize_nf4_ker
       if (amax == 0.0f) word = 0x77777777u;  // every index is the exact-zero codepoint
       if (inb[p]) *reinterpret_cast<uint32_t *>(packed + (ch0 + c) * 32 + li * 4) = word;
     }
+    }
     __syncthreads();  // amax_s[it & 1] complete; every thread is done with the stage
     if (kBulk && tid == 0 && grp + kQStages * G < ngroups) {
       fence_proxy_async_smem();
@@ -332,7 +347,38 @@ __global__ void __launch_bounds__(quant_threads<kBf16In, kR>()) quantize_nf4_ker
     // group: the block maxima are double-buffered, and the 8 warps meet at a
     // barrier of their own (the next CTA-wide barrier, after the next group's
     // elements, orders this step before the buffers are reused).
-    if (tid < 256) {
+    if (kDqWarp) {
+      // the extra warp: lane L takes blocks 8L .. 8L + 7 of the group, whose
+      // double-quantisation group spans group / 8 consecutive lanes; it
+      // reaches the next CTA-wide barrier only when done, so the pass warps
+      // cannot refill amax_s[it & 1] before it has read it
+      if (warp == kT / 32) {
+        const float *am = amax_s[it & 1];
+        float a[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a[j] = am[8 * lane + j];
+        const int64_t gb0 = blk0 + 8 * lane;
+        if (group == 0) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (gb0 + j < nblocks) absf[gb0 + j] = a[j];
+        } else {
+          float m = a[0];
+#pragma unroll
+          for (int j = 1; j < 8; ++j) m = fmaxf(m, a[j]);
+          for (int o = 1; o < (group >> 3); o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+          const float s2 = __fdiv_rn(m, 127.0f);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            float c = 0.0f;
+            if (s2 != 0.0f) c = rintf(__fdiv_rn(a[j], s2));
+            c = fminf(fmaxf(c, -127.0f), 127.0f);
+            if (gb0 + j < nblocks) codes[gb0 + j] = (int8_t)(int)c;
+          }
+          if (((8 * lane) & (group - 1)) == 0 && gb0 < nblocks) scale2[gb0 / group] = s2;
+        }
+      }
+    } else if (tid < 256) {
       const float a = amax_s[it & 1][tid];
       const int64_t gb = blk0 + tid;
       if (group == 0) {
@@ -437,13 +483,13 @@ static cudaError_t launch_q(const void *W, int64_t nblocks, int group, uint8_t *
   }
   int per_sm = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &per_sm, quantize_nf4_kernel<kBf16In, kR>, quant_threads<kBf16In, kR>(), smem);
+      &per_sm, quantize_nf4_kernel<kBf16In, kR>, quant_launch_threads<kBf16In, kR>(), smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
   const int64_t ngroups = (nblocks + 255) / 256;
   int64_t grid = (int64_t)num_sms * per_sm;
   if (grid > ngroups) grid = ngroups;
-  quantize_nf4_kernel<kBf16In, kR><<<(unsigned)grid, quant_threads<kBf16In, kR>(), smem, s>>>(
+  quantize_nf4_kernel<kBf16In, kR><<<(unsigned)grid, quant_launch_threads<kBf16In, kR>(), smem, s>>>(
       W, nblocks, group, packed, codes, absf, scale2, nonfinite_flag, tab);
   return cudaGetLastError();
 }
