@@ -9,7 +9,7 @@
 // again to int8 with one fp32 scale per group of block constants.
 //
 // Both kernels are HBM-bound.  Layout of the work:
-//   quantise: persistent CTAs of 512 or 1024 threads, each taking groups of 256
+//   quantise: persistent CTAs of 512 (+ 32) or 1024 threads, each taking groups of 256
 //     consecutive blocks (one double quantisation group of 256, or several
 //     smaller groups), the input of each group brought into shared memory
 //     by one bulk copy a few groups ahead.  Eight lanes share a block
@@ -89,7 +89,8 @@ template <bool kBf16In, int kR>
 __host__ __device__ constexpr bool quant_bulk() { return kBf16In || kR == 1; }
 // 32 warps per SM either way: bf16 weights in 64-weight blocks run two CTAs
 // of 512 threads per SM (two 96 KB stage rings; half the warps at each
-// barrier), the other staged cases one CTA of 1024 threads (a 192 KB ring),
+// barrier; each CTA with one more warp for the double quantisation), the
+// other staged cases one CTA of 1024 threads (a 192 KB ring),
 // and fp32 weights in 128-weight blocks, which hold all their pieces in
 // registers, one CTA of 512.
 template <bool kBf16In, int kR>
