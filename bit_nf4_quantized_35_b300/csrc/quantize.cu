@@ -150,7 +150,17 @@ __global__ void __launch_bounds__(quant_launch_threads<kBf16In, kR>(),
     bt_s[tid] = __float_as_uint(tab.thp[tid]);
     bt_s[34 + tid] = (uint32_t)tab.base[tid];
   }
+  // mbarriers: full[kQStages] (the stage's copy landed); with the extra
+  // warp also empty[kQStages] (every pass warp has read the stage),
+  // amax_full[2] (every pass warp has written the group's block maxima) and
+  // amax_free[2] (the extra warp has read them), which take the place of a
+  // CTA-wide barrier per group
   if (kBulk && tid < kQStages) mbar_init(bars_u + tid * 8, 1);
+  if (kDqWarp && tid < kQStages) mbar_init(bars_u + (kQStages + tid) * 8, kT / 32);
+  if (kDqWarp && tid < 2) {
+    mbar_init(bars_u + (2 * kQStages + tid) * 8, kT / 32);
+    mbar_init(bars_u + (2 * kQStages + 2 + tid) * 8, 1);
+  }
   if (tid == 0) qerr_s = 0u;
   if (kBulk) fence_barrier_init();
   __syncthreads();  // tables and barriers ready
@@ -171,6 +181,21 @@ __global__ void __launch_bounds__(quant_launch_threads<kBf16In, kR>(),
   if (kBulk && tid == 0)
     for (int st = 0; st < kQStages; ++st)
       if (blockIdx.x + st * G < ngroups) issue(blockIdx.x + st * G, st);
+  // bounded wait (~2 s); past the limit the error is recorded and the work
+  // goes on with whatever the buffers hold
+  auto bwait = [&](uint32_t bar, uint32_t ph) {
+    if (!mbar_try_wait(bar, ph)) {
+      const long long t0 = clock64();
+      while (!mbar_try_wait(bar, ph))
+        if (clock64() - t0 > (1ll << 32)) {
+          qerr_s = 1u;
+          break;
+        }
+    }
+  };
+  const uint32_t empty_u = bars_u + kQStages * 8;       // empty[st]
+  const uint32_t afull_u = bars_u + 2 * kQStages * 8;   // amax_full[b]
+  const uint32_t afree_u = afull_u + 2 * 8;             // amax_free[b]
 
   int nonfinite = 0;
   int it = 0;
@@ -185,16 +210,7 @@ __global__ void __launch_bounds__(quant_launch_threads<kBf16In, kR>(),
     if constexpr (kBulk) {
       // bounded wait on the stage (~2 s); past the limit the group is
       // computed from whatever the stage holds and the error is reported
-      const uint32_t bar = bars_u + st * 8;
-      const uint32_t ph = (uint32_t)(it / kQStages) & 1u;
-      if (!mbar_try_wait(bar, ph)) {
-        const long long t0 = clock64();
-        while (!mbar_try_wait(bar, ph))
-          if (clock64() - t0 > (1ll << 32)) {
-            qerr_s = 1u;
-            break;
-          }
-      }
+      bwait(bars_u + st * 8, (uint32_t)(it / kQStages) & 1u);
       const uint8_t *stg = qsm + st * kStage;
 #pragma unroll
       for (int p = 0; p < kPasses; ++p) {
@@ -207,6 +223,10 @@ __global__ void __launch_bounds__(quant_launch_threads<kBf16In, kR>(),
           const uint4 u1 = src[1];
           raw[p][4] = u1.x, raw[p][5] = u1.y, raw[p][6] = u1.z, raw[p][7] = u1.w;
         }
+      }
+      if constexpr (kDqWarp) {  // this warp is done with the stage
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_u + st * 8);
       }
     } else {
 #pragma unroll
@@ -237,6 +257,8 @@ __global__ void __launch_bounds__(quant_launch_threads<kBf16In, kR>(),
       if (kBf16In) return (e & 1) ? bf16_hi(raw[p][e >> 1]) : bf16_lo(raw[p][e >> 1]);
       return __uint_as_float(raw[p][e]);
     };
+    // the extra warp has read the maxima of two groups ago from this buffer
+    if (kDqWarp && it >= 2) bwait(afree_u + (it & 1) * 8, (uint32_t)((it >> 1) - 1) & 1u);
 
 #pragma unroll
     for (int p = 0; p < kPasses; ++p) {
@@ -336,11 +358,17 @@ __global__ void __launch_bounds__(quant_launch_threads<kBf16In, kR>(),
       if (amax == 0.0f) word = 0x77777777u;  // every index is the exact-zero codepoint
       if (inb[p]) *reinterpret_cast<uint32_t *>(packed + (ch0 + c) * 32 + li * 4) = word;
     }
+    if constexpr (kDqWarp) {  // this warp's block maxima of the group are written
+      __syncwarp();
+      if (lane == 0) mbar_arrive(afull_u + (it & 1) * 8);
     }
-    __syncthreads();  // amax_s[it & 1] complete; every thread is done with the stage
-    if (kBulk && tid == 0 && grp + kQStages * G < ngroups) {
-      fence_proxy_async_smem();
-      issue(grp + kQStages * G, st);
+    }
+    if constexpr (!kDqWarp) {
+      __syncthreads();  // amax_s[it & 1] complete; every thread is done with the stage
+      if (kBulk && tid == 0 && grp + kQStages * G < ngroups) {
+        fence_proxy_async_smem();
+        issue(grp + kQStages * G, st);
+      }
     }
 
     // Second level: one scale per `group` consecutive block constants, by
@@ -349,11 +377,20 @@ __global__ void __launch_bounds__(quant_launch_threads<kBf16In, kR>(),
     // barrier of their own (the next CTA-wide barrier, after the next group's
     // elements, orders this step before the buffers are reused).
     if (kDqWarp) {
-      // the extra warp: lane L takes blocks 8L .. 8L + 7 of the group, whose
-      // double-quantisation group spans group / 8 consecutive lanes; it
-      // reaches the next CTA-wide barrier only when done, so the pass warps
-      // cannot refill amax_s[it & 1] before it has read it
+      // the extra warp: it refills the stage once every pass warp has read
+      // it, then, once they have all written the group's block maxima, runs
+      // the double quantisation (lane L: blocks 8L .. 8L + 7, whose group
+      // spans group / 8 consecutive lanes) and frees the maxima buffer
       if (warp == kT / 32) {
+        if (grp + kQStages * G < ngroups) {
+          if (lane == 0) {
+            bwait(empty_u + st * 8, (uint32_t)(it / kQStages) & 1u);
+            fence_proxy_async_smem();
+            issue(grp + kQStages * G, st);
+          }
+          __syncwarp();
+        }
+        bwait(afull_u + (it & 1) * 8, (uint32_t)(it >> 1) & 1u);
         const float *am = amax_s[it & 1];
         float a[8];
 #pragma unroll
@@ -378,6 +415,8 @@ __global__ void __launch_bounds__(quant_launch_threads<kBf16In, kR>(),
           }
           if (((8 * lane) & (group - 1)) == 0 && gb0 < nblocks) scale2[gb0 / group] = s2;
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(afree_u + (it & 1) * 8);
       }
     } else if (tid < 256) {
       const float a = amax_s[it & 1][tid];
@@ -405,6 +444,7 @@ __global__ void __launch_bounds__(quant_launch_threads<kBf16In, kR>(),
       }
     }
   }
+  __syncthreads();  // every warp done (a timeout of any of them is in qerr_s)
   if (nonfinite_flag) {
     nonfinite = __any_sync(0xffffffffu, nonfinite != 0);
     if (nonfinite && lane == 0) atomicExch(nonfinite_flag, 1);
