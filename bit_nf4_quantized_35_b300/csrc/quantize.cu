@@ -80,7 +80,9 @@ constexpr float kQuantBand = 9.5367431640625e-07f;  // 2^-20
 // kBulk: the group's input (contiguous, 32 kR KB of bf16 or 64 kR KB of fp32)
 // comes into one of kQStages shared-memory stages with a single bulk copy
 // (cp.async.bulk, completion on the stage's mbarrier); one thread refills a
-// stage as soon as every thread has read it, so the next stages' copies are
+// stage as soon as every thread has read it (after a CTA-wide barrier, or,
+// with the extra warp of the bf16 / 64 case, when the stage's "empty"
+// mbarrier has the 16 pass warps' arrivals), so the next stages' copies are
 // in flight while a group is computed.  Without kBulk (fp32 weights in
 // 128-weight blocks: three 128 KB stages would not fit) every thread loads
 // its pieces straight into registers.
