@@ -270,9 +270,13 @@ __global__ void __launch_bounds__(quant_launch_threads<kBf16In, kR>(),
       // element, and the maximum is then taken over the finite ones only.
       uint32_t mb;
       if (kBf16In) {
+        // two magnitudes per instruction: max of |a|, |b| (the sign of the
+        // result is not used), a NaN kept so that the test below sees it
         uint32_t m2 = 0;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) m2 = __vmaxu2(m2, raw[p][q] & 0x7fff7fffu);
+        for (int q = 0; q < 4; ++q)
+          asm("max.NaN.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(raw[p][q]));
+        m2 &= 0x7fff7fffu;
         mb = max(m2 << 16, m2 & 0xffff0000u);
       } else {
         mb = 0;
