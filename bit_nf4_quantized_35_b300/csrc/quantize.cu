@@ -33,15 +33,15 @@ namespace qlora {
 //   th[k]     the thresholds: index = #{k : x >= th[k]} (th[15] = 2)
 //   for the 1/16-wide bucket i of [-1, 1] (x in [-1 + i/16, -1 + (i + 1)/16),
 //   i = -1 .. 32), at slot i + 1:
-//   thp[]     the largest float below the one threshold inside the bucket
-//             (2 when there is none)
-//   base[]    the number of thresholds below the bucket
+//   nth[]     minus the one threshold inside the bucket (-2 when there is
+//             none)
+//   base1[]   one more than the number of thresholds below the bucket
 // (two 34-word arrays: a warp's lookups then meet no bank conflict unless two
 // lanes hold elements near -1 and near +1 at once)
 struct QuantTables {
   float th[16];
-  float thp[34];
-  int base[34];
+  float nth[34];
+  int base1[34];
   int exact_only;  // 1: some bucket holds two thresholds; divide every element
 };
 
@@ -62,12 +62,13 @@ __device__ __forceinline__ constexpr int nib_shift(int e) { return 8 * (e >> 1) 
 // the reciprocal-based decision may differ from the one on the IEEE quotient.
 // With y the hardware reciprocal (rcp.approx: at most 1 ulp from 1/a, so
 // y = (1/a)(1 + d1) with |d1| <= 2^-23 for a normal a and y), the fast path
-// compares the exact product z = w y (inside an FMA) with thp = pred(th):
+// compares the exact product z = w y (inside an FMA) with th:
 //   z = (w/a)(1 + d1),  RN(w/a) = (w/a)(1 + d3),  |d3| <= 2^-24,
-// so |z - RN(w/a)| < 2^-22.4 |w/a| <= 2^-22.4.  If [z > thp] and
-// [RN(w/a) >= th] differ, then |thp - z| <= 2^-22.4 (RN(w/a) >= th means
-// RN(w/a) > thp, and RN(w/a) < th means RN(w/a) <= thp), so every element
-// whose |RN(thp - z)| is at least 2^-20 is decided the same way by both.
+// so |z - RN(w/a)| < 2^-22.4 |w/a| <= 2^-22.4.  If [z >= th] and
+// [RN(w/a) >= th] differ, then |z - th| < 2^-22.4 (th is a float, so
+// RN(w/a) < th means RN(w/a) <= pred(th) and z < th + 2^-22.4; RN(w/a) >= th
+// means z > th - 2^-22.4), so every element whose |RN(z - th)| is at least
+// 2^-20 is decided the same way by both.
 constexpr float kQuantBand = 9.5367431640625e-07f;  // 2^-20
 
 // kR = block / 64.  A CTA of T threads takes groups of 256 consecutive
@@ -129,7 +130,7 @@ __global__ void __launch_bounds__(quant_launch_threads<kBf16In, kR>(),
                                                              const QuantTables tab) {
   extern __shared__ __align__(128) uint8_t qsm[];  // [stage][group input]; mbarriers at the end
   __shared__ float th_s[16];
-  __shared__ uint32_t bt_s[68];  // thp[34] then base[34]
+  __shared__ uint32_t bt_s[68];  // nth[34] then base1[34]
   __shared__ float amax_s[2][256];  // block maxima of the last two groups
   __shared__ float wmax_s[8];
   __shared__ uint32_t qerr_s;
@@ -149,8 +150,8 @@ __global__ void __launch_bounds__(quant_launch_threads<kBf16In, kR>(),
   const uint32_t bars_u = sm_u + kQStages * kStage;  // kQStages mbarriers (kBulk)
   if (tid < 16) th_s[tid] = tab.th[tid];
   if (tid < 34) {
-    bt_s[tid] = __float_as_uint(tab.thp[tid]);
-    bt_s[34 + tid] = (uint32_t)tab.base[tid];
+    bt_s[tid] = __float_as_uint(tab.nth[tid]);
+    bt_s[34 + tid] = (uint32_t)tab.base1[tid];
   }
   // mbarriers: full[kQStages] (the stage's copy landed); with the extra
   // warp also empty[kQStages] (every pass warp has read the stage),
@@ -331,26 +332,34 @@ __global__ void __launch_bounds__(quant_launch_threads<kBf16In, kR>(),
       const float y16 = y * 16.0f;
       // u = RD(16 w y + 16 + 1.5 . 2^23) = 1.5 . 2^23 + i, i = floor(16 z + 16)
       // in [-1, 32] (|w| <= a), exactly (one rounding, toward -inf, to the
-      // integers); the bit pattern of u is 0x4b400000 + i, so thp[i + 1]
+      // integers); the bit pattern of u is 0x4b400000 + i, so nth[i + 1]
       // lies at bits(u) . 4 + (bt_s + 4 - 0x4b400000 . 4), modulo 2^32, and
-      // base[i + 1] 136 bytes further.
+      // base1[i + 1] 136 bytes further.  Both FMAs take the lane's elements
+      // in pairs (packed f32x2: the two halves are rounded independently).
       const uint32_t tb = smem_u32(bt_s) + 4u - 0x2d000000u;
       uint32_t word = 0;
-      float dmin = 1.0f;  // smallest |thp - z| of the lane's elements
+      float dmin = 1.0f;  // smallest |z - th| of the lane's elements
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float w = elem(p, e);
-        const float u = __fmaf_rd(w, y16, 12582928.0f);
-        const uint32_t ad = __float_as_uint(u) * 4u + tb;
-        uint32_t thp, base;
+      for (int e = 0; e < 8; e += 2) {
+        const float w0 = elem(p, e), w1 = elem(p, e + 1);
+        float u0, u1;
+        asm("{.reg .b64 rw, ry, rc, rd;\n\tmov.b64 rw, {%2, %3};\n\tmov.b64 ry, {%4, %4};\n\t"
+            "mov.b64 rc, {%5, %5};\n\tfma.rm.f32x2 rd, rw, ry, rc;\n\tmov.b64 {%0, %1}, rd;}"
+            : "=f"(u0), "=f"(u1) : "f"(w0), "f"(w1), "f"(y16), "f"(12582928.0f));
+        uint32_t t0, b0, t1, b1;
         asm("ld.shared.u32 %0, [%2];\n\tld.shared.u32 %1, [%2+136];"
-            : "=r"(thp), "=r"(base)
-            : "r"(ad));
-        // d = RN(thp - z): negative exactly when z > thp (a zero is +0)
-        const float d = fmaf(-w, y, __uint_as_float(thp));
-        dmin = fminf(dmin, fabsf(d));
-        const uint32_t q = base + (__float_as_uint(d) >> 31);
-        word |= q << nib_shift(e);
+            : "=r"(t0), "=r"(b0) : "r"(__float_as_uint(u0) * 4u + tb));
+        asm("ld.shared.u32 %0, [%2];\n\tld.shared.u32 %1, [%2+136];"
+            : "=r"(t1), "=r"(b1) : "r"(__float_as_uint(u1) * 4u + tb));
+        // d = RN(z - th): non-negative exactly when z >= th (a zero is +0),
+        // so the index is base1 - sign(d)
+        float d0, d1;
+        asm("{.reg .b64 rw, ry, rt, rd;\n\tmov.b64 rw, {%2, %3};\n\tmov.b64 ry, {%4, %4};\n\t"
+            "mov.b64 rt, {%5, %6};\n\tfma.rn.f32x2 rd, rw, ry, rt;\n\tmov.b64 {%0, %1}, rd;}"
+            : "=f"(d0), "=f"(d1) : "f"(w0), "f"(w1), "f"(y), "r"(t0), "r"(t1));
+        dmin = fminf(dmin, fminf(fabsf(d0), fabsf(d1)));
+        word |= (b0 - (__float_as_uint(d0) >> 31)) << nib_shift(e);
+        word |= (b1 - (__float_as_uint(d1) >> 31)) << nib_shift(e + 1);
       }
       // The vote is taken by every lane of the warp (lanes of all-zero
       // blocks and of blocks past the end included), outside any branch.
@@ -510,8 +519,8 @@ static void build_quant_tables(const float th[15], QuantTables &t) {
       }
     }
     if (inside > 1) ok = false;
-    t.thp[s] = inside ? std::nextafterf(th_in, -INFINITY) : 2.0f;
-    t.base[s] = base;
+    t.nth[s] = inside ? -th_in : -2.0f;
+    t.base1[s] = base + 1;
   }
   t.exact_only = ok ? 0 : 1;
 }
