@@ -167,6 +167,7 @@ __global__ void __launch_bounds__(quant_launch_threads<kBf16In, kR>(),
   if (tid == 0) qerr_s = 0u;
   if (kBulk) fence_barrier_init();
   __syncthreads();  // tables and barriers ready
+  pdl_wait_release();  // every global access below follows the previous kernel
 
   // one bulk copy of group grp's input into stage st (thread 0)
   auto issue = [&](int64_t grp, int st) {
@@ -476,6 +477,7 @@ __global__ void __launch_bounds__(256) dequant_nf4_kernel(const uint8_t *__restr
                                                           int piece_shift,
                                                           uint16_t *__restrict__ out,
                                                           const Codebook cb) {
+  pdl_wait_release();
   // piece q (16 elements) lies in block q >> piece_shift (block / 16 pieces)
   for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < npieces;
        q += (int64_t)gridDim.x * blockDim.x) {
@@ -545,8 +547,17 @@ static cudaError_t launch_q(const void *W, int64_t nblocks, int group, uint8_t *
   const int64_t ngroups = (nblocks + 255) / 256;
   int64_t grid = (int64_t)num_sms * per_sm;
   if (grid > ngroups) grid = ngroups;
-  quantize_nf4_kernel<kBf16In, kR><<<(unsigned)grid, quant_launch_threads<kBf16In, kR>(), smem, s>>>(
-      W, nblocks, group, packed, codes, absf, scale2, nonfinite_flag, tab);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(quant_launch_threads<kBf16In, kR>(), 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1] = {pdl_attr()};
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, quantize_nf4_kernel<kBf16In, kR>, W, nblocks, group, packed, codes,
+                         absf, scale2, nonfinite_flag, tab);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -579,8 +590,16 @@ cudaError_t launch_dequant(const uint8_t *packed, const int8_t *codes, const flo
   int64_t grid = (work + 255) / 256;
   const int64_t cap = (int64_t)num_sms * 8 * 4;
   if (grid > cap) grid = cap;
-  dequant_nf4_kernel<<<(unsigned)grid, 256, 0, s>>>(packed, codes, absf, scale2, group, work,
-                                                    block == 64 ? 2 : 3, out, cb);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute at[1] = {pdl_attr()};
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, dequant_nf4_kernel, packed, codes, absf, scale2, group,
+                                     work, block == 64 ? 2 : 3, out, cb);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
