@@ -338,8 +338,12 @@ __global__ void __launch_bounds__(quant_launch_threads<kBf16In, kR>(),
       // base1[i + 1] 136 bytes further.  Both FMAs take the lane's elements
       // in pairs (packed f32x2: the two halves are rounded independently).
       const uint32_t tb = smem_u32(bt_s) + 4u - 0x2d000000u;
+      // word = sum of base1_e << nib_shift(e) minus the sign bits of the d_e
+      // at the same places (each nibble base1 - [d < 0] is in 0..15, so the
+      // difference is the packed word; borrows cancel across the sum)
       uint32_t word = 0;
       float dmin = 1.0f;  // smallest |z - th| of the lane's elements
+      uint32_t db[8];     // bit patterns of the d_e
 #pragma unroll
       for (int e = 0; e < 8; e += 2) {
         const float w0 = elem(p, e), w1 = elem(p, e + 1);
@@ -353,14 +357,23 @@ __global__ void __launch_bounds__(quant_launch_threads<kBf16In, kR>(),
         asm("ld.shared.u32 %0, [%2];\n\tld.shared.u32 %1, [%2+136];"
             : "=r"(t1), "=r"(b1) : "r"(__float_as_uint(u1) * 4u + tb));
         // d = RN(z - th): non-negative exactly when z >= th (a zero is +0),
-        // so the index is base1 - sign(d)
+        // so the index is base1 - [d < 0]
         float d0, d1;
         asm("{.reg .b64 rw, ry, rt, rd;\n\tmov.b64 rw, {%2, %3};\n\tmov.b64 ry, {%4, %4};\n\t"
             "mov.b64 rt, {%5, %6};\n\tfma.rn.f32x2 rd, rw, ry, rt;\n\tmov.b64 {%0, %1}, rd;}"
             : "=f"(d0), "=f"(d1) : "f"(w0), "f"(w1), "f"(y), "r"(t0), "r"(t1));
         dmin = fminf(dmin, fminf(fabsf(d0), fabsf(d1)));
-        word |= (b0 - (__float_as_uint(d0) >> 31)) << nib_shift(e);
-        word |= (b1 - (__float_as_uint(d1) >> 31)) << nib_shift(e + 1);
+        word += b0 << nib_shift(e);
+        word += b1 << nib_shift(e + 1);
+        db[e] = __float_as_uint(d0);
+        db[e + 1] = __float_as_uint(d1);
+      }
+      {
+        // sign-replicating byte permutes: byte j of se is 0xff when d_{2j} < 0,
+        // of so when d_{2j+1} < 0
+        const uint32_t se = prmt(prmt(db[0], db[2], 0x00FBu), prmt(db[4], db[6], 0xFB00u), 0x7610u);
+        const uint32_t so = prmt(prmt(db[1], db[3], 0x00FBu), prmt(db[5], db[7], 0xFB00u), 0x7610u);
+        word -= (se & 0x10101010u) | (so & 0x01010101u);
       }
       // The vote is taken by every lane of the warp (lanes of all-zero
       // blocks and of blocks past the end included), outside any branch.
