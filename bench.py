@@ -537,6 +537,7 @@ def sub_benchmarks(capi, layers, device, stream, args):
     bytes_total = nw * (2 + 0.5 + 1 / 64 + 4 / 16384)
     rows["quantize_bulk"] = {"matrices": nmat, "weights": nw, "ms": round(qms, 3),
                              "GBps_total": round(bytes_total / (qms * 1e-3) / 1e9, 1),
+                             "GBps_input": round(nw * 2 / (qms * 1e-3) / 1e9, 1),
                              "frac_of_hbm": round(bytes_total / (qms * 1e-3) / 1e9 / hbm, 4),
                              "note": "8 distinct 117 MB matrices cycled (> L2)"}
     # dequantisation to bf16 of the same matrices
