@@ -504,12 +504,26 @@ def sub_benchmarks(capi, layers, device, stream, args):
         y = torch.empty((Mg, N), dtype=torch.bfloat16, device=device)
         t = torch.empty((Mg, RANK_R), dtype=torch.float32, device=device)
         ws = capi.Workspace(Mg, N, K, RANK_R, device=device)
+        call = lambda i: capi.linear_fwd(copies[i % 8], x, A, B, ALPHA, ws, y=y, t_save=t,
+                                         stream=s)
         with torch.cuda.stream(s):
-            ms = time_graph(lambda i: capi.linear_fwd(copies[i % 8], x, A, B, ALPHA, ws, y=y,
-                                                      t_save=t, stream=s), 64, s)
+            ms = time_graph(call, 64, s)
+            # the same 64 calls launched one by one from the host: the difference is the
+            # per-call launch overhead that the graph replay hides
+            for i in range(8):
+                call(i)
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev0.record(s)
+            for i in range(64):
+                call(i)
+            ev1.record(s)
+        torch.cuda.synchronize()
+        eager_ms = ev0.elapsed_time(ev1) / 64
         gbs = packed_bytes / (ms * 1e-3) / 1e9
         rows[f"gemv_gate_M{Mg}"] = {"us": round(ms * 1e3, 2), "packed_GBps": round(gbs, 1),
-                                    "frac_of_hbm": round(gbs / hbm, 4)}
+                                    "frac_of_hbm": round(gbs / hbm, 4),
+                                    "eager_us": round(eager_ms * 1e3, 2),
+                                    "launch_overhead_us": round((eager_ms - ms) * 1e3, 2)}
     del copies
     # bulk quantisation: 136 x (4096 x 14336) bf16 -> NF4 + DQ (streamed in chunks of 8)
     nmat = 136 if not args.quick else 16
