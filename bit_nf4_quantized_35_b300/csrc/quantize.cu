@@ -8,7 +8,9 @@
 // codepoint, two indices share a byte, and the block maxima are quantised
 // again to int8 with one fp32 scale per group of block constants.
 //
-// Both kernels are HBM-bound.  Layout of the work:
+// Both kernels stream the weight through HBM once; the quantiser is limited
+// by instruction issue, the dequantiser by the integer pipe (the byte
+// permutes).  Layout of the work:
 //   quantise: persistent CTAs of 512 (+ 32) or 1024 threads, each taking groups of 256
 //     consecutive blocks (one double quantisation group of 256, or several
 //     smaller groups), the input of each group brought into shared memory
@@ -90,7 +92,7 @@ constexpr float kQuantBand = 9.5367431640625e-07f;  // 2^-20
 constexpr int kQStages = 3;
 template <bool kBf16In, int kR>
 __host__ __device__ constexpr bool quant_bulk() { return kBf16In || kR == 1; }
-// 32 warps per SM either way: bf16 weights in 64-weight blocks run two CTAs
+// 32 pass warps per SM either way: bf16 weights in 64-weight blocks run two CTAs
 // of 512 threads per SM (two 96 KB stage rings; half the warps at each
 // barrier; each CTA with one more warp for the double quantisation), the
 // other staged cases one CTA of 1024 threads (a 192 KB ring),
